@@ -1,0 +1,165 @@
+"""CPU oracle for the W4A16 matmul. TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package. The product library never loads it, and this package
+imports nothing from the product package.
+
+The arithmetic lives in ``w4a16_oracle.c`` (plain C, FP64, k-ascending sums);
+this module compiles it with gcc and marshals numpy arrays through ctypes.
+Definitions and citations are in the C file's header.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_w4a16.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile the oracle library with gcc (no GPU needed)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        lib.w4o_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.w4o_half_to_double.restype = ctypes.c_double
+        lib.w4o_decode_halves.argtypes = [P, P, ctypes.c_size_t]
+        lib.w4o_dequant.argtypes = [P, P, I, I, I, P]
+        lib.w4o_gemm.argtypes = [P, P, P, I, I, I, I, P, P, I]
+        lib.w4o_gemm.restype = I
+        lib.w4o_gemm_sample.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
+        lib.w4o_gemm_sample.restype = I
+        lib.w4o_packed_words.argtypes = [I, I]
+        lib.w4o_packed_words.restype = ctypes.c_size_t
+        lib.w4o_locate.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(I)]
+        lib.w4o_unpack.argtypes = [P, I, I, P]
+        lib.w4o_unpack.restype = ctypes.c_longlong
+        lib.w4o_pack.argtypes = [P, I, I, P]
+        lib.w4o_unpack_scales.argtypes = [P, I, I, P]
+        lib.w4o_unpack_scales.restype = ctypes.c_longlong
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    assert a.dtype == np.uint16
+    return a
+
+
+def n_groups(K, G):
+    return -(-K // G)
+
+
+def half_to_double(bits):
+    """Decode binary16 bit patterns (uint16 array) to float64 with the oracle's decoder."""
+    b = _bits16(np.asarray(bits))
+    out = np.empty(b.shape, np.float64)
+    _load().w4o_decode_halves(_ptr(b), _ptr(out), b.size)
+    return out
+
+
+def dequant(q, s, G):
+    """w[k][n] = (q[k][n] - 8) * s[k // G][n] in float64."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _bits16(s)
+    K, N = q.shape
+    assert s.shape == (n_groups(K, G), N)
+    w = np.empty((K, N), np.float64)
+    _load().w4o_dequant(_ptr(q), _ptr(s), K, N, G, _ptr(w))
+    return w
+
+
+def _threads(threads):
+    return threads if threads else (os.cpu_count() or 1)
+
+
+def gemm(x, q, s, G, threads=None):
+    """(y, absum): y = x @ dequant(q, s) in float64 (k ascending), absum = sum |x*w|."""
+    x = _bits16(x)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _bits16(s)
+    M, K = x.shape
+    K2, N = q.shape
+    assert K == K2 and s.shape == (n_groups(K, G), N)
+    y = np.empty((M, N), np.float64)
+    a = np.empty((M, N), np.float64)
+    rc = _load().w4o_gemm(_ptr(x), _ptr(q), _ptr(s), M, N, K, G, _ptr(y), _ptr(a),
+                          _threads(threads))
+    assert rc == 0
+    return y, a
+
+
+def gemm_sample(x, q, s, G, rows, cols, threads=None):
+    """(y, absum) restricted to rows x cols: y[i][j] = y_ref[rows[i]][cols[j]]."""
+    x = _bits16(x)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _bits16(s)
+    M, K = x.shape
+    N = q.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    cols = np.ascontiguousarray(cols, dtype=np.int32)
+    y = np.empty((rows.size, cols.size), np.float64)
+    a = np.empty((rows.size, cols.size), np.float64)
+    rc = _load().w4o_gemm_sample(_ptr(x), _ptr(q), _ptr(s), M, N, K, G, _ptr(rows), rows.size,
+                                 _ptr(cols), cols.size, _ptr(y), _ptr(a), _threads(threads))
+    assert rc == 0
+    return y, a
+
+
+def packed_words(K, N):
+    return int(_load().w4o_packed_words(K, N))
+
+
+def locate(K, k, n):
+    """(word index, nibble) of weight (k, n) in the packed layout."""
+    w = ctypes.c_size_t()
+    i = ctypes.c_int()
+    _load().w4o_locate(K, k, n, ctypes.byref(w), ctypes.byref(i))
+    return w.value, i.value
+
+
+def unpack(packed, K, N):
+    """(codes[K][N], number of padding nibbles that are not 8)."""
+    p = np.ascontiguousarray(packed, dtype=np.uint32)
+    assert p.size == packed_words(K, N)
+    codes = np.empty((K, N), np.uint8)
+    bad = _load().w4o_unpack(_ptr(p), K, N, _ptr(codes))
+    return codes, int(bad)
+
+
+def pack(codes):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    K, N = codes.shape
+    out = np.empty(packed_words(K, N), np.uint32)
+    _load().w4o_pack(_ptr(codes), K, N, _ptr(out))
+    return out
+
+
+def unpack_scales(sp, ng, N):
+    """(s[ng][N] as uint16 bits, number of padding entries that are not 0)."""
+    sp = _bits16(sp)
+    s = np.empty((ng, N), np.uint16)
+    bad = _load().w4o_unpack_scales(_ptr(sp), ng, N, _ptr(s))
+    return s, int(bad)

@@ -1,0 +1,243 @@
+/*
+ * CPU oracle for the W4A16 weight-only INT4 matmul. TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may load
+ * this file's library. Nothing in the CUDA library includes, links or calls it,
+ * and it includes nothing from the CUDA library: the two share no code.
+ *
+ * What it computes (the plain definition, no blocking, no reordering):
+ *
+ *   w[k][n]   = (q[k][n] - 8) * s[k / G][n]                       (dequantisation)
+ *   y[m][n]   = sum_{k=0}^{K-1} x[m][k] * w[k][n]   (k ascending, FP64)
+ *   abs[m][n] = sum_{k=0}^{K-1} |x[m][k] * w[k][n]|               (tolerance term)
+ *
+ * Sources: "quant_marlin_kernel" (aicassindra.com), "The architecture: every
+ * piece explained": weights are INT4 codes packed eight to a 32-bit word with one
+ * FP16 scale per group of weights along the reduction dimension (commonly 128);
+ * a thread unpacks the codes to FP16 and multiplies by the group scale; the
+ * tensor-core MMA multiplies the dequantised weight tile by the FP16
+ * activations. "End-to-end flow": activations (tokens x in-features) times
+ * weights (in-features x out-features). The zero-point 8 (codes 0..15 map to
+ * -8..7) is the symmetric reading of the pages, which never print a zero-point.
+ *
+ * FP16 inputs arrive as IEEE-754 binary16 bit patterns and are decoded by this
+ * file's own decoder (sign, 5-bit exponent with bias 15, 10-bit fraction,
+ * subnormals). Every product x*(q-8)*s has at most 26 significant bits, so it
+ * is exact in FP64; only the k-ascending summation rounds.
+ *
+ * The packed-layout functions at the end restate the packed word layout that
+ * the library's pack entry point documents (the pages fix only "eight 4-bit
+ * values per 32-bit word in a permuted order"; the order itself is free), so
+ * that the tests can unpack what the GPU packed and compare it bit for bit.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* IEEE-754 binary16 -> double, from the format's definition. */
+double w4o_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);            /* subnormal: 0.f * 2^-14 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25); /* 1.f * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+void w4o_decode_halves(const uint16_t* h, double* out, size_t count)
+{
+    for (size_t i = 0; i < count; ++i) out[i] = w4o_half_to_double(h[i]);
+}
+
+/* Group index of row k. group_size == K means one group per column. */
+static int group_of(int k, int G) { return k / G; }
+
+/* Dequantise column n of the weight matrix into w_col[K]. */
+static void dequant_column(const uint8_t* q, const uint16_t* s, int K, int N, int G,
+                           int n, double* w_col)
+{
+    for (int k = 0; k < K; ++k) {
+        int code = q[(size_t)k * N + n];
+        double scale = w4o_half_to_double(s[(size_t)group_of(k, G) * N + n]);
+        w_col[k] = (double)(code - 8) * scale;
+    }
+}
+
+/* Full dequantised matrix w[K][N] (FP64), for inspection in tests. */
+void w4o_dequant(const uint8_t* q, const uint16_t* s, int K, int N, int G, double* w)
+{
+    double* col = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int n = 0; n < N; ++n) {
+        dequant_column(q, s, K, N, G, n, col);
+        for (int k = 0; k < K; ++k) w[(size_t)k * N + n] = col[k];
+    }
+    free(col);
+}
+
+typedef struct {
+    const uint16_t* x; const uint8_t* q; const uint16_t* s;
+    int M, N, K, G;
+    const int* rows; int nrows;      /* rows of y to evaluate           */
+    const int* cols; int ncols;      /* columns of y to evaluate        */
+    double* y; double* absum;        /* [nrows][ncols], may be NULL     */
+    int col_begin, col_end;          /* this worker's share of cols     */
+    const double* xd;                /* decoded x rows [nrows][K]       */
+} job_t;
+
+static void* worker(void* arg)
+{
+    job_t* j = (job_t*)arg;
+    double* w_col = (double*)malloc(sizeof(double) * (size_t)j->K);
+    for (int c = j->col_begin; c < j->col_end; ++c) {
+        dequant_column(j->q, j->s, j->K, j->N, j->G, j->cols[c], w_col);
+        for (int r = 0; r < j->nrows; ++r) {
+            const double* xr = j->xd + (size_t)r * j->K;
+            double acc = 0.0, acc_abs = 0.0;
+            for (int k = 0; k < j->K; ++k) {
+                double t = xr[k] * w_col[k];
+                acc += t;
+                acc_abs += fabs(t);
+            }
+            j->y[(size_t)r * j->ncols + c] = acc;
+            if (j->absum) j->absum[(size_t)r * j->ncols + c] = acc_abs;
+        }
+    }
+    free(w_col);
+    return NULL;
+}
+
+/*
+ * y[r][c] = y_ref[rows[r]][cols[c]] for the listed rows and columns (every
+ * element is an independent sum, so a sample of elements is exact for those
+ * elements). x is [M][K], q is [K][N] (codes 0..15), s is [ceil(K/G)][N].
+ * Work is split over `threads` POSIX threads by column; the arithmetic of each
+ * element does not depend on the split.
+ */
+int w4o_gemm_sample(const uint16_t* x, const uint8_t* q, const uint16_t* s,
+                    int M, int N, int K, int G,
+                    const int* rows, int nrows, const int* cols, int ncols,
+                    double* y, double* absum, int threads)
+{
+    if (M < 0 || N < 0 || K < 0 || G <= 0 || nrows < 0 || ncols < 0) return 1;
+    double* xd = (double*)malloc(sizeof(double) * ((size_t)nrows * K + 1));
+    for (int r = 0; r < nrows; ++r) {
+        if (rows[r] < 0 || rows[r] >= M) { free(xd); return 1; }
+        for (int k = 0; k < K; ++k)
+            xd[(size_t)r * K + k] = w4o_half_to_double(x[(size_t)rows[r] * K + k]);
+    }
+    for (int c = 0; c < ncols; ++c)
+        if (cols[c] < 0 || cols[c] >= N) { free(xd); return 1; }
+    if (threads < 1) threads = 1;
+    if (threads > ncols) threads = ncols > 0 ? ncols : 1;
+    pthread_t* tid = (pthread_t*)malloc(sizeof(pthread_t) * threads);
+    job_t* jobs = (job_t*)malloc(sizeof(job_t) * threads);
+    for (int t = 0; t < threads; ++t) {
+        job_t j = {x, q, s, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+                   (int)((long long)ncols * t / threads),
+                   (int)((long long)ncols * (t + 1) / threads), xd};
+        jobs[t] = j;
+    }
+    for (int t = 1; t < threads; ++t) pthread_create(&tid[t], NULL, worker, &jobs[t]);
+    worker(&jobs[0]);
+    for (int t = 1; t < threads; ++t) pthread_join(tid[t], NULL);
+    free(jobs); free(tid); free(xd);
+    return 0;
+}
+
+/* The whole output: y[M][N] and absum[M][N]. */
+int w4o_gemm(const uint16_t* x, const uint8_t* q, const uint16_t* s,
+             int M, int N, int K, int G, double* y, double* absum, int threads)
+{
+    int* rows = (int*)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
+    int* cols = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+    for (int i = 0; i < M; ++i) rows[i] = i;
+    for (int i = 0; i < N; ++i) cols[i] = i;
+    int rc = w4o_gemm_sample(x, q, s, M, N, K, G, rows, M, cols, N, y, absum, threads);
+    free(rows); free(cols);
+    return rc;
+}
+
+/*
+ * Packed layout, restated for the round-trip check. Column tiles of 128
+ * output features, reduction chunks of 64. For tile nt, chunk kc, half j
+ * (32 rows of k), feature n_in within the tile and word w within the half:
+ *
+ *   word index = (((nt * KC + kc) * 2 + j) * 128 + n_in) * 4 + w,  KC = ceil(K/64)
+ *   word holds k0 = kc*64 + j*32 + w*8 .. k0+7 of column n = nt*128 + n_in;
+ *   nibble i (bits 4i..4i+3) holds k = k0 + 2*(i mod 4) + i/4.
+ *
+ * Positions with k >= K or n >= N hold code 8 (weight 0).
+ * Scales: scales_packed[(nt * ng + g) * 128 + n_in] = s[g][nt*128 + n_in], 0 for n >= N.
+ */
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+size_t w4o_packed_words(int K, int N) { return (size_t)ceil_div(N, 128) * ceil_div(K, 64) * 1024; }
+
+/* Where (k, n) lives: word index and nibble. */
+void w4o_locate(int K, int k, int n, size_t* word, int* nibble)
+{
+    int KC = ceil_div(K, 64);
+    int nt = n / 128, n_in = n % 128;
+    int kc = k / 64, r = k % 64;
+    int j = r / 32, r2 = r % 32;
+    int w = r2 / 8, o = r2 % 8;                  /* o = 2*(i mod 4) + i/4 */
+    int i = (o % 2) * 4 + o / 2;
+    *word = ((((size_t)nt * KC + kc) * 2 + j) * 128 + n_in) * 4 + w;
+    *nibble = i;
+}
+
+/* Unpack codes[K][N] from packed words; returns the number of padding nibbles != 8. */
+long long w4o_unpack(const uint32_t* packed, int K, int N, uint8_t* codes)
+{
+    int KC = ceil_div(K, 64), NT = ceil_div(N, 128);
+    long long bad_pad = 0;
+    for (int nt = 0; nt < NT; ++nt)
+        for (int k = 0; k < KC * 64; ++k)
+            for (int n_in = 0; n_in < 128; ++n_in) {
+                int n = nt * 128 + n_in;
+                size_t word; int nib;
+                w4o_locate(K, k, n, &word, &nib);
+                int c = (packed[word] >> (4 * nib)) & 0xF;
+                if (k < K && n < N) codes[(size_t)k * N + n] = (uint8_t)c;
+                else if (c != 8) ++bad_pad;
+            }
+    return bad_pad;
+}
+
+/* The oracle's own pack, used only to check that unpack inverts it. */
+void w4o_pack(const uint8_t* codes, int K, int N, uint32_t* packed)
+{
+    size_t total = w4o_packed_words(K, N);
+    for (size_t i = 0; i < total; ++i) packed[i] = 0x88888888u;
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) {
+            size_t word; int nib;
+            w4o_locate(K, k, n, &word, &nib);
+            packed[word] &= ~(0xFu << (4 * nib));
+            packed[word] |= (uint32_t)(codes[(size_t)k * N + n] & 0xF) << (4 * nib);
+        }
+}
+
+/* Unpack scales[ng][N] from the tile-ordered copy; returns count of nonzero pads. */
+long long w4o_unpack_scales(const uint16_t* sp, int ng, int N, uint16_t* s)
+{
+    int NT = ceil_div(N, 128);
+    long long bad_pad = 0;
+    for (int nt = 0; nt < NT; ++nt)
+        for (int g = 0; g < ng; ++g)
+            for (int n_in = 0; n_in < 128; ++n_in) {
+                int n = nt * 128 + n_in;
+                uint16_t v = sp[((size_t)nt * ng + g) * 128 + n_in];
+                if (n < N) s[(size_t)g * N + n] = v;
+                else if (v != 0) ++bad_pad;
+            }
+    return bad_pad;
+}

@@ -1,0 +1,279 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+* the binary16 decoder against numpy's float16 over all 65536 bit patterns;
+* brute force in exact rational arithmetic on tiny inputs (all group sizes,
+  K not a multiple of G, subnormal scales);
+* the hand-worked 1x8x8 example in tests/golden/hand_1x8x8.txt;
+* invariants: zero scales, all codes 8, a single nonzero code, linearity in x,
+  doubling the scales, one-hot rows of x;
+* mutants: a copy of the oracle with one planted mistake must fail a pin.
+"""
+import os
+import re
+import shutil
+import subprocess
+import tempfile
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from weight_only_int4_02_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_1x8x8.txt")
+
+
+def read_golden():
+    out = {}
+    with open(GOLDEN) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            key, vals = line.split(":", 1)
+            out[key.strip()] = np.array([float(v) for v in vals.split()])
+    return out
+
+
+def hand_inputs(G):
+    x = np.array([1, -1, 2, -2, 0.5, -0.5, 1, 0], np.float16).reshape(1, 8)
+    q = np.array([[(3 * k + n) % 16 for n in range(8)] for k in range(8)], np.uint8)
+    base = np.array([0.25 * (1 + n % 4) for n in range(8)])
+    if G == 4:
+        s = np.stack([base, base / 2]).astype(np.float16)
+    else:
+        s = base.reshape(1, 8).astype(np.float16)
+    return x, q, s
+
+
+def test_half_decoder_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle_mod.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # a few fixed points of the format
+    named = {0x3C00: 1.0, 0xC000: -2.0, 0x0001: 2.0 ** -24, 0x0400: 2.0 ** -14,
+             0x7BFF: 65504.0, 0x6400: 1024.0, 0x8000: -0.0}
+    for b, v in named.items():
+        assert oracle_mod.half_to_double(np.array([b], np.uint16))[0] == v
+
+
+def exact_reference(x, q, s, G):
+    """Exact rationals: each FP16 value converts to Fraction without rounding."""
+    M, K = x.shape
+    N = q.shape[1]
+    xf = [[Fraction(float(v)) for v in row] for row in x.astype(np.float64)]
+    sf = [[Fraction(float(v)) for v in row] for row in s.astype(np.float64)]
+    y = [[Fraction(0)] * N for _ in range(M)]
+    a = [[Fraction(0)] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            acc, acc_abs = Fraction(0), Fraction(0)
+            for k in range(K):
+                t = xf[m][k] * (int(q[k][n]) - 8) * sf[k // G][n]
+                acc += t
+                acc_abs += abs(t)
+            y[m][n], a[m][n] = acc, acc_abs
+    return y, a
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_brute_force_exact(oracle_mod, seed):
+    r = np.random.default_rng(1000 + seed)
+    M, K, N = (int(v) for v in r.integers(1, 9, size=3))
+    G = int(r.choice([1, 2, 3, 4, K]))
+    x = (r.standard_normal((M, K)) * 4).astype(np.float16)
+    q = r.integers(0, 16, size=(K, N)).astype(np.uint8)
+    ng = -(-K // G)
+    s = np.abs(r.standard_normal((ng, N))).astype(np.float16)
+    if seed % 3 == 0:   # subnormal scales: multiples of 2^-24 below 2^-14
+        s = (r.integers(1, 1024, size=(ng, N)) * 2.0 ** -24).astype(np.float16)
+    y, a = oracle_mod.gemm(x, q, s, G)
+    ye, ae = exact_reference(x, q, s, G)
+    for m in range(M):
+        for n in range(N):
+            bound = (K * 2.0 ** -53) * float(ae[m][n])
+            assert abs(Fraction(y[m][n]) - ye[m][n]) <= Fraction(bound)
+            assert abs(Fraction(a[m][n]) - ae[m][n]) <= Fraction(bound)
+
+
+def test_hand_example(oracle_mod):
+    g = read_golden()
+    for G, key in ((4, "G4"), (8, "G8")):
+        x, q, s = hand_inputs(G)
+        assert np.array_equal(x[0].astype(np.float64), g["x"])
+        y, a = oracle_mod.gemm(x, q, s, G)
+        assert np.array_equal(y[0], g[key + "_y"]), (G, y[0])
+        assert np.array_equal(a[0], g[key + "_abs"]), (G, a[0])
+
+
+def small_problem(M=5, K=96, N=24, G=32, seed=7):
+    return inputs.problem(M, K, N, G, seed=seed)
+
+
+def test_zero_scales_give_zero(oracle_mod):
+    x, q, s = small_problem()
+    y, _ = oracle_mod.gemm(x, q, np.zeros_like(s), 32)
+    assert np.all(y == 0)
+
+
+def test_all_codes_eight_give_zero(oracle_mod):
+    x, q, s = small_problem()
+    y, _ = oracle_mod.gemm(x, np.full_like(q, 8), s, 32)
+    assert np.all(y == 0)
+
+
+def test_single_code_gives_single_column(oracle_mod):
+    x, q, s = small_problem()
+    K, N = q.shape
+    G = 32
+    k0, n0, code = 45, 17, 3
+    q1 = np.full_like(q, 8)
+    q1[k0, n0] = code
+    y, _ = oracle_mod.gemm(x, q1, s, G)
+    expect = x[:, k0].astype(np.float64) * (code - 8) * float(s[k0 // G, n0])
+    assert np.array_equal(y[:, n0], expect)
+    others = np.delete(y, n0, axis=1)
+    assert np.all(others == 0)
+
+
+def test_linearity_in_x(oracle_mod):
+    x, q, s = small_problem()
+    M, K = x.shape
+    x1 = x.copy()
+    x1[:, 1::2] = 0      # disjoint supports keep 2*x1 + 0.5*x2 exact in FP16
+    x2 = x.copy()
+    x2[:, 0::2] = 0
+    xs = (2 * x1.astype(np.float32) + 0.5 * x2.astype(np.float32)).astype(np.float16)
+    assert np.array_equal(xs.astype(np.float32), 2 * x1.astype(np.float32) + 0.5 * x2.astype(np.float32))
+    y, a = oracle_mod.gemm(xs, q, s, 32)
+    y1, _ = oracle_mod.gemm(x1, q, s, 32)
+    y2, _ = oracle_mod.gemm(x2, q, s, 32)
+    assert np.all(np.abs(y - (2 * y1 + 0.5 * y2)) <= 4 * K * 2.0 ** -53 * a)
+
+
+def test_doubling_scales_doubles_output(oracle_mod):
+    x, q, s = small_problem()
+    y, _ = oracle_mod.gemm(x, q, s, 32)
+    y2, _ = oracle_mod.gemm(x, q, (s.astype(np.float32) * 2).astype(np.float16), 32)
+    assert np.array_equal(y2, 2 * y)
+
+
+def test_one_hot_rows_return_dequantised_rows(oracle_mod):
+    _, q, s = small_problem()
+    K, N = q.shape
+    rows = [0, 31, 32, 95]
+    x = np.zeros((len(rows), K), np.float16)
+    for i, k in enumerate(rows):
+        x[i, k] = 1.0
+    y, _ = oracle_mod.gemm(x, q, s, 32)
+    w = oracle_mod.dequant(q, s, 32)
+    for i, k in enumerate(rows):
+        assert np.array_equal(y[i], w[k])
+        assert np.array_equal(w[k], (q[k].astype(np.float64) - 8) * s[k // 32].astype(np.float64))
+
+
+def test_per_column_group_equals_single_group(oracle_mod):
+    x, q, _ = small_problem(K=64)
+    s1 = inputs.scales(64, q.shape[1], 64, seed=3)
+    y_a, _ = oracle_mod.gemm(x, q, s1, 64)
+    s_rep = np.repeat(s1, 2, axis=0)
+    y_b, _ = oracle_mod.gemm(x, q, s_rep, 32)
+    assert np.array_equal(y_a, y_b)
+
+
+def test_sample_matches_full_and_threads_do_not_matter(oracle_mod):
+    x, q, s = inputs.problem(9, 200, 70, 64, seed=11)
+    y, a = oracle_mod.gemm(x, q, s, 64, threads=1)
+    y4, a4 = oracle_mod.gemm(x, q, s, 64, threads=4)
+    assert np.array_equal(y, y4) and np.array_equal(a, a4)
+    rows, cols = [8, 0, 3], [69, 1, 33, 34]
+    ys, as_ = oracle_mod.gemm_sample(x, q, s, 64, rows, cols, threads=3)
+    assert np.array_equal(ys, y[np.ix_(rows, cols)])
+    assert np.array_equal(as_, a[np.ix_(rows, cols)])
+
+
+@pytest.mark.parametrize("K,N", [(64, 128), (200, 130), (8, 8), (4040, 256)])
+def test_layout_is_a_bijection_and_round_trips(oracle_mod, K, N):
+    KC, NT = -(-K // 64), -(-N // 128)
+    total = oracle_mod.packed_words(K, N)
+    assert total == KC * NT * 1024
+    if K * N <= 64 * 1024:
+        seen = set()
+        for k in range(KC * 64):
+            for n in range(NT * 128):
+                w, i = oracle_mod.locate(K, k, n)
+                assert 0 <= w < total and 0 <= i < 8
+                seen.add((w, i))
+        assert len(seen) == total * 8
+    q = inputs.codes(K, N, seed=5)
+    p = oracle_mod.pack(q)
+    q2, bad = oracle_mod.unpack(p, K, N)
+    assert bad == 0 and np.array_equal(q, q2)
+    for pattern in (0, 15):
+        qq = np.full((K, N), pattern, np.uint8)
+        q3, bad = oracle_mod.unpack(oracle_mod.pack(qq), K, N)
+        assert bad == 0 and np.array_equal(q3, qq)
+
+
+def test_layout_pairs_adjacent_k_in_nibbles_i_and_i_plus_4(oracle_mod):
+    # nibble i of a word holds k0 + 2*(i mod 4) + i//4: the two halves of a
+    # 16-bit lane pair hold k and k+1.
+    for k in range(64):
+        w, i = oracle_mod.locate(64, k, 0)
+        assert (k % 8) == 2 * (i % 4) + i // 4
+        w2, i2 = oracle_mod.locate(64, k, 1)
+        assert w2 == w + 4 and i2 == i
+
+
+def test_scales_unpack(oracle_mod):
+    N, ng = 200, 3
+    s = inputs.scales(3 * 32, N, 32, seed=2)
+    sp = np.zeros(-(-N // 128) * ng * 128, np.uint16)
+    for g in range(ng):
+        for n in range(N):
+            sp[((n // 128) * ng + g) * 128 + n % 128] = s.view(np.uint16)[g, n]
+    s2, bad = oracle_mod.unpack_scales(sp, ng, N)
+    assert bad == 0 and np.array_equal(s2, s.view(np.uint16))
+
+
+MUTANTS = {
+    "zero_point_7": ("(double)(code - 8)", "(double)(code - 7)"),
+    "no_groups": ("static int group_of(int k, int G) { return k / G; }",
+                  "static int group_of(int k, int G) { (void)k; (void)G; return 0; }"),
+    "transposed_weights": ("int code = q[(size_t)k * N + n];", "int code = q[(size_t)n * N + k];"),
+    "exponent_bias": ("ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)"),
+    "subnormal_scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "dropped_abs": ("acc_abs += fabs(t);", "acc_abs += t;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_fail_a_pin(oracle_mod, name):
+    """Each planted mistake in a copy of the oracle must break a pin above."""
+    import importlib.util
+    src_dir = os.path.dirname(oracle_mod.__file__)
+    old, new = MUTANTS[name]
+    text = open(os.path.join(src_dir, "w4a16_oracle.c")).read()
+    assert old in text
+    with tempfile.TemporaryDirectory() as d:
+        mdir = os.path.join(d, "oracle_mutant")
+        os.mkdir(mdir)
+        shutil.copy(os.path.join(src_dir, "__init__.py"), mdir)
+        with open(os.path.join(mdir, "w4a16_oracle.c"), "w") as f:
+            f.write(text.replace(old, new))
+        spec = importlib.util.spec_from_file_location("oracle_mutant", os.path.join(mdir, "__init__.py"))
+        mut = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mut)
+        mut.build(force=True)
+        failures = 0
+        for check in (test_hand_example, test_half_decoder_all_patterns,
+                      test_all_codes_eight_give_zero, test_per_column_group_equals_single_group,
+                      lambda o: test_brute_force_exact(o, 0), lambda o: test_brute_force_exact(o, 1)):
+            try:
+                check(mut)
+            except AssertionError:
+                failures += 1
+                break
+        assert failures > 0, name
