@@ -1,0 +1,564 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 matmul on one GB300 (or N replicas under torchrun).
+
+One step = one pass of the workload's GEMMs (default: the Llama-2-7B-like
+decode sweep, M in {1..128} x the four layer shapes, group 128), each reading
+its own copy of the packed weights so the step streams more distinct bytes
+than L2 holds. Steps are replayed from CUDA Graphs with an event node around
+every launch, so per-kernel durations come from CUDA events on the launching
+stream. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload.
+"""
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from weight_only_int4_02_gb300 import inputs  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DEFAULT_WORKLOAD = "llama2_7b_decode_sweep"
+
+
+# --------------------------------------------------------------------------- accounting
+def n_groups(K, G):
+    return -(-K // G)
+
+
+def weight_bytes(K, N, G):
+    """Packed INT4 codes (K padded to a whole group) plus FP16 group scales."""
+    ng = n_groups(K, G)
+    return ng * G * N // 2 + ng * N * 2
+
+
+def algorithmic_bytes(M, K, N, G):
+    return weight_bytes(K, N, G) + 2 * M * K + 2 * M * N
+
+
+def flops(M, K, N):
+    return 2 * M * N * K
+
+
+def fp16_over_int4_byte_ratio(G):
+    """Bytes per weight, FP16 over INT4 with one FP16 scale per G weights."""
+    return 2.0 / (0.5 + 2.0 / G)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def roofline_seconds(M, K, N, G, peaks):
+    return max(algorithmic_bytes(M, K, N, G) / (peaks["hbm_gbs"] * 1e9),
+               flops(M, K, N) / (peaks["bf16_tflops"] * 1e12))
+
+
+# --------------------------------------------------------------------------- runtime helpers
+class Cudart:
+    """The few CUDA runtime calls torch does not expose (event nodes in graphs)."""
+
+    def __init__(self):
+        import torch
+        self.lib = None
+        cands = ["libcudart.so.13", "libcudart.so"]
+        cands += glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib", "libcudart.so*"))
+        cands += ["/usr/local/cuda/lib64/libcudart.so"]
+        for c in cands:
+            try:
+                self.lib = ctypes.CDLL(c)
+                break
+            except OSError:
+                continue
+        if self.lib is None:
+            raise RuntimeError("libcudart not found")
+        self.lib.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.lib.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+
+    def event(self):
+        e = ctypes.c_void_p()
+        rc = self.lib.cudaEventCreate(ctypes.byref(e))
+        if rc != 0:
+            raise RuntimeError("cudaEventCreate failed: %d" % rc)
+        return e
+
+    def record_external(self, ev, stream):
+        rc = self.lib.cudaEventRecordWithFlags(ev, ctypes.c_void_p(stream.cuda_stream), 1)
+        if rc != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed: %d" % rc)
+
+    def elapsed_ms(self, a, b):
+        ms = ctypes.c_float()
+        rc = self.lib.cudaEventElapsedTime(ctypes.byref(ms), a, b)
+        if rc != 0:
+            raise RuntimeError("cudaEventElapsedTime failed: %d" % rc)
+        return ms.value
+
+    def destroy(self, ev):
+        self.lib.cudaEventDestroy(ev)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, wall0, wall1):
+        """Summary of the samples taken between wall-clock times wall0 and wall1."""
+        import datetime
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside, near = [], []
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sample = (float(r[2]), float(r[3]), [n for n, v in zip(names, r[6:10]) if v.strip() == "Active"])
+            except ValueError:
+                continue
+            if wall0 <= ts <= wall1:
+                inside.append(sample)
+            elif wall0 - 0.2 <= ts <= wall1 + 0.2:
+                near.append(sample)
+        use = inside if inside else near
+        reasons = sorted(set(r for s in use for r in s[2]))
+        return {"sm_mhz": statistics.median(s[0] for s in use) if use else None,
+                "sm_max_mhz": max(s[1] for s in use) if use else None,
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "within 0.2 s of the timed region"}
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "weight_only_int4_02_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    with open(path) as f:
+        for line in f:
+            kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
+            if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src") == digest:
+                return float(kv["bytes_per_launch"])
+    return None
+
+
+# --------------------------------------------------------------------------- CPU baseline (oracle)
+def oracle_sample_run(cases, G, scale_mult, outlier_frac, col_stride, threads, data_cache):
+    """Time the oracle over every case, on every col_stride-th column. Returns (seconds, flops done)."""
+    import oracle
+    done = 0
+    t = 0.0
+    for (M, K, N) in cases:
+        key = (K, N)
+        if key not in data_cache:
+            data_cache[key] = (inputs.codes(K, N, 0), inputs.scales(K, N, G, 0, "halfnormal", scale_mult))
+        q, s = data_cache[key]
+        x = data_cache.setdefault(("x", M, K), inputs.activations(M, K, 0, outlier_frac))
+        cols = np.arange(0, N, col_stride, dtype=np.int32)
+        rows = np.arange(M, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.gemm_sample(x, q, s, G, rows, cols, threads=threads)
+        t += time.perf_counter() - t0
+        done += flops(M, K, len(cols))
+    return t, done
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    cache = {}
+    cases = wl["cases"]
+    total = sum(flops(*c) for c in cases)
+    # calibrate on a coarse sample, then size the timed sample to the budget
+    stride = 512
+    t, done = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride,
+                                threads, cache)
+    rate = done / max(t, 1e-9)
+    want = rate * budget_s
+    stride = max(1, int(total / max(want, 1.0)))
+    t, done = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride,
+                                threads, cache)
+    return {"value": done / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "every case of the workload, all rows, every %d-th output column (%.3g of the "
+                      "workload's flops), %.1f s" % (stride, done / total, t),
+            "seconds": t}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = inputs.WORKLOADS[args.workload]
+    G = wl["group_size"]
+    cases = wl["cases"]
+    peaks = load_peaks()
+    cud = Cudart()
+
+    # ---- data: pack each layer once, then give every case its own copy
+    layer_data = {}
+    for (M, K, N) in cases:
+        if (K, N) not in layer_data:
+            q = inputs.codes(K, N, 0)
+            s = inputs.scales(K, N, G, 0, "halfnormal", wl["scale_mult"])
+            layer_data[(K, N)] = w4a16.pack(torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev), G)
+            del q
+    per_case = []
+    for (M, K, N) in cases:
+        packed, sp = layer_data[(K, N)]
+        x = torch.from_numpy(inputs.activations(M, K, 0, wl.get("outlier_frac", 0.0))).to(dev)
+        per_case.append(dict(M=M, K=K, N=N, packed=packed.clone(), sp=sp.clone(), x=x,
+                             y=torch.empty((M, N), dtype=torch.float16, device=dev)))
+    del layer_data
+    distinct_bytes = sum(c["packed"].numel() * 4 + c["sp"].numel() * 2 for c in per_case)
+    torch.cuda.synchronize()
+
+    def launch_all():
+        for c in per_case:
+            w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"])
+
+    launch_all()   # first call allocates the library's workspace (outside capture)
+    torch.cuda.synchronize()
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("kernel wait timed out during warm-up")
+
+    # ---- a pool of instrumented graphs (event node after every launch), replayed in turn
+    cap = torch.cuda.Stream()
+    K = args.steps
+    pool = min(K, 64)
+    graphs, evs = [], []
+    for gi in range(pool):
+        ev = [cud.event() for _ in range(len(per_case) + 1)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            st = torch.cuda.current_stream()
+            cud.record_external(ev[0], st)
+            for ci, c in enumerate(per_case):
+                w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
+                cud.record_external(ev[ci + 1], st)
+        graphs.append(g)
+        evs.append(ev)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % pool].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record()
+    for i in range(K):
+        graphs[i % pool].replay()
+    t1.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(wall0, wall1)
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / K
+    status = w4a16.check_device_status()
+    if status != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+
+    # ---- per-launch durations from the event nodes (the last `pool` steps of the timed region)
+    dur = np.zeros((pool, len(per_case)))
+    for gi in range(pool):
+        for ci in range(len(per_case)):
+            dur[gi, ci] = cud.elapsed_ms(evs[gi][ci], evs[gi][ci + 1])
+    mean_ms = dur.mean(axis=0)
+    step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    # ---- per kernel instance and per M
+    kernels = {}
+    for ci, c in enumerate(per_case):
+        path, tile_m, grid = w4a16.plan(c["M"], c["N"], c["K"], G)
+        name = "w4a16_tc_kernel<%d>" % tile_m
+        k = kernels.setdefault(name, dict(ms=0.0, bytes=0, flops=0, launches=0, t_roof=0.0))
+        k["ms"] += mean_ms[ci]
+        k["bytes"] += algorithmic_bytes(c["M"], c["K"], c["N"], G)
+        k["flops"] += flops(c["M"], c["K"], c["N"])
+        k["launches"] += 1
+        c["plan"] = (path, tile_m, grid)
+    dom_name = max(kernels, key=lambda n: kernels[n]["ms"])
+    dom = kernels[dom_name]
+    hbm_s = dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    tc_s = dom["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if hbm_s >= tc_s:
+        achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    roof["traffic"] = load_traffic(dom_name, args.workload)
+    roof["kernel"] = dom_name
+    roof["launches_per_step"] = dom["launches"]
+    roof["algorithmic_bytes_per_launch"] = dom["bytes"] / dom["launches"]
+    roof["avg_launch_us"] = dom["ms"] * 1e3 / dom["launches"]
+    roof["peak_source"] = peaks["source"] + (" (HBM copy)" if roof["bound"] == "hbm" else " (bf16 burst)")
+
+    per_m = {}
+    for ci, c in enumerate(per_case):
+        d = per_m.setdefault(c["M"], dict(ms=0.0, fl=0, wb=0, roof_s=0.0))
+        d["ms"] += mean_ms[ci]
+        d["fl"] += flops(c["M"], c["K"], c["N"])
+        d["wb"] += weight_bytes(c["K"], c["N"], G)
+        d["roof_s"] += roofline_seconds(c["M"], c["K"], c["N"], G, peaks)
+
+    # ---- FP16-weight GEMM of the same shapes (cuBLAS through torch.matmul), same protocol
+    fp16 = fp16_baseline(per_case, dev, reps=max(3, min(K, 50)))
+
+    per_m_out = []
+    for M in sorted(per_m):
+        d = per_m[M]
+        entry = {"M": M, "tflops": d["fl"] / (d["ms"] * 1e-3) / 1e12,
+                 "weight_gbs": d["wb"] / (d["ms"] * 1e-3) / 1e9,
+                 "roofline_frac": d["roof_s"] / (d["ms"] * 1e-3),
+                 "us": d["ms"] * 1e3}
+        if fp16 is not None:
+            entry["fp16_us"] = fp16[M] * 1e3
+            entry["speedup_vs_fp16"] = fp16[M] / d["ms"]
+        per_m_out.append(entry)
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(per_case, G, dev, K, args.warmup, world)
+
+    out = {
+        "metric": "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM/tensor roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": args.workload, "gemms_per_step": len(per_case),
+                   "shapes": "M in %s x (K,N) in %s, group %d" % (
+                       sorted(set(c["M"] for c in per_case)), sorted(set((c["K"], c["N"]) for c in per_case)), G),
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2: every GEMM reads its own copy of the packed weights "
+                         "(%.0f MB distinct per step vs 129 MB L2)" % (distinct_bytes / 1e6),
+                   "timing": "CUDA Graph per step with an event node after every launch; per-launch "
+                             "durations are the mean over the last %d steps of the timed region" % pool},
+        "roofline": roof,
+        "gpu_launches": K * len(per_case),
+        "clocks": clocks,
+        "e2e": e2e,
+        "per_M": per_m_out,
+        "kernels": {n: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3} for n, v in kernels.items()},
+        "byte_ratio_fp16_over_w4g128": fp16_over_int4_byte_ratio(G),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    return out
+
+
+def fp16_baseline(per_case, dev, reps):
+    """Mean time per M of torch.matmul with FP16 weights of the same shapes (own copy per case)."""
+    import torch
+    try:
+        mats = []
+        for c in per_case:
+            wgt = torch.randn((c["K"], c["N"]), dtype=torch.float16, device=dev)
+            mats.append((c["x"], wgt, torch.empty((c["M"], c["N"]), dtype=torch.float16, device=dev)))
+        for x, wgt, y in mats:
+            torch.matmul(x, wgt, out=y)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mats) + 1)] for _ in range(reps)]
+        for r in range(reps):
+            ev[r][0].record()
+            for i, (x, wgt, y) in enumerate(mats):
+                torch.matmul(x, wgt, out=y)
+                ev[r][i + 1].record()
+        torch.cuda.synchronize()
+        per_m = {}
+        for i, c in enumerate(per_case):
+            ms = statistics.median(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps))
+            per_m[c["M"]] = per_m.get(c["M"], 0.0) + ms
+        del mats
+        torch.cuda.empty_cache()
+        return per_m
+    except RuntimeError:
+        return None
+
+
+def run_e2e(per_case, G, dev, K, W, world):
+    """Same metric through the public API with host buffers: per step, pinned X -> device,
+    the GEMMs, device Y -> pinned host, all inside the timed region (one graph per step)."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    xs_h = [c["x"].cpu().pin_memory() for c in per_case]
+    ys_h = [torch.empty((c["M"], c["N"]), dtype=torch.float16).pin_memory() for c in per_case]
+    h2d = sum(x.numel() * 2 for x in xs_h)
+    d2h = sum(y.numel() * 2 for y in ys_h)
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        st = torch.cuda.current_stream()
+        for c, xh, yh in zip(per_case, xs_h, ys_h):
+            c["x"].copy_(xh, non_blocking=True)
+            w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
+            yh.copy_(c["y"], non_blocking=True)
+    for _ in range(max(W, 1)):
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
+    ok = all(torch.equal(yh, c["y"].cpu()) for c, yh in zip(per_case, ys_h))
+    return {"value": step_flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "outputs_match_device": ok}
+
+
+# --------------------------------------------------------------------------- reference arm (oracle)
+def run_reference(args):
+    import oracle
+    oracle.build()
+    wl = inputs.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    cache = {}
+    cases = wl["cases"]
+    total = sum(flops(*c) for c in cases)
+    t, done = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), 1024,
+                                threads, cache)
+    rate = done / max(t, 1e-9)
+    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))   # whole run within a few minutes
+    stride = max(1, int(total / max(rate * budget, 1.0)))
+    for _ in range(args.warmup):
+        oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride, threads,
+                          cache)
+    t_all, d_all = 0.0, 0
+    for _ in range(args.steps):
+        t, d = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride,
+                                 threads, cache)
+        t_all += t
+        d_all += d
+    v = d_all / t_all / 1e12
+    sample = ("CPU oracle (FP64 C, %d threads): per step every case of the workload, all rows, every %d-th "
+              "output column (%.3g of the workload's flops)" % (threads, stride, d_all / args.steps / total))
+    return {"impl": "reference", "metric": "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM/tensor roofline",
+            "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_all / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

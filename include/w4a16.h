@@ -1,0 +1,143 @@
+/*
+ * w4a16.h — C ABI of libw4a16.so: weight-only INT4 x FP16 matmul on GB300 (sm_103a).
+ *
+ *   Y[M][N] = X[M][K] (FP16) x dequant(Wq)[K][N],   dequant(Wq)[k][n] = (q[k][n] - 8) * s[k/G][n]
+ *
+ * accumulated in FP32 and stored as FP16 (round to nearest even).
+ *
+ * The operation is the one the pages on the Marlin kernel describe:
+ *  - "quant_marlin_kernel" (aicassindra.com), "The architecture: every piece
+ *    explained": INT4 codes packed eight to a 32-bit word in a kernel-specific
+ *    permuted order, one FP16 scale per group of weights along the reduction
+ *    dimension (commonly 128), unpack to FP16 and multiply by the group scale,
+ *    tensor-core MMA against FP16 activations, split-K with a global reduction
+ *    of partial sums; activations stay FP16 and the output is FP16.
+ *  - same page, "End-to-end flow": activations (tokens x in-features) times
+ *    weights (in-features x out-features); repacking is done once, offline.
+ *  - "Low-Precision Quantization Kernels in Production" (llms.blog), section 1
+ *    (Marlin, "Pre-Permuted Weight Layouts"): the packed layout is a contract
+ *    between the repacking step and the kernel; section 3 (FlashInfer): split-K
+ *    with a deterministic reduction in global memory, CUDA Graph capture.
+ * The zero-point 8 is the symmetric reading (the pages print no zero-point).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device pointers of the current device,
+ *    owned by the caller, and must be 16-byte aligned. Arrays are row-major and
+ *    contiguous. FP16 values are passed as IEEE binary16 bit patterns (uint16_t).
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *    call returns without synchronising. Results are ready when the stream is.
+ *  - A call that returns anything but W4A16_OK has launched nothing, except
+ *    W4A16_ERR_CUDA from a failed launch (see w4a16_last_cuda_error()).
+ *  - Group size G must be 32, 64 or 128, or equal to K (one scale per column);
+ *    G = -1 is accepted as "equal to K". K must be a multiple of 8 (16-byte X
+ *    rows) and N a multiple of 8 (16-byte Y rows).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* w4a16_stream_t;
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or group size is invalid */
+    W4A16_ERR_UNSUPPORTED = 2,  /* the device is not sm_103 / sm_100 class             */
+    W4A16_ERR_CUDA = 3,         /* a CUDA runtime call failed; code in w4a16_last_cuda_error() */
+    W4A16_ERR_TIMEOUT = 4,      /* a kernel gave up waiting on one of its own pipeline barriers */
+    W4A16_ERR_WORKSPACE = 5     /* the caller's workspace is smaller than w4a16_workspace_bytes() */
+} w4a16_status;
+
+/* Version of the packed layout written by w4a16_pack and read by the GEMM. Packed
+ * buffers are a contract with this library: repack when the version changes. */
+int w4a16_layout_version(void);
+
+/* Static text for a status code. */
+const char* w4a16_status_string(int status);
+
+/* The cudaError_t of the last W4A16_ERR_CUDA returned on this host thread (0 if none). */
+int w4a16_last_cuda_error(void);
+
+/* Number of uint32 words of the packed weights: ceil(N/128) * ceil(K/64) * 1024.
+ * Returns 0 for invalid sizes. */
+size_t w4a16_packed_words(int K, int N, int group_size);
+
+/* Number of FP16 elements of the packed scales: ceil(N/128) * ceil(K/G) * 128.
+ * Returns 0 for invalid sizes. */
+size_t w4a16_scales_elems(int K, int N, int group_size);
+
+/*
+ * Repack codes and scales once, offline ("End-to-end flow": the layout is
+ * computed once and exploited on every forward pass).
+ *   codes          device, uint8 [K][N], values 0..15 (only the low nibble is read)
+ *   scales         device, binary16 [ceil(K/G)][N]
+ *   packed         device out, uint32 [w4a16_packed_words(K, N, G)]
+ *   scales_packed  device out, binary16 [w4a16_scales_elems(K, N, G)]
+ * Packed layout (version 1): column tiles of 128 output features, reduction
+ * chunks of 64. For tile nt, chunk kc, half j (32 values of k), feature n_in
+ * and word w: word index (((nt*KC + kc)*2 + j)*128 + n_in)*4 + w with
+ * KC = ceil(K/64); the word holds k0 = kc*64 + j*32 + w*8 .. k0+7 of column
+ * n = nt*128 + n_in, nibble i (bits 4i..4i+3) holding k = k0 + 2*(i%4) + i/4.
+ * Positions outside K x N hold code 8 (weight 0). Scales: element
+ * (nt*ceil(K/G) + g)*128 + n_in holds s[g][nt*128 + n_in] (0 outside N).
+ */
+w4a16_status w4a16_pack(const uint8_t* codes, const uint16_t* scales,
+                        uint32_t* packed, uint16_t* scales_packed,
+                        int K, int N, int group_size, w4a16_stream_t stream);
+
+/*
+ * Y = X x dequant(W), FP32 accumulation, FP16 output.
+ *   x              device, binary16 [M][K]
+ *   packed         device, output of w4a16_pack for (K, N, G)
+ *   scales_packed  device, output of w4a16_pack for (K, N, G)
+ *   y              device out, binary16 [M][N]; must not overlap the inputs
+ * M = 0 is a no-op. Uses a per-device workspace that the library allocates on
+ * the first call on each device (about 40 MB); make that first call outside
+ * CUDA Graph capture. Calls on one device that run concurrently on different
+ * streams share that workspace and must not overlap in time; use
+ * w4a16_gemm_ws with separate workspaces for that. Repeated calls with equal
+ * inputs give bit-identical outputs.
+ */
+w4a16_status w4a16_gemm(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
+                        uint16_t* y, int M, int N, int K, int group_size, w4a16_stream_t stream);
+
+/* Bytes of caller workspace w4a16_gemm_ws needs for this shape (0 for invalid sizes). */
+size_t w4a16_workspace_bytes(int M, int N, int K, int group_size);
+
+/*
+ * As w4a16_gemm, with a caller-owned device workspace of at least
+ * w4a16_workspace_bytes(M, N, K, G) bytes, 256-byte aligned, ZEROED ONCE by the
+ * caller before its first use; the kernels leave it ready for the next call.
+ * This variant never allocates, so it can be captured into a CUDA Graph on
+ * its first call. Returns W4A16_ERR_WORKSPACE if ws_bytes is too small.
+ */
+w4a16_status w4a16_gemm_ws(const uint16_t* x, const uint32_t* packed,
+                           const uint16_t* scales_packed, uint16_t* y,
+                           int M, int N, int K, int group_size,
+                           void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the error word that the kernels
+ * set when one of their bounded waits gave up (W4A16_ERR_TIMEOUT), for the
+ * given workspace (NULL = the library's own workspace of the current device).
+ * After a timeout the workspace's split-K counters are reset as well.
+ */
+w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
+
+/* Which kernel path and tile the dispatcher picks for a shape on the current
+ * device: *path = 1 (small-M, group scaling on FP32 accumulators) or
+ * 2 (large-M, per-weight scaling); *tile_m = rows of X per tile; *grid = CTAs. */
+w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

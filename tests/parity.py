@@ -1,0 +1,22 @@
+"""Shared helpers of the parity tests: the acceptance bound and GPU plumbing."""
+import numpy as np
+
+# Per-element acceptance: |y - y_ref| <= 1e-3 * sum_k |x_k w_kn| + 2^-10 * |y_ref|,
+# y the GPU's FP16 output taken exactly to FP64, y_ref and the sum from the oracle.
+REL_SUM = 1e-3
+REL_OUT = 2.0 ** -10
+
+
+def check_within(y_gpu, y_ref, absum, what=""):
+    y = np.asarray(y_gpu, dtype=np.float64)
+    bound = REL_SUM * absum + REL_OUT * np.abs(y_ref)
+    err = np.abs(y - y_ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        worst = np.max(err / np.maximum(bound, 1e-300))
+        raise AssertionError("%s: %d of %d outside the bound (worst err/bound %.3g); first at %s: gpu %s ref %s bound %s"
+                             % (what, int(bad.sum()), bad.size, worst, idx.tolist(),
+                                [y[tuple(i)] for i in idx], [y_ref[tuple(i)] for i in idx],
+                                [bound[tuple(i)] for i in idx]))
+    return float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0

@@ -1,0 +1,80 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects invalid arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from weight_only_int4_02_gb300 import build
+    build.build()
+    from weight_only_int4_02_gb300 import w4a16
+    return w4a16.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "w4a16.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for name in names:
+        assert hasattr(lib, name), name
+    from weight_only_int4_02_gb300 import w4a16
+    for name in w4a16.EXPORTS:
+        assert name in names
+
+
+def test_sizes(lib):
+    assert lib.w4a16_layout_version() == 1
+    assert lib.w4a16_packed_words(4096, 4096, 128) == 32 * 64 * 1024
+    assert lib.w4a16_packed_words(4040, 4096, 128) == 32 * 64 * 1024
+    assert lib.w4a16_packed_words(8, 8, 8) == 1024
+    assert lib.w4a16_scales_elems(4096, 4096, 128) == 32 * 32 * 128
+    assert lib.w4a16_scales_elems(4000, 4096, 128) == 32 * 32 * 128
+    assert lib.w4a16_scales_elems(4096, 4096, -1) == 32 * 1 * 128
+    assert lib.w4a16_scales_elems(4096, 256, 32) == 2 * 128 * 128
+    # packed bytes of the 72k x 18k layer
+    assert lib.w4a16_packed_words(18432, 73728, 128) * 4 == 18432 * 73728 // 2
+
+
+@pytest.mark.parametrize("K,N,G", [(0, 8, 8), (8, 0, 8), (12, 8, 12), (8, 12, 8), (4096, 4096, 16),
+                                   (4096, 4096, 96), (4096, 4096, 256), (-8, 8, 32)])
+def test_invalid_sizes(lib, K, N, G):
+    assert lib.w4a16_packed_words(K, N, G) == 0
+    assert lib.w4a16_scales_elems(K, N, G) == 0
+
+
+def test_invalid_arguments_return_before_any_device_work(lib):
+    from weight_only_int4_02_gb300 import w4a16 as w
+    buf = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    # bad sizes, bad group, null pointers: INVALID_ARG without a device
+    assert lib.w4a16_gemm(p, p, p, p, 4, 12, 64, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm(p, p, p, p, 4, 64, 64, 48, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm(None, p, p, p, 4, 64, 64, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm(p, p, p, p, -1, 64, 64, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm(p, p, p, p, 0, 64, 64, 64, None) == w.OK   # M = 0 is a no-op
+    assert lib.w4a16_pack(p, p, p, p, 64, 60, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm_ws(p, p, p, p, 4, 64, 64, 64, None, 0, None) == w.ERR_INVALID_ARG
+    odd = ctypes.c_void_p(ctypes.addressof(buf) + 8)
+    assert lib.w4a16_gemm(odd, p, p, p, 4, 64, 64, 64, None) in (w.ERR_INVALID_ARG,)
+    for s in range(6):
+        assert lib.w4a16_status_string(s)
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "weight_only_int4_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f

@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Small and ragged shapes are compared element by element; the full-size
+workloads (in the launch configuration the benchmark times) on sampled
+elements, which the oracle evaluates one by one. The acceptance bound is
+|y - y_ref| <= 1e-3 * sum_k |x w| + 2^-10 |y_ref| per element.
+"""
+import numpy as np
+import pytest
+
+from tests.parity import check_within
+from tests.test_oracle import hand_inputs, read_golden
+from weight_only_int4_02_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_only_int4_02_gb300 import w4a16
+    w4a16.lib()
+    return w4a16
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_gpu(w, x, q, s, G, N=None):
+    K, N = q.shape
+    packed, sp = w.pack(to_dev(q), to_dev(s), G)
+    y = w.gemm(to_dev(x), packed, sp, N, G)
+    torch.cuda.synchronize()
+    return y.cpu().numpy(), packed, sp
+
+
+def test_pack_round_trip(w, oracle_mod):
+    for (K, N, G) in [(64, 128, 64), (200, 136, 200), (8, 8, 8), (4040, 256, 128), (4096, 384, 32), (520, 264, 32)]:
+        q = inputs.codes(K, N, seed=K + N)
+        s = inputs.scales(K, N, G, seed=3)
+        packed, sp = w.pack(to_dev(q), to_dev(s), G)
+        torch.cuda.synchronize()
+        p = packed.cpu().numpy().view(np.uint32)
+        q2, bad = oracle_mod.unpack(p, K, N)
+        assert bad == 0 and np.array_equal(q2, q), (K, N, G)
+        assert np.array_equal(p, oracle_mod.pack(q))
+        s2, bad = oracle_mod.unpack_scales(sp.cpu().numpy().view(np.uint16), -(-K // G), N)
+        assert bad == 0 and np.array_equal(s2, s.view(np.uint16))
+    for pattern in (0, 15):
+        q = np.full((256, 256), pattern, np.uint8)
+        packed, _ = w.pack(to_dev(q), to_dev(np.ones((2, 256), np.float16)), 128)
+        q2, bad = oracle_mod.unpack(packed.cpu().numpy().view(np.uint32), 256, 256)
+        assert bad == 0 and np.array_equal(q2, q)
+
+
+def test_pack_masks_codes_to_low_nibble(w, oracle_mod):
+    q = inputs.codes(64, 128, seed=9)
+    packed, _ = w.pack(to_dev(q | 0xF0), to_dev(np.ones((1, 128), np.float16)), 64)
+    q2, bad = oracle_mod.unpack(packed.cpu().numpy().view(np.uint32), 64, 128)
+    assert bad == 0 and np.array_equal(q2, q)
+
+
+def test_hand_example_is_bit_exact(w):
+    g = read_golden()
+    x, q, s = hand_inputs(8)           # G = K = 8, one scale per column
+    y, _, _ = run_gpu(w, x, q, s, 8)
+    assert np.array_equal(y[0].astype(np.float64), g["G8_y"]), y
+
+
+SMALL = [
+    # (M, N, K, G, scale kind) spanning several tiles, ragged M/N/K tails
+    (16, 4096, 4096, 128, "halfnormal"),      # single GEMM, M=16, K=N=4096
+    (1, 8, 8, 8, "halfnormal"),
+    (3, 136, 200, 200, "halfnormal"),
+    (17, 264, 520, 32, "loguniform"),
+    (1, 4096, 4096, 32, "loguniform"),
+    (127, 384, 1024, 64, "halfnormal"),
+    (33, 512, 2048, 128, "halfnormal"),
+    (64, 640, 1024, 128, "halfnormal"),
+    (100, 256, 640, 128, "halfnormal"),
+    (130, 256, 640, 128, "halfnormal"),
+    (300, 264, 136, 32, "halfnormal"),
+    (517, 392, 776, 128, "halfnormal"),
+    (5, 4096, 4040, 128, "halfnormal"),
+    (17, 4096, 4000, 4000, "loguniform"),
+    (3, 256, 16384, 128, "loguniform"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,G,kind", SMALL)
+def test_parity_small(w, oracle_mod, M, N, K, G, kind):
+    x, q, s = inputs.problem(M, K, N, G, seed=M * 7 + K, scale_kind=kind)
+    y, _, _ = run_gpu(w, x, q, s, G)
+    y_ref, absum = oracle_mod.gemm(x, q, s, G)
+    check_within(y, y_ref, absum, "M=%d N=%d K=%d G=%d" % (M, N, K, G))
+
+
+def test_subnormal_scales(w, oracle_mod):
+    M, N, K, G = 9, 256, 512, 128
+    x, q, _ = inputs.problem(M, K, N, G, seed=4)
+    s = (np.random.default_rng(0).integers(1, 1024, size=(K // G, N)) * 2.0 ** -24).astype(np.float16)
+    y, _, _ = run_gpu(w, x, q, s, G)
+    y_ref, absum = oracle_mod.gemm(x, q, s, G)
+    check_within(y, y_ref, absum, "subnormal scales")
+
+
+def test_invariants(w):
+    M, N, K, G = 20, 256, 512, 64
+    x, q, s = inputs.problem(M, K, N, G, seed=5)
+    y0, _, _ = run_gpu(w, x, q, np.zeros_like(s), G)
+    assert np.all(y0 == 0)
+    y8, _, _ = run_gpu(w, x, np.full_like(q, 8), s, G)
+    assert np.all(y8 == 0)
+    q1 = np.full_like(q, 8)
+    q1[77, 130] = 13
+    y1, _, _ = run_gpu(w, x, q1, s, G)
+    expect = (x[:, 77].astype(np.float64) * 5 * float(s[77 // G, 130])).astype(np.float16)
+    others = np.delete(y1, 130, axis=1)
+    assert np.all(others == 0)
+    assert np.allclose(y1[:, 130].astype(np.float64), expect.astype(np.float64), rtol=2e-3, atol=0)
+    # doubling the scales doubles the output exactly (products and sums scale by 2)
+    y, _, _ = run_gpu(w, x, q, s, G)
+    y2, _, _ = run_gpu(w, x, q, (s.astype(np.float32) * 2).astype(np.float16), G)
+    assert np.array_equal(y2.astype(np.float32), 2 * y.astype(np.float32))
+
+
+def test_deterministic(w):
+    M, N, K, G = 16, 4096, 4096, 128
+    x, q, s = inputs.problem(M, K, N, G, seed=0)
+    packed, sp = w.pack(to_dev(q), to_dev(s), G)
+    xd = to_dev(x)
+    ys = [w.gemm(xd, packed, sp, N, G).cpu().numpy() for _ in range(3)]
+    assert np.array_equal(ys[0].view(np.uint16), ys[1].view(np.uint16))
+    assert np.array_equal(ys[0].view(np.uint16), ys[2].view(np.uint16))
+    assert w.check_device_status() == w.OK
+
+
+def test_workspace_variant_and_graph_capture(w):
+    M, N, K, G = 37, 1024, 2048, 128
+    x, q, s = inputs.problem(M, K, N, G, seed=2)
+    packed, sp = w.pack(to_dev(q), to_dev(s), G)
+    xd = to_dev(x)
+    y_ref = w.gemm(xd, packed, sp, N, G)
+    nbytes = w.workspace_bytes(M, N, K, G)
+    ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device="cuda")
+    y = w.gemm_ws(xd, packed, sp, N, G, ws)
+    assert torch.equal(y, y_ref)
+    with pytest.raises(w.W4A16Error) as e:
+        w.gemm_ws(xd, packed, sp, N, G, ws[: nbytes - 1024])
+    assert e.value.status == w.ERR_WORKSPACE
+    # capture into a CUDA graph and replay
+    y_g = torch.empty_like(y_ref)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        w.gemm_ws(xd, packed, sp, N, G, ws, y=y_g)
+    for _ in range(3):
+        y_g.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y_g, y_ref)
+    assert w.check_device_status(ws) == w.OK
+
+
+def test_invalid_arguments_on_device(w):
+    x = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
+    packed, sp = w.pack(torch.zeros((64, 128), dtype=torch.uint8, device="cuda"),
+                        torch.ones((1, 128), dtype=torch.float16, device="cuda"), 64)
+    with pytest.raises(w.W4A16Error) as e:
+        w.gemm(x, packed, sp, 128, 48)
+    assert e.value.status == w.ERR_INVALID_ARG
+    xo = torch.zeros(4 * 64 + 1, dtype=torch.float16, device="cuda")[1:].view(4, 64)
+    with pytest.raises(w.W4A16Error) as e:
+        w.gemm(xo, packed, sp, 128, 64)
+    assert e.value.status == w.ERR_INVALID_ARG
+    y = w.gemm(torch.zeros((0, 64), dtype=torch.float16, device="cuda"), packed, sp, 128, 64)
+    assert y.shape == (0, 128)
+
+
+def sampled_parity(w, oracle_mod, cases, G, scale_mult, outlier_frac=0.0, n_rows=8, n_cols=512, seed=0):
+    """Full-size problems, compared at a seeded sample of rows x columns."""
+    by_shape = {}
+    for (M, K, N) in cases:
+        by_shape.setdefault((K, N), []).append(M)
+    rs = np.random.default_rng(seed)
+    worst = 0.0
+    for (K, N), Ms in by_shape.items():
+        q = inputs.codes(K, N, seed)
+        s = inputs.scales(K, N, G, seed, "halfnormal", scale_mult)
+        packed, sp = w.pack(to_dev(q), to_dev(s), G)
+        for M in Ms:
+            x = inputs.activations(M, K, seed, outlier_frac)
+            y = w.gemm(to_dev(x), packed, sp, N, G)
+            rows = np.unique(np.concatenate([[0, M - 1], rs.integers(0, M, size=n_rows)]))
+            cols = np.unique(np.concatenate([[0, N - 1], rs.integers(0, N, size=n_cols)]))
+            y_s = y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+            y_ref, absum = oracle_mod.gemm_sample(x, q, s, G, rows, cols)
+            worst = max(worst, check_within(y_s, y_ref, absum, "M=%d K=%d N=%d" % (M, K, N)))
+        del packed, sp
+    return worst
+
+
+def test_full_size_decode_sweep(w, oracle_mod):
+    wl = inputs.WORKLOADS["llama2_7b_decode_sweep"]
+    sampled_parity(w, oracle_mod, wl["cases"], wl["group_size"], wl["scale_mult"])
+
+
+def test_full_size_large_layer(w, oracle_mod):
+    wl = inputs.WORKLOADS["large_layer_18432x73728"]
+    sampled_parity(w, oracle_mod, wl["cases"], wl["group_size"], wl["scale_mult"], n_cols=256)
+
+
+def test_full_size_prefill(w, oracle_mod):
+    wl = inputs.WORKLOADS["llama2_13b_prefill"]
+    sampled_parity(w, oracle_mod, wl["cases"], wl["group_size"], wl["scale_mult"], wl["outlier_frac"],
+                   n_rows=6, n_cols=128)
+
+
+def test_edge_sweep(w, oracle_mod):
+    for M in inputs.EDGE_M:
+        for (N, K, G) in [(4096, 4096, 4096), (4096, 4096, 32), (256, 16384, 128), (4096, 4000, 128),
+                          (4096, 4040, 128)]:
+            x, q, s = inputs.problem(M, K, N, G, seed=M + K, scale_kind="loguniform")
+            y, _, _ = run_gpu(w, x, q, s, G)
+            cols = np.arange(0, N, 7)
+            y_ref, absum = oracle_mod.gemm_sample(x, q, s, G, np.arange(M), cols)
+            check_within(y[:, cols], y_ref, absum, "edge M=%d N=%d K=%d G=%d" % (M, N, K, G))

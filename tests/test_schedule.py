@@ -1,0 +1,161 @@
+"""Host-side check of the tcgen05 kernel's work split and buffer indexing.
+
+A Python mirror of the kernel's stream-K arithmetic (cta_begin, cta_of, slot_of,
+segment walk) and of its global-memory address ranges, run over the shapes the
+tests and the benchmark launch: every (tile, chunk) is processed exactly once,
+every bulk copy and partial-slot access stays inside its buffer, and the
+split-K reducer reads exactly the slots the contributors wrote.
+"""
+import re
+import os
+
+import pytest
+
+from weight_only_int4_02_gb300 import inputs
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                    "weight_only_int4_02_gb300", "csrc")
+MAX_GRID = 1024
+SMS = 152
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+def tile_m_for(M):
+    for t in (16, 32, 64, 128):
+        if M <= t:
+            return t
+    return 256
+
+
+def plan(M, N, K, G, sms=SMS):
+    tm = tile_m_for(M)
+    m_tiles, n_tiles, KC, ng = ceil_div(M, tm), ceil_div(N, 128), ceil_div(K, 64), ceil_div(K, G)
+    total = n_tiles * m_tiles * KC
+    grid = min(sms, MAX_GRID, total)
+    return dict(tm=tm, m_tiles=m_tiles, n_tiles=n_tiles, KC=KC, ng=ng, total=total, grid=grid)
+
+
+def cta_begin(P, c):
+    return c * P["total"] // P["grid"]
+
+
+def cta_of(P, i):
+    c = (i * P["grid"]) // P["total"]
+    while c + 1 < P["grid"] and cta_begin(P, c + 1) <= i:
+        c += 1
+    while c > 0 and cta_begin(P, c) > i:
+        c -= 1
+    return c
+
+
+def slot_of(P, c, t):
+    return 2 * c if cta_begin(P, c) >= t * P["KC"] else 2 * c + 1
+
+
+def segments(P, c):
+    i, end = cta_begin(P, c), cta_begin(P, c + 1)
+    while i < end:
+        t = i // P["KC"]
+        kb = i - t * P["KC"]
+        ke = min(P["KC"], kb + (end - i))
+        yield t, kb, ke
+        i += ke - kb
+
+
+def check_shape(M, N, K, G, sms=SMS):
+    P = plan(M, N, K, G, sms)
+    KC, ng, tm = P["KC"], P["ng"], P["tm"]
+    packed_words = P["n_tiles"] * KC * 1024
+    scales_elems = P["n_tiles"] * ng * 128
+    partial_floats = 2 * P["grid"] * tm * 128
+    covered = {}
+    writers = {}
+    for c in range(P["grid"]):
+        for (t, kb, ke) in segments(P, c):
+            assert 0 <= t < P["n_tiles"] * P["m_tiles"] and 0 <= kb < ke <= KC
+            nt, mt = divmod(t, P["m_tiles"])
+            for kc in range(kb, ke):
+                key = (t, kc)
+                assert key not in covered
+                covered[key] = c
+                w0 = (nt * KC + kc) * 1024
+                assert 0 <= w0 and w0 + 1024 <= packed_words
+                g0 = min(kc * 64 // G, ng - 1)
+                g1 = min((kc * 64 + 63) // G, ng - 1)
+                assert 1 <= g1 - g0 + 1 <= 2          # fits the 512-byte scale slot
+                for half in (0, 1):
+                    g = min((kc * 64 + half * 32) // G, ng - 1)
+                    assert g0 <= g <= g1
+                e0 = (nt * ng + g0) * 128
+                assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
+                # TMA X coordinates: inner coordinate 16-byte aligned
+                assert (kc * 64 * 2) % 16 == 0 and mt * tm < M
+            split = kb != 0 or ke != KC
+            if split:
+                slot = slot_of(P, c, t)
+                assert 0 <= slot < 2 * P["grid"]
+                assert (slot + 1) * tm * 128 <= partial_floats
+                writers.setdefault(t, []).append((c, slot))
+    assert len(covered) == P["total"]
+    counter_ids = set()
+    for t, ws in writers.items():
+        c_lo, c_hi = cta_of(P, t * KC), cta_of(P, t * KC + KC - 1)
+        assert c_lo < P["grid"] and c_lo not in counter_ids
+        counter_ids.add(c_lo)
+        read = [(cc, slot_of(P, cc, t)) for cc in range(c_lo, c_hi + 1)]
+        assert sorted(read) == sorted(ws), (t, read, ws)
+        assert len(set(s for _, s in ws)) == len(ws)
+    # a slot is written by one tile only
+    all_slots = [s for ws in writers.values() for _, s in ws]
+    assert len(all_slots) == len(set(all_slots))
+    return P
+
+
+SHAPES = sorted(set(
+    [(m, n, k, 128) for (m, k, n) in inputs.WORKLOADS["llama2_7b_decode_sweep"]["cases"]]
+    + [(m, n, k, 128) for (m, k, n) in inputs.WORKLOADS["llama2_13b_prefill"]["cases"]]
+    + [(m, n, k, 128) for (m, k, n) in inputs.WORKLOADS["large_layer_18432x73728"]["cases"]]
+    + [(16, 4096, 4096, 128)]
+    + [(m, 4096, 4096, g) for m in inputs.EDGE_M for g in (32, 4096)]
+    + [(m, 256, 16384, 128) for m in inputs.EDGE_M]
+    + [(m, 4096, k, 128) for m in inputs.EDGE_M for k in (4000, 4040)]
+    + [(1, 8, 8, 8), (1, 128, 64, 64), (3, 136, 200, 200), (300, 264, 136, 32), (1, 8, 4040, 4040)]))
+
+
+@pytest.mark.parametrize("M,N,K,G", SHAPES)
+def test_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
+    check_shape(M, N, K, G)
+
+
+@pytest.mark.parametrize("sms", [1, 7, 148, 160])
+def test_schedule_other_sm_counts(sms):
+    for shp in [(16, 4096, 4096, 128), (1, 256, 16384, 128), (4096, 5120, 13824, 128), (3, 136, 200, 200)]:
+        check_shape(*shp, sms=sms)
+
+
+def _constexpr(src, name):
+    m = re.search(r"constexpr int %s = ([^;]+);" % name, src)
+    return m.group(1)
+
+
+def test_shared_memory_layout_fits():
+    """Mirror of TcCfg: stage rings, barriers and alignment inside the dynamic allocation."""
+    src = open(os.path.join(CSRC, "gemm_tc.cuh")).read()
+    assert _constexpr(src, "kChunkBytes") == "4096" and _constexpr(src, "kScaleSlotBytes") == "512"
+    for tm in (16, 32, 64, 128, 256):
+        xb = tm * 128
+        stage = xb + 4096 + 512
+        S = min(16, (200 * 1024) // stage)
+        off_pk = S * xb
+        off_sc = off_pk + S * 4096
+        off_bar = off_sc + S * 512
+        nbars = 2 * S + 8 + 4 + 1
+        off_misc = off_bar + nbars * 8
+        smem = off_misc + 64 + 1024
+        assert smem <= 227 * 1024
+        assert xb % 1024 == 0 and off_pk % 16 == 0 and off_sc % 16 == 0 and off_bar % 8 == 0
+        cols = 4 * 32 + (2 if tm <= 128 else 1) * tm
+        assert cols <= (256 if cols <= 256 else 512) <= 512

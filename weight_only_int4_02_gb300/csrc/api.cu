@@ -1,0 +1,321 @@
+// C ABI of libw4a16.so: argument checks, the per-shape plan (dispatch), the
+// per-device workspace, the TMA descriptor of X, and the launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "gemm_tc.cuh"
+#include "w4a16.h"
+
+namespace w4a16 {
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,
+                        int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream);
+}
+
+namespace {
+
+using namespace w4a16;
+
+thread_local int t_last_cuda_error = 0;
+
+w4a16_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return W4A16_OK;
+    t_last_cuda_error = (int)e;
+    return W4A16_ERR_CUDA;
+}
+
+// Workspace layout (fixed, whatever the shape): error word at 0, split-K
+// counters at 256 (one int per CTA, at most kMaxGrid), FP32 partials after.
+constexpr size_t kCountersOff = 256;
+constexpr int kMaxGrid = 1024;
+constexpr size_t kPartialsOff = kCountersOff + 4 * kMaxGrid;
+constexpr int kMaxTileM = 256;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+long long g_wait_limit_ns = 1000000000LL;
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+int norm_group(int K, int G) { return G == -1 ? K : G; }
+
+bool valid_sizes(int K, int N, int G)
+{
+    if (K <= 0 || N <= 0 || (K % 8) != 0 || (N % 8) != 0) return false;
+    return G == 32 || G == 64 || G == 128 || G == K;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct Plan {
+    int path;     // 2 = per-weight scaling tcgen05 kernel
+    int tm;       // rows of X per tile (MMA N)
+    int m_tiles, n_tiles, KC, ng;
+    long long total;
+    int grid;
+    size_t ws_bytes;
+};
+
+size_t ws_bytes_for(int grid, int tm) { return kPartialsOff + (size_t)2 * grid * tm * kTileN * sizeof(float); }
+
+Plan make_plan(int M, int N, int K, int G, int sms)
+{
+    Plan P;
+    P.path = 2;
+    P.tm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    P.m_tiles = ceil_div(M, P.tm);
+    P.n_tiles = ceil_div(N, kTileN);
+    P.KC = ceil_div(K, kChunkK);
+    P.ng = ceil_div(K, G);
+    P.total = (long long)P.n_tiles * P.m_tiles * P.KC;
+    long long grid = sms < kMaxGrid ? sms : kMaxGrid;
+    if (grid > P.total) grid = P.total;
+    P.grid = (int)grid;
+    P.ws_bytes = ws_bytes_for(P.grid, P.tm);
+    return P;
+}
+
+w4a16_status device_state(DeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return from_cuda(e);
+        if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
+        if ((e = setup_tc<16>()) != cudaSuccess || (e = setup_tc<32>()) != cudaSuccess ||
+            (e = setup_tc<64>()) != cudaSuccess || (e = setup_tc<128>()) != cudaSuccess ||
+            (e = setup_tc<256>()) != cudaSuccess)
+            return from_cuda(e);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess) return from_cuda(e);
+            if (q != cudaDriverEntryPointSuccess || !fn) return W4A16_ERR_UNSUPPORTED;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            if (const char* s = std::getenv("W4A16_WAIT_LIMIT_NS")) g_wait_limit_ns = std::atoll(s);
+        }
+        st.sms = sms;
+        st.ready = true;
+    }
+    *out = &st;
+    return W4A16_OK;
+}
+
+// The library's own workspace on the current device, sized for the largest plan.
+w4a16_status own_workspace(DeviceState* st, void** ws, size_t* bytes)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!st->ws) {
+        const int grid = st->sms < kMaxGrid ? st->sms : kMaxGrid;
+        const size_t need = ws_bytes_for(grid, kMaxTileM);
+        void* p = nullptr;
+        cudaError_t e = cudaMalloc(&p, need);
+        if (e != cudaSuccess) return from_cuda(e);
+        if ((e = cudaMemset(p, 0, need)) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess) {
+            cudaFree(p);
+            return from_cuda(e);
+        }
+        st->ws = p;
+        st->ws_bytes = need;
+    }
+    *ws = st->ws;
+    *bytes = st->ws_bytes;
+    return W4A16_OK;
+}
+
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int tm)
+{
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)tm};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
+                       int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream)
+{
+    G = norm_group(K, G);
+    if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    if (M == 0) return W4A16_OK;
+    if (!x || !packed || !scales_packed || !y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales_packed) || !aligned16(y))
+        return W4A16_ERR_INVALID_ARG;
+    if (!own_ws && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0)) return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    const Plan P = make_plan(M, N, K, G, st->sms);
+    if (own_ws) {
+        rc = own_workspace(st, &ws, &ws_bytes);
+        if (rc != W4A16_OK) return rc;
+    }
+    if (ws_bytes < P.ws_bytes) return W4A16_ERR_WORKSPACE;
+
+    GemmParams p;
+    p.packed = packed;
+    p.scales = reinterpret_cast<const __half*>(scales_packed);
+    p.y = reinterpret_cast<__half*>(y);
+    p.status = reinterpret_cast<int*>(ws);
+    p.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + kCountersOff);
+    p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kPartialsOff);
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.G = G;
+    p.ng = P.ng;
+    p.n_tiles = P.n_tiles;
+    p.m_tiles = P.m_tiles;
+    p.KC = P.KC;
+    p.total_iters = P.total;
+    p.grid = P.grid;
+    p.wait_limit_ns = g_wait_limit_ns;
+
+    CUtensorMap map;
+    if (!encode_x_map(&map, x, M, K, P.tm)) return W4A16_ERR_INVALID_ARG;
+    cudaError_t e;
+    switch (P.tm) {
+        case 16: e = launch_tc<16>(map, p, stream); break;
+        case 32: e = launch_tc<32>(map, p, stream); break;
+        case 64: e = launch_tc<64>(map, p, stream); break;
+        case 128: e = launch_tc<128>(map, p, stream); break;
+        default: e = launch_tc<256>(map, p, stream); break;
+    }
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_layout_version(void) { return 1; }
+
+const char* w4a16_status_string(int status)
+{
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4A16_ERR_INVALID_ARG: return "invalid argument";
+        case W4A16_ERR_UNSUPPORTED: return "unsupported device";
+        case W4A16_ERR_CUDA: return "CUDA error";
+        case W4A16_ERR_TIMEOUT: return "a kernel wait timed out";
+        case W4A16_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
+
+size_t w4a16_packed_words(int K, int N, int group_size)
+{
+    if (!valid_sizes(K, N, norm_group(K, group_size))) return 0;
+    return (size_t)ceil_div(N, kTileN) * ceil_div(K, kChunkK) * kChunkWords;
+}
+
+size_t w4a16_scales_elems(int K, int N, int group_size)
+{
+    const int G = norm_group(K, group_size);
+    if (!valid_sizes(K, N, G)) return 0;
+    return (size_t)ceil_div(N, kTileN) * ceil_div(K, G) * kTileN;
+}
+
+w4a16_status w4a16_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,
+                        int K, int N, int group_size, w4a16_stream_t stream)
+{
+    const int G = norm_group(K, group_size);
+    if (!valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    if (!codes || !scales || !packed || !scales_packed) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(scales_packed)) return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    return from_cuda(launch_pack(codes, scales, packed, scales_packed, K, N, ceil_div(K, kChunkK),
+                                 ceil_div(N, kTileN), ceil_div(K, G), st->sms,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_gemm(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
+                        int N, int K, int group_size, w4a16_stream_t stream)
+{
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, nullptr, 0, true,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K, int group_size)
+{
+    const int G = norm_group(K, group_size);
+    if (M < 0 || !valid_sizes(K, N, G)) return 0;
+    DeviceState* st = nullptr;
+    int sms = kMaxGrid;
+    if (device_state(&st) == W4A16_OK) sms = st->sms;
+    if (M == 0) return kPartialsOff;
+    return make_plan(M, N, K, G, sms).ws_bytes;
+}
+
+w4a16_status w4a16_gemm_ws(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y,
+                           int M, int N, int K, int group_size, void* workspace, size_t ws_bytes,
+                           w4a16_stream_t stream)
+{
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, false,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    if (!workspace) {
+        DeviceState* st = nullptr;
+        w4a16_status rc = device_state(&st);
+        if (rc != W4A16_OK) return rc;
+        workspace = st->ws;
+        if (!workspace) return W4A16_OK;
+    }
+    int word = 0;
+    if ((e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return from_cuda(e);
+    if (word == 0) return W4A16_OK;
+    if ((e = cudaMemset(workspace, 0, kPartialsOff)) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess)
+        return from_cuda(e);
+    return W4A16_ERR_TIMEOUT;
+}
+
+w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid)
+{
+    const int G = norm_group(K, group_size);
+    if (M <= 0 || !valid_sizes(K, N, G) || !path || !tile_m || !grid) return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    const Plan P = make_plan(M, N, K, G, st->sms);
+    *path = P.path;
+    *tile_m = P.tm;
+    *grid = P.grid;
+    return W4A16_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Offline repack of INT4 codes and FP16 group scales into the tile order the
+// tcgen05 kernels stream ("quant_marlin_kernel" (aicassindra.com), "The
+// architecture: every piece explained": eight 4-bit values per 32-bit word in a
+// permuted order chosen once, offline, so the inner loop needs no shuffles).
+//
+// Word (((nt*KC + kc)*2 + j)*128 + n_in)*4 + w holds k0 = kc*64 + j*32 + w*8 .. k0+7
+// of column n = nt*128 + n_in; nibble i holds k0 + 2*(i%4) + i/4, so that the
+// magic-number unpack of nibbles (i, i+4) yields the FP16 pair (k, k+1) that
+// one 32-bit TMEM column of the MMA's A operand holds. A 64-value chunk of one
+// 128-column tile is 4 KB of contiguous words (one bulk copy per pipeline stage);
+// within it, the 16 bytes a dequant thread reads for its column are adjacent
+// to its neighbours' (conflict-free 128-bit shared loads).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+__global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, uint32_t* __restrict__ packed, int K, int N,
+                                  int KC, long long total_words)
+{
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total_words;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int w = (int)(idx & 3);
+        const int n_in = (int)((idx >> 2) & 127);
+        const int j = (int)((idx >> 9) & 1);
+        const long long rest = idx >> 10;
+        const int kc = (int)(rest % KC);
+        const int nt = (int)(rest / KC);
+        const int n = nt * 128 + n_in;
+        const int k0 = kc * 64 + j * 32 + w * 8;
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = k0 + 2 * (i & 3) + (i >> 2);
+            const uint32_t c = (k < K && n < N) ? (uint32_t)(codes[(size_t)k * N + n] & 0xF) : 8u;
+            word |= c << (4 * i);
+        }
+        packed[idx] = word;
+    }
+}
+
+__global__ void pack_scales_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, int N, int ng,
+                                   long long total)
+{
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int n_in = (int)(idx & 127);
+        const long long rest = idx >> 7;
+        const int g = (int)(rest % ng);
+        const int nt = (int)(rest / ng);
+        const int n = nt * 128 + n_in;
+        out[idx] = n < N ? scales[(size_t)g * N + n] : (uint16_t)0;
+    }
+}
+
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,
+                        int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream)
+{
+    const long long words = (long long)n_tiles * KC * 1024;
+    const long long selems = (long long)n_tiles * ng * 128;
+    const int threads = 256;
+    long long blocks = (words + threads - 1) / threads;
+    const long long cap = (long long)sms * 16;
+    if (blocks > cap) blocks = cap;
+    pack_codes_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, packed, K, N, KC, words);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    blocks = (selems + threads - 1) / threads;
+    if (blocks > cap) blocks = cap;
+    pack_scales_kernel<<<(unsigned)blocks, threads, 0, stream>>>(scales, scales_packed, N, ng, selems);
+    return cudaGetLastError();
+}
+
+}  // namespace w4a16

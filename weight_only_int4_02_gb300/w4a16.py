@@ -1,0 +1,146 @@
+"""Python binding of libw4a16.so (ctypes; argument marshalling only).
+
+Every step of the matmul runs in the library's CUDA kernels. Tensors are torch
+CUDA tensors used as plain device buffers; FP16 data crosses the ABI as binary16
+bit patterns. There is no fallback: if the library is not built, or the device
+is not an sm_103 GPU, the calls raise.
+"""
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libw4a16.so")
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
+
+EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error", "w4a16_packed_words",
+           "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
+           "w4a16_check_device_status", "w4a16_plan"]
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        msg = "%s: %s" % (what, lib().w4a16_status_string(status).decode())
+        if status == ERR_CUDA:
+            msg += " (cudaError %d)" % lib().w4a16_last_cuda_error()
+        super().__init__(msg)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libw4a16.so is not built (%s); run __graft_entry__.build()" % _LIB_PATH)
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.w4a16_layout_version.restype = I
+        L.w4a16_status_string.argtypes = [I]
+        L.w4a16_status_string.restype = ctypes.c_char_p
+        L.w4a16_last_cuda_error.restype = I
+        L.w4a16_packed_words.argtypes = [I, I, I]
+        L.w4a16_packed_words.restype = Z
+        L.w4a16_scales_elems.argtypes = [I, I, I]
+        L.w4a16_scales_elems.restype = Z
+        L.w4a16_pack.argtypes = [P, P, P, P, I, I, I, P]
+        L.w4a16_pack.restype = I
+        L.w4a16_gemm.argtypes = [P, P, P, P, I, I, I, I, P]
+        L.w4a16_gemm.restype = I
+        L.w4a16_workspace_bytes.argtypes = [I, I, I, I]
+        L.w4a16_workspace_bytes.restype = Z
+        L.w4a16_gemm_ws.argtypes = [P, P, P, P, I, I, I, I, P, Z, P]
+        L.w4a16_gemm_ws.restype = I
+        L.w4a16_check_device_status.argtypes = [P, P]
+        L.w4a16_check_device_status.restype = I
+        L.w4a16_plan.argtypes = [I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
+        L.w4a16_plan.restype = I
+        _lib = L
+    return _lib
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != OK:
+        raise W4A16Error(status, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def layout_version():
+    return lib().w4a16_layout_version()
+
+
+def packed_words(K, N, group_size):
+    return lib().w4a16_packed_words(K, N, group_size)
+
+
+def scales_elems(K, N, group_size):
+    return lib().w4a16_scales_elems(K, N, group_size)
+
+
+def workspace_bytes(M, N, K, group_size):
+    return lib().w4a16_workspace_bytes(M, N, K, group_size)
+
+
+def pack(codes, scales, group_size, stream=None, out=None):
+    """Repack codes (uint8 [K][N]) and scales (float16 [ceil(K/G)][N]) on the GPU.
+
+    Returns (packed int32 words, packed float16 scales)."""
+    K, N = codes.shape
+    assert codes.dtype == torch.uint8 and scales.dtype == torch.float16
+    assert codes.is_cuda and scales.is_cuda and codes.is_contiguous() and scales.is_contiguous()
+    nw, ns = packed_words(K, N, group_size), scales_elems(K, N, group_size)
+    if nw == 0 or ns == 0:
+        raise W4A16Error(ERR_INVALID_ARG, "pack")
+    if out is None:
+        packed = torch.empty(nw, dtype=torch.int32, device=codes.device)
+        sp = torch.empty(ns, dtype=torch.float16, device=codes.device)
+    else:
+        packed, sp = out
+    _check(lib().w4a16_pack(_ptr(codes), _ptr(scales), _ptr(packed), _ptr(sp), K, N, group_size, _stream(stream)),
+           "w4a16_pack")
+    return packed, sp
+
+
+def gemm(x, packed, scales_packed, N, group_size, y=None, stream=None):
+    """y = x @ dequant(W) for x float16 [M][K]; returns y float16 [M][N]."""
+    M, K = x.shape
+    assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib().w4a16_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
+                            _stream(stream)), "w4a16_gemm")
+    return y
+
+
+def gemm_ws(x, packed, scales_packed, N, group_size, workspace, y=None, stream=None):
+    """As gemm, with a caller-owned workspace (uint8 CUDA tensor, zeroed once before first use)."""
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib().w4a16_gemm_ws(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "w4a16_gemm_ws")
+    return y
+
+
+def check_device_status(workspace=None, stream=None):
+    """Synchronise and return the status of the kernels' bounded waits (OK or ERR_TIMEOUT)."""
+    return lib().w4a16_check_device_status(_ptr(workspace), _stream(stream))
+
+
+def plan(M, N, K, group_size):
+    """(path, tile_m, grid) chosen for this shape on the current device."""
+    p, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().w4a16_plan(M, N, K, group_size, ctypes.byref(p), ctypes.byref(t), ctypes.byref(g)), "w4a16_plan")
+    return p.value, t.value, g.value
