@@ -65,7 +65,8 @@ const char* w4a16_status_string(int status);
 /* The cudaError_t of the last W4A16_ERR_CUDA returned on this host thread (0 if none). */
 int w4a16_last_cuda_error(void);
 
-/* Number of uint32 words of the packed weights: ceil(N/128) * ceil(K/64) * 1024.
+/* Number of uint32 words of the packed weights: ceil(N/128) * KC * 1024, with
+ * KC = ceil(K/64) rounded up to a multiple of 4 (K padded to a multiple of 256).
  * Returns 0 for invalid sizes. */
 size_t w4a16_packed_words(int K, int N, int group_size);
 
@@ -80,11 +81,11 @@ size_t w4a16_scales_elems(int K, int N, int group_size);
  *   scales         device, binary16 [ceil(K/G)][N]
  *   packed         device out, uint32 [w4a16_packed_words(K, N, G)]
  *   scales_packed  device out, binary16 [w4a16_scales_elems(K, N, G)]
- * Packed layout (version 1): column tiles of 128 output features, reduction
+ * Packed layout (version 2): column tiles of 128 output features, reduction
  * chunks of 64. For tile nt, chunk kc, half j (32 values of k), feature n_in
  * and word w: word index (((nt*KC + kc)*2 + j)*128 + n_in)*4 + w with
- * KC = ceil(K/64); the word holds k0 = kc*64 + j*32 + w*8 .. k0+7 of column
- * n = nt*128 + n_in, nibble i (bits 4i..4i+3) holding k = k0 + 2*(i%4) + i/4.
+ * KC = ceil(K/64) rounded up to a multiple of 4; the word holds
+ * k0 = kc*64 + j*32 + w*8 .. k0+7 of column n = nt*128 + n_in, nibble i (bits 4i..4i+3) holding k = k0 + 2*(i%4) + i/4.
  * Positions outside K x N hold code 8 (weight 0). Scales: element
  * (nt*ceil(K/G) + g)*128 + n_in holds s[g][nt*128 + n_in] (0 outside N).
  */

@@ -170,7 +170,8 @@ int w4o_gemm(const uint16_t* x, const uint8_t* q, const uint16_t* s,
  * output features, reduction chunks of 64. For tile nt, chunk kc, half j
  * (32 rows of k), feature n_in within the tile and word w within the half:
  *
- *   word index = (((nt * KC + kc) * 2 + j) * 128 + n_in) * 4 + w,  KC = ceil(K/64)
+ *   word index = (((nt * KC + kc) * 2 + j) * 128 + n_in) * 4 + w,
+ *   KC = ceil(K/64) rounded up to a multiple of 4 (K padded to a multiple of 256)
  *   word holds k0 = kc*64 + j*32 + w*8 .. k0+7 of column n = nt*128 + n_in;
  *   nibble i (bits 4i..4i+3) holds k = k0 + 2*(i mod 4) + i/4.
  *
@@ -179,12 +180,14 @@ int w4o_gemm(const uint16_t* x, const uint8_t* q, const uint16_t* s,
  */
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-size_t w4o_packed_words(int K, int N) { return (size_t)ceil_div(N, 128) * ceil_div(K, 64) * 1024; }
+static int chunks_per_column(int K) { return ceil_div(ceil_div(K, 64), 4) * 4; }
+
+size_t w4o_packed_words(int K, int N) { return (size_t)ceil_div(N, 128) * chunks_per_column(K) * 1024; }
 
 /* Where (k, n) lives: word index and nibble. */
 void w4o_locate(int K, int k, int n, size_t* word, int* nibble)
 {
-    int KC = ceil_div(K, 64);
+    int KC = chunks_per_column(K);
     int nt = n / 128, n_in = n % 128;
     int kc = k / 64, r = k % 64;
     int j = r / 32, r2 = r % 32;
@@ -197,7 +200,7 @@ void w4o_locate(int K, int k, int n, size_t* word, int* nibble)
 /* Unpack codes[K][N] from packed words; returns the number of padding nibbles != 8. */
 long long w4o_unpack(const uint32_t* packed, int K, int N, uint8_t* codes)
 {
-    int KC = ceil_div(K, 64), NT = ceil_div(N, 128);
+    int KC = chunks_per_column(K), NT = ceil_div(N, 128);
     long long bad_pad = 0;
     for (int nt = 0; nt < NT; ++nt)
         for (int k = 0; k < KC * 64; ++k)

@@ -34,10 +34,12 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_sizes(lib):
-    assert lib.w4a16_layout_version() == 1
+    assert lib.w4a16_layout_version() == 2
     assert lib.w4a16_packed_words(4096, 4096, 128) == 32 * 64 * 1024
     assert lib.w4a16_packed_words(4040, 4096, 128) == 32 * 64 * 1024
-    assert lib.w4a16_packed_words(8, 8, 8) == 1024
+    assert lib.w4a16_packed_words(8, 8, 8) == 4 * 1024
+    assert lib.w4a16_packed_words(4000, 4096, 128) == 32 * 64 * 1024
+    assert lib.w4a16_packed_words(11008, 4096, 128) == 32 * 172 * 1024
     assert lib.w4a16_scales_elems(4096, 4096, 128) == 32 * 32 * 128
     assert lib.w4a16_scales_elems(4000, 4096, 128) == 32 * 32 * 128
     assert lib.w4a16_scales_elems(4096, 4096, -1) == 32 * 1 * 128

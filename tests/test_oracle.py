@@ -196,7 +196,7 @@ def test_sample_matches_full_and_threads_do_not_matter(oracle_mod):
 
 @pytest.mark.parametrize("K,N", [(64, 128), (200, 130), (8, 8), (4040, 256)])
 def test_layout_is_a_bijection_and_round_trips(oracle_mod, K, N):
-    KC, NT = -(-K // 64), -(-N // 128)
+    KC, NT = -(-(-(-K // 64)) // 4) * 4, -(-N // 128)
     total = oracle_mod.packed_words(K, N)
     assert total == KC * NT * 1024
     if K * N <= 64 * 1024:

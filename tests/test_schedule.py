@@ -32,10 +32,14 @@ def tile_m_for(M):
 
 def plan(M, N, K, G, sms=SMS):
     tm = tile_m_for(M)
-    m_tiles, n_tiles, KC, ng = ceil_div(M, tm), ceil_div(N, 128), ceil_div(K, 64), ceil_div(K, G)
-    total = n_tiles * m_tiles * KC
+    ksub = 4 if tm <= 64 else 2
+    m_tiles, n_tiles, ng = ceil_div(M, tm), ceil_div(N, 128), ceil_div(K, G)
+    KC = ceil_div(ceil_div(K, 64), 4) * 4
+    iters = KC // ksub
+    total = n_tiles * m_tiles * iters
     grid = min(sms, MAX_GRID, total)
-    return dict(tm=tm, m_tiles=m_tiles, n_tiles=n_tiles, KC=KC, ng=ng, total=total, grid=grid)
+    return dict(tm=tm, ksub=ksub, m_tiles=m_tiles, n_tiles=n_tiles, KC=KC, iters=iters, ng=ng, total=total,
+                grid=grid)
 
 
 def cta_begin(P, c):
@@ -52,22 +56,22 @@ def cta_of(P, i):
 
 
 def slot_of(P, c, t):
-    return 2 * c if cta_begin(P, c) >= t * P["KC"] else 2 * c + 1
+    return 2 * c if cta_begin(P, c) >= t * P["iters"] else 2 * c + 1
 
 
 def segments(P, c):
     i, end = cta_begin(P, c), cta_begin(P, c + 1)
     while i < end:
-        t = i // P["KC"]
-        kb = i - t * P["KC"]
-        ke = min(P["KC"], kb + (end - i))
+        t = i // P["iters"]
+        kb = i - t * P["iters"]
+        ke = min(P["iters"], kb + (end - i))
         yield t, kb, ke
         i += ke - kb
 
 
 def check_shape(M, N, K, G, sms=SMS):
     P = plan(M, N, K, G, sms)
-    KC, ng, tm = P["KC"], P["ng"], P["tm"]
+    KC, ng, tm, ks, iters = P["KC"], P["ng"], P["tm"], P["ksub"], P["iters"]
     packed_words = P["n_tiles"] * KC * 1024
     scales_elems = P["n_tiles"] * ng * 128
     partial_floats = 2 * P["grid"] * tm * 128
@@ -75,25 +79,27 @@ def check_shape(M, N, K, G, sms=SMS):
     writers = {}
     for c in range(P["grid"]):
         for (t, kb, ke) in segments(P, c):
-            assert 0 <= t < P["n_tiles"] * P["m_tiles"] and 0 <= kb < ke <= KC
+            assert 0 <= t < P["n_tiles"] * P["m_tiles"] and 0 <= kb < ke <= iters
             nt, mt = divmod(t, P["m_tiles"])
-            for kc in range(kb, ke):
-                key = (t, kc)
+            for st in range(kb, ke):
+                key = (t, st)
                 assert key not in covered
                 covered[key] = c
-                w0 = (nt * KC + kc) * 1024
-                assert 0 <= w0 and w0 + 1024 <= packed_words
-                g0 = min(kc * 64 // G, ng - 1)
-                g1 = min((kc * 64 + 63) // G, ng - 1)
-                assert 1 <= g1 - g0 + 1 <= 2          # fits the 512-byte scale slot
-                for half in (0, 1):
-                    g = min((kc * 64 + half * 32) // G, ng - 1)
-                    assert g0 <= g <= g1
+                k0 = st * ks * 64
+                w0 = (nt * KC + st * ks) * 1024            # one bulk copy of ks sub-chunks
+                assert 0 <= w0 and w0 + ks * 1024 <= packed_words
+                g0 = min(k0 // G, ng - 1)
+                g1 = min((k0 + ks * 64 - 1) // G, ng - 1)
+                assert 1 <= g1 - g0 + 1 <= 2 * ks          # fits the scale slot
+                for j in range(ks):
+                    for half in (0, 1):
+                        g = min((k0 + j * 64 + half * 32) // G, ng - 1)
+                        assert g0 <= g <= g1
+                    assert ((k0 + j * 64) * 2) % 16 == 0    # TMA inner coordinate, 16-byte aligned
                 e0 = (nt * ng + g0) * 128
                 assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
-                # TMA X coordinates: inner coordinate 16-byte aligned
-                assert (kc * 64 * 2) % 16 == 0 and mt * tm < M
-            split = kb != 0 or ke != KC
+                assert mt * tm < M
+            split = kb != 0 or ke != iters
             if split:
                 slot = slot_of(P, c, t)
                 assert 0 <= slot < 2 * P["grid"]
@@ -102,7 +108,7 @@ def check_shape(M, N, K, G, sms=SMS):
     assert len(covered) == P["total"]
     counter_ids = set()
     for t, ws in writers.items():
-        c_lo, c_hi = cta_of(P, t * KC), cta_of(P, t * KC + KC - 1)
+        c_lo, c_hi = cta_of(P, t * iters), cta_of(P, t * iters + iters - 1)
         assert c_lo < P["grid"] and c_lo not in counter_ids
         counter_ids.add(c_lo)
         read = [(cc, slot_of(P, cc, t)) for cc in range(c_lo, c_hi + 1)]
@@ -141,21 +147,24 @@ def _constexpr(src, name):
     return m.group(1)
 
 
-def test_shared_memory_layout_fits():
-    """Mirror of TcCfg: stage rings, barriers and alignment inside the dynamic allocation."""
+def test_shared_memory_and_tmem_layout_fits():
+    """Mirror of TcCfg: stage rings, barriers, alignment and TMEM columns."""
     src = open(os.path.join(CSRC, "gemm_tc.cuh")).read()
-    assert _constexpr(src, "kChunkBytes") == "4096" and _constexpr(src, "kScaleSlotBytes") == "512"
-    for tm in (16, 32, 64, 128, 256):
-        xb = tm * 128
-        stage = xb + 4096 + 512
-        S = min(16, (200 * 1024) // stage)
+    assert _constexpr(src, "kChunkBytes") == "4096" and _constexpr(src, "kKPad") == "4"
+    for tm, ks in ((16, 4), (32, 4), (64, 4), (128, 2), (256, 2)):
+        xblock = tm * 128
+        xb, pk, sc = ks * xblock, ks * 4096, 2 * ks * 256
+        S = min(8, (220 * 1024) // (xb + pk + sc))
+        dbufs = 2 if tm <= 128 else 1
+        A = min(4, (512 - dbufs * tm) // (ks * 32))
+        assert S >= 2 and A >= 2
         off_pk = S * xb
-        off_sc = off_pk + S * 4096
-        off_bar = off_sc + S * 512
-        nbars = 2 * S + 8 + 4 + 1
-        off_misc = off_bar + nbars * 8
-        smem = off_misc + 64 + 1024
-        assert smem <= 227 * 1024
-        assert xb % 1024 == 0 and off_pk % 16 == 0 and off_sc % 16 == 0 and off_bar % 8 == 0
-        cols = 4 * 32 + (2 if tm <= 128 else 1) * tm
-        assert cols <= (256 if cols <= 256 else 512) <= 512
+        off_sc = off_pk + S * pk
+        off_bar = off_sc + S * sc
+        nbars = 2 * S + 2 * A + 4 + 1
+        smem = off_bar + nbars * 8 + 64 + 1024
+        assert smem <= 227 * 1024, (tm, smem)
+        assert xblock % 1024 == 0 and off_pk % 16 == 0 and off_sc % 16 == 0 and off_bar % 8 == 0
+        assert A * ks * 32 + dbufs * tm <= 512
+        threads = 32 * (4 + 4 * ks + 3)
+        assert threads <= 1024 and threads * 88 <= 65536

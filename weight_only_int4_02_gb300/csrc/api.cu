@@ -63,7 +63,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 struct Plan {
     int path;     // 2 = per-weight scaling tcgen05 kernel
     int tm;       // rows of X per tile (MMA N)
-    int m_tiles, n_tiles, KC, ng;
+    int ksub;     // 64-value sub-chunks per pipeline stage
+    int m_tiles, n_tiles, KC, ng, iters;
     long long total;
     int grid;
     size_t ws_bytes;
@@ -78,9 +79,11 @@ Plan make_plan(int M, int N, int K, int G, int sms)
     P.tm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     P.m_tiles = ceil_div(M, P.tm);
     P.n_tiles = ceil_div(N, kTileN);
-    P.KC = ceil_div(K, kChunkK);
+    P.ksub = P.tm <= 64 ? 4 : 2;
+    P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
+    P.iters = P.KC / P.ksub;
     P.ng = ceil_div(K, G);
-    P.total = (long long)P.n_tiles * P.m_tiles * P.KC;
+    P.total = (long long)P.n_tiles * P.m_tiles * P.iters;
     long long grid = sms < kMaxGrid ? sms : kMaxGrid;
     if (grid > P.total) grid = P.total;
     P.grid = (int)grid;
@@ -103,9 +106,9 @@ w4a16_status device_state(DeviceState** out)
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
-        if ((e = setup_tc<16>()) != cudaSuccess || (e = setup_tc<32>()) != cudaSuccess ||
-            (e = setup_tc<64>()) != cudaSuccess || (e = setup_tc<128>()) != cudaSuccess ||
-            (e = setup_tc<256>()) != cudaSuccess)
+        if ((e = setup_tc<16, 4>()) != cudaSuccess || (e = setup_tc<32, 4>()) != cudaSuccess ||
+            (e = setup_tc<64, 4>()) != cudaSuccess || (e = setup_tc<128, 2>()) != cudaSuccess ||
+            (e = setup_tc<256, 2>()) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
             void* fn = nullptr;
@@ -189,9 +192,15 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.K = K;
     p.G = G;
     p.ng = P.ng;
+    p.g_shift = 30;
+    if ((G & (G - 1)) == 0) {
+        p.g_shift = 0;
+        while ((1 << p.g_shift) < G) ++p.g_shift;
+    }
     p.n_tiles = P.n_tiles;
     p.m_tiles = P.m_tiles;
     p.KC = P.KC;
+    p.iters = P.iters;
     p.total_iters = P.total;
     p.grid = P.grid;
     p.wait_limit_ns = g_wait_limit_ns;
@@ -200,11 +209,11 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     if (!encode_x_map(&map, x, M, K, P.tm)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     switch (P.tm) {
-        case 16: e = launch_tc<16>(map, p, stream); break;
-        case 32: e = launch_tc<32>(map, p, stream); break;
-        case 64: e = launch_tc<64>(map, p, stream); break;
-        case 128: e = launch_tc<128>(map, p, stream); break;
-        default: e = launch_tc<256>(map, p, stream); break;
+        case 16: e = launch_tc<16, 4>(map, p, stream); break;
+        case 32: e = launch_tc<32, 4>(map, p, stream); break;
+        case 64: e = launch_tc<64, 4>(map, p, stream); break;
+        case 128: e = launch_tc<128, 2>(map, p, stream); break;
+        default: e = launch_tc<256, 2>(map, p, stream); break;
     }
     return from_cuda(e);
 }
@@ -213,7 +222,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
 
 extern "C" {
 
-int w4a16_layout_version(void) { return 1; }
+int w4a16_layout_version(void) { return 2; }
 
 const char* w4a16_status_string(int status)
 {
@@ -233,7 +242,7 @@ int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
 size_t w4a16_packed_words(int K, int N, int group_size)
 {
     if (!valid_sizes(K, N, norm_group(K, group_size))) return 0;
-    return (size_t)ceil_div(N, kTileN) * ceil_div(K, kChunkK) * kChunkWords;
+    return (size_t)ceil_div(N, kTileN) * (ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad) * kChunkWords;
 }
 
 size_t w4a16_scales_elems(int K, int N, int group_size)
@@ -253,7 +262,8 @@ w4a16_status w4a16_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* 
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    return from_cuda(launch_pack(codes, scales, packed, scales_packed, K, N, ceil_div(K, kChunkK),
+    return from_cuda(launch_pack(codes, scales, packed, scales_packed, K, N,
+                                 ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad,
                                  ceil_div(N, kTileN), ceil_div(K, G), st->sms,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }

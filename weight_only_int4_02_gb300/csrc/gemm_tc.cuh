@@ -3,23 +3,29 @@
 // Y[M][N] = X[M][K] * W[K][N], W[k][n] = (q - 8) * s[k/G][n], FP32 accumulate, FP16 out.
 //
 // The MMA runs "swapped": D[n][m] = sum_k W^T[n][k] * X^T[k][m], so the weight
-// tile is the 128-row A operand and X supplies the N operand (tile_m rows of X,
-// 16..256). A lives in tensor memory: dequant warps unpack the INT4 codes
-// with bit operations (magic-number FP16 construction) straight into TMEM
-// columns, so dequantised weights never touch shared memory; B (X) is loaded
-// by TMA into 128-byte-swizzled shared memory; D accumulates in TMEM.
+// tile is the 128-row A operand and X supplies the N operand (TM rows of X,
+// 16..256). A lives in tensor memory: dequant warps unpack the INT4 codes with
+// bit operations (magic-number FP16 construction) straight into TMEM columns,
+// so dequantised weights never touch shared memory; B (X) is loaded by TMA into
+// 128-byte-swizzled shared memory; D accumulates in TMEM.
 //
-// Warp roles (448 threads):
-//   warps 0-3   epilogue: TMEM -> registers -> FP16 Y, or FP32 partials + fix-up
-//   warps 4-11  dequant: packed words (shared) -> FP16 (q-8)*s -> TMEM A ring
-//   warp 12     producer: TMA X tile, bulk copy of packed words and scales
-//   warp 13     MMA issuer (one thread) and TMEM owner
+// A pipeline stage covers KSUB sub-chunks of 64 reduction values (KSUB = 4 for
+// the memory-bound tiles, 2 for the compute-bound ones), so every barrier wait,
+// commit and copy issue is paid once per 16 (or 8) MMAs.
 //
-// Work split ("stream-K"): the iteration space (tile, 64-wide K chunk) is cut
-// into one contiguous range per CTA. A tile whose chunks span several CTAs is
-// reduced in global memory: every contributor stores its FP32 partial, and the
-// last one to arrive on the tile's counter sums all partials in contributor
-// order, so the result does not depend on arrival order.
+// Warp roles (32 * (7 + 4*KSUB) threads):
+//   warps 0-3           epilogue: TMEM -> registers -> FP16 Y, or FP32 partials + fix-up
+//   warps 4 .. 4+4K-1   dequant, KSUB groups of four warps (one per TMEM lane
+//                       quarter); group g unpacks sub-chunk g of every stage
+//   next warp           producer X: TMA of the X tiles and bulk copy of the scales
+//   next warp           producer W: bulk copy of the packed words
+//   last warp           MMA issuer (one elected lane) and TMEM owner
+//
+// Work split ("stream-K"): the iteration space (tile, stage) is cut into one
+// contiguous range per CTA. A tile whose stages span several CTAs is reduced
+// in global memory: every contributor stores its FP32 partial, and the last
+// one to arrive on the tile's counter sums all partials in contributor order,
+// so the result does not depend on arrival order.
 //
 // Sources: "quant_marlin_kernel" (aicassindra.com), "The architecture: every
 // piece explained" (packed INT4, group scales, register-level unpack, async
@@ -35,50 +41,65 @@
 namespace w4a16 {
 
 constexpr int kTileN = 128;        // weight rows (output features) per tile = TMEM lanes
-constexpr int kChunkK = 64;        // K values per pipeline stage
-constexpr int kChunkWords = 1024;  // packed words per (tile, chunk): 128 * 64 / 8
+constexpr int kChunkK = 64;        // reduction values per sub-chunk
+constexpr int kChunkWords = 1024;  // packed words per (tile, sub-chunk): 128 * 64 / 8
 constexpr int kChunkBytes = 4096;
-constexpr int kScaleSlotBytes = 512;  // up to two groups of 128 FP16 scales per chunk
-constexpr int kThreads = 448;
-constexpr int kAStages = 4;        // TMEM A ring depth (32 columns each)
+constexpr int kKPad = 4;           // the packed layout pads K to a multiple of 4 sub-chunks
 
 struct GemmParams {
     const uint32_t* packed;
-    const __half* scales;  // tile-ordered scales [n_tiles][ng][128]
+    const __half* scales;   // tile-ordered scales [n_tiles][ng][128]
     __half* y;
-    float* partials;       // [2 * grid][tile_m][128] FP32
-    int* counters;         // [grid], zero between launches
-    int* status;           // error word, bit 0 = a wait timed out
+    float* partials;        // [2 * grid][TM][128] FP32
+    int* counters;          // [grid], zero between launches
+    int* status;            // error word, bit 0 = a wait timed out
     int M, N, K, G, ng;
-    int n_tiles, m_tiles, KC;
-    long long total_iters;  // n_tiles * m_tiles * KC
+    int g_shift;            // log2(G) for G a power of two; 30 when there is one group
+    int n_tiles, m_tiles;
+    int KC;                 // 64-value sub-chunks per weight column in the packed layout
+    int iters;              // stages per tile = KC / KSUB
+    long long total_iters;  // n_tiles * m_tiles * iters
     int grid;
     long long wait_limit_ns;
 };
 
-template <int TM>
+template <int TM, int KSUB>
 struct TcCfg {
-    static constexpr int kXBytes = TM * 128;  // TM rows x 64 FP16
-    static constexpr int kStageBytes = kXBytes + kChunkBytes + kScaleSlotBytes;
-    static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
+    static constexpr int kStageK = KSUB * kChunkK;
+    static constexpr int kXBlock = TM * 128;              // one 64-wide K block of X (TM rows)
+    static constexpr int kXBytes = KSUB * kXBlock;
+    static constexpr int kPkBytes = KSUB * kChunkBytes;
+    static constexpr int kScBytes = 2 * KSUB * 256;       // G = 32 puts 2*KSUB groups in a stage
+    static constexpr int kStageBytes = kXBytes + kPkBytes + kScBytes;
+    static constexpr int kStagesRaw = (220 * 1024) / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kDqWarps = 4 * KSUB;
+    static constexpr int kDqWarp0 = 4;
+    static constexpr int kProdXWarp = kDqWarp0 + kDqWarps;
+    static constexpr int kProdWWarp = kProdXWarp + 1;
+    static constexpr int kMmaWarp = kProdWWarp + 1;
+    static constexpr int kThreads = 32 * (kMmaWarp + 1);
     static constexpr int kDBufs = TM <= 128 ? 2 : 1;
+    static constexpr int kASlotCols = KSUB * 32;          // 16-bit A values, two per column
+    static constexpr int kAFit = (512 - kDBufs * TM) / kASlotCols;
+    static constexpr int kAStages = kAFit > 4 ? 4 : kAFit;
     static constexpr int kACol = 0;
-    static constexpr int kDCol = kAStages * 32;
-    static constexpr int kColsUsed = kDCol + kDBufs * TM;
-    static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
+    static constexpr int kDCol = kAStages * kASlotCols;
+    static constexpr int kTmemCols = 512;
     // shared memory layout, offsets from a 1024-aligned base
     static constexpr int kOffX = 0;
     static constexpr int kOffPk = kOffX + kStages * kXBytes;
-    static constexpr int kOffSc = kOffPk + kStages * kChunkBytes;
-    static constexpr int kOffBar = kOffSc + kStages * kScaleSlotBytes;
-    // barriers: full[S], empty[S], afull[4], aempty[4], dfull[2], dempty[2], teardown
+    static constexpr int kOffSc = kOffPk + kStages * kPkBytes;
+    static constexpr int kOffBar = kOffSc + kStages * kScBytes;
+    // barriers: full[S], empty[S], afull[A], aempty[A], dfull[2], dempty[2], teardown
     static constexpr int kNumBars = 2 * kStages + 2 * kAStages + 4 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
-    static_assert(kXBytes % 1024 == 0, "X stages must stay 1024-byte aligned");
+    static_assert(kXBlock % 1024 == 0, "X blocks must stay 1024-byte aligned");
+    static_assert(kStages >= 2 && kAStages >= 2, "pipeline depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    static_assert(kColsUsed <= 512, "tensor memory");
+    static_assert(kDCol + kDBufs * TM <= 512, "tensor memory");
+    static_assert(kKPad % KSUB == 0, "stages must tile the padded K");
 };
 
 __device__ __forceinline__ long long cta_begin(const GemmParams& p, int c)
@@ -98,13 +119,13 @@ __device__ __forceinline__ int cta_of(const GemmParams& p, long long i)
 // Partial slot of CTA c for tile t: 2c if t holds c's first iteration, else 2c+1.
 __device__ __forceinline__ int slot_of(const GemmParams& p, int c, int t)
 {
-    return cta_begin(p, c) >= (long long)t * p.KC ? 2 * c : 2 * c + 1;
+    return cta_begin(p, c) >= (long long)t * p.iters ? 2 * c : 2 * c + 1;
 }
 
-// Group range of chunk kc, clamped to the last group (chunks past K hold code 8).
-__device__ __forceinline__ int group_lo(const GemmParams& p, int kc)
+// Group of reduction index k, clamped to the last group (padding past K holds code 8).
+__device__ __forceinline__ int group_of(const GemmParams& p, int k)
 {
-    return min(kc * kChunkK / p.G, p.ng - 1);
+    return min(k >> p.g_shift, p.ng - 1);
 }
 
 // (q - 8) * s as four FP16 pairs (k, k+1) ... (k+6, k+7) from one packed word whose
@@ -135,12 +156,27 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t* o
     out[3] = *reinterpret_cast<uint32_t*>(&hd);
 }
 
-template <int TM>
-__global__ void __launch_bounds__(kThreads, 1)
+// One segment of a CTA's range: tile t, stages [kb, ke).
+struct Segment {
+    int t, kb, ke;
+};
+
+__device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, long long it_end)
+{
+    Segment g;
+    g.t = (int)(i / p.iters);
+    g.kb = (int)(i - (long long)g.t * p.iters);
+    g.ke = (int)min((long long)p.iters, g.kb + (it_end - i));
+    return g;
+}
+
+template <int TM, int KSUB>
+__global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
-    using C = TcCfg<TM>;
+    using C = TcCfg<TM, KSUB>;
     constexpr int S = C::kStages;
+    constexpr int A = C::kAStages;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled X tiles.
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -151,10 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto afull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * S + kAStages + a); };
-    auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 * kAStages + d); };
-    auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 * kAStages + 2 + d); };
-    const uint32_t teardown_bar = bar0 + 8u * (2 * S + 2 * kAStages + 4);
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * S + A + a); };
+    auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 * A + d); };
+    auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 * A + 2 + d); };
+    const uint32_t teardown_bar = bar0 + 8u * (2 * S + 2 * A + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16);
@@ -165,11 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 8 + 1);  // 8 dequant warps + MMA commit
+            mbar_init(full_bar(s), 2);                    // the two producer warps
+            mbar_init(empty_bar(s), C::kDqWarps + 1);     // every dequant warp + MMA commit
         }
-        for (int a = 0; a < kAStages; ++a) {
-            mbar_init(afull_bar(a), 8);
+        for (int a = 0; a < A; ++a) {
+            mbar_init(afull_bar(a), C::kDqWarps);
             mbar_init(aempty_bar(a), 1);
         }
         for (int d = 0; d < 2; ++d) {
@@ -180,8 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 12 && lane == 0) prefetch_tmap(&tmap_x);
-    if (warp == 13) {
+    if (warp == C::kProdXWarp && lane == 0) prefetch_tmap(&tmap_x);
+    if (warp == C::kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -194,118 +230,146 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long it_begin = cta_begin(p, cta);
     const long long it_end = cta_begin(p, cta + 1);
 
-    if (warp == 12) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (long long i = it_begin; ok && i < it_end;) {
-                const int t = (int)(i / p.KC);
-                const int kb = (int)(i - (long long)t * p.KC);
-                const int ke = (int)min((long long)p.KC, kb + (it_end - i));
-                const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
-                for (int kc = kb; kc < ke; ++kc) {
-                    if (!wait_one(empty_bar(s), ph ^ 1, ctl)) { ok = false; break; }
-                    const int g0 = group_lo(p, kc);
-                    const int g1 = min((kc * kChunkK + kChunkK - 1) / p.G, p.ng - 1);
-                    const uint32_t sc_bytes = (uint32_t)(g1 - g0 + 1) * 256u;
-                    mbar_arrive_expect_tx(full_bar(s), C::kXBytes + kChunkBytes + sc_bytes);
-                    tma_load_2d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, full_bar(s), kc * kChunkK, mt * TM);
-                    bulk_load(sbase + C::kOffPk + s * kChunkBytes,
-                              p.packed + ((size_t)nt * p.KC + kc) * kChunkWords, kChunkBytes, full_bar(s));
-                    bulk_load(sbase + C::kOffSc + s * kScaleSlotBytes,
-                              p.scales + ((size_t)nt * p.ng + g0) * kTileN, sc_bytes, full_bar(s));
-                    ++issued;
-                    if (++s == S) { s = 0; ph ^= 1; }
+    // Every role walks the same stage sequence seq = 0, 1, ... over the CTA's
+    // range; stage seq uses slot seq % S of the shared ring and slot seq % A of
+    // the TMEM A ring. Each role visits every seq in order, so no waiter can be
+    // a whole phase ahead of a barrier (parity waits cannot tell p from p + 2).
+    if (warp == C::kProdXWarp || warp == C::kProdWWarp) {
+        // ------------------------------------------------------------ producers
+        const bool is_x = warp == C::kProdXWarp;
+        uint32_t seq = 0;
+        bool ok = true;
+        for (long long i = it_begin; ok && i < it_end;) {
+            const Segment g = segment_at(p, i, it_end);
+            const int nt = g.t / p.m_tiles, mt = g.t - nt * p.m_tiles;
+            for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
+                const int s = (int)(seq % S);
+                if (!wait_warp(empty_bar(s), ((seq / S) & 1) ^ 1, ctl)) { ok = false; break; }
+                if (lane == 0) {
+                    const int k0 = kc * C::kStageK;
+                    if (is_x) {
+                        const int g0 = group_of(p, k0);
+                        const int g1 = group_of(p, k0 + C::kStageK - 1);
+                        const uint32_t sc_bytes = (uint32_t)(g1 - g0 + 1) * 256u;
+                        mbar_arrive_expect_tx(full_bar(s), C::kXBytes + sc_bytes);
+#pragma unroll
+                        for (int j = 0; j < KSUB; ++j)
+                            tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * C::kXBlock, &tmap_x, full_bar(s),
+                                        k0 + j * kChunkK, mt * TM);
+                        bulk_load(sbase + C::kOffSc + s * C::kScBytes, p.scales + ((size_t)nt * p.ng + g0) * kTileN,
+                                  sc_bytes, full_bar(s));
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(s), C::kPkBytes);
+                        bulk_load(sbase + C::kOffPk + s * C::kPkBytes,
+                                  p.packed + ((size_t)nt * p.KC + (size_t)kc * KSUB) * kChunkWords, C::kPkBytes,
+                                  full_bar(s));
+                    }
                 }
-                i += ke - kb;
+                __syncwarp();
             }
-            // Wind down: let the last copies land before the CTA can exit.
-            const long long inflight = issued < S ? issued : S;
-            for (long long k = 1; k <= inflight; ++k) {
-                int ss = s - (int)k;
-                uint32_t pp = ph;
-                if (ss < 0) { ss += S; pp ^= 1; }
-                wait_drain(full_bar(ss), pp, 1000000000LL);
+            i += g.ke - g.kb;
+        }
+        // Wind down: let the last copies land before the CTA can exit.
+        if (lane == 0) {
+            const uint32_t inflight = seq < (uint32_t)S ? seq : (uint32_t)S;
+            for (uint32_t k = 1; k <= inflight; ++k) {
+                const uint32_t q = seq - k;
+                wait_drain(full_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
             }
         }
-    } else if (warp == 13) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(128, TM);
-            int s = 0, a = 0, d = 0;
-            uint32_t ph = 0, aph = 0, dph = 0;
-            bool ok = true;
-            for (long long i = it_begin; ok && i < it_end;) {
-                const int t = (int)(i / p.KC);
-                const int kb = (int)(i - (long long)t * p.KC);
-                const int ke = (int)min((long long)p.KC, kb + (it_end - i));
-                if (!wait_one(dempty_bar(d), dph ^ 1, ctl)) break;
+        constexpr uint32_t idesc = idesc_f16_f32(128, TM);
+        uint32_t seq = 0;
+        int d = 0;
+        uint32_t dph = 0;
+        bool ok = true;
+        for (long long i = it_begin; ok && i < it_end;) {
+            const Segment g = segment_at(p, i, it_end);
+            if (!wait_warp(dempty_bar(d), dph ^ 1, ctl)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + C::kDCol + d * TM;
+            for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
+                const int s = (int)(seq % S);
+                const int a = (int)(seq % A);
+                if (!wait_warp(full_bar(s), (seq / S) & 1, ctl) || !wait_warp(afull_bar(a), (seq / A) & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + C::kDCol + d * TM;
-                for (int kc = kb; kc < ke; ++kc) {
-                    if (!wait_one(full_bar(s), ph, ctl) || !wait_one(afull_bar(a), aph, ctl)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t x_addr = sbase + C::kOffX + s * C::kXBytes;
+                if (elect_one()) {
+                    const uint64_t b0 = smem_desc_k_sw128(sbase + C::kOffX + s * C::kXBytes);
+                    const uint32_t a0 = tmem + C::kACol + a * C::kASlotCols;
+                    // The descriptor's start address counts 16-byte units: +2 per 16 K values
+                    // inside a 128-byte row, +kXBlock/16 per 64-wide K block.
 #pragma unroll
-                    for (int kk = 0; kk < kChunkK / 16; ++kk) {
-                        mma_f16_ts(d_tmem, tmem + C::kACol + a * 32 + kk * 8, smem_desc_k_sw128(x_addr + kk * 32),
-                                   idesc, (kc > kb || kk > 0) ? 1u : 0u);
+                    for (int j = 0; j < KSUB; ++j) {
+#pragma unroll
+                        for (int kk = 0; kk < kChunkK / 16; ++kk) {
+                            const uint64_t bd = b0 + (uint64_t)(j * (C::kXBlock >> 4) + kk * 2);
+                            mma_f16_ts(d_tmem, a0 + j * 32 + kk * 8, bd, idesc,
+                                       (kc > g.kb || j > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit(empty_bar(s));
                     mma_commit(aempty_bar(a));
-                    if (++s == S) { s = 0; ph ^= 1; }
-                    if (++a == kAStages) { a = 0; aph ^= 1; }
                 }
-                if (!ok) break;
-                mma_commit(dfull_bar(d));
-                if (++d == C::kDBufs) { d = 0; dph ^= 1; }
-                i += ke - kb;
+                __syncwarp();
             }
-            // Wind down: every MMA issued so far completes before TMEM is freed.
+            if (!ok) break;
+            if (elect_one()) mma_commit(dfull_bar(d));
+            __syncwarp();
+            if (++d == C::kDBufs) { d = 0; dph ^= 1; }
+            i += g.ke - g.kb;
+        }
+        // Wind down: every MMA issued so far completes before TMEM is freed.
+        if (lane == 0) {
             mma_commit(teardown_bar);
             wait_drain(teardown_bar, 0, 1000000000LL);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= C::kDqWarp0) {
         // ------------------------------------------------------------ dequant
-        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const int half = (warp - 4) >> 2;         // K values 32*half .. +31 of each chunk
+        const int grp = (warp - C::kDqWarp0) >> 2;   // sub-chunk of every stage this group unpacks
+        const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
         const int n_in = quarter * 32 + lane;
-        int s = 0, a = 0;
-        uint32_t ph = 0, aph = 0;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        uint32_t seq = 0;
         bool ok = true;
         for (long long i = it_begin; ok && i < it_end;) {
-            const int t = (int)(i / p.KC);
-            const int kb = (int)(i - (long long)t * p.KC);
-            const int ke = (int)min((long long)p.KC, kb + (it_end - i));
-            for (int kc = kb; kc < ke; ++kc) {
-                if (!wait_warp(full_bar(s), ph, ctl)) { ok = false; break; }
-                const uint4 pk = *reinterpret_cast<const uint4*>(smem + C::kOffPk + s * kChunkBytes +
-                                                                 (half * kTileN + n_in) * 16);
-                const int g0 = group_lo(p, kc);
-                const int g = min((kc * kChunkK + half * 32) / p.G, p.ng - 1);
-                const __half sc = *reinterpret_cast<const __half*>(smem + C::kOffSc + s * kScaleSlotBytes +
-                                                                   ((g - g0) * kTileN + n_in) * 2);
-                const __half2 s2 = __halves2half2(sc, sc);
-                uint32_t v[16];
-                dequant_word(pk.x, s2, v + 0);
-                dequant_word(pk.y, s2, v + 4);
-                dequant_word(pk.z, s2, v + 8);
-                dequant_word(pk.w, s2, v + 12);
+            const Segment g = segment_at(p, i, it_end);
+            for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
+                const int s = (int)(seq % S);
+                const int a = (int)(seq % A);
+                if (!wait_warp(full_bar(s), (seq / S) & 1, ctl)) { ok = false; break; }
+                const uint8_t* pk = smem + C::kOffPk + s * C::kPkBytes + grp * kChunkBytes + n_in * 16;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(pk);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(pk + kTileN * 16);
+                const int k0 = kc * C::kStageK + grp * kChunkK;
+                const int gs = group_of(p, kc * C::kStageK);
+                const __half* sc = reinterpret_cast<const __half*>(smem + C::kOffSc + s * C::kScBytes) + n_in;
+                const __half s_lo = sc[(group_of(p, k0) - gs) * kTileN];
+                const __half s_hi = sc[(group_of(p, k0 + 32) - gs) * kTileN];
+                const __half2 s2lo = __halves2half2(s_lo, s_lo);
+                const __half2 s2hi = __halves2half2(s_hi, s_hi);
+                uint32_t v[32];
+                dequant_word(w0.x, s2lo, v + 0);
+                dequant_word(w0.y, s2lo, v + 4);
+                dequant_word(w0.z, s2lo, v + 8);
+                dequant_word(w0.w, s2lo, v + 12);
+                dequant_word(w1.x, s2hi, v + 16);
+                dequant_word(w1.y, s2hi, v + 20);
+                dequant_word(w1.z, s2hi, v + 24);
+                dequant_word(w1.w, s2hi, v + 28);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
-                if (!wait_warp(aempty_bar(a), aph ^ 1, ctl)) { ok = false; break; }
+                if (!wait_warp(aempty_bar(a), ((seq / A) & 1) ^ 1, ctl)) { ok = false; break; }
                 tc_fence_after();
-                tmem_st16(tmem + ((uint32_t)(quarter * 32) << 16) + C::kACol + a * 32 + half * 16, v);
+                tmem_st32(tmem + lane_base + C::kACol + a * C::kASlotCols + grp * 32, v);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull_bar(a));
-                if (++s == S) { s = 0; ph ^= 1; }
-                if (++a == kAStages) { a = 0; aph ^= 1; }
             }
-            i += ke - kb;
+            i += g.ke - g.kb;
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -313,15 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int d = 0;
         uint32_t dph = 0;
         for (long long i = it_begin; i < it_end;) {
-            const int t = (int)(i / p.KC);
-            const int kb = (int)(i - (long long)t * p.KC);
-            const int ke = (int)min((long long)p.KC, kb + (it_end - i));
+            const Segment g = segment_at(p, i, it_end);
+            const int t = g.t;
             const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
             const int n = nt * kTileN + n_in;
             const int m0 = mt * TM;
             const int valid = min(TM, p.M - m0);
             const int chunks = (valid + 15) >> 4;
-            const bool split = (kb != 0 || ke != p.KC);
+            const bool split = (g.kb != 0 || g.ke != p.iters);
             // All four epilogue warps leave together: they share named barriers.
             const bool ok = wait_warp(dfull_bar(d), dph, ctl);
             if (named_bar_or(1, 128, !ok)) break;
@@ -348,15 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dempty_bar(d));
             if (++d == C::kDBufs) { d = 0; dph ^= 1; }
-            i += ke - kb;
+            i += g.ke - g.kb;
 
             if (split) {
                 // Deterministic split-K fix-up: the last contributor sums every
                 // contributor's partial in CTA order.
                 __threadfence();
                 named_bar_sync(1, 128);
-                const int c_lo = cta_of(p, (long long)t * p.KC);
-                const int c_hi = cta_of(p, (long long)t * p.KC + p.KC - 1);
+                const int c_lo = cta_of(p, (long long)t * p.iters);
+                const int c_hi = cta_of(p, (long long)t * p.iters + p.iters - 1);
                 if (threadIdx.x == 0) {
                     const int prev = atomicAdd(p.counters + c_lo, 1);
                     const int last = (prev == c_hi - c_lo);
@@ -367,13 +430,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int last = *last_flag;
                 if (last) {
                     __threadfence();
-                    for (int col = 0; col < valid; ++col) {
-                        float acc = 0.f;
-                        for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            const float* src = p.partials + (size_t)slot_of(p, cc, t) * TM * kTileN;
-                            acc += __ldcg(src + (size_t)col * kTileN + n_in);
+                    for (int c = 0; c < chunks; ++c) {
+                        float acc[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+                        int cc = c_lo;
+                        for (; cc + 1 <= c_hi; cc += 2) {   // two contributors' loads in flight
+                            const float* s0 = p.partials + ((size_t)slot_of(p, cc, t) * TM + c * 16) * kTileN + n_in;
+                            const float* s1 =
+                                p.partials + ((size_t)slot_of(p, cc + 1, t) * TM + c * 16) * kTileN + n_in;
+                            float v0[16], v1[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v0[e] = __ldcg(s0 + e * kTileN);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v1[e] = __ldcg(s1 + e * kTileN);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) acc[e] = (acc[e] + v0[e]) + v1[e];
                         }
-                        if (n < p.N) p.y[(size_t)(m0 + col) * p.N + n] = __float2half_rn(acc);
+                        if (cc <= c_hi) {
+                            const float* s0 = p.partials + ((size_t)slot_of(p, cc, t) * TM + c * 16) * kTileN + n_in;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) acc[e] += __ldcg(s0 + e * kTileN);
+                        }
+                        if (n < p.N) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = m0 + c * 16 + e;
+                                if (m < p.M) p.y[(size_t)m * p.N + n] = __float2half_rn(acc[e]);
+                            }
+                        }
                     }
                 }
                 named_bar_sync(1, 128);
@@ -383,17 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 13) {
+    if (warp == C::kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
-template <int TM>
+template <int TM, int KSUB>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream);
 
-template <int TM>
+template <int TM, int KSUB>
 cudaError_t setup_tc();
+
+// Sub-chunks per stage for a tile height: 4 for the memory-bound tiles, 2 above.
+constexpr int ksub_for(int tm) { return tm <= 64 ? 4 : 2; }
 
 }  // namespace w4a16

@@ -1,33 +1,33 @@
-// Host-side launch and set-up of w4a16_tc_kernel<TM>; included by one .cu file per TM.
+// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB>; included by one .cu file per tile shape.
 #pragma once
 #include "gemm_tc.cuh"
 
 namespace w4a16 {
 
-template <int TM>
+template <int TM, int KSUB>
 cudaError_t setup_tc()
 {
-    return cudaFuncSetAttribute(w4a16_tc_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TcCfg<TM>::kSmemBytes);
+    return cudaFuncSetAttribute(w4a16_tc_kernel<TM, KSUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TcCfg<TM, KSUB>::kSmemBytes);
 }
 
-template <int TM>
+template <int TM, int KSUB>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = TcCfg<TM>::kSmemBytes;
+    cfg.blockDim = dim3(TcCfg<TM, KSUB>::kThreads);
+    cfg.dynamicSmemBytes = TcCfg<TM, KSUB>::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM>, tmap, p);
+    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB>, tmap, p);
 }
 
 }  // namespace w4a16
 
-#define W4A16_INSTANTIATE_TC(TM)                                                                  \
-    namespace w4a16 {                                                                             \
-    template cudaError_t setup_tc<TM>();                                                          \
-    template cudaError_t launch_tc<TM>(const CUtensorMap&, const GemmParams&, cudaStream_t);      \
+#define W4A16_INSTANTIATE_TC(TM, KSUB)                                                              \
+    namespace w4a16 {                                                                               \
+    template cudaError_t setup_tc<TM, KSUB>();                                                      \
+    template cudaError_t launch_tc<TM, KSUB>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
     }

@@ -4,7 +4,8 @@
 // permuted order chosen once, offline, so the inner loop needs no shuffles).
 //
 // Word (((nt*KC + kc)*2 + j)*128 + n_in)*4 + w holds k0 = kc*64 + j*32 + w*8 .. k0+7
-// of column n = nt*128 + n_in; nibble i holds k0 + 2*(i%4) + i/4, so that the
+// of column n = nt*128 + n_in, with KC = ceil(K/64) rounded up to a multiple of 4
+// (a 256-value pipeline stage never runs past the buffer); nibble i holds k0 + 2*(i%4) + i/4, so that the
 // magic-number unpack of nibbles (i, i+4) yields the FP16 pair (k, k+1) that
 // one 32-bit TMEM column of the MMA's A operand holds. A 64-value chunk of one
 // 128-column tile is 4 KB of contiguous words (one bulk copy per pipeline stage);

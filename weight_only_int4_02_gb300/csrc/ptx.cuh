@@ -53,6 +53,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Test for completion of phase `parity`; a thread whose phase is not complete
+// yet is suspended (not spinning) for up to `hint_ns` or until the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Shared state of one CTA's bounded waits: a wait that exceeds `limit_ns` sets
 // the CTA's abort flag and the launch's error word; every other wait of the CTA
 // then gives up at its next check, so the CTA winds down instead of hanging.
@@ -62,20 +77,20 @@ struct WaitCtl {
     long long limit_ns;
 };
 
+constexpr uint32_t kSleepHintNs = 20000;
+
 // One thread waits for phase `parity` of `bar` to complete.
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtl& c)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0) {
-            if (*c.abort_flag) return false;
-            if ((long long)(global_timer_ns() - t0) > c.limit_ns) {
-                *c.abort_flag = 1;
-                atomicOr(c.status, 1);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (*c.abort_flag) return false;
+        if ((long long)(global_timer_ns() - t0) > c.limit_ns) {
+            *c.abort_flag = 1;
+            atomicOr(c.status, 1);
+            return false;
         }
     }
 }
@@ -84,22 +99,20 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Wa
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c)
 {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-        if ((it & 15u) == 0) {
-            int stop = 0;
-            if ((threadIdx.x & 31) == 0) {
-                if (*c.abort_flag) {
-                    stop = 1;
-                } else if ((long long)(global_timer_ns() - t0) > c.limit_ns) {
-                    *c.abort_flag = 1;
-                    atomicOr(c.status, 1);
-                    stop = 1;
-                }
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepHintNs))) return true;
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0) {
+            if (*c.abort_flag) {
+                stop = 1;
+            } else if ((long long)(global_timer_ns() - t0) > c.limit_ns) {
+                *c.abort_flag = 1;
+                atomicOr(c.status, 1);
+                stop = 1;
             }
-            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
         }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
 }
 
@@ -107,7 +120,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long long limit_ns)
 {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
         if ((long long)(global_timer_ns() - t0) > limit_ns) return false;
     }
     return true;
@@ -202,6 +215,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+// Each lane of the warp writes 32 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major tile written by TMA with 128-byte
 // swizzle (rows of 64 FP16 values, 8-row atoms of 1024 bytes).
 __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr)
@@ -239,6 +267,18 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred)
         : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
         : "memory");
     return r != 0;
+}
+
+// True in exactly one lane of the (fully active) warp.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // (a & b) | c in one instruction.
