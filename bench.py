@@ -419,6 +419,10 @@ def run_ours(args, rank, world):
         "clocks": clocks,
         "e2e": e2e,
         "per_M": per_m_out,
+        "per_case": [{"M": c["M"], "K": c["K"], "N": c["N"], "us": float(mean_ms[ci] * 1e3),
+                      "weight_gbs": weight_bytes(c["K"], c["N"], G) / (mean_ms[ci] * 1e-3) / 1e9,
+                      "roofline_frac": roofline_seconds(c["M"], c["K"], c["N"], G, peaks) / (mean_ms[ci] * 1e-3)}
+                     for ci, c in enumerate(per_case)],
         "kernels": {n: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3} for n, v in kernels.items()},
         "byte_ratio_fp16_over_w4g128": fp16_over_int4_byte_ratio(G),
     }

@@ -148,15 +148,31 @@ w4a16_status own_workspace(DeviceState* st, void** ws, size_t* bytes)
     return W4A16_OK;
 }
 
-bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int tm)
+// X as a 3-D view {64, M, K/64} (strides K*2 and 128 bytes) when K is a multiple of
+// 64, so one TMA brings a stage's KSUB blocks of 64 columns; else the plain 2-D
+// map {K, M}, one TMA per block, with the ragged K edge zero-filled.
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int tm, int ksub, int* is_3d)
 {
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (K % kChunkK == 0) {
+        cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)M, (cuuint64_t)(K / kChunkK)};
+        cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kChunkK * 2};
+        cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)tm, (cuuint32_t)ksub};
+        CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS) {
+            *is_3d = 1;
+            return true;
+        }
+    }
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)tm};
-    cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *is_3d = 0;
     return r == CUDA_SUCCESS;
 }
 
@@ -206,7 +222,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.wait_limit_ns = g_wait_limit_ns;
 
     CUtensorMap map;
-    if (!encode_x_map(&map, x, M, K, P.tm)) return W4A16_ERR_INVALID_ARG;
+    if (!encode_x_map(&map, x, M, K, P.tm, P.ksub, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     switch (P.tm) {
         case 16: e = launch_tc<16, 4>(map, p, stream); break;

@@ -17,8 +17,8 @@
 //   warps 0-3           epilogue: TMEM -> registers -> FP16 Y, or FP32 partials + fix-up
 //   warps 4 .. 4+4K-1   dequant, KSUB groups of four warps (one per TMEM lane
 //                       quarter); group g unpacks sub-chunk g of every stage
-//   next warp           producer X: TMA of the X tiles and bulk copy of the scales
-//   next warp           producer W: bulk copy of the packed words
+//   next warp           producer X: TMA of the X tiles (one 3-D TMA per stage)
+//   next warp           producer W: bulk copies of the packed words and the scales
 //   last warp           MMA issuer (one elected lane) and TMEM owner
 //
 // Work split ("stream-K"): the iteration space (tile, stage) is cut into one
@@ -60,6 +60,7 @@ struct GemmParams {
     int iters;              // stages per tile = KC / KSUB
     long long total_iters;  // n_tiles * m_tiles * iters
     int grid;
+    int x_3d;               // X tensor map is 3-D {64, M, K/64}: one TMA per stage
     long long wait_limit_ns;
 };
 
@@ -201,8 +202,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 2);                    // the two producer warps
-            mbar_init(empty_bar(s), C::kDqWarps + 1);     // every dequant warp + MMA commit
+            mbar_init(full_bar(s), 2);  // the two producer warps
+            // Released by the MMA commit alone: the MMAs of a stage start only after
+            // every dequant warp has read its packed words.
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < A; ++a) {
             mbar_init(afull_bar(a), C::kDqWarps);
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) launch_dependents();
 
     const int cta = blockIdx.x;
     const long long it_begin = cta_begin(p, cta);
@@ -236,7 +240,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     // a whole phase ahead of a barrier (parity waits cannot tell p from p + 2).
     if (warp == C::kProdXWarp || warp == C::kProdWWarp) {
         // ------------------------------------------------------------ producers
+        // W streams packed words and scales, which no earlier kernel writes, so it
+        // starts at once; X may be the previous kernel's output, so the X producer
+        // first waits for that kernel to complete.
         const bool is_x = warp == C::kProdXWarp;
+        if (is_x) wait_prior_grid();
         uint32_t seq = 0;
         bool ok = true;
         for (long long i = it_begin; ok && i < it_end;) {
@@ -248,21 +256,26 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 if (lane == 0) {
                     const int k0 = kc * C::kStageK;
                     if (is_x) {
+                        mbar_arrive_expect_tx(full_bar(s), C::kXBytes);
+                        if (p.x_3d) {
+                            tma_load_3d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, full_bar(s), 0, mt * TM,
+                                        kc * KSUB);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < KSUB; ++j)
+                                tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * C::kXBlock, &tmap_x,
+                                            full_bar(s), k0 + j * kChunkK, mt * TM);
+                        }
+                    } else {
                         const int g0 = group_of(p, k0);
                         const int g1 = group_of(p, k0 + C::kStageK - 1);
                         const uint32_t sc_bytes = (uint32_t)(g1 - g0 + 1) * 256u;
-                        mbar_arrive_expect_tx(full_bar(s), C::kXBytes + sc_bytes);
-#pragma unroll
-                        for (int j = 0; j < KSUB; ++j)
-                            tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * C::kXBlock, &tmap_x, full_bar(s),
-                                        k0 + j * kChunkK, mt * TM);
-                        bulk_load(sbase + C::kOffSc + s * C::kScBytes, p.scales + ((size_t)nt * p.ng + g0) * kTileN,
-                                  sc_bytes, full_bar(s));
-                    } else {
-                        mbar_arrive_expect_tx(full_bar(s), C::kPkBytes);
+                        mbar_arrive_expect_tx(full_bar(s), C::kPkBytes + sc_bytes);
                         bulk_load(sbase + C::kOffPk + s * C::kPkBytes,
                                   p.packed + ((size_t)nt * p.KC + (size_t)kc * KSUB) * kChunkWords, C::kPkBytes,
                                   full_bar(s));
+                        bulk_load(sbase + C::kOffSc + s * C::kScBytes, p.scales + ((size_t)nt * p.ng + g0) * kTileN,
+                                  sc_bytes, full_bar(s));
                     }
                 }
                 __syncwarp();
@@ -360,8 +373,6 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 dequant_word(w1.y, s2hi, v + 20);
                 dequant_word(w1.z, s2hi, v + 24);
                 dequant_word(w1.w, s2hi, v + 28);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(s));
                 if (!wait_warp(aempty_bar(a), ((seq / A) & 1) ^ 1, ctl)) { ok = false; break; }
                 tc_fence_after();
                 tmem_st32(tmem + lane_base + C::kACol + a * C::kASlotCols + grp * 32, v);

@@ -19,8 +19,13 @@ cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t
     cfg.blockDim = dim3(TcCfg<TM, KSUB>::kThreads);
     cfg.dynamicSmemBytes = TcCfg<TM, KSUB>::kSmemBytes;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    // Programmatic dependent launch: the next kernel may start its prologue and
+    // weight stream while this one drains; it waits for this one before reading X.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB>, tmap, p);
 }
 
