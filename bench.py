@@ -288,20 +288,26 @@ def run_ours(args, rank, world):
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("kernel wait timed out during warm-up")
 
-    # ---- a pool of instrumented graphs (event node after every launch), replayed in turn
+    # ---- a pool of graphs, one step each, with an event node at every change of M
+    # (launches of one M overlap through programmatic dependent launch; an event
+    # node between two launches would serialise them)
+    bounds = [0] + [ci for ci in range(1, len(per_case)) if per_case[ci]["M"] != per_case[ci - 1]["M"]]
+    bounds.append(len(per_case))
     cap = torch.cuda.Stream()
     K = args.steps
     pool = min(K, 64)
     graphs, evs = [], []
     for gi in range(pool):
-        ev = [cud.event() for _ in range(len(per_case) + 1)]
+        ev = [cud.event() for _ in range(len(bounds))]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
             st = torch.cuda.current_stream()
             cud.record_external(ev[0], st)
-            for ci, c in enumerate(per_case):
-                w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
-                cud.record_external(ev[ci + 1], st)
+            for b in range(len(bounds) - 1):
+                for ci in range(bounds[b], bounds[b + 1]):
+                    c = per_case[ci]
+                    w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
+                cud.record_external(ev[b + 1], st)
         graphs.append(g)
         evs.append(ev)
     torch.cuda.synchronize()
@@ -336,26 +342,33 @@ def run_ours(args, rank, world):
     if status != w4a16.OK:
         raise RuntimeError("a kernel wait timed out in the timed region")
 
-    # ---- per-launch durations from the event nodes (the last `pool` steps of the timed region)
-    dur = np.zeros((pool, len(per_case)))
+    # ---- per-M durations from the event nodes (the last `pool` steps of the timed region)
+    grp_ms = np.zeros((pool, len(bounds) - 1))
     for gi in range(pool):
-        for ci in range(len(per_case)):
-            dur[gi, ci] = cud.elapsed_ms(evs[gi][ci], evs[gi][ci + 1])
-    mean_ms = dur.mean(axis=0)
+        for b in range(len(bounds) - 1):
+            grp_ms[gi, b] = cud.elapsed_ms(evs[gi][b], evs[gi][b + 1])
+    grp_mean = grp_ms.mean(axis=0)
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
     value = step_flops * world / (ms_step * 1e-3) / 1e12
 
-    # ---- per kernel instance and per M
+    # ---- per kernel instance (all launches of one M use one instance) and per M
     kernels = {}
-    for ci, c in enumerate(per_case):
-        path, tile_m, grid = w4a16.plan(c["M"], c["N"], c["K"], G)
+    per_m = {}
+    for b in range(len(bounds) - 1):
+        group = per_case[bounds[b]:bounds[b + 1]]
+        M = group[0]["M"]
+        path, tile_m, grid = w4a16.plan(M, group[0]["N"], group[0]["K"], G)
         name = "w4a16_tc_kernel<%d>" % tile_m
-        k = kernels.setdefault(name, dict(ms=0.0, bytes=0, flops=0, launches=0, t_roof=0.0))
-        k["ms"] += mean_ms[ci]
-        k["bytes"] += algorithmic_bytes(c["M"], c["K"], c["N"], G)
-        k["flops"] += flops(c["M"], c["K"], c["N"])
-        k["launches"] += 1
-        c["plan"] = (path, tile_m, grid)
+        k = kernels.setdefault(name, dict(ms=0.0, bytes=0, flops=0, launches=0))
+        k["ms"] += grp_mean[b]
+        k["bytes"] += sum(algorithmic_bytes(c["M"], c["K"], c["N"], G) for c in group)
+        k["flops"] += sum(flops(c["M"], c["K"], c["N"]) for c in group)
+        k["launches"] += len(group)
+        d = per_m.setdefault(M, dict(ms=0.0, fl=0, wb=0, roof_s=0.0))
+        d["ms"] += grp_mean[b]
+        d["fl"] += sum(flops(c["M"], c["K"], c["N"]) for c in group)
+        d["wb"] += sum(weight_bytes(c["K"], c["N"], G) for c in group)
+        d["roof_s"] += sum(roofline_seconds(c["M"], c["K"], c["N"], G, peaks) for c in group)
     dom_name = max(kernels, key=lambda n: kernels[n]["ms"])
     dom = kernels[dom_name]
     hbm_s = dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
@@ -375,13 +388,21 @@ def run_ours(args, rank, world):
     roof["avg_launch_us"] = dom["ms"] * 1e3 / dom["launches"]
     roof["peak_source"] = peaks["source"] + (" (HBM copy)" if roof["bound"] == "hbm" else " (bf16 burst)")
 
-    per_m = {}
-    for ci, c in enumerate(per_case):
-        d = per_m.setdefault(c["M"], dict(ms=0.0, fl=0, wb=0, roof_s=0.0))
-        d["ms"] += mean_ms[ci]
-        d["fl"] += flops(c["M"], c["K"], c["N"])
-        d["wb"] += weight_bytes(c["K"], c["N"], G)
-        d["roof_s"] += roofline_seconds(c["M"], c["K"], c["N"], G, peaks)
+    # ---- diagnostic, outside the timed region: every launch between two event nodes
+    diag = torch.cuda.CUDAGraph()
+    diag_ev = [cud.event() for _ in range(len(per_case) + 1)]
+    with torch.cuda.graph(diag, stream=cap):
+        st = torch.cuda.current_stream()
+        cud.record_external(diag_ev[0], st)
+        for ci, c in enumerate(per_case):
+            w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
+            cud.record_external(diag_ev[ci + 1], st)
+    mean_ms = np.zeros(len(per_case))
+    for r in range(8):
+        diag.replay()
+        torch.cuda.synchronize()
+        if r >= 3:
+            mean_ms += np.array([cud.elapsed_ms(diag_ev[ci], diag_ev[ci + 1]) for ci in range(len(per_case))]) / 5
 
     # ---- FP16-weight GEMM of the same shapes (cuBLAS through torch.matmul), same protocol
     fp16 = fp16_baseline(per_case, dev, reps=max(3, min(K, 50)))
@@ -412,14 +433,16 @@ def run_ours(args, rank, world):
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: every GEMM reads its own copy of the packed weights "
                          "(%.0f MB distinct per step vs 129 MB L2)" % (distinct_bytes / 1e6),
-                   "timing": "CUDA Graph per step with an event node after every launch; per-launch "
-                             "durations are the mean over the last %d steps of the timed region" % pool},
+                   "timing": "CUDA Graph per step with an event node at every change of M; per-kernel "
+                             "durations are the mean over the last %d steps of the timed region; "
+                             "per_case_isolated has an event node after every launch (outside the timed "
+                             "region), which removes the overlap of consecutive launches" % pool},
         "roofline": roof,
         "gpu_launches": K * len(per_case),
         "clocks": clocks,
         "e2e": e2e,
         "per_M": per_m_out,
-        "per_case": [{"M": c["M"], "K": c["K"], "N": c["N"], "us": float(mean_ms[ci] * 1e3),
+        "per_case_isolated": [{"M": c["M"], "K": c["K"], "N": c["N"], "us": float(mean_ms[ci] * 1e3),
                       "weight_gbs": weight_bytes(c["K"], c["N"], G) / (mean_ms[ci] * 1e-3) / 1e9,
                       "roofline_frac": roofline_seconds(c["M"], c["K"], c["N"], G, peaks) / (mean_ms[ci] * 1e-3)}
                      for ci, c in enumerate(per_case)],

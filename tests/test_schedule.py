@@ -37,7 +37,7 @@ def plan(M, N, K, G, sms=SMS):
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     iters = KC // ksub
     total = n_tiles * m_tiles * iters
-    grid = min(sms, MAX_GRID, total)
+    grid = max(1, min(sms, MAX_GRID, -(-total // 4)))
     return dict(tm=tm, ksub=ksub, m_tiles=m_tiles, n_tiles=n_tiles, KC=KC, iters=iters, ng=ng, total=total,
                 grid=grid)
 

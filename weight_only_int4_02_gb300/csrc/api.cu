@@ -34,6 +34,7 @@ constexpr size_t kCountersOff = 256;
 constexpr int kMaxGrid = 1024;
 constexpr size_t kPartialsOff = kCountersOff + 4 * kMaxGrid;
 constexpr int kMaxTileM = 256;
+constexpr int kMinItersPerCta = 4;
 
 struct DeviceState {
     bool ready = false;
@@ -84,8 +85,12 @@ Plan make_plan(int M, int N, int K, int G, int sms)
     P.iters = P.KC / P.ksub;
     P.ng = ceil_div(K, G);
     P.total = (long long)P.n_tiles * P.m_tiles * P.iters;
+    // One CTA per SM, but never fewer than kMinItersPerCta stages per CTA: below
+    // that, the split-K reduction of a tile gathers too many partials.
     long long grid = sms < kMaxGrid ? sms : kMaxGrid;
-    if (grid > P.total) grid = P.total;
+    const long long by_work = (P.total + kMinItersPerCta - 1) / kMinItersPerCta;
+    if (grid > by_work) grid = by_work;
+    if (grid < 1) grid = 1;
     P.grid = (int)grid;
     P.ws_bytes = ws_bytes_for(P.grid, P.tm);
     return P;

@@ -171,6 +171,43 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
     return g;
 }
 
+// Split-K fix-up of one output row n by the last contributor: the sum of every
+// contributor's FP32 partial, added in contributor (CTA) order. A round issues
+// LOADS loads (LOADS/NCP columns of NCP contributors) before any is added, so it
+// costs one global round trip.
+template <int TM, int NCP, int LOADS>
+__device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0, int n,
+                                           int n_in)
+{
+    constexpr int CPR = LOADS / NCP;
+    for (int col0 = 0; col0 < valid; col0 += CPR) {
+        float acc[CPR];
+#pragma unroll
+        for (int e = 0; e < CPR; ++e) acc[e] = 0.f;
+        for (int cc0 = c_lo; cc0 <= c_hi; cc0 += NCP) {
+            float v[NCP][CPR];
+#pragma unroll
+            for (int u = 0; u < NCP; ++u) {
+                const int cc = cc0 + u;
+                const float* src = p.partials + ((size_t)slot_of(p, min(cc, c_hi), t) * TM + col0) * kTileN + n_in;
+#pragma unroll
+                for (int e = 0; e < CPR; ++e)
+                    v[u][e] = (cc <= c_hi && col0 + e < valid) ? __ldcg(src + e * kTileN) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < NCP; ++u)
+#pragma unroll
+                for (int e = 0; e < CPR; ++e)
+                    if (cc0 + u <= c_hi) acc[e] += v[u][e];
+        }
+        if (n < p.N) {
+#pragma unroll
+            for (int e = 0; e < CPR; ++e)
+                if (col0 + e < valid) p.y[(size_t)(m0 + col0 + e) * p.N + n] = __float2half_rn(acc[e]);
+        }
+    }
+}
+
 template <int TM, int KSUB>
 __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
@@ -415,7 +452,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) part[(size_t)(c * 16 + e) * kTileN] = __uint_as_float(r[e]);
+                    for (int e = 0; e < 16; ++e)
+                        if (c * 16 + e < valid) part[(size_t)(c * 16 + e) * kTileN] = __uint_as_float(r[e]);
                 }
             }
             tc_fence_before();
@@ -441,36 +479,17 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 const int last = *last_flag;
                 if (last) {
                     __threadfence();
-                    for (int c = 0; c < chunks; ++c) {
-                        float acc[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-                        int cc = c_lo;
-                        for (; cc + 1 <= c_hi; cc += 2) {   // two contributors' loads in flight
-                            const float* s0 = p.partials + ((size_t)slot_of(p, cc, t) * TM + c * 16) * kTileN + n_in;
-                            const float* s1 =
-                                p.partials + ((size_t)slot_of(p, cc + 1, t) * TM + c * 16) * kTileN + n_in;
-                            float v0[16], v1[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v0[e] = __ldcg(s0 + e * kTileN);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v1[e] = __ldcg(s1 + e * kTileN);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) acc[e] = (acc[e] + v0[e]) + v1[e];
-                        }
-                        if (cc <= c_hi) {
-                            const float* s0 = p.partials + ((size_t)slot_of(p, cc, t) * TM + c * 16) * kTileN + n_in;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) acc[e] += __ldcg(s0 + e * kTileN);
-                        }
-                        if (n < p.N) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = m0 + c * 16 + e;
-                                if (m < p.M) p.y[(size_t)m * p.N + n] = __float2half_rn(acc[e]);
-                            }
-                        }
-                    }
+                    const int ncontrib = c_hi - c_lo + 1;
+                    // 16 loads per round where 23 warps cap registers at 80, else 32.
+                    constexpr int L = KSUB == 4 ? 16 : 32;
+                    if (ncontrib <= 2)
+                        fix_reduce<TM, 2, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                    else if (ncontrib <= 4)
+                        fix_reduce<TM, 4, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                    else if (ncontrib <= 8)
+                        fix_reduce<TM, 8, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                    else
+                        fix_reduce<TM, 16, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
                 }
                 named_bar_sync(1, 128);
             }
