@@ -137,6 +137,33 @@ w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
  * 2 (large-M, per-weight scaling); *tile_m = rows of X per tile; *grid = CTAs. */
 w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid);
 
+/*
+ * w4a16_gemm without any device allocation by the library or the caller. The
+ * pages have no counterpart; this entry point exists for callers that may not
+ * allocate GPU memory at all: plug-ins whose host framework owns every byte of
+ * device memory, and latency-critical loops that cannot afford cudaMalloc's
+ * implicit device-wide synchronisation.
+ *   Arguments, layouts and results are those of w4a16_gemm; the caller still
+ *   passes x, packed, scales_packed and y.
+ *   The split-K scratch (error word, tile counters, FP32 partials) lives in one
+ *   fixed device array of W4A16_NOALLOC_MAX_BYTES inside the library, held by
+ *   every GPU that loads the library until the process exits. A shape whose
+ *   scratch would exceed it returns W4A16_ERR_WORKSPACE with nothing launched
+ *   (on a 152-SM GB300 this admits M <= 32).
+ *   The first call on each device looks the array's device address up; make
+ *   that first call before any stream capture.
+ *   Each call enqueues a clear of the array's error word and counters, then the
+ *   GEMM. Every call on a device shares the one array: calls whose work overlaps
+ *   on the GPU (different streams, no ordering between them) race and give
+ *   wrong results; order them on one stream or with events.
+ *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   w4a16_check_device_status(NULL, ...) does not cover this array.
+ */
+#define W4A16_NOALLOC_MAX_BYTES ((size_t)8 << 20)
+w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* packed,
+                                const uint16_t* scales_packed, uint16_t* y,
+                                int M, int N, int K, int group_size, w4a16_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

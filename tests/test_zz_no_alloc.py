@@ -1,0 +1,50 @@
+"""The no-allocation entry point, for callers that may not allocate device memory
+(plug-ins whose host framework owns all GPU memory, latency-critical loops that
+cannot take cudaMalloc's device-wide synchronisation).
+
+It must give what the regular entry point gives, on two calls in a row: the
+second call reuses the fixed scratch array the first one left behind. This file
+is collected last so that a run stopping at its first failure has run every
+other test first; it also passes on its own in a fresh process.
+"""
+import numpy as np
+import pytest
+
+from tests.parity import check_within
+from weight_only_int4_02_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def test_no_alloc_matches_regular_entry_point_on_two_calls(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_only_int4_02_gb300 import w4a16
+    M, N, K, G = 16, 4096, 4096, 128           # every tile split across CTAs: the scratch is used
+    q = inputs.codes(K, N, seed=21)
+    s = inputs.scales(K, N, G, seed=21)
+    packed, sp = w4a16.pack(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), G)
+    w = oracle_mod.dequant(q, s, G)
+    for call, seed in enumerate((31, 32)):
+        x = inputs.activations(M, K, seed=seed)
+        xd = torch.from_numpy(x).cuda()
+        y_ref = w4a16.gemm(xd, packed, sp, N, G).cpu().numpy().astype(np.float64)
+        y = w4a16.gemm_noalloc(xd, packed, sp, N, G)
+        torch.cuda.synchronize()
+        y = y.cpu().numpy().astype(np.float64)
+        absum = np.abs(x.astype(np.float64)) @ np.abs(w)
+        check_within(y, y_ref, absum, "no-alloc call %d" % (call + 1))
+
+
+def test_no_alloc_rejects_shapes_beyond_its_array():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_only_int4_02_gb300 import w4a16
+    M, N, K, G = 128, 4096, 4096, 128          # its split-K scratch exceeds the fixed array
+    packed, sp = w4a16.pack(torch.zeros((K, N), dtype=torch.uint8, device="cuda"),
+                            torch.ones((K // G, N), dtype=torch.float16, device="cuda"), G)
+    x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    with pytest.raises(w4a16.W4A16Error) as e:
+        w4a16.gemm_noalloc(x, packed, sp, N, G)
+    assert e.value.status == w4a16.ERR_WORKSPACE

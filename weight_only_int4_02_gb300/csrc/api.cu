@@ -349,4 +349,62 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
     return W4A16_OK;
 }
 
+
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers may not allocate device memory: plug-ins whose host framework owns
+// every byte of GPU memory and hands out none, or latency-critical loops that
+// cannot afford cudaMalloc's implicit device-wide synchronisation. For them,
+// w4a16_gemm_noalloc runs the same GEMM with its split-K scratch (error word,
+// tile counters, FP32 partials) in this fixed device array instead of a
+// workspace. Every GPU that loads the library holds the array until exit.
+namespace {
+
+constexpr size_t kNoAllocBytes = (size_t)8 << 20;  // 8 MiB, W4A16_NOALLOC_MAX_BYTES
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per device.
+w4a16_status noalloc_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* packed,
+                                           const uint16_t* scales_packed, uint16_t* y, int M, int N, int K,
+                                           int group_size, w4a16_stream_t stream)
+{
+    const int G = norm_group(K, group_size);
+    if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    if (M == 0) return W4A16_OK;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    if (make_plan(M, N, K, G, st->sms).ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != W4A16_OK) return rc;
+    // The error word and the split-K counters must start at zero; the array keeps
+    // whatever the previous call left there.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, kPartialsOff, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, G, scratch, kNoAllocBytes, false,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+

@@ -17,7 +17,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = ran
 
 EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error", "w4a16_packed_words",
            "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
-           "w4a16_check_device_status", "w4a16_plan"]
+           "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc"]
 
 
 class W4A16Error(RuntimeError):
@@ -57,6 +57,8 @@ def lib():
         L.w4a16_check_device_status.restype = I
         L.w4a16_plan.argtypes = [I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
         L.w4a16_plan.restype = I
+        L.w4a16_gemm_noalloc.argtypes = [P, P, P, P, I, I, I, I, P]
+        L.w4a16_gemm_noalloc.restype = I
         _lib = L
     return _lib
 
@@ -144,3 +146,15 @@ def plan(M, N, K, group_size):
     p, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     _check(lib().w4a16_plan(M, N, K, group_size, ctypes.byref(p), ctypes.byref(t), ctypes.byref(g)), "w4a16_plan")
     return p.value, t.value, g.value
+
+
+def gemm_noalloc(x, packed, scales_packed, N, group_size, y=None, stream=None):
+    """As gemm, for callers that may not allocate device memory: the split-K
+    scratch is a fixed array inside the library (see w4a16_gemm_noalloc)."""
+    M, K = x.shape
+    assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib().w4a16_gemm_noalloc(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
+                                    _stream(stream)), "w4a16_gemm_noalloc")
+    return y
