@@ -557,6 +557,44 @@ def run_reference(args):
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """One GEMM shape, launched back to back from a CUDA Graph over rotating copies
+    of the packed weights (more bytes than L2); prints the mean time per launch.
+    Used as the small, repeatable command for profiling single kernels."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    M, K, N = (int(v) for v in args.case.split(","))
+    G = 128
+    q = inputs.codes(K, N, 0)
+    s = inputs.scales(K, N, G, 0)
+    packed, sp = w4a16.pack(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), G)
+    wbytes = packed.numel() * 4 + sp.numel() * 2
+    copies = [(packed.clone(), sp.clone()) for _ in range(max(2, int(400e6 // wbytes) + 1))]
+    x = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    for c in copies:
+        w4a16.gemm(x, c[0], c[1], N, G, y=y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        for r in range(args.reps):
+            c = copies[r % len(copies)]
+            w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / args.reps
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    print(json.dumps({"case": [M, K, N], "us_per_launch": us, "weight_gbs": wbytes / us / 1e3,
+                      "tflops": flops(M, K, N) / us / 1e6, "plan": w4a16.plan(M, N, K, G),
+                      "launches_before_timed": len(copies) + args.reps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -565,12 +603,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, help="M,K,N: time one GEMM shape (profiling aid)")
+    ap.add_argument("--reps", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 
+    if args.case:
+        run_case(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)

@@ -156,13 +156,13 @@ w4a16_status own_workspace(DeviceState* st, void** ws, size_t* bytes)
 // X as a 3-D view {64, M, K/64} (strides K*2 and 128 bytes) when K is a multiple of
 // 64, so one TMA brings a stage's KSUB blocks of 64 columns; else the plain 2-D
 // map {K, M}, one TMA per block, with the ragged K edge zero-filled.
-bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int tm, int ksub, int* is_3d)
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int ksub, int* is_3d)
 {
     cuuint32_t estr[3] = {1, 1, 1};
     if (K % kChunkK == 0) {
         cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)M, (cuuint64_t)(K / kChunkK)};
         cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kChunkK * 2};
-        cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)tm, (cuuint32_t)ksub};
+        cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)rows, (cuuint32_t)ksub};
         CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -173,7 +173,7 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int tm, int ksu
     }
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)tm};
+    cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)rows};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -227,7 +227,10 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.wait_limit_ns = g_wait_limit_ns;
 
     CUtensorMap map;
-    if (!encode_x_map(&map, x, M, K, P.tm, P.ksub, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
+    // With one row tile, a box of M rows rounded up to the 8-row swizzle atom is
+    // enough: MMA rows past M feed only output columns that are never stored.
+    p.x_rows = P.m_tiles == 1 ? ((M + 7) / 8) * 8 : P.tm;
+    if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     switch (P.tm) {
         case 16: e = launch_tc<16, 4>(map, p, stream); break;

@@ -15,8 +15,9 @@
 //
 // Warp roles (32 * (7 + 4*KSUB) threads):
 //   warps 0-3           epilogue: TMEM -> registers -> FP16 Y, or FP32 partials + fix-up
-//   warps 4 .. 4+4K-1   dequant, KSUB groups of four warps (one per TMEM lane
-//                       quarter); group g unpacks sub-chunk g of every stage
+//   warps 4 .. 4+4K-1   dequant, two teams taking alternate stages; a team has
+//                       KSUB/2 groups of four warps (one per TMEM lane quarter),
+//                       group g unpacking sub-chunks 2g and 2g+1 of its stages
 //   next warp           producer X: TMA of the X tiles (one 3-D TMA per stage)
 //   next warp           producer W: bulk copies of the packed words and the scales
 //   last warp           MMA issuer (one elected lane) and TMEM owner
@@ -61,6 +62,8 @@ struct GemmParams {
     long long total_iters;  // n_tiles * m_tiles * iters
     int grid;
     int x_3d;               // X tensor map is 3-D {64, M, K/64}: one TMA per stage
+    int x_rows;             // rows of X each TMA box brings (<= TM, a multiple of 8); the
+                            // MMA's B rows past them feed only output columns >= M
     long long wait_limit_ns;
 };
 
@@ -71,9 +74,13 @@ struct TcCfg {
     static constexpr int kXBytes = KSUB * kXBlock;
     static constexpr int kPkBytes = KSUB * kChunkBytes;
     static constexpr int kScBytes = 2 * KSUB * 256;       // G = 32 puts 2*KSUB groups in a stage
-    static constexpr int kStageBytes = kXBytes + kPkBytes + kScBytes;
-    static constexpr int kStagesRaw = (220 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    // Two rings in shared memory: W (packed words + scales), freed by the dequant
+    // warps once they hold their words, so the HBM stream never waits on the MMA;
+    // and X, freed by the MMA's commit.
+    static constexpr int kWStageBytes = kPkBytes + kScBytes;
+    static constexpr int kWStages = (TM <= 32 || KSUB == 2) ? 8 : 6;  // even (two dequant teams)
+    static constexpr int kXFit = (220 * 1024 - kWStages * kWStageBytes) / kXBytes;
+    static constexpr int kXStages = kXFit > 8 ? 8 : kXFit;
     static constexpr int kDqWarps = 4 * KSUB;
     static constexpr int kDqWarp0 = 4;
     static constexpr int kProdXWarp = kDqWarp0 + kDqWarps;
@@ -83,21 +90,24 @@ struct TcCfg {
     static constexpr int kDBufs = TM <= 128 ? 2 : 1;
     static constexpr int kASlotCols = KSUB * 32;          // 16-bit A values, two per column
     static constexpr int kAFit = (512 - kDBufs * TM) / kASlotCols;
-    static constexpr int kAStages = kAFit > 4 ? 4 : kAFit;
+    static constexpr int kAStages = kAFit >= 4 ? 4 : 2;               // even (two dequant teams)
     static constexpr int kACol = 0;
     static constexpr int kDCol = kAStages * kASlotCols;
     static constexpr int kTmemCols = 512;
     // shared memory layout, offsets from a 1024-aligned base
     static constexpr int kOffX = 0;
-    static constexpr int kOffPk = kOffX + kStages * kXBytes;
-    static constexpr int kOffSc = kOffPk + kStages * kPkBytes;
-    static constexpr int kOffBar = kOffSc + kStages * kScBytes;
-    // barriers: full[S], empty[S], afull[A], aempty[A], dfull[2], dempty[2], teardown
-    static constexpr int kNumBars = 2 * kStages + 2 * kAStages + 4 + 1;
+    static constexpr int kOffPk = kOffX + kXStages * kXBytes;
+    static constexpr int kOffSc = kOffPk + kWStages * kPkBytes;
+    static constexpr int kOffBar = kOffSc + kWStages * kScBytes;
+    // barriers: wfull[SW], wempty[SW], xfull[SX], xempty[SX], afull[A], aempty[A],
+    // dfull[2], dempty[2], teardown
+    static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kAStages + 4 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(kXBlock % 1024 == 0, "X blocks must stay 1024-byte aligned");
-    static_assert(kStages >= 2 && kAStages >= 2, "pipeline depth");
+    static_assert(kWStages >= 2 && kXStages >= 2 && kAStages >= 2, "pipeline depth");
+    static_assert(kWStages % 2 == 0 && kAStages % 2 == 0, "rings shared by two alternating dequant teams");
+    static_assert(KSUB % 2 == 0, "a dequant warp unpacks two sub-chunks");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert(kDCol + kDBufs * TM <= 512, "tensor memory");
     static_assert(kKPad % KSUB == 0, "stages must tile the padded K");
@@ -213,7 +223,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
     using C = TcCfg<TM, KSUB>;
-    constexpr int S = C::kStages;
+    constexpr int SW = C::kWStages;
+    constexpr int SX = C::kXStages;
     constexpr int A = C::kAStages;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled X tiles.
@@ -222,13 +233,16 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     const uint32_t sbase = smem_addr(smem);
 
     const uint32_t bar0 = sbase + C::kOffBar;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * S + A + a); };
-    auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 * A + d); };
-    auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 * A + 2 + d); };
-    const uint32_t teardown_bar = bar0 + 8u * (2 * S + 2 * A + 4);
+    auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (SW + s); };
+    auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * SW + s); };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (2 * SW + SX + s); };
+    constexpr int kB1 = 2 * SW + 2 * SX;
+    auto afull_bar = [&](int a) { return bar0 + 8u * (kB1 + a); };
+    auto aempty_bar = [&](int a) { return bar0 + 8u * (kB1 + A + a); };
+    auto dfull_bar = [&](int d) { return bar0 + 8u * (kB1 + 2 * A + d); };
+    auto dempty_bar = [&](int d) { return bar0 + 8u * (kB1 + 2 * A + 2 + d); };
+    const uint32_t teardown_bar = bar0 + 8u * (kB1 + 2 * A + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16);
@@ -238,14 +252,16 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 2);  // the two producer warps
-            // Released by the MMA commit alone: the MMAs of a stage start only after
-            // every dequant warp has read its packed words.
-            mbar_init(empty_bar(s), 1);
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(wfull_bar(s), 1);
+            mbar_init(wempty_bar(s), 2 * KSUB);      // the stage's dequant team, once it holds its words
+        }
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xempty_bar(s), 1);             // the MMA commit
         }
         for (int a = 0; a < A; ++a) {
-            mbar_init(afull_bar(a), C::kDqWarps);
+            mbar_init(afull_bar(a), 2 * KSUB);       // the stage's dequant team
             mbar_init(aempty_bar(a), 1);
         }
         for (int d = 0; d < 2; ++d) {
@@ -282,6 +298,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         // first waits for that kernel to complete.
         const bool is_x = warp == C::kProdXWarp;
         if (is_x) wait_prior_grid();
+        const int S = is_x ? SX : SW;
         uint32_t seq = 0;
         bool ok = true;
         for (long long i = it_begin; ok && i < it_end;) {
@@ -289,30 +306,31 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
             const int nt = g.t / p.m_tiles, mt = g.t - nt * p.m_tiles;
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
                 const int s = (int)(seq % S);
-                if (!wait_warp(empty_bar(s), ((seq / S) & 1) ^ 1, ctl)) { ok = false; break; }
+                const uint32_t empty = is_x ? xempty_bar(s) : wempty_bar(s);
+                if (!wait_warp(empty, ((seq / S) & 1) ^ 1, ctl)) { ok = false; break; }
                 if (lane == 0) {
                     const int k0 = kc * C::kStageK;
                     if (is_x) {
-                        mbar_arrive_expect_tx(full_bar(s), C::kXBytes);
+                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(KSUB * p.x_rows * 128));
                         if (p.x_3d) {
-                            tma_load_3d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, full_bar(s), 0, mt * TM,
+                            tma_load_3d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, xfull_bar(s), 0, mt * TM,
                                         kc * KSUB);
                         } else {
 #pragma unroll
                             for (int j = 0; j < KSUB; ++j)
-                                tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * C::kXBlock, &tmap_x,
-                                            full_bar(s), k0 + j * kChunkK, mt * TM);
+                                tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
+                                            xfull_bar(s), k0 + j * kChunkK, mt * TM);
                         }
                     } else {
                         const int g0 = group_of(p, k0);
                         const int g1 = group_of(p, k0 + C::kStageK - 1);
                         const uint32_t sc_bytes = (uint32_t)(g1 - g0 + 1) * 256u;
-                        mbar_arrive_expect_tx(full_bar(s), C::kPkBytes + sc_bytes);
+                        mbar_arrive_expect_tx(wfull_bar(s), C::kPkBytes + sc_bytes);
                         bulk_load(sbase + C::kOffPk + s * C::kPkBytes,
                                   p.packed + ((size_t)nt * p.KC + (size_t)kc * KSUB) * kChunkWords, C::kPkBytes,
-                                  full_bar(s));
+                                  wfull_bar(s));
                         bulk_load(sbase + C::kOffSc + s * C::kScBytes, p.scales + ((size_t)nt * p.ng + g0) * kTileN,
-                                  sc_bytes, full_bar(s));
+                                  sc_bytes, wfull_bar(s));
                     }
                 }
                 __syncwarp();
@@ -324,7 +342,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
             const uint32_t inflight = seq < (uint32_t)S ? seq : (uint32_t)S;
             for (uint32_t k = 1; k <= inflight; ++k) {
                 const uint32_t q = seq - k;
-                wait_drain(full_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
+                wait_drain(is_x ? xfull_bar((int)(q % S)) : wfull_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
             }
         }
     } else if (warp == C::kMmaWarp) {
@@ -340,9 +358,9 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + C::kDCol + d * TM;
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
-                const int s = (int)(seq % S);
+                const int s = (int)(seq % SX);
                 const int a = (int)(seq % A);
-                if (!wait_warp(full_bar(s), (seq / S) & 1, ctl) || !wait_warp(afull_bar(a), (seq / A) & 1, ctl)) {
+                if (!wait_warp(xfull_bar(s), (seq / SX) & 1, ctl) || !wait_warp(afull_bar(a), (seq / A) & 1, ctl)) {
                     ok = false;
                     break;
                 }
@@ -351,17 +369,18 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                     const uint64_t b0 = smem_desc_k_sw128(sbase + C::kOffX + s * C::kXBytes);
                     const uint32_t a0 = tmem + C::kACol + a * C::kASlotCols;
                     // The descriptor's start address counts 16-byte units: +2 per 16 K values
-                    // inside a 128-byte row, +kXBlock/16 per 64-wide K block.
+                    // inside a 128-byte row, +x_rows*128/16 per 64-wide K block (blocks of
+                    // x_rows rows sit back to back, each 1024-byte aligned).
 #pragma unroll
                     for (int j = 0; j < KSUB; ++j) {
 #pragma unroll
                         for (int kk = 0; kk < kChunkK / 16; ++kk) {
-                            const uint64_t bd = b0 + (uint64_t)(j * (C::kXBlock >> 4) + kk * 2);
+                            const uint64_t bd = b0 + (uint64_t)(j * p.x_rows * 8 + kk * 2);
                             mma_f16_ts(d_tmem, a0 + j * 32 + kk * 8, bd, idesc,
                                        (kc > g.kb || j > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    mma_commit(empty_bar(s));
+                    mma_commit(xempty_bar(s));
                     mma_commit(aempty_bar(a));
                 }
                 __syncwarp();
@@ -379,7 +398,14 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         }
     } else if (warp >= C::kDqWarp0) {
         // ------------------------------------------------------------ dequant
-        const int grp = (warp - C::kDqWarp0) >> 2;   // sub-chunk of every stage this group unpacks
+        // Two teams take alternate stages, so one team's waits overlap the other's
+        // arithmetic. Within a team, group gi unpacks sub-chunks 2gi and 2gi+1.
+        // Ring depths are even: a ring slot's successive uses all fall to one team,
+        // which visits its stages in order (no waiter is a whole phase ahead).
+        constexpr int kWarpsPerTeam = 2 * KSUB;
+        const int dw = warp - C::kDqWarp0;
+        const int team = dw / kWarpsPerTeam;
+        const int gi = (dw % kWarpsPerTeam) >> 2;
         const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
         const int n_in = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -388,31 +414,47 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         for (long long i = it_begin; ok && i < it_end;) {
             const Segment g = segment_at(p, i, it_end);
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
-                const int s = (int)(seq % S);
+                if ((int)(seq & 1) != team) continue;
+                const int s = (int)(seq % SW);
                 const int a = (int)(seq % A);
-                if (!wait_warp(full_bar(s), (seq / S) & 1, ctl)) { ok = false; break; }
-                const uint8_t* pk = smem + C::kOffPk + s * C::kPkBytes + grp * kChunkBytes + n_in * 16;
-                const uint4 w0 = *reinterpret_cast<const uint4*>(pk);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(pk + kTileN * 16);
-                const int k0 = kc * C::kStageK + grp * kChunkK;
+                if (!wait_warp(wfull_bar(s), (seq / SW) & 1, ctl)) { ok = false; break; }
                 const int gs = group_of(p, kc * C::kStageK);
                 const __half* sc = reinterpret_cast<const __half*>(smem + C::kOffSc + s * C::kScBytes) + n_in;
-                const __half s_lo = sc[(group_of(p, k0) - gs) * kTileN];
-                const __half s_hi = sc[(group_of(p, k0 + 32) - gs) * kTileN];
-                const __half2 s2lo = __halves2half2(s_lo, s_lo);
-                const __half2 s2hi = __halves2half2(s_hi, s_hi);
-                uint32_t v[32];
-                dequant_word(w0.x, s2lo, v + 0);
-                dequant_word(w0.y, s2lo, v + 4);
-                dequant_word(w0.z, s2lo, v + 8);
-                dequant_word(w0.w, s2lo, v + 12);
-                dequant_word(w1.x, s2hi, v + 16);
-                dequant_word(w1.y, s2hi, v + 20);
-                dequant_word(w1.z, s2hi, v + 24);
-                dequant_word(w1.w, s2hi, v + 28);
-                if (!wait_warp(aempty_bar(a), ((seq / A) & 1) ^ 1, ctl)) { ok = false; break; }
-                tc_fence_after();
-                tmem_st32(tmem + lane_base + C::kACol + a * C::kASlotCols + grp * 32, v);
+                uint4 w[2][2];
+                __half2 s2[2][2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = 2 * gi + h;
+                    const uint8_t* pk = smem + C::kOffPk + s * C::kPkBytes + j * kChunkBytes + n_in * 16;
+                    w[h][0] = *reinterpret_cast<const uint4*>(pk);
+                    w[h][1] = *reinterpret_cast<const uint4*>(pk + kTileN * 16);
+                    const int k0 = kc * C::kStageK + j * kChunkK;
+                    const __half s_lo = sc[(group_of(p, k0) - gs) * kTileN];
+                    const __half s_hi = sc[(group_of(p, k0 + 32) - gs) * kTileN];
+                    s2[h][0] = __halves2half2(s_lo, s_lo);
+                    s2[h][1] = __halves2half2(s_hi, s_hi);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wempty_bar(s));   // words and scales are in registers
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    dequant_word(w[h][0].x, s2[h][0], v + 0);
+                    dequant_word(w[h][0].y, s2[h][0], v + 4);
+                    dequant_word(w[h][0].z, s2[h][0], v + 8);
+                    dequant_word(w[h][0].w, s2[h][0], v + 12);
+                    dequant_word(w[h][1].x, s2[h][1], v + 16);
+                    dequant_word(w[h][1].y, s2[h][1], v + 20);
+                    dequant_word(w[h][1].z, s2[h][1], v + 24);
+                    dequant_word(w[h][1].w, s2[h][1], v + 28);
+                    if (h == 0) {
+                        // the A slot is free once the MMAs that read it two stages ago completed
+                        if (!wait_warp(aempty_bar(a), ((seq / A) & 1) ^ 1, ctl)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    tmem_st32(tmem + lane_base + C::kACol + a * C::kASlotCols + (2 * gi + h) * 32, v);
+                }
+                if (!ok) break;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull_bar(a));
