@@ -184,31 +184,35 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
 // Split-K fix-up of one output row n by the last contributor: the sum of every
 // contributor's FP32 partial, added in contributor (CTA) order. A round issues
 // LOADS loads (LOADS/NCP columns of NCP contributors) before any is added, so it
-// costs one global round trip.
+// costs one global round trip. When own_tmem is nonzero the last contributor's
+// own partial is read from its TMEM accumulator (own_c is its CTA index) instead
+// of from global memory.
 template <int TM, int NCP, int LOADS>
 __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0, int n,
-                                           int n_in)
+                                           int n_in, int own_c, uint32_t own_tmem)
 {
     constexpr int CPR = LOADS / NCP;
+    static_assert(TM % CPR == 0, "a round's columns stay inside the tile");
     for (int col0 = 0; col0 < valid; col0 += CPR) {
-        float acc[CPR];
+        float acc[CPR], own[CPR];
 #pragma unroll
         for (int e = 0; e < CPR; ++e) acc[e] = 0.f;
+        if (own_tmem) tmem_ld_f32<CPR>(own_tmem + col0, own);
         for (int cc0 = c_lo; cc0 <= c_hi; cc0 += NCP) {
             float v[NCP][CPR];
 #pragma unroll
             for (int u = 0; u < NCP; ++u) {
                 const int cc = cc0 + u;
+                const bool remote = cc <= c_hi && !(own_tmem && cc == own_c);
                 const float* src = p.partials + ((size_t)slot_of(p, min(cc, c_hi), t) * TM + col0) * kTileN + n_in;
 #pragma unroll
-                for (int e = 0; e < CPR; ++e)
-                    v[u][e] = (cc <= c_hi && col0 + e < valid) ? __ldcg(src + e * kTileN) : 0.f;
+                for (int e = 0; e < CPR; ++e) v[u][e] = (remote && col0 + e < valid) ? __ldcg(src + e * kTileN) : 0.f;
             }
 #pragma unroll
             for (int u = 0; u < NCP; ++u)
 #pragma unroll
                 for (int e = 0; e < CPR; ++e)
-                    if (cc0 + u <= c_hi) acc[e] += v[u][e];
+                    if (cc0 + u <= c_hi) acc[e] += (own_tmem && cc0 + u == own_c) ? own[e] : v[u][e];
         }
         if (n < p.N) {
 #pragma unroll
@@ -498,9 +502,18 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                         if (c * 16 + e < valid) part[(size_t)(c * 16 + e) * kTileN] = __uint_as_float(r[e]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dempty_bar(d));
+            // With two D buffers and wide tiles, a split tile keeps its accumulator
+            // until the fix-up is done (the last contributor reads its own partial
+            // back from TMEM); with one buffer the next tile's MMAs need it at once,
+            // and the narrow memory-bound tiles have few valid rows to reduce.
+            constexpr bool kHoldable = C::kDBufs == 2 && KSUB == 2;
+            const bool hold = split && kHoldable;
+            const int d_used = d;
+            if (!hold) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dempty_bar(d));
+            }
             if (++d == C::kDBufs) { d = 0; dph ^= 1; }
             i += g.ke - g.kb;
 
@@ -524,16 +537,31 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                     const int ncontrib = c_hi - c_lo + 1;
                     // 16 loads per round where 23 warps cap registers at 80, else 32.
                     constexpr int L = KSUB == 4 ? 16 : 32;
-                    if (ncontrib <= 2)
-                        fix_reduce<TM, 2, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                    const uint32_t own = hold ? d_tmem : 0u;
+                    if constexpr (!kHoldable) {
+                        if (ncontrib <= 2)
+                            fix_reduce<TM, 2, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                        else if (ncontrib <= 4)
+                            fix_reduce<TM, 4, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                        else if (ncontrib <= 8)
+                            fix_reduce<TM, 8, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                        else
+                            fix_reduce<TM, 16, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                    } else if (ncontrib <= 2)
+                        fix_reduce<TM, 2, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                     else if (ncontrib <= 4)
-                        fix_reduce<TM, 4, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                        fix_reduce<TM, 4, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                     else if (ncontrib <= 8)
-                        fix_reduce<TM, 8, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                        fix_reduce<TM, 8, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                     else
-                        fix_reduce<TM, 16, L>(p, t, c_lo, c_hi, valid, m0, n, n_in);
+                        fix_reduce<TM, 16, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                 }
                 named_bar_sync(1, 128);
+                if (hold) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty_bar(d_used));
+                }
             }
         }
     }

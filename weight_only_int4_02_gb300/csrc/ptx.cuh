@@ -218,6 +218,49 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "memory");
 }
 
+// Each lane of the warp reads N (1..32, a power of two) consecutive 32-bit columns
+// of its own TMEM lane, as floats.
+template <int N>
+__device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float (&v)[N])
+{
+    uint32_t r[N];
+    if constexpr (N == 1) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]) : "r"(taddr) : "memory");
+    } else if constexpr (N == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];\n\ttcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
+    } else if constexpr (N == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\ttcgen05.wait::ld.sync.aligned;"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
+    } else if constexpr (N == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\ttcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+            : "r"(taddr)
+            : "memory");
+    } else {
+        static_assert(N % 16 == 0 && N <= 32, "tmem_ld_f32 width");
+#pragma unroll
+        for (int c = 0; c < N / 16; ++c) {
+            uint32_t q[16];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+                "tcgen05.wait::ld.sync.aligned;"
+                : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]),
+                  "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]),
+                  "=r"(q[15])
+                : "r"(taddr + c * 16)
+                : "memory");
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[c * 16 + e] = q[e];
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = __uint_as_float(r[e]);
+}
+
 // Each lane of the warp writes 16 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
