@@ -33,30 +33,34 @@ def tile_m_for(M):
 def plan(M, N, K, G, sms=SMS):
     tm = tile_m_for(M)
     ksub = 4 if tm <= 64 else 2
+    cl = 2 if tm >= 64 else 1
     m_tiles, n_tiles, ng = ceil_div(M, tm), ceil_div(N, 128), ceil_div(K, G)
+    n_blocks = ceil_div(n_tiles, cl)
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     iters = KC // ksub
-    total = n_tiles * m_tiles * iters
-    grid = max(1, min(sms, MAX_GRID, -(-total // 4)))
-    return dict(tm=tm, ksub=ksub, m_tiles=m_tiles, n_tiles=n_tiles, KC=KC, iters=iters, ng=ng, total=total,
-                grid=grid)
+    total = n_blocks * m_tiles * iters
+    min_iters = max(4, iters // 2 if tm >= 64 else (iters // 4 if tm == 32 else 0))
+    units = max(1, min(min(sms, MAX_GRID) // cl, -(-total // min_iters)))
+    return dict(tm=tm, ksub=ksub, cl=cl, m_tiles=m_tiles, n_tiles=n_tiles, n_blocks=n_blocks, KC=KC,
+                iters=iters, ng=ng, total=total, units=units, grid=units * cl)
 
 
 def cta_begin(P, c):
-    return c * P["total"] // P["grid"]
+    return c * P["total"] // P["units"]
 
 
 def cta_of(P, i):
-    c = (i * P["grid"]) // P["total"]
-    while c + 1 < P["grid"] and cta_begin(P, c + 1) <= i:
+    c = (i * P["units"]) // P["total"]
+    while c + 1 < P["units"] and cta_begin(P, c + 1) <= i:
         c += 1
     while c > 0 and cta_begin(P, c) > i:
         c -= 1
     return c
 
 
-def slot_of(P, c, t):
-    return 2 * c if cta_begin(P, c) >= t * P["iters"] else 2 * c + 1
+def slot_of(P, c, t, rank):
+    cta = c * P["cl"] + rank
+    return 2 * cta if cta_begin(P, c) >= t * P["iters"] else 2 * cta + 1
 
 
 def segments(P, c):
@@ -70,48 +74,54 @@ def segments(P, c):
 
 
 def check_shape(M, N, K, G, sms=SMS):
+    """Every (weight tile, stage) is computed once; every global access of the
+    producers, the partial slots and the counters stays inside its buffer; the
+    reducer of a split tile reads exactly the slots its contributors wrote."""
     P = plan(M, N, K, G, sms)
-    KC, ng, tm, ks, iters = P["KC"], P["ng"], P["tm"], P["ksub"], P["iters"]
+    KC, ng, tm, ks, iters, cl = P["KC"], P["ng"], P["tm"], P["ksub"], P["iters"], P["cl"]
     packed_words = P["n_tiles"] * KC * 1024
     scales_elems = P["n_tiles"] * ng * 128
     partial_floats = 2 * P["grid"] * tm * 128
+    assert P["grid"] <= MAX_GRID
     covered = {}
     writers = {}
-    for c in range(P["grid"]):
-        for (t, kb, ke) in segments(P, c):
-            assert 0 <= t < P["n_tiles"] * P["m_tiles"] and 0 <= kb < ke <= iters
-            nt, mt = divmod(t, P["m_tiles"])
-            for st in range(kb, ke):
-                key = (t, st)
-                assert key not in covered
-                covered[key] = c
-                k0 = st * ks * 64
-                w0 = (nt * KC + st * ks) * 1024            # one bulk copy of ks sub-chunks
-                assert 0 <= w0 and w0 + ks * 1024 <= packed_words
-                g0 = min(k0 // G, ng - 1)
-                g1 = min((k0 + ks * 64 - 1) // G, ng - 1)
-                assert 1 <= g1 - g0 + 1 <= 2 * ks          # fits the scale slot
-                for j in range(ks):
-                    for half in (0, 1):
-                        g = min((k0 + j * 64 + half * 32) // G, ng - 1)
-                        assert g0 <= g <= g1
-                    assert ((k0 + j * 64) * 2) % 16 == 0    # TMA inner coordinate, 16-byte aligned
-                e0 = (nt * ng + g0) * 128
-                assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
-                assert mt * tm < M
-            split = kb != 0 or ke != iters
-            if split:
-                slot = slot_of(P, c, t)
-                assert 0 <= slot < 2 * P["grid"]
-                assert (slot + 1) * tm * 128 <= partial_floats
-                writers.setdefault(t, []).append((c, slot))
-    assert len(covered) == P["total"]
+    for c in range(P["units"]):
+        for rank in range(cl):
+            for (t, kb, ke) in segments(P, c):
+                assert 0 <= t < P["n_blocks"] * P["m_tiles"] and 0 <= kb < ke <= iters
+                nb, mt = divmod(t, P["m_tiles"])
+                nt = nb * cl + rank
+                phantom = nt >= P["n_tiles"]
+                for st in range(kb, ke):
+                    k0 = st * ks * 64
+                    if not phantom:
+                        key = (nt, mt, st)
+                        assert key not in covered
+                        covered[key] = (c, rank)
+                        w0 = (nt * KC + st * ks) * 1024            # one bulk copy of ks sub-chunks
+                        assert 0 <= w0 and w0 + ks * 1024 <= packed_words
+                        g0 = min(k0 // G, ng - 1)
+                        g1 = min((k0 + ks * 64 - 1) // G, ng - 1)
+                        assert 1 <= g1 - g0 + 1 <= 2 * ks          # fits the scale slot
+                        e0 = (nt * ng + g0) * 128
+                        assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
+                    for j in range(ks):
+                        assert ((k0 + j * 64) * 2) % 16 == 0    # TMA inner coordinate, 16-byte aligned
+                    assert mt * tm < M
+                split = kb != 0 or ke != iters
+                if split:
+                    slot = slot_of(P, c, t, rank)
+                    assert 0 <= slot < 2 * P["grid"]
+                    assert (slot + 1) * tm * 128 <= partial_floats
+                    writers.setdefault((t, rank), []).append((c, slot))
+    assert len(covered) == P["n_tiles"] * P["m_tiles"] * iters
     counter_ids = set()
-    for t, ws in writers.items():
+    for (t, rank), ws in writers.items():
         c_lo, c_hi = cta_of(P, t * iters), cta_of(P, t * iters + iters - 1)
-        assert c_lo < P["grid"] and c_lo not in counter_ids
-        counter_ids.add(c_lo)
-        read = [(cc, slot_of(P, cc, t)) for cc in range(c_lo, c_hi + 1)]
+        counter = c_lo * cl + rank
+        assert counter < P["grid"] and counter not in counter_ids
+        counter_ids.add(counter)
+        read = [(cc, slot_of(P, cc, t, rank)) for cc in range(c_lo, c_hi + 1)]
         assert sorted(read) == sorted(ws), (t, read, ws)
         assert len(set(s for _, s in ws)) == len(ws)
     # a slot is written by one tile only
@@ -168,5 +178,6 @@ def test_shared_memory_and_tmem_layout_fits():
         assert smem <= 227 * 1024, (tm, smem)
         assert xblock % 1024 == 0 and off_pk % 16 == 0 and off_sc % 16 == 0 and off_bar % 8 == 0
         assert A * ks * 32 + dbufs * tm <= 512
+        assert SW % 2 == 0 and A % 2 == 0
         threads = 32 * (4 + 4 * ks + 3)
         assert threads <= 1024

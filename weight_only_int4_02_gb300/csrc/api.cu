@@ -39,6 +39,7 @@ constexpr int kMinItersPerCta = 4;
 struct DeviceState {
     bool ready = false;
     int sms = 0;
+    int max_clusters[3] = {0, 0, 0};  // co-resident 2-CTA clusters for tile heights 64, 128, 256
     void* ws = nullptr;
     size_t ws_bytes = 0;
 };
@@ -65,15 +66,19 @@ struct Plan {
     int path;     // 2 = per-weight scaling tcgen05 kernel
     int tm;       // rows of X per tile (MMA N)
     int ksub;     // 64-value sub-chunks per pipeline stage
-    int m_tiles, n_tiles, KC, ng, iters;
+    int cluster;  // CTAs per cluster; 2 share each X tile by TMA multicast
+    int m_tiles, n_tiles, n_blocks, KC, ng, iters;
     long long total;
-    int grid;
+    int units;    // work units (clusters)
+    int grid;     // CTAs
     size_t ws_bytes;
 };
 
 size_t ws_bytes_for(int grid, int tm) { return kPartialsOff + (size_t)2 * grid * tm * kTileN * sizeof(float); }
 
-Plan make_plan(int M, int N, int K, int G, int sms)
+// max_clusters: how many 2-CTA clusters of this tile height the device holds at
+// once (0 = unknown).
+Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
 {
     Plan P;
     P.path = 2;
@@ -81,19 +86,34 @@ Plan make_plan(int M, int N, int K, int G, int sms)
     P.m_tiles = ceil_div(M, P.tm);
     P.n_tiles = ceil_div(N, kTileN);
     P.ksub = P.tm <= 64 ? 4 : 2;
+    // From 64 rows of X up, X is the larger operand per stage: two CTAs on
+    // adjacent weight tiles load it once, by multicast.
+    P.cluster = P.tm >= 64 ? 2 : 1;
+    P.n_blocks = ceil_div(P.n_tiles, P.cluster);
     P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
     P.iters = P.KC / P.ksub;
     P.ng = ceil_div(K, G);
-    P.total = (long long)P.n_tiles * P.m_tiles * P.iters;
-    // One CTA per SM, but never fewer than kMinItersPerCta stages per CTA: below
-    // that, the split-K reduction of a tile gathers too many partials.
-    long long grid = sms < kMaxGrid ? sms : kMaxGrid;
-    const long long by_work = (P.total + kMinItersPerCta - 1) / kMinItersPerCta;
-    if (grid > by_work) grid = by_work;
-    if (grid < 1) grid = 1;
-    P.grid = (int)grid;
+    P.total = (long long)P.n_blocks * P.m_tiles * P.iters;
+    // One CTA per SM, but a work unit takes at least kMinItersPerCta stages, and
+    // with 32 or more rows of X at least a quarter (32 rows) or a half (64 and up)
+    // of a tile's stages: the last contributor of a split tile reads every other
+    // contributor's partial, which costs about one round trip per 16 rows.
+    long long units = (sms < kMaxGrid ? sms : kMaxGrid) / P.cluster;
+    if (P.cluster > 1 && max_clusters > 0 && units > max_clusters) units = max_clusters;
+    int min_iters = P.tm >= 64 ? P.iters / 2 : P.tm == 32 ? P.iters / 4 : 0;
+    if (min_iters < kMinItersPerCta) min_iters = kMinItersPerCta;
+    const long long by_work = (P.total + min_iters - 1) / min_iters;
+    if (units > by_work) units = by_work;
+    if (units < 1) units = 1;
+    P.units = (int)units;
+    P.grid = P.units * P.cluster;
     P.ws_bytes = ws_bytes_for(P.grid, P.tm);
     return P;
+}
+
+int max_clusters_for(const DeviceState* st, int tm)
+{
+    return tm == 64 ? st->max_clusters[0] : tm == 128 ? st->max_clusters[1] : tm == 256 ? st->max_clusters[2] : 0;
 }
 
 w4a16_status device_state(DeviceState** out)
@@ -111,9 +131,11 @@ w4a16_status device_state(DeviceState** out)
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
-        if ((e = setup_tc<16, 4>()) != cudaSuccess || (e = setup_tc<32, 4>()) != cudaSuccess ||
-            (e = setup_tc<64, 4>()) != cudaSuccess || (e = setup_tc<128, 2>()) != cudaSuccess ||
-            (e = setup_tc<256, 2>()) != cudaSuccess)
+        int unused = 0;
+        if ((e = setup_tc<16, 4, 1>(&unused)) != cudaSuccess || (e = setup_tc<32, 4, 1>(&unused)) != cudaSuccess ||
+            (e = setup_tc<64, 4, 2>(&st.max_clusters[0])) != cudaSuccess ||
+            (e = setup_tc<128, 2, 2>(&st.max_clusters[1])) != cudaSuccess ||
+            (e = setup_tc<256, 2, 2>(&st.max_clusters[2])) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
             void* fn = nullptr;
@@ -156,10 +178,10 @@ w4a16_status own_workspace(DeviceState* st, void** ws, size_t* bytes)
 // X as a 3-D view {64, M, K/64} (strides K*2 and 128 bytes) when K is a multiple of
 // 64, so one TMA brings a stage's KSUB blocks of 64 columns; else the plain 2-D
 // map {K, M}, one TMA per block, with the ragged K edge zero-filled.
-bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int ksub, int* is_3d)
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int ksub, bool allow_3d, int* is_3d)
 {
     cuuint32_t estr[3] = {1, 1, 1};
-    if (K % kChunkK == 0) {
+    if (allow_3d && K % kChunkK == 0) {
         cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)M, (cuuint64_t)(K / kChunkK)};
         cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kChunkK * 2};
         cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)rows, (cuuint32_t)ksub};
@@ -194,7 +216,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    const Plan P = make_plan(M, N, K, G, st->sms);
+    const Plan P = make_plan(M, N, K, G, st->sms, max_clusters_for(st, make_plan(M, N, K, G, st->sms).tm));
     if (own_ws) {
         rc = own_workspace(st, &ws, &ws_bytes);
         if (rc != W4A16_OK) return rc;
@@ -224,20 +246,24 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.iters = P.iters;
     p.total_iters = P.total;
     p.grid = P.grid;
+    p.cluster = P.cluster;
+    p.units = P.units;
+    p.n_blocks = P.n_blocks;
     p.wait_limit_ns = g_wait_limit_ns;
 
     CUtensorMap map;
     // With one row tile, a box of M rows rounded up to the 8-row swizzle atom is
     // enough: MMA rows past M feed only output columns that are never stored.
     p.x_rows = P.m_tiles == 1 ? ((M + 7) / 8) * 8 : P.tm;
-    if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
+    // Clusters split a stage's X blocks between their CTAs: one 2-D TMA per block.
+    if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     switch (P.tm) {
-        case 16: e = launch_tc<16, 4>(map, p, stream); break;
-        case 32: e = launch_tc<32, 4>(map, p, stream); break;
-        case 64: e = launch_tc<64, 4>(map, p, stream); break;
-        case 128: e = launch_tc<128, 2>(map, p, stream); break;
-        default: e = launch_tc<256, 2>(map, p, stream); break;
+        case 16: e = launch_tc<16, 4, 1>(map, p, stream); break;
+        case 32: e = launch_tc<32, 4, 1>(map, p, stream); break;
+        case 64: e = launch_tc<64, 4, 2>(map, p, stream); break;
+        case 128: e = launch_tc<128, 2, 2>(map, p, stream); break;
+        default: e = launch_tc<256, 2, 2>(map, p, stream); break;
     }
     return from_cuda(e);
 }
@@ -307,7 +333,8 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size)
     int sms = kMaxGrid;
     if (device_state(&st) == W4A16_OK) sms = st->sms;
     if (M == 0) return kPartialsOff;
-    return make_plan(M, N, K, G, sms).ws_bytes;
+    const int mc = st ? max_clusters_for(st, make_plan(M, N, K, G, sms).tm) : 0;
+    return make_plan(M, N, K, G, sms, mc).ws_bytes;
 }
 
 w4a16_status w4a16_gemm_ws(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y,
@@ -345,7 +372,7 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    const Plan P = make_plan(M, N, K, G, st->sms);
+    const Plan P = make_plan(M, N, K, G, st->sms, max_clusters_for(st, make_plan(M, N, K, G, st->sms).tm));
     *path = P.path;
     *tile_m = P.tm;
     *grid = P.grid;
@@ -399,7 +426,8 @@ extern "C" w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* pa
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    if (make_plan(M, N, K, G, st->sms).ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
+    const int mc = max_clusters_for(st, make_plan(M, N, K, G, st->sms).tm);
+    if (make_plan(M, N, K, G, st->sms, mc).ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc != W4A16_OK) return rc;

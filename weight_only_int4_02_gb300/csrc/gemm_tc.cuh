@@ -52,15 +52,18 @@ struct GemmParams {
     const __half* scales;   // tile-ordered scales [n_tiles][ng][128]
     __half* y;
     float* partials;        // [2 * grid][TM][128] FP32
-    int* counters;          // [grid], zero between launches
+    int* counters;          // [grid], zero between launches (index = cluster * p.cluster + rank)
     int* status;            // error word, bit 0 = a wait timed out
     int M, N, K, G, ng;
     int g_shift;            // log2(G) for G a power of two; 30 when there is one group
     int n_tiles, m_tiles;
     int KC;                 // 64-value sub-chunks per weight column in the packed layout
     int iters;              // stages per tile = KC / KSUB
-    long long total_iters;  // n_tiles * m_tiles * iters
-    int grid;
+    long long total_iters;  // n_blocks * m_tiles * iters
+    int grid;               // CTAs
+    int cluster;            // CTAs per cluster (1, or 2 sharing each X tile by multicast)
+    int units;              // grid / cluster: the work split is over clusters
+    int n_blocks;           // ceil(n_tiles / cluster): a cluster takes `cluster` adjacent weight tiles
     int x_3d;               // X tensor map is 3-D {64, M, K/64}: one TMA per stage
     int x_rows;             // rows of X each TMA box brings (<= TM, a multiple of 8); the
                             // MMA's B rows past them feed only output columns >= M
@@ -78,10 +81,12 @@ struct TcCfg {
     // warps once they hold their words, so the HBM stream never waits on the MMA;
     // and X, freed by the MMA's commit.
     static constexpr int kWStageBytes = kPkBytes + kScBytes;
-    static constexpr int kWStages = (TM <= 32 || KSUB == 2) ? 8 : 6;  // even (two dequant teams)
+    static constexpr int kWStages = (TM <= 32 || KSUB == 2) ? 8 : 6;  // a multiple of the team count
     static constexpr int kXFit = (220 * 1024 - kWStages * kWStageBytes) / kXBytes;
     static constexpr int kXStages = kXFit > 8 ? 8 : kXFit;
-    static constexpr int kDqWarps = 4 * KSUB;
+    // Dequant teams take stages in turn; a team is KSUB/2 groups of four warps.
+    static constexpr int kTeams = 2;
+    static constexpr int kDqWarps = kTeams * 2 * KSUB;
     static constexpr int kDqWarp0 = 4;
     static constexpr int kProdXWarp = kDqWarp0 + kDqWarps;
     static constexpr int kProdWWarp = kProdXWarp + 1;
@@ -90,7 +95,7 @@ struct TcCfg {
     static constexpr int kDBufs = TM <= 128 ? 2 : 1;
     static constexpr int kASlotCols = KSUB * 32;          // 16-bit A values, two per column
     static constexpr int kAFit = (512 - kDBufs * TM) / kASlotCols;
-    static constexpr int kAStages = kAFit >= 4 ? 4 : 2;               // even (two dequant teams)
+    static constexpr int kAStages = kAFit >= 4 ? 4 : 2;               // a multiple of the team count
     static constexpr int kACol = 0;
     static constexpr int kDCol = kAStages * kASlotCols;
     static constexpr int kTmemCols = 512;
@@ -106,31 +111,34 @@ struct TcCfg {
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(kXBlock % 1024 == 0, "X blocks must stay 1024-byte aligned");
     static_assert(kWStages >= 2 && kXStages >= 2 && kAStages >= 2, "pipeline depth");
-    static_assert(kWStages % 2 == 0 && kAStages % 2 == 0, "rings shared by two alternating dequant teams");
+    static_assert(kWStages % kTeams == 0 && kAStages % kTeams == 0, "rings shared by dequant teams in turn");
     static_assert(KSUB % 2 == 0, "a dequant warp unpacks two sub-chunks");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert(kDCol + kDBufs * TM <= 512, "tensor memory");
     static_assert(kKPad % KSUB == 0, "stages must tile the padded K");
 };
 
+// First iteration of work unit (cluster) c.
 __device__ __forceinline__ long long cta_begin(const GemmParams& p, int c)
 {
-    return (long long)c * p.total_iters / p.grid;
+    return (long long)c * p.total_iters / p.units;
 }
 
-// The CTA whose range holds iteration i.
+// The work unit whose range holds iteration i.
 __device__ __forceinline__ int cta_of(const GemmParams& p, long long i)
 {
-    int c = (int)((i * p.grid) / p.total_iters);
-    while (c + 1 < p.grid && cta_begin(p, c + 1) <= i) ++c;
+    int c = (int)((i * p.units) / p.total_iters);
+    while (c + 1 < p.units && cta_begin(p, c + 1) <= i) ++c;
     while (c > 0 && cta_begin(p, c) > i) --c;
     return c;
 }
 
-// Partial slot of CTA c for tile t: 2c if t holds c's first iteration, else 2c+1.
-__device__ __forceinline__ int slot_of(const GemmParams& p, int c, int t)
+// Partial slot of the CTA of rank `rank` in unit c for tile t: 2*cta if t holds
+// the unit's first iteration, else 2*cta + 1 (cta = c * cluster + rank).
+__device__ __forceinline__ int slot_of(const GemmParams& p, int c, int t, int rank)
 {
-    return cta_begin(p, c) >= (long long)t * p.iters ? 2 * c : 2 * c + 1;
+    const int cta = c * p.cluster + rank;
+    return cta_begin(p, c) >= (long long)t * p.iters ? 2 * cta : 2 * cta + 1;
 }
 
 // Group of reduction index k, clamped to the last group (padding past K holds code 8).
@@ -188,8 +196,8 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
 // own partial is read from its TMEM accumulator (own_c is its CTA index) instead
 // of from global memory.
 template <int TM, int NCP, int LOADS>
-__device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0, int n,
-                                           int n_in, int own_c, uint32_t own_tmem)
+__device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
+                                           int n, int n_in, int own_c, uint32_t own_tmem)
 {
     constexpr int CPR = LOADS / NCP;
     static_assert(TM % CPR == 0, "a round's columns stay inside the tile");
@@ -204,7 +212,8 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo,
             for (int u = 0; u < NCP; ++u) {
                 const int cc = cc0 + u;
                 const bool remote = cc <= c_hi && !(own_tmem && cc == own_c);
-                const float* src = p.partials + ((size_t)slot_of(p, min(cc, c_hi), t) * TM + col0) * kTileN + n_in;
+                const float* src =
+                    p.partials + ((size_t)slot_of(p, min(cc, c_hi), t, rank) * TM + col0) * kTileN + n_in;
 #pragma unroll
                 for (int e = 0; e < CPR; ++e) v[u][e] = (remote && col0 + e < valid) ? __ldcg(src + e * kTileN) : 0.f;
             }
@@ -222,10 +231,11 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo,
     }
 }
 
-template <int TM, int KSUB>
+template <int TM, int KSUB, int CL>
 __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
+    static_assert(CL == 1 || (CL == 2 && KSUB % 2 == 0), "cluster of two splits a stage's X blocks");
     using C = TcCfg<TM, KSUB>;
     constexpr int SW = C::kWStages;
     constexpr int SX = C::kXStages;
@@ -258,11 +268,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SW; ++s) {
             mbar_init(wfull_bar(s), 1);
-            mbar_init(wempty_bar(s), 2 * KSUB);      // the stage's dequant team, once it holds its words
+            mbar_init(wempty_bar(s), 2 * KSUB);      // the stage's dequant team (2*KSUB warps), once it holds its words
         }
         for (int s = 0; s < SX; ++s) {
             mbar_init(xfull_bar(s), 1);
-            mbar_init(xempty_bar(s), 1);             // the MMA commit
+            mbar_init(xempty_bar(s), CL);            // the MMA commit of every CTA of the cluster
         }
         for (int a = 0; a < A; ++a) {
             mbar_init(afull_bar(a), 2 * KSUB);       // the stage's dequant team
@@ -283,11 +293,15 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // The cluster's CTAs write into each other's X ring and barriers: all of them
+    // must be initialised first.
+    if constexpr (CL > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (threadIdx.x == 0) launch_dependents();
 
-    const int cta = blockIdx.x;
+    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const int cta = blockIdx.x / CL;                 // work unit (cluster) index
     const long long it_begin = cta_begin(p, cta);
     const long long it_end = cta_begin(p, cta + 1);
 
@@ -307,14 +321,23 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         bool ok = true;
         for (long long i = it_begin; ok && i < it_end;) {
             const Segment g = segment_at(p, i, it_end);
-            const int nt = g.t / p.m_tiles, mt = g.t - nt * p.m_tiles;
+            const int nb = g.t / p.m_tiles, mt = g.t - nb * p.m_tiles;
+            const int nt = nb * CL + rank;
+            const bool phantom = nt >= p.n_tiles;   // odd tile count: the last cluster's second tile
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
                 const int s = (int)(seq % S);
                 const uint32_t empty = is_x ? xempty_bar(s) : wempty_bar(s);
                 if (!wait_warp(empty, ((seq / S) & 1) ^ 1, ctl)) { ok = false; break; }
                 if (lane == 0) {
                     const int k0 = kc * C::kStageK;
-                    if (is_x) {
+                    if (is_x && CL > 1) {
+                        // each CTA brings its share of the stage's X blocks into both CTAs
+                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(KSUB * p.x_rows * 128));
+#pragma unroll
+                        for (int j = rank; j < KSUB; j += CL)
+                            tma_load_2d_mc(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
+                                           xfull_bar(s), k0 + j * kChunkK, mt * TM, (uint16_t)((1u << CL) - 1));
+                    } else if (is_x) {
                         mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(KSUB * p.x_rows * 128));
                         if (p.x_3d) {
                             tma_load_3d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, xfull_bar(s), 0, mt * TM,
@@ -325,6 +348,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                                 tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
                                             xfull_bar(s), k0 + j * kChunkK, mt * TM);
                         }
+                    } else if (phantom) {
+                        mbar_arrive(wfull_bar(s));   // no weights to stream; the output is never stored
                     } else {
                         const int g0 = group_of(p, k0);
                         const int g1 = group_of(p, k0 + C::kStageK - 1);
@@ -384,7 +409,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                                        (kc > g.kb || j > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    mma_commit(xempty_bar(s));
+                    if constexpr (CL > 1)
+                        mma_commit_mc(xempty_bar(s), (uint16_t)((1u << CL) - 1));
+                    else
+                        mma_commit(xempty_bar(s));
                     mma_commit(aempty_bar(a));
                 }
                 __syncwarp();
@@ -402,10 +430,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         }
     } else if (warp >= C::kDqWarp0) {
         // ------------------------------------------------------------ dequant
-        // Two teams take alternate stages, so one team's waits overlap the other's
+        // Teams take stages in turn, so one team's waits overlap the others'
         // arithmetic. Within a team, group gi unpacks sub-chunks 2gi and 2gi+1.
-        // Ring depths are even: a ring slot's successive uses all fall to one team,
-        // which visits its stages in order (no waiter is a whole phase ahead).
+        // Ring depths are multiples of the team count: a ring slot's successive uses
+        // all fall to one team, which visits its stages in order (no waiter is a
+        // whole phase ahead).
         constexpr int kWarpsPerTeam = 2 * KSUB;
         const int dw = warp - C::kDqWarp0;
         const int team = dw / kWarpsPerTeam;
@@ -418,7 +447,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         for (long long i = it_begin; ok && i < it_end;) {
             const Segment g = segment_at(p, i, it_end);
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
-                if ((int)(seq & 1) != team) continue;
+                if ((int)(seq % C::kTeams) != team) continue;
                 const int s = (int)(seq % SW);
                 const int a = (int)(seq % A);
                 if (!wait_warp(wfull_bar(s), (seq / SW) & 1, ctl)) { ok = false; break; }
@@ -473,8 +502,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
         for (long long i = it_begin; i < it_end;) {
             const Segment g = segment_at(p, i, it_end);
             const int t = g.t;
-            const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
-            const int n = nt * kTileN + n_in;
+            const int nb = t / p.m_tiles, mt = t - nb * p.m_tiles;
+            const int n = (nb * CL + rank) * kTileN + n_in;   // n >= N for a phantom tile: nothing stored
             const int m0 = mt * TM;
             const int valid = min(TM, p.M - m0);
             const int chunks = (valid + 15) >> 4;
@@ -484,7 +513,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
             if (named_bar_or(1, 128, !ok)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + ((uint32_t)(warp * 32) << 16) + C::kDCol + d * TM;
-            float* part = p.partials + (size_t)slot_of(p, cta, t) * TM * kTileN + n_in;
+            float* part = p.partials + (size_t)slot_of(p, cta, t, rank) * TM * kTileN + n_in;
             for (int c = 0; c < chunks; ++c) {
                 uint32_t r[16];
                 tmem_ld16(d_tmem + c * 16, r);
@@ -525,9 +554,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 const int c_lo = cta_of(p, (long long)t * p.iters);
                 const int c_hi = cta_of(p, (long long)t * p.iters + p.iters - 1);
                 if (threadIdx.x == 0) {
-                    const int prev = atomicAdd(p.counters + c_lo, 1);
+                    int* counter = p.counters + c_lo * CL + rank;
+                    const int prev = atomicAdd(counter, 1);
                     const int last = (prev == c_hi - c_lo);
-                    if (last) p.counters[c_lo] = 0;
+                    if (last) *counter = 0;
                     *last_flag = last;
                 }
                 named_bar_sync(1, 128);
@@ -540,21 +570,21 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                     const uint32_t own = hold ? d_tmem : 0u;
                     if constexpr (!kHoldable) {
                         if (ncontrib <= 2)
-                            fix_reduce<TM, 2, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                            fix_reduce<TM, 2, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
                         else if (ncontrib <= 4)
-                            fix_reduce<TM, 4, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                            fix_reduce<TM, 4, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
                         else if (ncontrib <= 8)
-                            fix_reduce<TM, 8, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                            fix_reduce<TM, 8, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
                         else
-                            fix_reduce<TM, 16, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
+                            fix_reduce<TM, 16, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
                     } else if (ncontrib <= 2)
-                        fix_reduce<TM, 2, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                        fix_reduce<TM, 2, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                     else if (ncontrib <= 4)
-                        fix_reduce<TM, 4, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                        fix_reduce<TM, 4, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                     else if (ncontrib <= 8)
-                        fix_reduce<TM, 8, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                        fix_reduce<TM, 8, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                     else
-                        fix_reduce<TM, 16, L>(p, t, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                        fix_reduce<TM, 16, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
                 }
                 named_bar_sync(1, 128);
                 if (hold) {
@@ -568,6 +598,9 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    // No CTA may leave while its peer can still write into its X ring or arrive on
+    // its barriers.
+    if constexpr (CL > 1) cluster_sync();
     if (warp == C::kMmaWarp) {
         __syncwarp();
         tc_fence_after();
@@ -575,13 +608,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     }
 }
 
-template <int TM, int KSUB>
+template <int TM, int KSUB, int CL>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream);
 
-template <int TM, int KSUB>
-cudaError_t setup_tc();
-
-// Sub-chunks per stage for a tile height: 4 for the memory-bound tiles, 2 above.
-constexpr int ksub_for(int tm) { return tm <= 64 ? 4 : 2; }
+template <int TM, int KSUB, int CL>
+cudaError_t setup_tc(int* max_clusters);
 
 }  // namespace w4a16

@@ -1,17 +1,40 @@
-// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB>; included by one .cu file per tile shape.
+// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL>; included by one .cu file per tile shape.
 #pragma once
 #include "gemm_tc.cuh"
 
 namespace w4a16 {
 
-template <int TM, int KSUB>
-cudaError_t setup_tc()
+// Dynamic shared memory, and for clusters the number of clusters the device can
+// hold at once (0 when the query fails).
+template <int TM, int KSUB, int CL>
+cudaError_t setup_tc(int* max_clusters)
 {
-    return cudaFuncSetAttribute(w4a16_tc_kernel<TM, KSUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TcCfg<TM, KSUB>::kSmemBytes);
+    auto kernel = w4a16_tc_kernel<TM, KSUB, CL>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<TM, KSUB>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    *max_clusters = 0;
+    if (CL > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * CL);
+        cfg.blockDim = dim3(TcCfg<TM, KSUB>::kThreads);
+        cfg.dynamicSmemBytes = TcCfg<TM, KSUB>::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(max_clusters, kernel, &cfg) != cudaSuccess) {
+            *max_clusters = 0;
+            cudaGetLastError();
+        }
+    }
+    return cudaSuccess;
 }
 
-template <int TM, int KSUB>
+template <int TM, int KSUB, int CL>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
@@ -21,18 +44,26 @@ cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t
     cfg.stream = stream;
     // Programmatic dependent launch: the next kernel may start its prologue and
     // weight stream while this one drains; it waits for this one before reading X.
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (CL > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = CL;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB>, tmap, p);
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL>, tmap, p);
 }
 
 }  // namespace w4a16
 
-#define W4A16_INSTANTIATE_TC(TM, KSUB)                                                              \
-    namespace w4a16 {                                                                               \
-    template cudaError_t setup_tc<TM, KSUB>();                                                      \
-    template cudaError_t launch_tc<TM, KSUB>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
+#define W4A16_INSTANTIATE_TC(TM, KSUB, CL)                                                              \
+    namespace w4a16 {                                                                                   \
+    template cudaError_t setup_tc<TM, KSUB, CL>(int*);                                                  \
+    template cudaError_t launch_tc<TM, KSUB, CL>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
     }
