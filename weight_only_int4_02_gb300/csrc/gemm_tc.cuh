@@ -373,6 +373,15 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 const uint32_t q = seq - k;
                 wait_drain(is_x ? xfull_bar((int)(q % S)) : wfull_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
             }
+            // In a cluster, the peer's MMA commits arrive on this CTA's X ring: wait
+            // until the last use of every slot has received all of them, so that no
+            // arrival can land after this CTA (and reach whatever runs here next).
+            if (is_x && CL > 1) {
+                for (uint32_t k = 1; k <= inflight; ++k) {
+                    const uint32_t q = seq - k;
+                    wait_drain(xempty_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
+                }
+            }
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
