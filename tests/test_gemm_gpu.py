@@ -229,3 +229,16 @@ def test_edge_sweep(w, oracle_mod):
             cols = np.arange(0, N, 7)
             y_ref, absum = oracle_mod.gemm_sample(x, q, s, G, np.arange(M), cols)
             check_within(y[:, cols], y_ref, absum, "edge M=%d N=%d K=%d G=%d" % (M, N, K, G))
+
+
+def test_device_plan_matches_host_mirror(w):
+    """The dispatcher on the device picks the grid that the schedule mirror (whose
+    coverage and bounds the CPU tests check) computes for the same SM count."""
+    from tests.test_schedule import plan as mirror_plan
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = [(m, n, k) for (m, k, n) in inputs.WORKLOADS["llama2_7b_decode_sweep"]["cases"] if m <= 32]
+    shapes += [(1, 256, 16384), (3, 136, 200), (17, 4096, 4000), (1, 73728, 18432), (16, 73728, 18432)]
+    for (M, N, K) in shapes:
+        path, tm, grid = w.plan(M, N, K, 128)
+        P = mirror_plan(M, N, K, 128, sms)
+        assert (tm, grid) == (P["tm"], P["grid"]), (M, N, K, tm, grid, P["tm"], P["grid"])

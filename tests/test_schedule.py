@@ -39,8 +39,25 @@ def plan(M, N, K, G, sms=SMS):
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     iters = KC // ksub
     total = n_blocks * m_tiles * iters
-    min_iters = max(4, iters // 2 if tm >= 64 else (iters // 4 if tm == 32 else 0))
-    units = max(1, min(min(sms, MAX_GRID) // cl, -(-total // min_iters)))
+    units = min(sms, MAX_GRID) // cl
+    work_tiles = n_blocks * m_tiles
+    if cl == 1 and work_tiles < units:
+        # tile-aligned split: s parts per tile, chosen by the measured cost model
+        rows = M if m_tiles == 1 else tm
+        best_s, best = 1, 0.0
+        s = 1
+        while s <= units // work_tiles and s <= iters:
+            n = float(iters) / float(s)
+            pre = n if n < 8.0 else 8.0
+            cost = pre * 0.20 + (n - pre) * 0.55 + ((0.46 + 0.062 * rows * float(s - 1)) if s > 1 else 0.0)
+            if s == 1 or cost < best:
+                best, best_s = cost, s
+            s += 1
+        units = work_tiles * best_s
+    else:
+        min_iters = max(4, iters // 2 if tm >= 64 else (iters // 4 if tm == 32 else 0))
+        units = min(units, -(-total // min_iters))
+    units = max(1, units)
     return dict(tm=tm, ksub=ksub, cl=cl, m_tiles=m_tiles, n_tiles=n_tiles, n_blocks=n_blocks, KC=KC,
                 iters=iters, ng=ng, total=total, units=units, grid=units * cl)
 
@@ -181,3 +198,18 @@ def test_shared_memory_and_tmem_layout_fits():
         assert SW % 2 == 0 and A % 2 == 0
         threads = 32 * (4 + 4 * ks + 3)
         assert threads <= 1024
+
+
+def test_small_layer_splits_are_tile_aligned():
+    """With fewer tiles than SMs, every tile has the same number of contributors
+    and unit boundaries fall on tile boundaries; the measured best splits of the
+    decode layers are chosen (quarters at M = 1, halves at M = 16, whole tiles at
+    M = 32 for 4096x4096; whole tiles for 12288x4096; quarters for 4096x11008)."""
+    expect = {(1, 4096, 4096): 4, (16, 4096, 4096): 2, (32, 4096, 4096): 2, (1, 12288, 4096): 1,
+              (16, 12288, 4096): 1, (1, 4096, 11008): 4, (16, 4096, 11008): 4}
+    for (M, N, K), s in expect.items():
+        P = plan(M, N, K, 128)
+        work_tiles = P["n_blocks"] * P["m_tiles"]
+        assert P["units"] == work_tiles * s, (M, N, K, P["units"])
+        for t in range(work_tiles):
+            assert cta_begin(P, t * s) == t * P["iters"]

@@ -35,6 +35,13 @@ constexpr int kMaxGrid = 1024;
 constexpr size_t kPartialsOff = kCountersOff + 4 * kMaxGrid;
 constexpr int kMaxTileM = 256;
 constexpr int kMinItersPerCta = 4;
+// Split cost model for fewer tiles than SMs (make_plan), fitted to per-launch
+// times of the 16-row kernel on GB300 (4096x4096, 4096x12288, 11008x4096 layers).
+constexpr double kRingStages = 8;            // weight ring depth of the 16/32-row kernels
+constexpr double kPrefetchedStageUs = 0.20;
+constexpr double kStreamedStageUs = 0.55;
+constexpr double kFixupUs = 0.46;
+constexpr double kFixupRowUs = 0.062;
 
 struct DeviceState {
     bool ready = false;
@@ -94,16 +101,44 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
     P.iters = P.KC / P.ksub;
     P.ng = ceil_div(K, G);
     P.total = (long long)P.n_blocks * P.m_tiles * P.iters;
-    // One CTA per SM, but a work unit takes at least kMinItersPerCta stages, and
-    // with 32 or more rows of X at least a quarter (32 rows) or a half (64 and up)
-    // of a tile's stages: the last contributor of a split tile reads every other
-    // contributor's partial, which costs about one round trip per 16 rows.
     long long units = (sms < kMaxGrid ? sms : kMaxGrid) / P.cluster;
     if (P.cluster > 1 && max_clusters > 0 && units > max_clusters) units = max_clusters;
-    int min_iters = P.tm >= 64 ? P.iters / 2 : P.tm == 32 ? P.iters / 4 : 0;
-    if (min_iters < kMinItersPerCta) min_iters = kMinItersPerCta;
-    const long long by_work = (P.total + min_iters - 1) / min_iters;
-    if (units > by_work) units = by_work;
+    const long long work_tiles = (long long)P.n_blocks * P.m_tiles;
+    if (P.cluster == 1 && work_tiles < units) {
+        // Fewer tiles than SMs (the small decode layers): every tile is cut into
+        // the same number s of parts, so that unit boundaries fall on tile
+        // boundaries and each split tile has exactly s contributors. s trades the
+        // stages a unit runs against the split-K fix-up, whose last contributor
+        // reads every other partial; the costs are measured on GB300 (µs): a stage
+        // whose weights were prefetched into the ring before X arrived, a stage
+        // streamed after it, and the fix-up per split tile and per valid row and
+        // extra contributor.
+        const int rows = P.m_tiles == 1 ? M : P.tm;
+        const long long s_max = units / work_tiles;
+        long long best_s = 1;
+        double best = 0.0;
+        for (long long s = 1; s <= s_max && s <= P.iters; ++s) {
+            const double n = (double)P.iters / (double)s;   // stages per unit
+            const double prefetched = n < kRingStages ? n : kRingStages;
+            const double cost = prefetched * kPrefetchedStageUs + (n - prefetched) * kStreamedStageUs +
+                                (s > 1 ? kFixupUs + kFixupRowUs * rows * (double)(s - 1) : 0.0);
+            if (s == 1 || cost < best) {
+                best = cost;
+                best_s = s;
+            }
+        }
+        units = work_tiles * best_s;
+    } else {
+        // Stream-K over every SM, but a work unit takes at least kMinItersPerCta
+        // stages, and with 32 or more rows of X at least a quarter (32 rows) or a
+        // half (64 and up) of a tile's stages: the last contributor of a split
+        // tile reads every other contributor's partial, which costs about one
+        // round trip per 16 rows.
+        int min_iters = P.tm >= 64 ? P.iters / 2 : P.tm == 32 ? P.iters / 4 : 0;
+        if (min_iters < kMinItersPerCta) min_iters = kMinItersPerCta;
+        const long long by_work = (P.total + min_iters - 1) / min_iters;
+        if (units > by_work) units = by_work;
+    }
     if (units < 1) units = 1;
     P.units = (int)units;
     P.grid = P.units * P.cluster;
