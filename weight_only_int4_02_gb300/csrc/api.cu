@@ -35,13 +35,17 @@ constexpr int kMaxGrid = 1024;
 constexpr size_t kPartialsOff = kCountersOff + 4 * kMaxGrid;
 constexpr int kMaxTileM = 256;
 constexpr int kMinItersPerCta = 4;
-// Split cost model for fewer tiles than SMs (make_plan), fitted to per-launch
-// times of the 16-row kernel on GB300 (4096x4096, 4096x12288, 11008x4096 layers).
-constexpr double kRingStages = 8;            // weight ring depth of the 16/32-row kernels
-constexpr double kPrefetchedStageUs = 0.20;
-constexpr double kStreamedStageUs = 0.55;
-constexpr double kFixupUs = 0.46;
-constexpr double kFixupRowUs = 0.062;
+// Split cost model for fewer tiles than work units (make_plan), fitted to
+// per-launch times on GB300 of the 4096x4096, 4096x12288 and 11008x4096 layers:
+// µs per stage whose weights were prefetched into the ring before X arrived
+// (up to `ring` stages), per stage streamed after it, and the split-K fix-up per
+// split tile and per valid row and extra contributor.
+struct SplitCost {
+    double ring, prefetched_us, streamed_us, fixup_us, fixup_row_us;
+};
+constexpr SplitCost kSplit16 = {8, 0.20, 0.55, 0.46, 0.062};     // 16- and 32-row tiles, 16 KB stages
+constexpr SplitCost kSplit64 = {0, 0.465, 0.465, 1.4, 0.0754};  // 64-row tile pairs, 16 KB stages
+constexpr SplitCost kSplit128 = {0, 0.31, 0.31, 1.4, 0.0405};   // 128-row tile pairs, 8 KB stages
 
 struct DeviceState {
     bool ready = false;
@@ -104,24 +108,22 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
     long long units = (sms < kMaxGrid ? sms : kMaxGrid) / P.cluster;
     if (P.cluster > 1 && max_clusters > 0 && units > max_clusters) units = max_clusters;
     const long long work_tiles = (long long)P.n_blocks * P.m_tiles;
-    if (P.cluster == 1 && work_tiles < units) {
-        // Fewer tiles than SMs (the small decode layers): every tile is cut into
-        // the same number s of parts, so that unit boundaries fall on tile
-        // boundaries and each split tile has exactly s contributors. s trades the
-        // stages a unit runs against the split-K fix-up, whose last contributor
-        // reads every other partial; the costs are measured on GB300 (µs): a stage
-        // whose weights were prefetched into the ring before X arrived, a stage
-        // streamed after it, and the fix-up per split tile and per valid row and
-        // extra contributor.
+    if (P.tm <= 128 && work_tiles < units) {
+        // Fewer tiles (or tile pairs) than work units: every tile is cut into the
+        // same number s of parts, so that unit boundaries fall on tile boundaries
+        // and each split tile has exactly s contributors. s trades the stages a
+        // unit runs against the split-K fix-up, whose last contributor reads every
+        // other partial (costs measured on GB300, kSplit*).
+        const SplitCost& sc = P.tm <= 32 ? kSplit16 : P.tm == 64 ? kSplit64 : kSplit128;
         const int rows = P.m_tiles == 1 ? M : P.tm;
         const long long s_max = units / work_tiles;
         long long best_s = 1;
         double best = 0.0;
         for (long long s = 1; s <= s_max && s <= P.iters; ++s) {
             const double n = (double)P.iters / (double)s;   // stages per unit
-            const double prefetched = n < kRingStages ? n : kRingStages;
-            const double cost = prefetched * kPrefetchedStageUs + (n - prefetched) * kStreamedStageUs +
-                                (s > 1 ? kFixupUs + kFixupRowUs * rows * (double)(s - 1) : 0.0);
+            const double prefetched = n < sc.ring ? n : sc.ring;
+            const double cost = prefetched * sc.prefetched_us + (n - prefetched) * sc.streamed_us +
+                                (s > 1 ? sc.fixup_us + sc.fixup_row_us * rows * (double)(s - 1) : 0.0);
             if (s == 1 || cost < best) {
                 best = cost;
                 best_s = s;
