@@ -46,6 +46,7 @@ struct SplitCost {
 constexpr SplitCost kSplit16 = {8, 0.20, 0.55, 0.46, 0.062};     // 16- and 32-row tiles, 16 KB stages
 constexpr SplitCost kSplit64 = {0, 0.465, 0.465, 1.4, 0.0754};  // 64-row tile pairs, 16 KB stages
 constexpr SplitCost kSplit128 = {0, 0.31, 0.31, 1.4, 0.0405};   // 128-row tile pairs, 8 KB stages
+constexpr SplitCost kSplit256 = {0, 0.59, 0.59, 0.0, 0.059};    // 256-row tile pairs, 8 KB stages (prefill)
 
 struct DeviceState {
     bool ready = false;
@@ -108,13 +109,13 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
     long long units = (sms < kMaxGrid ? sms : kMaxGrid) / P.cluster;
     if (P.cluster > 1 && max_clusters > 0 && units > max_clusters) units = max_clusters;
     const long long work_tiles = (long long)P.n_blocks * P.m_tiles;
-    if (P.tm <= 128 && work_tiles < units) {
+    if (work_tiles < units) {
         // Fewer tiles (or tile pairs) than work units: every tile is cut into the
         // same number s of parts, so that unit boundaries fall on tile boundaries
         // and each split tile has exactly s contributors. s trades the stages a
         // unit runs against the split-K fix-up, whose last contributor reads every
         // other partial (costs measured on GB300, kSplit*).
-        const SplitCost& sc = P.tm <= 32 ? kSplit16 : P.tm == 64 ? kSplit64 : kSplit128;
+        const SplitCost& sc = P.tm <= 32 ? kSplit16 : P.tm == 64 ? kSplit64 : P.tm == 128 ? kSplit128 : kSplit256;
         const int rows = P.m_tiles == 1 ? M : P.tm;
         const long long s_max = units / work_tiles;
         long long best_s = 1;
