@@ -189,44 +189,62 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
     return g;
 }
 
-// Split-K fix-up of one output row n by the last contributor: the sum of every
-// contributor's FP32 partial, added in contributor (CTA) order. A round issues
-// LOADS loads (LOADS/NCP columns of NCP contributors) before any is added, so it
-// costs one global round trip. When own_tmem is nonzero the last contributor's
-// own partial is read from its TMEM accumulator (own_c is its CTA index) instead
-// of from global memory.
-template <int TM, int NCP, int LOADS>
+// Split-K fix-up of a tile by its last contributor: Y = the sum of every
+// contributor's FP32 partial, added in contributor (CTA) order. Partials are
+// column-major ([TM][128] per slot), so one 16-byte load brings four rows of a
+// column: thread j of the four epilogue warps takes rows 4(j mod 32) .. +3 of
+// columns j/32, j/32 + 4, j/32 + 8, ... A round issues L4 such loads (L4/NCP
+// columns of NCP contributors) before any is added, so it costs one global
+// round trip. n_base is the tile's first output feature.
+template <int TM, int NCP, int L4>
 __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
-                                           int n, int n_in, int own_c, uint32_t own_tmem)
+                                           int n_base)
 {
-    constexpr int CPR = LOADS / NCP;
-    static_assert(TM % CPR == 0, "a round's columns stay inside the tile");
-    for (int col0 = 0; col0 < valid; col0 += CPR) {
-        float acc[CPR], own[CPR];
+    constexpr int CPR = L4 / NCP;
+    const int rg = threadIdx.x & 31;
+    const int m_first = threadIdx.x >> 5;
+    const int ncols = valid > m_first ? (valid - m_first + 3) >> 2 : 0;   // columns m_first + 4q, q < ncols
+    const int n = n_base + 4 * rg;
+    for (int q0 = 0; q0 < ncols; q0 += CPR) {
+        float4 acc[CPR];
 #pragma unroll
-        for (int e = 0; e < CPR; ++e) acc[e] = 0.f;
-        if (own_tmem) tmem_ld_f32<CPR>(own_tmem + col0, own);
+        for (int e = 0; e < CPR; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int cc0 = c_lo; cc0 <= c_hi; cc0 += NCP) {
-            float v[NCP][CPR];
+            float4 v[NCP][CPR];
 #pragma unroll
             for (int u = 0; u < NCP; ++u) {
                 const int cc = cc0 + u;
-                const bool remote = cc <= c_hi && !(own_tmem && cc == own_c);
-                const float* src =
-                    p.partials + ((size_t)slot_of(p, min(cc, c_hi), t, rank) * TM + col0) * kTileN + n_in;
+                const float* base = p.partials + (size_t)slot_of(p, min(cc, c_hi), t, rank) * TM * kTileN + 4 * rg;
 #pragma unroll
-                for (int e = 0; e < CPR; ++e) v[u][e] = (remote && col0 + e < valid) ? __ldcg(src + e * kTileN) : 0.f;
+                for (int e = 0; e < CPR; ++e) {
+                    const int m = m_first + 4 * (q0 + e);
+                    v[u][e] = (cc <= c_hi && q0 + e < ncols)
+                                  ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)m * kTileN))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < NCP; ++u)
+            for (int u = 0; u < NCP; ++u) {
+                if (cc0 + u > c_hi) continue;
 #pragma unroll
-                for (int e = 0; e < CPR; ++e)
-                    if (cc0 + u <= c_hi) acc[e] += (own_tmem && cc0 + u == own_c) ? own[e] : v[u][e];
+                for (int e = 0; e < CPR; ++e) {
+                    acc[e].x += v[u][e].x;
+                    acc[e].y += v[u][e].y;
+                    acc[e].z += v[u][e].z;
+                    acc[e].w += v[u][e].w;
+                }
+            }
         }
-        if (n < p.N) {
+        if (n < p.N) {   // N is a multiple of 8, so n .. n+3 are all in range
 #pragma unroll
-            for (int e = 0; e < CPR; ++e)
-                if (col0 + e < valid) p.y[(size_t)(m0 + col0 + e) * p.N + n] = __float2half_rn(acc[e]);
+            for (int e = 0; e < CPR; ++e) {
+                if (q0 + e >= ncols) continue;
+                __half* out = p.y + (size_t)(m0 + m_first + 4 * (q0 + e)) * p.N + n;
+                out[0] = __float2half_rn(acc[e].x);
+                out[1] = __float2half_rn(acc[e].y);
+                out[2] = __float2half_rn(acc[e].z);
+                out[3] = __float2half_rn(acc[e].w);
+            }
         }
     }
 }
@@ -540,18 +558,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                         if (c * 16 + e < valid) part[(size_t)(c * 16 + e) * kTileN] = __uint_as_float(r[e]);
                 }
             }
-            // With two D buffers and wide tiles, a split tile keeps its accumulator
-            // until the fix-up is done (the last contributor reads its own partial
-            // back from TMEM); with one buffer the next tile's MMAs need it at once,
-            // and the narrow memory-bound tiles have few valid rows to reduce.
-            constexpr bool kHoldable = C::kDBufs == 2 && KSUB == 2;
-            const bool hold = split && kHoldable;
-            const int d_used = d;
-            if (!hold) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(dempty_bar(d));
-            }
+            // The accumulator is free once its values are in global memory; the
+            // fix-up reads every partial, this CTA's own included, back from L2.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty_bar(d));
             if (++d == C::kDBufs) { d = 0; dph ^= 1; }
             i += g.ke - g.kb;
 
@@ -574,33 +585,17 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 if (last) {
                     __threadfence();
                     const int ncontrib = c_hi - c_lo + 1;
-                    // 16 loads per round where 23 warps cap registers at 80, else 32.
-                    constexpr int L = KSUB == 4 ? 16 : 32;
-                    const uint32_t own = hold ? d_tmem : 0u;
-                    if constexpr (!kHoldable) {
-                        if (ncontrib <= 2)
-                            fix_reduce<TM, 2, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
-                        else if (ncontrib <= 4)
-                            fix_reduce<TM, 4, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
-                        else if (ncontrib <= 8)
-                            fix_reduce<TM, 8, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
-                        else
-                            fix_reduce<TM, 16, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, 0u);
-                    } else if (ncontrib <= 2)
-                        fix_reduce<TM, 2, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                    const int n_base = n - n_in;
+                    // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
+                    constexpr int L4 = KSUB == 4 ? 8 : 16;
+                    if (ncontrib <= 2)
+                        fix_reduce<TM, 2, L4>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                     else if (ncontrib <= 4)
-                        fix_reduce<TM, 4, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
-                    else if (ncontrib <= 8)
-                        fix_reduce<TM, 8, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                        fix_reduce<TM, 4, L4>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                     else
-                        fix_reduce<TM, 16, L>(p, t, rank, c_lo, c_hi, valid, m0, n, n_in, cta, own);
+                        fix_reduce<TM, 8, L4>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                 }
                 named_bar_sync(1, 128);
-                if (hold) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(dempty_bar(d_used));
-                }
             }
         }
     }
