@@ -35,17 +35,18 @@ constexpr int kMaxGrid = 1024;
 constexpr size_t kPartialsOff = kCountersOff + 4 * kMaxGrid;
 constexpr int kMaxTileM = 256;
 constexpr int kMinItersPerCta = 4;
-// Split cost model for fewer tiles than work units (make_plan), fitted to
-// per-launch times on GB300 of the 4096x4096, 4096x12288 and 11008x4096 layers:
+// Split cost model for fewer tiles than work units (make_plan), fitted (least
+// squares) to per-launch times on GB300 of the 4096x4096, 4096x12288 and
+// 11008x4096 layers at M = 1 ... 128 over every tile-aligned split:
 // µs per stage whose weights were prefetched into the ring before X arrived
 // (up to `ring` stages), per stage streamed after it, and the split-K fix-up per
 // split tile and per valid row and extra contributor.
 struct SplitCost {
     double ring, prefetched_us, streamed_us, fixup_us, fixup_row_us;
 };
-constexpr SplitCost kSplit16 = {8, 0.20, 0.55, 0.46, 0.062};     // 16- and 32-row tiles, 16 KB stages
-constexpr SplitCost kSplit64 = {0, 0.465, 0.465, 1.4, 0.0754};  // 64-row tile pairs, 16 KB stages
-constexpr SplitCost kSplit128 = {0, 0.31, 0.31, 1.4, 0.0405};   // 128-row tile pairs, 8 KB stages
+constexpr SplitCost kSplit16 = {8, 0.15, 0.40, 1.4, 0.03};      // 16- and 32-row tiles, 16 KB stages
+constexpr SplitCost kSplit64 = {0, 0.525, 0.525, 2.6, 0.04};    // 64-row tile pairs, 16 KB stages
+constexpr SplitCost kSplit128 = {0, 0.375, 0.375, 2.9, 0.02};   // 128-row tile pairs, 8 KB stages
 constexpr SplitCost kSplit256 = {0, 0.59, 0.59, 0.0, 0.059};    // 256-row tile pairs, 8 KB stages (prefill)
 
 struct DeviceState {
@@ -121,7 +122,7 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
         long long best_s = 1;
         double best = 0.0;
         for (long long s = 1; s <= s_max && s <= P.iters; ++s) {
-            const double n = (double)P.iters / (double)s;   // stages per unit
+            const double n = (double)((P.iters + s - 1) / s);   // stages of the longest unit
             const double prefetched = n < sc.ring ? n : sc.ring;
             const double cost = prefetched * sc.prefetched_us + (n - prefetched) * sc.streamed_us +
                                 (s > 1 ? sc.fixup_us + sc.fixup_row_us * rows * (double)(s - 1) : 0.0);
