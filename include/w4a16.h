@@ -124,6 +124,37 @@ w4a16_status w4a16_gemm_ws(const uint16_t* x, const uint32_t* packed,
                            int M, int N, int K, int group_size,
                            void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
+/* Activation of w4a16_gemm_fused, applied after the bias add. */
+typedef enum {
+    W4A16_ACT_NONE = 0,
+    W4A16_ACT_SILU = 1, /* z / (1 + e^-z) */
+    W4A16_ACT_RELU = 2  /* max(z, 0) */
+} w4a16_activation;
+
+/*
+ * Y = act(X x dequant(W) + bias) + residual: the GEMM with the operations that
+ * follow it in a layer fused into its epilogue ("quant_marlin_kernel", "End-to-end
+ * flow": the output tile flows straight into a bias add and an activation), so Y
+ * is written once instead of being re-read by separate kernels. The bias add, the
+ * activation and the residual add run in FP32 on the accumulator; the result is
+ * rounded once to FP16.
+ *   bias       device, binary16 [N], or NULL for none
+ *   residual   device, binary16 [M][N] row-major, or NULL for none; it may be the
+ *              same buffer as y (an in-place y += ...) but must not otherwise
+ *              overlap y
+ *   activation a w4a16_activation
+ *   workspace  as for w4a16_gemm_ws (ws_bytes bytes, zeroed once), or NULL to use
+ *              the library's own workspace as w4a16_gemm does
+ * Every other argument, layout and error is that of w4a16_gemm / w4a16_gemm_ws.
+ * Returns W4A16_ERR_INVALID_ARG for an unknown activation or an odd bias or
+ * residual address.
+ */
+w4a16_status w4a16_gemm_fused(const uint16_t* x, const uint32_t* packed,
+                              const uint16_t* scales_packed, uint16_t* y,
+                              int M, int N, int K, int group_size,
+                              const uint16_t* bias, const uint16_t* residual, int activation,
+                              void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
 /*
  * Synchronises `stream`, then reads and clears the error word that the kernels
  * set when one of their bounded waits gave up (W4A16_ERR_TIMEOUT), for the

@@ -163,3 +163,29 @@ def unpack_scales(sp, ng, N):
     s = np.empty((ng, N), np.uint16)
     bad = _load().w4o_unpack_scales(_ptr(sp), ng, N, _ptr(s))
     return s, int(bad)
+
+
+def epilogue(z, bias=None, residual=None, activation="none", rows=None, cols=None):
+    """The fused epilogue in float64 on GEMM results z (float64 [M][N], or the
+    sample rows x cols of it): act(z + bias[n]) + residual[m][n].
+
+    Follows "quant_marlin_kernel", "End-to-end flow" (the output tile flows into a
+    bias add, then an activation); the residual add after the activation is the
+    reading of a transformer block's skip connection. bias (float16 [N]) and
+    residual (float16 [M][N]) are decoded with the oracle's own binary16 decoder;
+    SiLU(z) = z / (1 + e^-z) with numpy's exp, ReLU(z) = max(z, 0)."""
+    z = np.array(z, dtype=np.float64, copy=True)
+    if bias is not None:
+        b = half_to_double(bias)
+        z += b if cols is None else b[np.asarray(cols)]
+    if activation == "silu":
+        with np.errstate(over="ignore"):
+            z = z / (1.0 + np.exp(-z))
+    elif activation == "relu":
+        z = np.maximum(z, 0.0)
+    else:
+        assert activation == "none", activation
+    if residual is not None:
+        r = half_to_double(residual)
+        z += r if rows is None else r[np.ix_(np.asarray(rows), np.asarray(cols))]
+    return z

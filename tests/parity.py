@@ -20,3 +20,26 @@ def check_within(y_gpu, y_ref, absum, what=""):
                                 [y[tuple(i)] for i in idx], [y_ref[tuple(i)] for i in idx],
                                 [bound[tuple(i)] for i in idx]))
     return float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+
+
+# Fused epilogue y = act(z + b) + r: the GEMM term grows by the activation's largest
+# slope (SiLU: 1.0998, ReLU and none: 1), plus FP32 rounding of the bias add, the
+# activation and the residual add (2^-20 covers them with margin); the output
+# rounding term is unchanged.
+LIPSCHITZ_ACT = 1.1
+REL_FP32_EPI = 2.0 ** -20
+
+
+def check_within_fused(y_gpu, y_ref, z_ref, absum, bias_abs, resid_abs, what=""):
+    y = np.asarray(y_gpu, dtype=np.float64)
+    bound = (LIPSCHITZ_ACT * REL_SUM * absum + REL_OUT * np.abs(y_ref)
+             + REL_FP32_EPI * (np.abs(z_ref) + bias_abs + resid_abs + 1.0))
+    err = np.abs(y - y_ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        worst = np.max(err / np.maximum(bound, 1e-300))
+        raise AssertionError("%s: %d of %d outside the bound (worst err/bound %.3g); first at %s: gpu %s ref %s"
+                             % (what, int(bad.sum()), bad.size, worst, idx.tolist(),
+                                [y[tuple(i)] for i in idx], [y_ref[tuple(i)] for i in idx]))
+    return float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0

@@ -277,3 +277,58 @@ def test_planted_mistakes_fail_a_pin(oracle_mod, name):
                 failures += 1
                 break
         assert failures > 0, name
+
+
+# --------------------------------------------------------------------------- fused epilogue
+def test_epilogue_bias_and_residual_are_exact_adds(oracle_mod):
+    rng = np.random.default_rng(7)
+    z = rng.integers(-1000, 1000, size=(5, 24)).astype(np.float64) / 8.0       # exact in any order
+    b = (rng.integers(-64, 64, size=24) / 4.0).astype(np.float16)
+    r = (rng.integers(-64, 64, size=(5, 24)) / 2.0).astype(np.float16)
+    assert np.array_equal(oracle_mod.epilogue(z, bias=b) - z, np.broadcast_to(b.astype(np.float64), z.shape))
+    assert np.array_equal(oracle_mod.epilogue(z, residual=r) - z, r.astype(np.float64))
+    assert np.array_equal(oracle_mod.epilogue(z), z)
+
+
+def test_epilogue_silu_matches_library_logistic(oracle_mod):
+    scipy_special = pytest.importorskip("scipy.special")
+    z = np.linspace(-40.0, 40.0, 4001)
+    got = oracle_mod.epilogue(z[None, :], activation="silu")[0]
+    want = z * scipy_special.expit(z)
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-300)
+    # special values and the reflection identity SiLU(-z) = SiLU(z) - z
+    assert oracle_mod.epilogue(np.zeros((1, 1)), activation="silu")[0, 0] == 0.0
+    assert np.allclose(oracle_mod.epilogue(-z[None, :], activation="silu")[0], got - z, rtol=1e-12, atol=1e-12)
+    big = oracle_mod.epilogue(np.array([[-1000.0, 1000.0]]), activation="silu")[0]
+    assert big[0] == 0.0 and big[1] == 1000.0
+
+
+def test_epilogue_relu_and_order_of_operations(oracle_mod):
+    z = np.array([[-3.0, -0.5, 0.0, 0.5, 3.0]])
+    b = np.array([1.0, 1.0, -1.0, -1.0, 0.0], np.float16)
+    r = np.array([[0.25, 0.25, 0.25, 0.25, 0.25]], np.float16)
+    # bias before the activation, residual after it
+    assert np.array_equal(oracle_mod.epilogue(z, bias=b, residual=r, activation="relu"),
+                          np.array([[0.25, 0.75, 0.25, 0.25, 3.25]]))
+
+
+def test_epilogue_on_the_hand_example(oracle_mod):
+    """The 1x8x8 hand example with G = K: y = [-4.125, -3.75, -4.875, -5.5, -3.125,
+    -5.75, -7.875, 22.5]; with bias b[n] = n/2 and ReLU every value is exact."""
+    x, q, s = hand_inputs(8)
+    y, _ = oracle_mod.gemm(x, q, s, 8)
+    b = (np.arange(8) / 2.0).astype(np.float16)
+    got = oracle_mod.epilogue(y, bias=b, activation="relu")[0]
+    want = np.maximum(np.array([-4.125, -3.75, -4.875, -5.5, -3.125, -5.75, -7.875, 22.5]) + np.arange(8) / 2.0, 0.0)
+    assert np.array_equal(got, want)
+
+
+def test_epilogue_sampled_matches_full(oracle_mod):
+    rng = np.random.default_rng(3)
+    z = rng.standard_normal((6, 40))
+    b = rng.standard_normal(40).astype(np.float16)
+    r = rng.standard_normal((6, 40)).astype(np.float16)
+    rows, cols = np.array([0, 5, 2]), np.array([39, 0, 17, 8])
+    full = oracle_mod.epilogue(z, bias=b, residual=r, activation="silu")
+    part = oracle_mod.epilogue(z[np.ix_(rows, cols)], bias=b, residual=r, activation="silu", rows=rows, cols=cols)
+    assert np.array_equal(part, full[np.ix_(rows, cols)])

@@ -243,7 +243,8 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int k
 }
 
 w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
-                       int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream)
+                       int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
+                       const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0)
 {
     G = norm_group(K, G);
     if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
@@ -289,6 +290,9 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.units = P.units;
     p.n_blocks = P.n_blocks;
     p.wait_limit_ns = g_wait_limit_ns;
+    p.bias = reinterpret_cast<const __half*>(bias);
+    p.residual = reinterpret_cast<const __half*>(residual);
+    p.act = act;
 
     CUtensorMap map;
     // With one row tile, a box of M rows rounded up to the 8-row swizzle atom is
@@ -382,6 +386,18 @@ w4a16_status w4a16_gemm_ws(const uint16_t* x, const uint32_t* packed, const uint
 {
     return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, false,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+w4a16_status w4a16_gemm_fused(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
+                              uint16_t* y, int M, int N, int K, int group_size, const uint16_t* bias,
+                              const uint16_t* residual, int activation, void* workspace, size_t ws_bytes,
+                              w4a16_stream_t stream)
+{
+    if (activation < W4A16_ACT_NONE || activation > W4A16_ACT_RELU) return W4A16_ERR_INVALID_ARG;
+    if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
+        return W4A16_ERR_INVALID_ARG;
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), bias, residual, activation);
 }
 
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream)

@@ -68,7 +68,24 @@ struct GemmParams {
     int x_rows;             // rows of X each TMA box brings (<= TM, a multiple of 8); the
                             // MMA's B rows past them feed only output columns >= M
     long long wait_limit_ns;
+    // Fused epilogue, applied to every FP32 result before its rounding to FP16:
+    // y = act(v + bias[n]) + residual[m][n]. Null pointers and act 0 leave v as is.
+    const __half* bias;      // [N] or null
+    const __half* residual;  // [M][N] or null (may be y itself)
+    int act;                 // 0 none, 1 SiLU, 2 ReLU
 };
+
+// The fused epilogue on the FP32 result v of output (m, n). SiLU(z) = z / (1 + e^-z).
+__device__ __forceinline__ float epilogue_op(const GemmParams& p, float v, int m, int n)
+{
+    if (p.bias) v += __half2float(p.bias[n]);
+    if (p.act == 1)
+        v = v / (1.f + expf(-v));
+    else if (p.act == 2)
+        v = fmaxf(v, 0.f);
+    if (p.residual) v += __half2float(p.residual[(size_t)m * p.N + n]);
+    return v;
+}
 
 template <int TM, int KSUB>
 struct TcCfg {
@@ -239,11 +256,12 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
 #pragma unroll
             for (int e = 0; e < CPR; ++e) {
                 if (q0 + e >= ncols) continue;
-                __half* out = p.y + (size_t)(m0 + m_first + 4 * (q0 + e)) * p.N + n;
-                out[0] = __float2half_rn(acc[e].x);
-                out[1] = __float2half_rn(acc[e].y);
-                out[2] = __float2half_rn(acc[e].z);
-                out[3] = __float2half_rn(acc[e].w);
+                const int m = m0 + m_first + 4 * (q0 + e);
+                __half* out = p.y + (size_t)m * p.N + n;
+                out[0] = __float2half_rn(epilogue_op(p, acc[e].x, m, n));
+                out[1] = __float2half_rn(epilogue_op(p, acc[e].y, m, n + 1));
+                out[2] = __float2half_rn(epilogue_op(p, acc[e].z, m, n + 2));
+                out[3] = __float2half_rn(epilogue_op(p, acc[e].w, m, n + 3));
             }
         }
     }
@@ -549,7 +567,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int m = m0 + c * 16 + e;
-                            if (m < p.M) p.y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(r[e]));
+                            if (m < p.M)
+                                p.y[(size_t)m * p.N + n] = __float2half_rn(epilogue_op(p, __uint_as_float(r[e]), m, n));
                         }
                     }
                 } else {

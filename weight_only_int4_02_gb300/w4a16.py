@@ -17,7 +17,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = ran
 
 EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error", "w4a16_packed_words",
            "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
-           "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc"]
+           "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused"]
+
+ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
 
 class W4A16Error(RuntimeError):
@@ -59,6 +61,8 @@ def lib():
         L.w4a16_plan.restype = I
         L.w4a16_gemm_noalloc.argtypes = [P, P, P, P, I, I, I, I, P]
         L.w4a16_gemm_noalloc.restype = I
+        L.w4a16_gemm_fused.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
+        L.w4a16_gemm_fused.restype = I
         _lib = L
     return _lib
 
@@ -157,4 +161,25 @@ def gemm_noalloc(x, packed, scales_packed, N, group_size, y=None, stream=None):
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check(lib().w4a16_gemm_noalloc(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                     _stream(stream)), "w4a16_gemm_noalloc")
+    return y
+
+
+def gemm_fused(x, packed, scales_packed, N, group_size, bias=None, residual=None, activation="none", y=None,
+               workspace=None, stream=None):
+    """y = act(x @ dequant(W) + bias) + residual, fused into the GEMM's epilogue.
+
+    bias: float16 [N] or None; residual: float16 [M][N] or None (may be y itself);
+    activation: "none", "silu" or "relu"; workspace: as gemm_ws, or None for the
+    library's own."""
+    M, K = x.shape
+    assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
+    for t, shape in ((bias, (N,)), (residual, (M, N))):
+        if t is not None:
+            assert t.dtype == torch.float16 and t.is_cuda and t.is_contiguous() and tuple(t.shape) == shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().w4a16_gemm_fused(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
+                                  _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
+                                  _stream(stream)), "w4a16_gemm_fused")
     return y
