@@ -449,9 +449,65 @@ def run_ours(args, rank, world):
         "kernels": {n: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3} for n, v in kernels.items()},
         "byte_ratio_fp16_over_w4g128": fp16_over_int4_byte_ratio(G),
     }
+    if args.workload == DEFAULT_WORKLOAD:
+        out["fused_epilogue"] = fused_epilogue_probe(G)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
+
+
+def fused_epilogue_probe(G):
+    """The fused epilogue on the gate/up layer (M = 16, K = 4096, N = 22016): mean time
+    per launch of the plain GEMM, of w4a16_gemm_fused with bias + SiLU, and of the plain
+    GEMM followed by torch's bias add and SiLU (two more kernels that re-read and
+    re-write Y), each launched back to back from a CUDA Graph over rotating copies of
+    the packed weights (more bytes than L2)."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    M, K, N = 16, 4096, 22016
+    q = inputs.codes(K, N, 0)
+    s = inputs.scales(K, N, G, 0)
+    packed, sp = w4a16.pack(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), G)
+    copies = [(packed.clone(), sp.clone()) for _ in range(max(2, int(400e6 // (packed.numel() * 4)) + 1))]
+    x = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
+    bias = torch.from_numpy(np.random.default_rng(1).standard_normal(N).astype(np.float16)).cuda()
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    tmp = torch.empty_like(y)
+    reps = 40
+
+    def timed(body):
+        for c in copies:
+            body(c)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+            for r in range(reps):
+                body(copies[r % len(copies)])
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    def plain(c):
+        w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream())
+
+    def fused(c):
+        w4a16.gemm_fused(x, c[0], c[1], N, G, bias=bias, activation="silu", y=y, stream=torch.cuda.current_stream())
+
+    def unfused(c):
+        w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream())
+        torch.add(y, bias, out=tmp)
+        torch.nn.functional.silu(tmp, inplace=True)
+
+    us_plain, us_fused, us_unfused = timed(plain), timed(fused), timed(unfused)
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return {"case": [M, K, N], "epilogue": "bias + SiLU", "us_gemm": us_plain, "us_fused": us_fused,
+            "us_gemm_then_torch_bias_silu": us_unfused}
 
 
 def fp16_baseline(per_case, dev, reps):

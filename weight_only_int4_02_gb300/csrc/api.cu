@@ -171,10 +171,14 @@ w4a16_status device_state(DeviceState** out)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
         int unused = 0;
-        if ((e = setup_tc<16, 4, 1>(&unused)) != cudaSuccess || (e = setup_tc<32, 4, 1>(&unused)) != cudaSuccess ||
-            (e = setup_tc<64, 4, 2>(&st.max_clusters[0])) != cudaSuccess ||
-            (e = setup_tc<128, 2, 2>(&st.max_clusters[1])) != cudaSuccess ||
-            (e = setup_tc<256, 2, 2>(&st.max_clusters[2])) != cudaSuccess)
+        if ((e = setup_tc<16, 4, 1, false>(&unused)) != cudaSuccess ||
+            (e = setup_tc<32, 4, 1, false>(&unused)) != cudaSuccess ||
+            (e = setup_tc<64, 4, 2, false>(&st.max_clusters[0])) != cudaSuccess ||
+            (e = setup_tc<128, 2, 2, false>(&st.max_clusters[1])) != cudaSuccess ||
+            (e = setup_tc<256, 2, 2, false>(&st.max_clusters[2])) != cudaSuccess ||
+            (e = setup_tc<16, 4, 1, true>(&unused)) != cudaSuccess ||
+            (e = setup_tc<32, 4, 1, true>(&unused)) != cudaSuccess || (e = setup_tc<64, 4, 2, true>(&unused)) != cudaSuccess ||
+            (e = setup_tc<128, 2, 2, true>(&unused)) != cudaSuccess || (e = setup_tc<256, 2, 2, true>(&unused)) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
             void* fn = nullptr;
@@ -301,12 +305,17 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     // Clusters split a stage's X blocks between their CTAs: one 2-D TMA per block.
     if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
+    const bool epi = bias || residual || act != 0;
     switch (P.tm) {
-        case 16: e = launch_tc<16, 4, 1>(map, p, stream); break;
-        case 32: e = launch_tc<32, 4, 1>(map, p, stream); break;
-        case 64: e = launch_tc<64, 4, 2>(map, p, stream); break;
-        case 128: e = launch_tc<128, 2, 2>(map, p, stream); break;
-        default: e = launch_tc<256, 2, 2>(map, p, stream); break;
+        case 16: e = epi ? launch_tc<16, 4, 1, true>(map, p, stream) : launch_tc<16, 4, 1, false>(map, p, stream); break;
+        case 32: e = epi ? launch_tc<32, 4, 1, true>(map, p, stream) : launch_tc<32, 4, 1, false>(map, p, stream); break;
+        case 64: e = epi ? launch_tc<64, 4, 2, true>(map, p, stream) : launch_tc<64, 4, 2, false>(map, p, stream); break;
+        case 128:
+            e = epi ? launch_tc<128, 2, 2, true>(map, p, stream) : launch_tc<128, 2, 2, false>(map, p, stream);
+            break;
+        default:
+            e = epi ? launch_tc<256, 2, 2, true>(map, p, stream) : launch_tc<256, 2, 2, false>(map, p, stream);
+            break;
     }
     return from_cuda(e);
 }

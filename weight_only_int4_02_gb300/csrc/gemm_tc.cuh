@@ -75,17 +75,23 @@ struct GemmParams {
     int act;                 // 0 none, 1 SiLU, 2 ReLU
 };
 
-// The fused epilogue on the FP32 result v of output (m, n). SiLU(z) = z / (1 + e^-z).
-__device__ __forceinline__ float epilogue_op(const GemmParams& p, float v, int m, int n)
+// The fused epilogue on the FP32 result v: act(v + b) + r, with b and r already
+// loaded (0 when absent). SiLU(z) = z / (1 + e^-z) with the fast exponential and
+// division (about 2^-21 relative error). Callers load every bias and
+// residual value they need before their stores of Y: the compiler cannot tell
+// that those stores do not alias the loads, and would otherwise wait out each
+// load after each store.
+__device__ __forceinline__ float epilogue_op(int act, float v, float b, float r)
 {
-    if (p.bias) v += __half2float(p.bias[n]);
-    if (p.act == 1)
-        v = v / (1.f + expf(-v));
-    else if (p.act == 2)
+    v += b;
+    if (act == 1)
+        v = __fdividef(v, 1.f + __expf(-v));   // e^-v overflowing to inf gives -0, the limit
+    else if (act == 2)
         v = fmaxf(v, 0.f);
-    if (p.residual) v += __half2float(p.residual[(size_t)m * p.N + n]);
-    return v;
+    return v + r;
 }
+
+__device__ __forceinline__ float load_half(const __half* base, size_t i) { return base ? __half2float(base[i]) : 0.f; }
 
 template <int TM, int KSUB>
 struct TcCfg {
@@ -213,7 +219,7 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
 // columns j/32, j/32 + 4, j/32 + 8, ... A round issues L4 such loads (L4/NCP
 // columns of NCP contributors) before any is added, so it costs one global
 // round trip. n_base is the tile's first output feature.
-template <int TM, int NCP, int L4>
+template <int TM, int NCP, int L4, bool EPI>
 __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
                                            int n_base)
 {
@@ -222,6 +228,9 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
     const int m_first = threadIdx.x >> 5;
     const int ncols = valid > m_first ? (valid - m_first + 3) >> 2 : 0;   // columns m_first + 4q, q < ncols
     const int n = n_base + 4 * rg;
+    float b4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (EPI && p.bias && n < p.N)
+        for (int j = 0; j < 4; ++j) b4[j] = __half2float(p.bias[n + j]);
     for (int q0 = 0; q0 < ncols; q0 += CPR) {
         float4 acc[CPR];
 #pragma unroll
@@ -258,16 +267,28 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
                 if (q0 + e >= ncols) continue;
                 const int m = m0 + m_first + 4 * (q0 + e);
                 __half* out = p.y + (size_t)m * p.N + n;
-                out[0] = __float2half_rn(epilogue_op(p, acc[e].x, m, n));
-                out[1] = __float2half_rn(epilogue_op(p, acc[e].y, m, n + 1));
-                out[2] = __float2half_rn(epilogue_op(p, acc[e].z, m, n + 2));
-                out[3] = __float2half_rn(epilogue_op(p, acc[e].w, m, n + 3));
+                if constexpr (EPI) {
+                    const size_t ri = (size_t)m * p.N + n;
+                    const float r0 = load_half(p.residual, ri), r1 = load_half(p.residual, ri + 1);
+                    const float r2 = load_half(p.residual, ri + 2), r3 = load_half(p.residual, ri + 3);
+                    out[0] = __float2half_rn(epilogue_op(p.act, acc[e].x, b4[0], r0));
+                    out[1] = __float2half_rn(epilogue_op(p.act, acc[e].y, b4[1], r1));
+                    out[2] = __float2half_rn(epilogue_op(p.act, acc[e].z, b4[2], r2));
+                    out[3] = __float2half_rn(epilogue_op(p.act, acc[e].w, b4[3], r3));
+                } else {
+                    out[0] = __float2half_rn(acc[e].x);
+                    out[1] = __float2half_rn(acc[e].y);
+                    out[2] = __float2half_rn(acc[e].z);
+                    out[3] = __float2half_rn(acc[e].w);
+                }
             }
         }
     }
 }
 
-template <int TM, int KSUB, int CL>
+// EPI: the instantiation with the fused epilogue (bias, activation, residual);
+// the plain one carries none of its code.
+template <int TM, int KSUB, int CL, bool EPI>
 __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
@@ -553,6 +574,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
             const int valid = min(TM, p.M - m0);
             const int chunks = (valid + 15) >> 4;
             const bool split = (g.kb != 0 || g.ke != p.iters);
+            // The bias of this row is fetched while the MMAs run.
+            const float bias_n = (EPI && n < p.N) ? load_half(p.bias, n) : 0.f;
             // All four epilogue warps leave together: they share named barriers.
             const bool ok = wait_warp(dfull_bar(d), dph, ctl);
             if (named_bar_or(1, 128, !ok)) break;
@@ -564,11 +587,27 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 tmem_ld16(d_tmem + c * 16, r);
                 if (!split) {
                     if (n < p.N) {
+                        if constexpr (EPI) {
+                            const float bv = bias_n;
+                            float rv[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int m = m0 + c * 16 + e;
-                            if (m < p.M)
-                                p.y[(size_t)m * p.N + n] = __float2half_rn(epilogue_op(p, __uint_as_float(r[e]), m, n));
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = m0 + c * 16 + e;
+                                rv[e] = m < p.M ? load_half(p.residual, (size_t)m * p.N + n) : 0.f;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = m0 + c * 16 + e;
+                                if (m < p.M)
+                                    p.y[(size_t)m * p.N + n] =
+                                        __float2half_rn(epilogue_op(p.act, __uint_as_float(r[e]), bv, rv[e]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = m0 + c * 16 + e;
+                                if (m < p.M) p.y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(r[e]));
+                            }
                         }
                     }
                 } else {
@@ -608,11 +647,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                     // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
                     constexpr int L4 = KSUB == 4 ? 8 : 16;
                     if (ncontrib <= 2)
-                        fix_reduce<TM, 2, L4>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                        fix_reduce<TM, 2, L4, EPI>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                     else if (ncontrib <= 4)
-                        fix_reduce<TM, 4, L4>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                        fix_reduce<TM, 4, L4, EPI>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                     else
-                        fix_reduce<TM, 8, L4>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                        fix_reduce<TM, 8, L4, EPI>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                 }
                 named_bar_sync(1, 128);
             }
@@ -631,10 +670,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     }
 }
 
-template <int TM, int KSUB, int CL>
+template <int TM, int KSUB, int CL, bool EPI>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream);
 
-template <int TM, int KSUB, int CL>
+template <int TM, int KSUB, int CL, bool EPI>
 cudaError_t setup_tc(int* max_clusters);
 
 }  // namespace w4a16

@@ -1,4 +1,4 @@
-// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL>; included by one .cu file per tile shape.
+// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL, EPI>; included by one .cu file per tile shape.
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -6,10 +6,10 @@ namespace w4a16 {
 
 // Dynamic shared memory, and for clusters the number of clusters the device can
 // hold at once (0 when the query fails).
-template <int TM, int KSUB, int CL>
+template <int TM, int KSUB, int CL, bool EPI>
 cudaError_t setup_tc(int* max_clusters)
 {
-    auto kernel = w4a16_tc_kernel<TM, KSUB, CL>;
+    auto kernel = w4a16_tc_kernel<TM, KSUB, CL, EPI>;
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<TM, KSUB>::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -34,7 +34,7 @@ cudaError_t setup_tc(int* max_clusters)
     return cudaSuccess;
 }
 
-template <int TM, int KSUB, int CL>
+template <int TM, int KSUB, int CL, bool EPI>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
@@ -57,13 +57,15 @@ cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL>, tmap, p);
+    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL, EPI>, tmap, p);
 }
 
 }  // namespace w4a16
 
-#define W4A16_INSTANTIATE_TC(TM, KSUB, CL)                                                              \
-    namespace w4a16 {                                                                                   \
-    template cudaError_t setup_tc<TM, KSUB, CL>(int*);                                                  \
-    template cudaError_t launch_tc<TM, KSUB, CL>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
+#define W4A16_INSTANTIATE_TC(TM, KSUB, CL)                                                                    \
+    namespace w4a16 {                                                                                         \
+    template cudaError_t setup_tc<TM, KSUB, CL, false>(int*);                                                 \
+    template cudaError_t setup_tc<TM, KSUB, CL, true>(int*);                                                  \
+    template cudaError_t launch_tc<TM, KSUB, CL, false>(const CUtensorMap&, const GemmParams&, cudaStream_t); \
+    template cudaError_t launch_tc<TM, KSUB, CL, true>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
     }
