@@ -242,3 +242,77 @@ def test_device_plan_matches_host_mirror(w):
         path, tm, grid = w.plan(M, N, K, 128)
         P = mirror_plan(M, N, K, 128, sms)
         assert (tm, grid) == (P["tm"], P["grid"]), (M, N, K, tm, grid, P["tm"], P["grid"])
+
+
+def _chain(w, x_d, layers, G, stream_sync):
+    """Back-to-back GEMMs where each one's X is the previous one's output (fused
+    SiLU on the widest layer, an in-place residual on the last), all on one stream."""
+    outs = []
+    h = x_d
+    for i, (packed, sp, N, epi) in enumerate(layers):
+        if epi == "silu":
+            h = w.gemm_fused(h, packed, sp, N, G, activation="silu")
+        elif epi == "residual":
+            r = outs[0][:, :N].clone()   # a fresh buffer, added to in place
+            h = w.gemm_fused(h, packed, sp, N, G, residual=r, y=r)
+        else:
+            h = w.gemm(h, packed, sp, N, G)
+        outs.append(h)
+        if stream_sync:
+            torch.cuda.synchronize()
+    return outs
+
+
+def test_chained_gemms_read_the_previous_output(w, oracle_mod):
+    """Each launch may start before the previous one ends (programmatic dependent
+    launch) but must read X only after it completes: a chain launched back to back,
+    plain and captured in a CUDA Graph, equals the same chain with a synchronisation
+    between launches bit for bit, and every stage matches the oracle applied to the
+    GPU's own input of that stage."""
+    G, M = 128, 16
+    dims = [(4096, 4096, None), (4096, 11008, "silu"), (11008, 4096, None), (4096, 4096, "residual")]
+    rng_seed = 40
+    layers, host = [], []
+    for i, (K, N, epi) in enumerate(dims):
+        q = inputs.codes(K, N, rng_seed + i)
+        s = inputs.scales(K, N, G, rng_seed + i, "halfnormal", 0.01)
+        packed, sp = w.pack(to_dev(q), to_dev(s), G)
+        layers.append((packed, sp, N, epi))
+        host.append((q, s))
+    x = inputs.activations(M, 4096, rng_seed)
+    ref = _chain(w, to_dev(x), layers, G, stream_sync=True)
+    ref = [o.clone() for o in ref]
+    got = _chain(w, to_dev(x), layers, G, stream_sync=False)
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    # the same chain captured in a CUDA graph (workspace allocated already)
+    xg = to_dev(x)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        outs_g = _chain(w, xg, layers, G, stream_sync=False)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(outs_g, ref):
+        assert torch.equal(a, b)
+    # each stage against the oracle on its actual input
+    cols = np.random.default_rng(1).choice(4096, 128, replace=False)
+    prev = x
+    for i, ((q, s), (_, _, N, epi)) in enumerate(zip(host, layers)):
+        rows = np.arange(M)
+        c = cols[cols < N]
+        z, absum = oracle_mod.gemm_sample(prev, q, s, G, rows, c)
+        y = ref[i].cpu().numpy()
+        if epi is None:
+            from tests.parity import check_within
+            check_within(y[:, c], z, absum, "chain stage %d" % i)
+        else:
+            from tests.parity import check_within_fused
+            resid = ref[0].cpu().numpy()[:, :N] if epi == "residual" else None
+            y_ref = oracle_mod.epilogue(z, residual=resid, activation="silu" if epi == "silu" else "none",
+                                        rows=rows if resid is not None else None, cols=c if resid is not None else None)
+            check_within_fused(y[:, c], y_ref, z, absum, 0.0,
+                               np.abs(resid[np.ix_(rows, c)].astype(np.float64)) if resid is not None else 0.0,
+                               "chain stage %d" % i)
+        prev = y
