@@ -451,6 +451,7 @@ def run_ours(args, rank, world):
     }
     if args.workload == DEFAULT_WORKLOAD:
         out["fused_epilogue"] = fused_epilogue_probe(G)
+        out["layer_chain"] = layer_chain_probe(G)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
@@ -508,6 +509,71 @@ def fused_epilogue_probe(G):
         raise RuntimeError("a kernel wait timed out")
     return {"case": [M, K, N], "epilogue": "bias + SiLU", "us_gemm": us_plain, "us_fused": us_fused,
             "us_gemm_then_torch_bias_silu": us_unfused}
+
+
+def layer_chain_probe(G):
+    """A Llama-2-7B-like decode layer as a chain of dependent GEMMs (each X is the
+    previous output, so every launch waits for its predecessor before reading X):
+    QKV (4096 -> 12288), O (the first 4096 columns -> 4096, residual add fused),
+    gate/up (4096 -> 22016, SiLU fused), down (the first 11008 columns -> 4096,
+    residual add fused); the two column slices are torch copies (attention and the
+    gate product, which are not W4A16 work, would produce fresh tensors there).
+    Mean time per chain from a CUDA Graph of back-to-back chains over rotating
+    copies of the packed weights, at M = 1 and 16."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    dims = [(4096, 12288), (4096, 4096), (4096, 22016), (11008, 4096)]
+    packs = []
+    for i, (K, N) in enumerate(dims):
+        q = inputs.codes(K, N, 50 + i)
+        s = inputs.scales(K, N, G, 50 + i, "halfnormal", 0.01)
+        pk = w4a16.pack(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), G)
+        packs.append(pk)
+    layer_bytes = sum(p[0].numel() * 4 + p[1].numel() * 2 for p in packs)
+    rot = max(2, int(500e6 // layer_bytes) + 1)
+    sets = [[(p[0].clone(), p[1].clone()) for p in packs] for _ in range(rot)]
+    out = {"layers": "QKV 4096x12288, O 4096x4096 (+residual), gate/up 4096x22016 (SiLU), down 11008x4096 (+residual)",
+           "weight_bytes_per_chain": layer_bytes}
+    reps = 20
+    for M in (1, 16):
+        x = torch.from_numpy(inputs.activations(M, 4096, 7)).cuda()
+        h_qkv = torch.empty((M, 12288), dtype=torch.float16, device="cuda")
+        a_in = torch.empty((M, 4096), dtype=torch.float16, device="cuda")
+        h_o = torch.empty((M, 4096), dtype=torch.float16, device="cuda")
+        h_gu = torch.empty((M, 22016), dtype=torch.float16, device="cuda")
+        d_in = torch.empty((M, 11008), dtype=torch.float16, device="cuda")
+        h_out = torch.empty((M, 4096), dtype=torch.float16, device="cuda")
+
+        def chain(ws):
+            st = torch.cuda.current_stream()
+            w4a16.gemm(x, ws[0][0], ws[0][1], 12288, G, y=h_qkv, stream=st)
+            a_in.copy_(h_qkv[:, :4096])
+            h_o.copy_(x)
+            w4a16.gemm_fused(a_in, ws[1][0], ws[1][1], 4096, G, residual=h_o, y=h_o, stream=st)
+            w4a16.gemm_fused(h_o, ws[2][0], ws[2][1], 22016, G, activation="silu", y=h_gu, stream=st)
+            d_in.copy_(h_gu[:, :11008])
+            h_out.copy_(h_o)
+            w4a16.gemm_fused(d_in, ws[3][0], ws[3][1], 4096, G, residual=h_out, y=h_out, stream=st)
+
+        for ws in sets:
+            chain(ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+            for r in range(reps):
+                chain(sets[r % rot])
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        out["M=%d" % M] = {"us_per_chain": us, "weight_gbs": layer_bytes / (us * 1e3)}
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return out
 
 
 def fp16_baseline(per_case, dev, reps):
