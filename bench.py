@@ -248,6 +248,23 @@ def cpu_baseline(wl, budget_s=15.0):
 
 
 # --------------------------------------------------------------------------- our arm
+def max_over_ranks(value, world, device):
+    """The largest value over the replicas (the slowest one sets the job's time);
+    the value itself when there is one rank. device: where the all-reduce tensor
+    lives (the GPU for NCCL, "cpu" for gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_replica, world, seconds):
+    """Whole-job throughput: every replica processes its own units (weak scaling)."""
+    return units_per_replica * world / seconds
+
+
 def run_ours(args, rank, world):
     import torch
     from weight_only_int4_02_gb300 import w4a16
@@ -332,11 +349,7 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop(wall0, wall1)
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms_total / K
     status = w4a16.check_device_status()
     if status != w4a16.OK:
@@ -349,7 +362,7 @@ def run_ours(args, rank, world):
             grp_ms[gi, b] = cud.elapsed_ms(evs[gi][b], evs[gi][b + 1])
     grp_mean = grp_ms.mean(axis=0)
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
-    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(step_flops, world, ms_step * 1e-3) / 1e12
 
     # ---- per kernel instance (all launches of one M use one instance) and per M
     kernels = {}
@@ -633,11 +646,7 @@ def run_e2e(per_case, G, dev, K, W, world):
         g.replay()
     b.record()
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / K
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(a.elapsed_time(b) / K, world, dev)
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
     ok = all(torch.equal(yh, c["y"].cpu()) for c, yh in zip(per_case, ys_h))
     return {"value": step_flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
