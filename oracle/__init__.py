@@ -39,11 +39,11 @@ def _load():
         lib.w4o_half_to_double.argtypes = [ctypes.c_uint16]
         lib.w4o_half_to_double.restype = ctypes.c_double
         lib.w4o_decode_halves.argtypes = [P, P, ctypes.c_size_t]
-        lib.w4o_dequant.argtypes = [P, P, I, I, I, P]
-        lib.w4o_gemm.argtypes = [P, P, P, I, I, I, I, P, P, I]
-        lib.w4o_gemm.restype = I
-        lib.w4o_gemm_sample.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
-        lib.w4o_gemm_sample.restype = I
+        lib.w4o_dequant_zp.argtypes = [P, P, P, I, I, I, P]
+        lib.w4o_gemm_zp.argtypes = [P, P, P, P, I, I, I, I, P, P, I]
+        lib.w4o_gemm_zp.restype = I
+        lib.w4o_gemm_sample_zp.argtypes = [P, P, P, P, I, I, I, I, P, I, P, I, P, P, I]
+        lib.w4o_gemm_sample_zp.restype = I
         lib.w4o_packed_words.argtypes = [I, I]
         lib.w4o_packed_words.restype = ctypes.c_size_t
         lib.w4o_locate.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(I)]
@@ -52,6 +52,8 @@ def _load():
         lib.w4o_pack.argtypes = [P, I, I, P]
         lib.w4o_unpack_scales.argtypes = [P, I, I, P]
         lib.w4o_unpack_scales.restype = ctypes.c_longlong
+        lib.w4o_unpack_zeros.argtypes = [P, I, I, P]
+        lib.w4o_unpack_zeros.restype = ctypes.c_longlong
         _lib = lib
     return _lib
 
@@ -80,14 +82,24 @@ def half_to_double(bits):
     return out
 
 
-def dequant(q, s, G):
-    """w[k][n] = (q[k][n] - 8) * s[k // G][n] in float64."""
+def _zeros(z, K, N, G):
+    """Zero-points as a contiguous uint8 [ceil(K/G)][N] array, or None for 8."""
+    if z is None:
+        return None
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    assert z.shape == (n_groups(K, G), N) and int(z.max(initial=0)) <= 15
+    return z
+
+
+def dequant(q, s, G, z=None):
+    """w[k][n] = (q[k][n] - z[k // G][n]) * s[k // G][n] in float64 (z = 8 when None)."""
     q = np.ascontiguousarray(q, dtype=np.uint8)
     s = _bits16(s)
     K, N = q.shape
     assert s.shape == (n_groups(K, G), N)
+    z = _zeros(z, K, N, G)
     w = np.empty((K, N), np.float64)
-    _load().w4o_dequant(_ptr(q), _ptr(s), K, N, G, _ptr(w))
+    _load().w4o_dequant_zp(_ptr(q), _ptr(s), _ptr(z) if z is not None else None, K, N, G, _ptr(w))
     return w
 
 
@@ -95,35 +107,38 @@ def _threads(threads):
     return threads if threads else (os.cpu_count() or 1)
 
 
-def gemm(x, q, s, G, threads=None):
-    """(y, absum): y = x @ dequant(q, s) in float64 (k ascending), absum = sum |x*w|."""
+def gemm(x, q, s, G, threads=None, z=None):
+    """(y, absum): y = x @ dequant(q, s, z) in float64 (k ascending), absum = sum |x*w|."""
     x = _bits16(x)
     q = np.ascontiguousarray(q, dtype=np.uint8)
     s = _bits16(s)
     M, K = x.shape
     K2, N = q.shape
     assert K == K2 and s.shape == (n_groups(K, G), N)
+    z = _zeros(z, K, N, G)
     y = np.empty((M, N), np.float64)
     a = np.empty((M, N), np.float64)
-    rc = _load().w4o_gemm(_ptr(x), _ptr(q), _ptr(s), M, N, K, G, _ptr(y), _ptr(a),
-                          _threads(threads))
+    rc = _load().w4o_gemm_zp(_ptr(x), _ptr(q), _ptr(s), _ptr(z) if z is not None else None, M, N, K, G,
+                             _ptr(y), _ptr(a), _threads(threads))
     assert rc == 0
     return y, a
 
 
-def gemm_sample(x, q, s, G, rows, cols, threads=None):
+def gemm_sample(x, q, s, G, rows, cols, threads=None, z=None):
     """(y, absum) restricted to rows x cols: y[i][j] = y_ref[rows[i]][cols[j]]."""
     x = _bits16(x)
     q = np.ascontiguousarray(q, dtype=np.uint8)
     s = _bits16(s)
     M, K = x.shape
     N = q.shape[1]
+    z = _zeros(z, K, N, G)
     rows = np.ascontiguousarray(rows, dtype=np.int32)
     cols = np.ascontiguousarray(cols, dtype=np.int32)
     y = np.empty((rows.size, cols.size), np.float64)
     a = np.empty((rows.size, cols.size), np.float64)
-    rc = _load().w4o_gemm_sample(_ptr(x), _ptr(q), _ptr(s), M, N, K, G, _ptr(rows), rows.size,
-                                 _ptr(cols), cols.size, _ptr(y), _ptr(a), _threads(threads))
+    rc = _load().w4o_gemm_sample_zp(_ptr(x), _ptr(q), _ptr(s), _ptr(z) if z is not None else None, M, N, K, G,
+                                    _ptr(rows), rows.size, _ptr(cols), cols.size, _ptr(y), _ptr(a),
+                                    _threads(threads))
     assert rc == 0
     return y, a
 
@@ -163,6 +178,16 @@ def unpack_scales(sp, ng, N):
     s = np.empty((ng, N), np.uint16)
     bad = _load().w4o_unpack_scales(_ptr(sp), ng, N, _ptr(s))
     return s, int(bad)
+
+
+def unpack_zeros(zp, ng, N):
+    """(z[ng][N] as uint8, number of padding nibbles that are not 8) from the
+    tile-ordered 4-bit zero-points."""
+    zp = np.ascontiguousarray(zp, dtype=np.uint8)
+    assert zp.size == -(-N // 128) * ng * 64
+    z = np.empty((ng, N), np.uint8)
+    bad = _load().w4o_unpack_zeros(_ptr(zp), ng, N, _ptr(z))
+    return z, int(bad)
 
 
 def epilogue(z, bias=None, residual=None, activation="none", rows=None, cols=None):

@@ -7,7 +7,7 @@
  *
  * What it computes (the plain definition, no blocking, no reordering):
  *
- *   w[k][n]   = (q[k][n] - 8) * s[k / G][n]                       (dequantisation)
+ *   w[k][n]   = (q[k][n] - z[k / G][n]) * s[k / G][n]             (dequantisation)
  *   y[m][n]   = sum_{k=0}^{K-1} x[m][k] * w[k][n]   (k ascending, FP64)
  *   abs[m][n] = sum_{k=0}^{K-1} |x[m][k] * w[k][n]|               (tolerance term)
  *
@@ -17,12 +17,17 @@
  * a thread unpacks the codes to FP16 and multiplies by the group scale; the
  * tensor-core MMA multiplies the dequantised weight tile by the FP16
  * activations. "End-to-end flow": activations (tokens x in-features) times
- * weights (in-features x out-features). The zero-point 8 (codes 0..15 map to
- * -8..7) is the symmetric reading of the pages, which never print a zero-point.
+ * weights (in-features x out-features). The zero-point z is 8 for every group
+ * (codes 0..15 map to -8..7) unless a zero-point array is given: the symmetric
+ * reading of the pages, which never print a zero-point. The asymmetric form, one
+ * integer zero-point 0..15 per (group, column), is the reading of "Low-Precision
+ * Quantization Kernels in Production" (llms.blog), section 1, which names AWQ
+ * checkpoints (whose 4-bit weights carry a per-group zero-point) among the
+ * formats the same kernel family serves.
  *
  * FP16 inputs arrive as IEEE-754 binary16 bit patterns and are decoded by this
  * file's own decoder (sign, 5-bit exponent with bias 15, 10-bit fraction,
- * subnormals). Every product x*(q-8)*s has at most 26 significant bits, so it
+ * subnormals). Every product x*(q-z)*s has at most 26 significant bits, so it
  * is exact in FP64; only the k-ascending summation rounds.
  *
  * The packed-layout functions at the end restate the packed word layout that
@@ -60,30 +65,38 @@ void w4o_decode_halves(const uint16_t* h, double* out, size_t count)
 /* Group index of row k. group_size == K means one group per column. */
 static int group_of(int k, int G) { return k / G; }
 
-/* Dequantise column n of the weight matrix into w_col[K]. */
-static void dequant_column(const uint8_t* q, const uint16_t* s, int K, int N, int G,
+/* Dequantise column n of the weight matrix into w_col[K]. z is [ceil(K/G)][N]
+ * integer zero-points, or NULL for the fixed zero-point 8. */
+static void dequant_column(const uint8_t* q, const uint16_t* s, const uint8_t* z, int K, int N, int G,
                            int n, double* w_col)
 {
     for (int k = 0; k < K; ++k) {
+        int g = group_of(k, G);
         int code = q[(size_t)k * N + n];
-        double scale = w4o_half_to_double(s[(size_t)group_of(k, G) * N + n]);
-        w_col[k] = (double)(code - 8) * scale;
+        int zero = z ? z[(size_t)g * N + n] : 8;
+        double scale = w4o_half_to_double(s[(size_t)g * N + n]);
+        w_col[k] = (double)(code - zero) * scale;
     }
 }
 
 /* Full dequantised matrix w[K][N] (FP64), for inspection in tests. */
-void w4o_dequant(const uint8_t* q, const uint16_t* s, int K, int N, int G, double* w)
+void w4o_dequant_zp(const uint8_t* q, const uint16_t* s, const uint8_t* z, int K, int N, int G, double* w)
 {
     double* col = (double*)malloc(sizeof(double) * (size_t)K);
     for (int n = 0; n < N; ++n) {
-        dequant_column(q, s, K, N, G, n, col);
+        dequant_column(q, s, z, K, N, G, n, col);
         for (int k = 0; k < K; ++k) w[(size_t)k * N + n] = col[k];
     }
     free(col);
 }
 
+void w4o_dequant(const uint8_t* q, const uint16_t* s, int K, int N, int G, double* w)
+{
+    w4o_dequant_zp(q, s, NULL, K, N, G, w);
+}
+
 typedef struct {
-    const uint16_t* x; const uint8_t* q; const uint16_t* s;
+    const uint16_t* x; const uint8_t* q; const uint16_t* s; const uint8_t* z;
     int M, N, K, G;
     const int* rows; int nrows;      /* rows of y to evaluate           */
     const int* cols; int ncols;      /* columns of y to evaluate        */
@@ -97,7 +110,7 @@ static void* worker(void* arg)
     job_t* j = (job_t*)arg;
     double* w_col = (double*)malloc(sizeof(double) * (size_t)j->K);
     for (int c = j->col_begin; c < j->col_end; ++c) {
-        dequant_column(j->q, j->s, j->K, j->N, j->G, j->cols[c], w_col);
+        dequant_column(j->q, j->s, j->z, j->K, j->N, j->G, j->cols[c], w_col);
         for (int r = 0; r < j->nrows; ++r) {
             const double* xr = j->xd + (size_t)r * j->K;
             double acc = 0.0, acc_abs = 0.0;
@@ -117,14 +130,15 @@ static void* worker(void* arg)
 /*
  * y[r][c] = y_ref[rows[r]][cols[c]] for the listed rows and columns (every
  * element is an independent sum, so a sample of elements is exact for those
- * elements). x is [M][K], q is [K][N] (codes 0..15), s is [ceil(K/G)][N].
+ * elements). x is [M][K], q is [K][N] (codes 0..15), s is [ceil(K/G)][N], z is
+ * [ceil(K/G)][N] (zero-points 0..15) or NULL for 8.
  * Work is split over `threads` POSIX threads by column; the arithmetic of each
  * element does not depend on the split.
  */
-int w4o_gemm_sample(const uint16_t* x, const uint8_t* q, const uint16_t* s,
-                    int M, int N, int K, int G,
-                    const int* rows, int nrows, const int* cols, int ncols,
-                    double* y, double* absum, int threads)
+int w4o_gemm_sample_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, const uint8_t* z,
+                       int M, int N, int K, int G,
+                       const int* rows, int nrows, const int* cols, int ncols,
+                       double* y, double* absum, int threads)
 {
     if (M < 0 || N < 0 || K < 0 || G <= 0 || nrows < 0 || ncols < 0) return 1;
     double* xd = (double*)malloc(sizeof(double) * ((size_t)nrows * K + 1));
@@ -140,7 +154,7 @@ int w4o_gemm_sample(const uint16_t* x, const uint8_t* q, const uint16_t* s,
     pthread_t* tid = (pthread_t*)malloc(sizeof(pthread_t) * threads);
     job_t* jobs = (job_t*)malloc(sizeof(job_t) * threads);
     for (int t = 0; t < threads; ++t) {
-        job_t j = {x, q, s, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+        job_t j = {x, q, s, z, M, N, K, G, rows, nrows, cols, ncols, y, absum,
                    (int)((long long)ncols * t / threads),
                    (int)((long long)ncols * (t + 1) / threads), xd};
         jobs[t] = j;
@@ -152,17 +166,31 @@ int w4o_gemm_sample(const uint16_t* x, const uint8_t* q, const uint16_t* s,
     return 0;
 }
 
+int w4o_gemm_sample(const uint16_t* x, const uint8_t* q, const uint16_t* s,
+                    int M, int N, int K, int G,
+                    const int* rows, int nrows, const int* cols, int ncols,
+                    double* y, double* absum, int threads)
+{
+    return w4o_gemm_sample_zp(x, q, s, NULL, M, N, K, G, rows, nrows, cols, ncols, y, absum, threads);
+}
+
 /* The whole output: y[M][N] and absum[M][N]. */
-int w4o_gemm(const uint16_t* x, const uint8_t* q, const uint16_t* s,
-             int M, int N, int K, int G, double* y, double* absum, int threads)
+int w4o_gemm_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, const uint8_t* z,
+                int M, int N, int K, int G, double* y, double* absum, int threads)
 {
     int* rows = (int*)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
     int* cols = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
     for (int i = 0; i < M; ++i) rows[i] = i;
     for (int i = 0; i < N; ++i) cols[i] = i;
-    int rc = w4o_gemm_sample(x, q, s, M, N, K, G, rows, M, cols, N, y, absum, threads);
+    int rc = w4o_gemm_sample_zp(x, q, s, z, M, N, K, G, rows, M, cols, N, y, absum, threads);
     free(rows); free(cols);
     return rc;
+}
+
+int w4o_gemm(const uint16_t* x, const uint8_t* q, const uint16_t* s,
+             int M, int N, int K, int G, double* y, double* absum, int threads)
+{
+    return w4o_gemm_zp(x, q, s, NULL, M, N, K, G, y, absum, threads);
 }
 
 /*
@@ -177,6 +205,8 @@ int w4o_gemm(const uint16_t* x, const uint8_t* q, const uint16_t* s,
  *
  * Positions with k >= K or n >= N hold code 8 (weight 0).
  * Scales: scales_packed[(nt * ng + g) * 128 + n_in] = s[g][nt*128 + n_in], 0 for n >= N.
+ * Zero-points: byte (nt * ng + g) * 64 + b of zeros_packed holds z[g][nt*128 + 2b] in
+ * bits 0..3 and z[g][nt*128 + 2b + 1] in bits 4..7; columns n >= N hold 8.
  */
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -241,6 +271,24 @@ long long w4o_unpack_scales(const uint16_t* sp, int ng, int N, uint16_t* s)
                 uint16_t v = sp[((size_t)nt * ng + g) * 128 + n_in];
                 if (n < N) s[(size_t)g * N + n] = v;
                 else if (v != 0) ++bad_pad;
+            }
+    return bad_pad;
+}
+
+/* Unpack zero-points z[ng][N] from the tile-ordered 4-bit copy; returns the
+ * number of padding nibbles that are not 8. */
+long long w4o_unpack_zeros(const uint8_t* zp, int ng, int N, uint8_t* z)
+{
+    int NT = ceil_div(N, 128);
+    long long bad_pad = 0;
+    for (int nt = 0; nt < NT; ++nt)
+        for (int g = 0; g < ng; ++g)
+            for (int n_in = 0; n_in < 128; ++n_in) {
+                int n = nt * 128 + n_in;
+                uint8_t byte = zp[((size_t)nt * ng + g) * 64 + n_in / 2];
+                uint8_t v = (uint8_t)((byte >> (4 * (n_in % 2))) & 0xF);
+                if (n < N) z[(size_t)g * N + n] = v;
+                else if (v != 8) ++bad_pad;
             }
     return bad_pad;
 }

@@ -6,7 +6,11 @@
 * the hand-worked 1x8x8 example in tests/golden/hand_1x8x8.txt;
 * invariants: zero scales, all codes 8, a single nonzero code, linearity in x,
   doubling the scales, one-hot rows of x;
-* mutants: a copy of the oracle with one planted mistake must fail a pin.
+* mutants: a copy of the oracle with one planted mistake must fail a pin;
+* per-group zero-points: brute force in exact rationals, zero-points of 8 equal
+  the symmetric form bit for bit, codes equal to their zero-points give 0, the
+  closed form of a unit step in one zero-point, numpy's matmul on the expanded
+  weights, the hand example with zero-point n in column n.
 """
 import os
 import re
@@ -59,8 +63,9 @@ def test_half_decoder_all_patterns(oracle_mod):
         assert oracle_mod.half_to_double(np.array([b], np.uint16))[0] == v
 
 
-def exact_reference(x, q, s, G):
-    """Exact rationals: each FP16 value converts to Fraction without rounding."""
+def exact_reference(x, q, s, G, z=None):
+    """Exact rationals: each FP16 value converts to Fraction without rounding.
+    z: integer zero-points [ceil(K/G)][N], or None for 8."""
     M, K = x.shape
     N = q.shape[1]
     xf = [[Fraction(float(v)) for v in row] for row in x.astype(np.float64)]
@@ -71,7 +76,8 @@ def exact_reference(x, q, s, G):
         for n in range(N):
             acc, acc_abs = Fraction(0), Fraction(0)
             for k in range(K):
-                t = xf[m][k] * (int(q[k][n]) - 8) * sf[k // G][n]
+                zero = 8 if z is None else int(z[k // G][n])
+                t = xf[m][k] * (int(q[k][n]) - zero) * sf[k // G][n]
                 acc += t
                 acc_abs += abs(t)
             y[m][n], a[m][n] = acc, acc_abs
@@ -239,7 +245,13 @@ def test_scales_unpack(oracle_mod):
 
 
 MUTANTS = {
-    "zero_point_7": ("(double)(code - 8)", "(double)(code - 7)"),
+    "zero_point_7": ("int zero = z ? z[(size_t)g * N + n] : 8;", "int zero = z ? z[(size_t)g * N + n] : 7;"),
+    "zero_points_ignored": ("int zero = z ? z[(size_t)g * N + n] : 8;", "int zero = 8;"),
+    "zero_point_of_first_group": ("int zero = z ? z[(size_t)g * N + n] : 8;",
+                                  "int zero = z ? z[n] : 8;"),
+    "zero_point_of_mirrored_column": ("int zero = z ? z[(size_t)g * N + n] : 8;",
+                                      "int zero = z ? z[(size_t)g * N + (N - 1 - n)] : 8;"),
+    "zero_point_sign": ("(double)(code - zero)", "(double)(zero - code)"),
     "no_groups": ("static int group_of(int k, int G) { return k / G; }",
                   "static int group_of(int k, int G) { (void)k; (void)G; return 0; }"),
     "transposed_weights": ("int code = q[(size_t)k * N + n];", "int code = q[(size_t)n * N + k];"),
@@ -270,13 +282,114 @@ def test_planted_mistakes_fail_a_pin(oracle_mod, name):
         failures = 0
         for check in (test_hand_example, test_half_decoder_all_patterns,
                       test_all_codes_eight_give_zero, test_per_column_group_equals_single_group,
-                      lambda o: test_brute_force_exact(o, 0), lambda o: test_brute_force_exact(o, 1)):
+                      lambda o: test_brute_force_exact(o, 0), lambda o: test_brute_force_exact(o, 1),
+                      lambda o: test_zero_points_brute_force_exact(o, 0),
+                      lambda o: test_zero_points_brute_force_exact(o, 1)):
             try:
                 check(mut)
             except AssertionError:
                 failures += 1
                 break
         assert failures > 0, name
+
+
+# --------------------------------------------------------------------------- per-group zero-points
+# w = (q - z[g][n]) * s[g][n] with an integer zero-point 0..15 per (group, column):
+# the asymmetric 4-bit format of AWQ checkpoints, which "Low-Precision
+# Quantization Kernels in Production" (llms.blog), section 1, lists among those the
+# Marlin kernel family serves.
+@pytest.mark.parametrize("seed", range(8))
+def test_zero_points_brute_force_exact(oracle_mod, seed):
+    r = np.random.default_rng(2000 + seed)
+    M, K, N = (int(v) for v in r.integers(1, 9, size=3))
+    G = int(r.choice([1, 2, 3, 4, K]))
+    ng = -(-K // G)
+    x = (r.standard_normal((M, K)) * 4).astype(np.float16)
+    q = r.integers(0, 16, size=(K, N)).astype(np.uint8)
+    z = r.integers(0, 16, size=(ng, N)).astype(np.uint8)
+    s = np.abs(r.standard_normal((ng, N))).astype(np.float16)
+    y, a = oracle_mod.gemm(x, q, s, G, z=z)
+    ye, ae = exact_reference(x, q, s, G, z)
+    for m in range(M):
+        for n in range(N):
+            bound = (K * 2.0 ** -53) * float(ae[m][n])
+            assert abs(Fraction(y[m][n]) - ye[m][n]) <= Fraction(bound)
+            assert abs(Fraction(a[m][n]) - ae[m][n]) <= Fraction(bound)
+
+
+def test_zero_points_of_eight_equal_the_symmetric_form(oracle_mod):
+    x, q, s = small_problem()
+    z = np.full((3, q.shape[1]), 8, np.uint8)
+    y, a = oracle_mod.gemm(x, q, s, 32)
+    yz, az = oracle_mod.gemm(x, q, s, 32, z=z)
+    assert np.array_equal(y, yz) and np.array_equal(a, az)
+    assert np.array_equal(oracle_mod.dequant(q, s, 32), oracle_mod.dequant(q, s, 32, z=z))
+
+
+def test_codes_equal_to_their_zero_points_give_zero(oracle_mod):
+    x, _, s = small_problem()
+    z = inputs.zeros(96, 24, 32, seed=4)
+    q = np.repeat(z, 32, axis=0)
+    y, a = oracle_mod.gemm(x, q, s, 32, z=z)
+    assert np.all(y == 0) and np.all(a == 0)
+
+
+def test_unit_step_in_one_zero_point(oracle_mod):
+    """Raising z[g][n] by one lowers column n by s[g][n] * sum of x over group g and
+    leaves every other column alone. Integer x and power-of-two scales keep every
+    sum exact, so the step is compared exactly."""
+    r = np.random.default_rng(5)
+    M, K, N, G = 4, 96, 24, 32
+    x = r.integers(-8, 9, size=(M, K)).astype(np.float16)
+    q = inputs.codes(K, N, seed=6)
+    s = (2.0 ** r.integers(-6, 0, size=(3, N))).astype(np.float16)
+    z = np.minimum(inputs.zeros(K, N, G, seed=6), 14)
+    y, _ = oracle_mod.gemm(x, q, s, G, z=z)
+    for g, n in ((0, 0), (1, 17), (2, 23)):
+        z1 = z.copy()
+        z1[g, n] += 1
+        y1, _ = oracle_mod.gemm(x, q, s, G, z=z1)
+        step = -float(s[g, n]) * x[:, g * G:(g + 1) * G].astype(np.float64).sum(axis=1)
+        assert np.array_equal(y1[:, n] - y[:, n], step)
+        assert np.array_equal(np.delete(y1, n, axis=1), np.delete(y, n, axis=1))
+
+
+def test_zero_points_against_numpy_matmul(oracle_mod):
+    x, q, s = inputs.problem(17, 300, 200, 64, seed=9)
+    z = inputs.zeros(300, 200, 64, seed=9)
+    w = (q.astype(np.float64) - np.repeat(z, 64, axis=0)[:300]) * np.repeat(s.astype(np.float64), 64, axis=0)[:300]
+    ref = x.astype(np.float64) @ w
+    y, a = oracle_mod.gemm(x, q, s, 64, z=z)
+    assert np.all(np.abs(y - ref) <= 2 * 300 * 2.0 ** -53 * a)
+    assert np.array_equal(oracle_mod.dequant(q, s, 64, z=z), w)
+    rows, cols = [16, 0, 7], [199, 3, 128]
+    ys, as_ = oracle_mod.gemm_sample(x, q, s, 64, rows, cols, z=z)
+    assert np.array_equal(ys, y[np.ix_(rows, cols)]) and np.array_equal(as_, a[np.ix_(rows, cols)])
+
+
+def test_zero_points_on_the_hand_example(oracle_mod):
+    """Hand example, one group (G = K = 8), zero-point n in column n: sum_k x_k = 1,
+    so y[n] = y_8[n] + (8 - n) * s[n] with y_8 the golden symmetric result."""
+    g = read_golden()
+    x, q, s = hand_inputs(8)
+    z = np.arange(8, dtype=np.uint8).reshape(1, 8)
+    y, _ = oracle_mod.gemm(x, q, s, 8, z=z)
+    assert float(x.astype(np.float64).sum()) == 1.0
+    assert np.array_equal(y[0], g["G8_y"] + (8 - np.arange(8)) * s[0].astype(np.float64))
+
+
+def test_zeros_unpack(oracle_mod):
+    N, ng = 200, 3
+    z = inputs.zeros(3 * 32, N, 32, seed=2)
+    zp = np.zeros(-(-N // 128) * ng * 64, np.uint8)
+    for g in range(ng):
+        for n in range(-(-N // 128) * 128):
+            v = int(z[g, n]) if n < N else 8
+            zp[((n // 128) * ng + g) * 64 + (n % 128) // 2] |= v << (4 * (n % 2))
+    z2, bad = oracle_mod.unpack_zeros(zp, ng, N)
+    assert bad == 0 and np.array_equal(z2, z)
+    zp[-1] = 0   # a padding column that does not hold 8
+    assert oracle_mod.unpack_zeros(zp, ng, N)[1] == 2
 
 
 # --------------------------------------------------------------------------- fused epilogue

@@ -2,7 +2,7 @@
 
 Both the CUDA path and the CPU oracle are fed from these generators, so they see
 identical bits. Every tensor draws from its own PCG64 stream keyed by
-(seed, stream id): activations 0, codes 1, scales 2, outlier mask 3.
+(seed, stream id): activations 0, codes 1, scales 2, outlier mask 3, zero-points 4.
 
 Distributions follow the workloads the pages measure (a layer sweep over batch
 sizes on Llama-2-like shapes, a 72k x 18k layer, prefill shapes):
@@ -10,11 +10,13 @@ sizes on Llama-2-like shapes, a 72k x 18k layer, prefill shapes):
     prefill workload multiplies an independent 1% of entries by 20 (outliers);
   * codes q ~ uniform on {0..15};
   * scales s = FP16(|N(0,1)| * c) per (group, column) with c = 0.02 (0.01 for
-    the 72k x 18k layer), or FP16(10^U(-4,-1)) for the edge sweep.
+    the 72k x 18k layer), or FP16(10^U(-4,-1)) for the edge sweep;
+  * zero-points z ~ uniform on {0..15} per (group, column) for the asymmetric
+    format (every value, the extremes 0 and 15 included, is exercised).
 """
 import numpy as np
 
-X_STREAM, CODE_STREAM, SCALE_STREAM, OUTLIER_STREAM = 0, 1, 2, 3
+X_STREAM, CODE_STREAM, SCALE_STREAM, OUTLIER_STREAM, ZERO_STREAM = 0, 1, 2, 3, 4
 
 
 def rng(seed, stream):
@@ -50,6 +52,11 @@ def scales(K, N, group_size, seed=0, kind="halfnormal", mult=0.02):
     else:
         raise ValueError(kind)
     return s.astype(np.float16)
+
+
+def zeros(K, N, group_size, seed=0):
+    """z[ceil(K/G)][N] uniform on 0..15 as uint8."""
+    return rng(seed, ZERO_STREAM).integers(0, 16, size=(n_groups(K, group_size), N), dtype=np.uint8)
 
 
 def problem(M, K, N, group_size, seed=0, scale_kind="halfnormal", scale_mult=0.02,
