@@ -465,9 +465,66 @@ def run_ours(args, rank, world):
     if args.workload == DEFAULT_WORKLOAD:
         out["fused_epilogue"] = fused_epilogue_probe(G)
         out["layer_chain"] = layer_chain_probe(G)
+        out["zero_points"] = zero_point_probe(G)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
+
+
+def graph_us_per_launch(body, copies, reps=40):
+    """Mean microseconds of body(copy) launched `reps` times back to back from one
+    CUDA Graph, cycling over `copies` (each its own packed weights)."""
+    import torch
+    for c in copies:
+        body(c)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        for r in range(reps):
+            body(copies[r % len(copies)])
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def zero_point_probe(G):
+    """The per-group zero-point format beside the symmetric one on the same shapes:
+    mean time per launch of w4a16_gemm and of w4a16_gemm_zp, launched back to back
+    from a CUDA Graph over rotating copies of the packed weights (more bytes than
+    L2), on the gate/up decode layer (M = 16, K = 4096, N = 22016) and a prefill
+    layer (M = 1024, K = 5120, N = 15360). The zero-points add ceil(K/G) * N / 2
+    bytes to the weight stream."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    rows = []
+    for M, K, N in ((16, 4096, 22016), (1024, 5120, 15360)):
+        q = torch.from_numpy(inputs.codes(K, N, 0)).cuda()
+        s = torch.from_numpy(inputs.scales(K, N, G, 0)).cuda()
+        z = torch.from_numpy(inputs.zeros(K, N, G, 0)).cuda()
+        packed, sp = w4a16.pack(q, s, G)
+        zp = w4a16.pack_zeros(z, K, G)
+        del q, s, z
+        n_copies = max(2, int(400e6 // (packed.numel() * 4)) + 1)
+        copies = [(packed.clone(), sp.clone(), zp.clone()) for _ in range(n_copies)]
+        del packed, sp, zp
+        x = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        us_sym = graph_us_per_launch(
+            lambda c: w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream()), copies)
+        us_zp = graph_us_per_launch(
+            lambda c: w4a16.gemm_zp(x, c[0], c[1], c[2], N, G, y=y, stream=torch.cuda.current_stream()), copies)
+        rows.append({"case": [M, K, N], "us_symmetric": us_sym, "us_zero_points": us_zp,
+                     "tflops_zero_points": flops(M, K, N) / (us_zp * 1e-6) / 1e12,
+                     "weight_gbs_zero_points": (weight_bytes(K, N, G) + n_groups(K, G) * N / 2) / (us_zp * 1e-6) / 1e9})
+        del copies
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return rows
 
 
 def fused_epilogue_probe(G):
@@ -487,24 +544,8 @@ def fused_epilogue_probe(G):
     bias = torch.from_numpy(np.random.default_rng(1).standard_normal(N).astype(np.float16)).cuda()
     y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     tmp = torch.empty_like(y)
-    reps = 40
-
     def timed(body):
-        for c in copies:
-            body(c)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
-            for r in range(reps):
-                body(copies[r % len(copies)])
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3 / reps
+        return graph_us_per_launch(body, copies)
 
     def plain(c):
         w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream())

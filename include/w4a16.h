@@ -19,6 +19,10 @@
  *    between the repacking step and the kernel; section 3 (FlashInfer): split-K
  *    with a deterministic reduction in global memory, CUDA Graph capture.
  * The zero-point 8 is the symmetric reading (the pages print no zero-point).
+ * w4a16_gemm_zp takes one integer zero-point z[g][n] in 0..15 per group and
+ * column instead: dequant(Wq)[k][n] = (q[k][n] - z[k/G][n]) * s[k/G][n], the
+ * 4-bit format of AWQ checkpoints, which "Low-Precision Quantization Kernels in
+ * Production" (llms.blog), section 1, lists among those the Marlin family serves.
  *
  * Conventions for every entry point:
  *  - Pointers named "device" are CUDA device pointers of the current device,
@@ -154,6 +158,38 @@ w4a16_status w4a16_gemm_fused(const uint16_t* x, const uint32_t* packed,
                               int M, int N, int K, int group_size,
                               const uint16_t* bias, const uint16_t* residual, int activation,
                               void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
+/* Bytes of the packed zero-points: ceil(N/128) * ceil(K/G) * 64 (two 4-bit
+ * zero-points a byte). Returns 0 for invalid sizes. */
+size_t w4a16_zeros_bytes(int K, int N, int group_size);
+
+/*
+ * Repack per-group zero-points once, offline, into the tile order the
+ * zero-point GEMM streams beside the scales.
+ *   zeros         device, uint8 [ceil(K/G)][N], values 0..15 (only the low nibble is read)
+ *   zeros_packed  device out, uint8 [w4a16_zeros_bytes(K, N, G)], 16-byte aligned
+ * Layout: byte (nt*ceil(K/G) + g)*64 + b holds z[g][nt*128 + 2b] in bits 0..3 and
+ * z[g][nt*128 + 2b + 1] in bits 4..7; columns past N hold 8.
+ * The codes and scales are packed by w4a16_pack as for the symmetric format.
+ */
+w4a16_status w4a16_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int K, int N, int group_size,
+                              w4a16_stream_t stream);
+
+/*
+ * Y = act(X x dequant(W) + bias) + residual with per-group zero-points:
+ * dequant(W)[k][n] = (q[k][n] - z[k/G][n]) * s[k/G][n]. (1024 + q) - (1024 + z)
+ * is formed exactly in FP16, so the dequantised weight is rounded once, at the
+ * product with the scale, as in the symmetric format.
+ *   zeros_packed   device, output of w4a16_pack_zeros for (K, N, G); must not be NULL
+ * Every other argument (bias, residual and activation may be NULL / 0 for a plain
+ * GEMM; workspace NULL for the library's own), layout and error is that of
+ * w4a16_gemm_fused. Zero-points all equal to 8 give bit-identical results to
+ * w4a16_gemm_fused.
+ */
+w4a16_status w4a16_gemm_zp(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
+                           const uint8_t* zeros_packed, uint16_t* y, int M, int N, int K, int group_size,
+                           const uint16_t* bias, const uint16_t* residual, int activation,
+                           void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the error word that the kernels

@@ -46,6 +46,11 @@ def test_sizes(lib):
     assert lib.w4a16_scales_elems(4096, 256, 32) == 2 * 128 * 128
     # packed bytes of the 72k x 18k layer
     assert lib.w4a16_packed_words(18432, 73728, 128) * 4 == 18432 * 73728 // 2
+    # 4-bit zero-points: 64 bytes per (column tile, group)
+    assert lib.w4a16_zeros_bytes(4096, 4096, 128) == 32 * 32 * 64
+    assert lib.w4a16_zeros_bytes(4000, 4096, 128) == 32 * 32 * 64
+    assert lib.w4a16_zeros_bytes(4096, 200, -1) == 2 * 1 * 64
+    assert lib.w4a16_zeros_bytes(4096, 4096, 96) == 0
 
 
 @pytest.mark.parametrize("K,N,G", [(0, 8, 8), (8, 0, 8), (12, 8, 12), (8, 12, 8), (4096, 4096, 16),
@@ -69,6 +74,15 @@ def test_invalid_arguments_return_before_any_device_work(lib):
     assert lib.w4a16_gemm_ws(p, p, p, p, 4, 64, 64, 64, None, 0, None) == w.ERR_INVALID_ARG
     odd = ctypes.c_void_p(ctypes.addressof(buf) + 8)
     assert lib.w4a16_gemm(odd, p, p, p, 4, 64, 64, 64, None) in (w.ERR_INVALID_ARG,)
+    # zero-point GEMM: zero-points required, aligned; activation in range
+    assert lib.w4a16_gemm_zp(p, p, p, None, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm_zp(p, p, p, odd, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm_zp(p, p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm_zp(p, p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_gemm_zp(p, p, p, p, p, 0, 64, 64, 64, None, None, 0, None, 0, None) == w.OK
+    assert lib.w4a16_pack_zeros(None, p, 64, 64, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_pack_zeros(p, odd, 64, 64, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_pack_zeros(p, p, 64, 60, 64, None) == w.ERR_INVALID_ARG
     for s in range(6):
         assert lib.w4a16_status_string(s)
 

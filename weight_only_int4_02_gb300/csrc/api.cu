@@ -13,6 +13,8 @@
 namespace w4a16 {
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,
                         int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream);
+cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N, int n_tiles, int ng, int sms,
+                              cudaStream_t stream);
 }
 
 namespace {
@@ -155,6 +157,34 @@ int max_clusters_for(const DeviceState* st, int tm)
     return tm == 64 ? st->max_clusters[0] : tm == 128 ? st->max_clusters[1] : tm == 256 ? st->max_clusters[2] : 0;
 }
 
+// Shared-memory attributes of every variant of one tile shape (epilogue x weight
+// format); the cluster count kept is the smallest over the variants.
+template <int TM, int KSUB, int CL>
+cudaError_t setup_shape(int* max_clusters)
+{
+    int mc[4] = {0, 0, 0, 0};
+    cudaError_t e;
+    if ((e = setup_tc<TM, KSUB, CL, false, false>(&mc[0])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, true, false>(&mc[1])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, false, true>(&mc[2])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, true, true>(&mc[3])) != cudaSuccess)
+        return e;
+    int m = mc[0];
+    for (int i = 1; i < 4; ++i) m = mc[i] < m ? mc[i] : m;
+    *max_clusters = m;
+    return cudaSuccess;
+}
+
+template <int TM, int KSUB, int CL>
+cudaError_t launch_shape(const CUtensorMap& map, const GemmParams& p, bool epi, bool zp, cudaStream_t stream)
+{
+    if (zp)
+        return epi ? launch_tc<TM, KSUB, CL, true, true>(map, p, stream)
+                   : launch_tc<TM, KSUB, CL, false, true>(map, p, stream);
+    return epi ? launch_tc<TM, KSUB, CL, true, false>(map, p, stream)
+               : launch_tc<TM, KSUB, CL, false, false>(map, p, stream);
+}
+
 w4a16_status device_state(DeviceState** out)
 {
     int dev = 0;
@@ -171,14 +201,10 @@ w4a16_status device_state(DeviceState** out)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
         int unused = 0;
-        if ((e = setup_tc<16, 4, 1, false>(&unused)) != cudaSuccess ||
-            (e = setup_tc<32, 4, 1, false>(&unused)) != cudaSuccess ||
-            (e = setup_tc<64, 4, 2, false>(&st.max_clusters[0])) != cudaSuccess ||
-            (e = setup_tc<128, 2, 2, false>(&st.max_clusters[1])) != cudaSuccess ||
-            (e = setup_tc<256, 2, 2, false>(&st.max_clusters[2])) != cudaSuccess ||
-            (e = setup_tc<16, 4, 1, true>(&unused)) != cudaSuccess ||
-            (e = setup_tc<32, 4, 1, true>(&unused)) != cudaSuccess || (e = setup_tc<64, 4, 2, true>(&unused)) != cudaSuccess ||
-            (e = setup_tc<128, 2, 2, true>(&unused)) != cudaSuccess || (e = setup_tc<256, 2, 2, true>(&unused)) != cudaSuccess)
+        if ((e = setup_shape<16, 4, 1>(&unused)) != cudaSuccess || (e = setup_shape<32, 4, 1>(&unused)) != cudaSuccess ||
+            (e = setup_shape<64, 4, 2>(&st.max_clusters[0])) != cudaSuccess ||
+            (e = setup_shape<128, 2, 2>(&st.max_clusters[1])) != cudaSuccess ||
+            (e = setup_shape<256, 2, 2>(&st.max_clusters[2])) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
             void* fn = nullptr;
@@ -248,13 +274,15 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int k
 
 w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
                        int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
-                       const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0)
+                       const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0,
+                       const uint8_t* zeros_packed = nullptr)
 {
     G = norm_group(K, G);
     if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
     if (M == 0) return W4A16_OK;
     if (!x || !packed || !scales_packed || !y) return W4A16_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales_packed) || !aligned16(y))
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales_packed) || !aligned16(y) ||
+        (zeros_packed && !aligned16(zeros_packed)))
         return W4A16_ERR_INVALID_ARG;
     if (!own_ws && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0)) return W4A16_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
@@ -270,6 +298,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     GemmParams p;
     p.packed = packed;
     p.scales = reinterpret_cast<const __half*>(scales_packed);
+    p.zeros = zeros_packed;
     p.y = reinterpret_cast<__half*>(y);
     p.status = reinterpret_cast<int*>(ws);
     p.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + kCountersOff);
@@ -306,16 +335,13 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     const bool epi = bias || residual || act != 0;
+    const bool zp = zeros_packed != nullptr;
     switch (P.tm) {
-        case 16: e = epi ? launch_tc<16, 4, 1, true>(map, p, stream) : launch_tc<16, 4, 1, false>(map, p, stream); break;
-        case 32: e = epi ? launch_tc<32, 4, 1, true>(map, p, stream) : launch_tc<32, 4, 1, false>(map, p, stream); break;
-        case 64: e = epi ? launch_tc<64, 4, 2, true>(map, p, stream) : launch_tc<64, 4, 2, false>(map, p, stream); break;
-        case 128:
-            e = epi ? launch_tc<128, 2, 2, true>(map, p, stream) : launch_tc<128, 2, 2, false>(map, p, stream);
-            break;
-        default:
-            e = epi ? launch_tc<256, 2, 2, true>(map, p, stream) : launch_tc<256, 2, 2, false>(map, p, stream);
-            break;
+        case 16: e = launch_shape<16, 4, 1>(map, p, epi, zp, stream); break;
+        case 32: e = launch_shape<32, 4, 1>(map, p, epi, zp, stream); break;
+        case 64: e = launch_shape<64, 4, 2>(map, p, epi, zp, stream); break;
+        case 128: e = launch_shape<128, 2, 2>(map, p, epi, zp, stream); break;
+        default: e = launch_shape<256, 2, 2>(map, p, epi, zp, stream); break;
     }
     return from_cuda(e);
 }
@@ -407,6 +433,39 @@ w4a16_status w4a16_gemm_fused(const uint16_t* x, const uint32_t* packed, const u
         return W4A16_ERR_INVALID_ARG;
     return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
                      reinterpret_cast<cudaStream_t>(stream), bias, residual, activation);
+}
+
+size_t w4a16_zeros_bytes(int K, int N, int group_size)
+{
+    const int G = norm_group(K, group_size);
+    if (!valid_sizes(K, N, G)) return 0;
+    return (size_t)ceil_div(N, kTileN) * ceil_div(K, G) * (kTileN / 2);
+}
+
+w4a16_status w4a16_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int K, int N, int group_size,
+                              w4a16_stream_t stream)
+{
+    const int G = norm_group(K, group_size);
+    if (!valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    if (!zeros || !zeros_packed || !aligned16(zeros_packed)) return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    return from_cuda(launch_pack_zeros(zeros, zeros_packed, N, ceil_div(N, kTileN), ceil_div(K, G), st->sms,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_gemm_zp(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
+                           const uint8_t* zeros_packed, uint16_t* y, int M, int N, int K, int group_size,
+                           const uint16_t* bias, const uint16_t* residual, int activation, void* workspace,
+                           size_t ws_bytes, w4a16_stream_t stream)
+{
+    if (!zeros_packed && M != 0) return W4A16_ERR_INVALID_ARG;
+    if (activation < W4A16_ACT_NONE || activation > W4A16_ACT_RELU) return W4A16_ERR_INVALID_ARG;
+    if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
+        return W4A16_ERR_INVALID_ARG;
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, zeros_packed);
 }
 
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream)

@@ -50,6 +50,8 @@ constexpr int kKPad = 4;           // the packed layout pads K to a multiple of 
 struct GemmParams {
     const uint32_t* packed;
     const __half* scales;   // tile-ordered scales [n_tiles][ng][128]
+    const uint8_t* zeros;   // tile-ordered 4-bit zero-points [n_tiles][ng][64 bytes] (kernels built
+                            // for them only; the others use the zero-point 8)
     __half* y;
     float* partials;        // [2 * grid][TM][128] FP32
     int* counters;          // [grid], zero between launches (index = cluster * p.cluster + rank)
@@ -93,17 +95,18 @@ __device__ __forceinline__ float epilogue_op(int act, float v, float b, float r)
 
 __device__ __forceinline__ float load_half(const __half* base, size_t i) { return base ? __half2float(base[i]) : 0.f; }
 
-template <int TM, int KSUB>
+template <int TM, int KSUB, bool ZP = false>
 struct TcCfg {
     static constexpr int kStageK = KSUB * kChunkK;
     static constexpr int kXBlock = TM * 128;              // one 64-wide K block of X (TM rows)
     static constexpr int kXBytes = KSUB * kXBlock;
     static constexpr int kPkBytes = KSUB * kChunkBytes;
     static constexpr int kScBytes = 2 * KSUB * 256;       // G = 32 puts 2*KSUB groups in a stage
-    // Two rings in shared memory: W (packed words + scales), freed by the dequant
-    // warps once they hold their words, so the HBM stream never waits on the MMA;
-    // and X, freed by the MMA's commit.
-    static constexpr int kWStageBytes = kPkBytes + kScBytes;
+    static constexpr int kZpBytes = ZP ? 2 * KSUB * 64 : 0;  // 4-bit zero-points of those groups
+    // Two rings in shared memory: W (packed words + scales [+ zero-points]), freed
+    // by the dequant warps once they hold their words, so the HBM stream never
+    // waits on the MMA; and X, freed by the MMA's commit.
+    static constexpr int kWStageBytes = kPkBytes + kScBytes + kZpBytes;
     static constexpr int kWStages = (TM <= 32 || KSUB == 2) ? 8 : 6;  // a multiple of the team count
     static constexpr int kXFit = (220 * 1024 - kWStages * kWStageBytes) / kXBytes;
     static constexpr int kXStages = kXFit > 8 ? 8 : kXFit;
@@ -126,7 +129,8 @@ struct TcCfg {
     static constexpr int kOffX = 0;
     static constexpr int kOffPk = kOffX + kXStages * kXBytes;
     static constexpr int kOffSc = kOffPk + kWStages * kPkBytes;
-    static constexpr int kOffBar = kOffSc + kWStages * kScBytes;
+    static constexpr int kOffZp = kOffSc + kWStages * kScBytes;
+    static constexpr int kOffBar = kOffZp + kWStages * kZpBytes;
     // barriers: wfull[SW], wempty[SW], xfull[SX], xempty[SX], afull[A], aempty[A],
     // dfull[2], dempty[2], teardown
     static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kAStages + 4 + 1;
@@ -170,24 +174,32 @@ __device__ __forceinline__ int group_of(const GemmParams& p, int k)
     return min(k >> p.g_shift, p.ng - 1);
 }
 
-// (q - 8) * s as four FP16 pairs (k, k+1) ... (k+6, k+7) from one packed word whose
+__device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
+
+// Dequantisation constants for the zero-point z (0..15), duplicated in both halves:
+// lo = 1024 + z (binary16 0x6400 | z) and hi = -(64 + z) (0xD400 | 16z; the ulp at
+// 64 is 1/16). z = 8 gives 1032 and -72.
+__device__ __forceinline__ __half2 zp_lo(uint32_t z) { return u32_as_half2((0x6400u | z) * 0x00010001u); }
+__device__ __forceinline__ __half2 zp_hi(uint32_t z) { return u32_as_half2((0xD400u | (z << 4)) * 0x00010001u); }
+
+// (q - z) * s as four FP16 pairs (k, k+1) ... (k+6, k+7) from one packed word whose
 // nibble i holds k + 2*(i%4) + i/4: OR-ing a nibble into the mantissa of 1024.0
-// gives 1024 + q (low nibble of a byte) or 1024 + 16q (high nibble), both exact.
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t* out)
+// gives 1024 + q (low nibble of a byte) or 1024 + 16q (high nibble), both exact;
+// (1024 + q) - (1024 + z) and (1024 + 16q) / 16 - (64 + z) are q - z exactly, and
+// the one rounding is that of the product with the scale.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c_lo, __half2 c_hi, uint32_t* out)
 {
     const uint32_t lo = 0x000F000Fu, hi = 0x00F000F0u, magic = 0x64006400u;
-    const __half2 c1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
     const __half2 c1_16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
-    const __half2 cm72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
     const uint32_t w8 = w >> 8;
     const uint32_t a = and_or(w, lo, magic);   // nibbles 0, 4 -> k+0, k+1
     const uint32_t b = and_or(w, hi, magic);   // nibbles 1, 5 -> k+2, k+3
     const uint32_t c = and_or(w8, lo, magic);  // nibbles 2, 6 -> k+4, k+5
     const uint32_t d = and_or(w8, hi, magic);  // nibbles 3, 7 -> k+6, k+7
-    __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), c1032);
-    __half2 hb = __hfma2(*reinterpret_cast<const __half2*>(&b), c1_16, cm72);
-    __half2 hc = __hsub2(*reinterpret_cast<const __half2*>(&c), c1032);
-    __half2 hd = __hfma2(*reinterpret_cast<const __half2*>(&d), c1_16, cm72);
+    __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), c_lo);
+    __half2 hb = __hfma2(*reinterpret_cast<const __half2*>(&b), c1_16, c_hi);
+    __half2 hc = __hsub2(*reinterpret_cast<const __half2*>(&c), c_lo);
+    __half2 hd = __hfma2(*reinterpret_cast<const __half2*>(&d), c1_16, c_hi);
     ha = __hmul2(ha, s2);
     hb = __hmul2(hb, s2);
     hc = __hmul2(hc, s2);
@@ -288,12 +300,12 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
 
 // EPI: the instantiation with the fused epilogue (bias, activation, residual);
 // the plain one carries none of its code.
-template <int TM, int KSUB, int CL, bool EPI>
-__global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
+template <int TM, int KSUB, int CL, bool EPI, bool ZP>
+__global__ void __launch_bounds__(TcCfg<TM, KSUB, ZP>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
     static_assert(CL == 1 || (CL == 2 && KSUB % 2 == 0), "cluster of two splits a stage's X blocks");
-    using C = TcCfg<TM, KSUB>;
+    using C = TcCfg<TM, KSUB, ZP>;
     constexpr int SW = C::kWStages;
     constexpr int SX = C::kXStages;
     constexpr int A = C::kAStages;
@@ -411,12 +423,16 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                         const int g0 = group_of(p, k0);
                         const int g1 = group_of(p, k0 + C::kStageK - 1);
                         const uint32_t sc_bytes = (uint32_t)(g1 - g0 + 1) * 256u;
-                        mbar_arrive_expect_tx(wfull_bar(s), C::kPkBytes + sc_bytes);
+                        const uint32_t zp_bytes = ZP ? (uint32_t)(g1 - g0 + 1) * 64u : 0u;
+                        mbar_arrive_expect_tx(wfull_bar(s), C::kPkBytes + sc_bytes + zp_bytes);
                         bulk_load(sbase + C::kOffPk + s * C::kPkBytes,
                                   p.packed + ((size_t)nt * p.KC + (size_t)kc * KSUB) * kChunkWords, C::kPkBytes,
                                   wfull_bar(s));
                         bulk_load(sbase + C::kOffSc + s * C::kScBytes, p.scales + ((size_t)nt * p.ng + g0) * kTileN,
                                   sc_bytes, wfull_bar(s));
+                        if constexpr (ZP)
+                            bulk_load(sbase + C::kOffZp + s * C::kZpBytes, p.zeros + ((size_t)nt * p.ng + g0) * 64,
+                                      zp_bytes, wfull_bar(s));
                     }
                 }
                 __syncwarp();
@@ -519,8 +535,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                 if (!wait_warp(wfull_bar(s), (seq / SW) & 1, ctl)) { ok = false; break; }
                 const int gs = group_of(p, kc * C::kStageK);
                 const __half* sc = reinterpret_cast<const __half*>(smem + C::kOffSc + s * C::kScBytes) + n_in;
+                const uint8_t* zb = smem + C::kOffZp + s * C::kZpBytes + (n_in >> 1);   // ZP only
+                const int zshift = 4 * (n_in & 1);
                 uint4 w[2][2];
                 __half2 s2[2][2];
+                __half2 clo[2][2], chi[2][2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int j = 2 * gi + h;
@@ -532,20 +551,31 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
                     const __half s_hi = sc[(group_of(p, k0 + 32) - gs) * kTileN];
                     s2[h][0] = __halves2half2(s_lo, s_lo);
                     s2[h][1] = __halves2half2(s_hi, s_hi);
+                    if constexpr (ZP) {
+                        const uint32_t z_lo = (zb[(group_of(p, k0) - gs) * 64] >> zshift) & 0xFu;
+                        const uint32_t z_hi = (zb[(group_of(p, k0 + 32) - gs) * 64] >> zshift) & 0xFu;
+                        clo[h][0] = zp_lo(z_lo);
+                        chi[h][0] = zp_hi(z_lo);
+                        clo[h][1] = zp_lo(z_hi);
+                        chi[h][1] = zp_hi(z_hi);
+                    } else {
+                        clo[h][0] = clo[h][1] = zp_lo(8);
+                        chi[h][0] = chi[h][1] = zp_hi(8);
+                    }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(wempty_bar(s));   // words and scales are in registers
+                if (lane == 0) mbar_arrive(wempty_bar(s));   // words, scales and zero-points are in registers
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t v[32];
-                    dequant_word(w[h][0].x, s2[h][0], v + 0);
-                    dequant_word(w[h][0].y, s2[h][0], v + 4);
-                    dequant_word(w[h][0].z, s2[h][0], v + 8);
-                    dequant_word(w[h][0].w, s2[h][0], v + 12);
-                    dequant_word(w[h][1].x, s2[h][1], v + 16);
-                    dequant_word(w[h][1].y, s2[h][1], v + 20);
-                    dequant_word(w[h][1].z, s2[h][1], v + 24);
-                    dequant_word(w[h][1].w, s2[h][1], v + 28);
+                    dequant_word(w[h][0].x, s2[h][0], clo[h][0], chi[h][0], v + 0);
+                    dequant_word(w[h][0].y, s2[h][0], clo[h][0], chi[h][0], v + 4);
+                    dequant_word(w[h][0].z, s2[h][0], clo[h][0], chi[h][0], v + 8);
+                    dequant_word(w[h][0].w, s2[h][0], clo[h][0], chi[h][0], v + 12);
+                    dequant_word(w[h][1].x, s2[h][1], clo[h][1], chi[h][1], v + 16);
+                    dequant_word(w[h][1].y, s2[h][1], clo[h][1], chi[h][1], v + 20);
+                    dequant_word(w[h][1].z, s2[h][1], clo[h][1], chi[h][1], v + 24);
+                    dequant_word(w[h][1].w, s2[h][1], clo[h][1], chi[h][1], v + 28);
                     if (h == 0) {
                         // the A slot is free once the MMAs that read it two stages ago completed
                         if (!wait_warp(aempty_bar(a), ((seq / A) & 1) ^ 1, ctl)) { ok = false; break; }
@@ -670,10 +700,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB>::kThreads, 1)
     }
 }
 
-template <int TM, int KSUB, int CL, bool EPI>
+template <int TM, int KSUB, int CL, bool EPI, bool ZP>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream);
 
-template <int TM, int KSUB, int CL, bool EPI>
+template <int TM, int KSUB, int CL, bool EPI, bool ZP>
 cudaError_t setup_tc(int* max_clusters);
 
 }  // namespace w4a16

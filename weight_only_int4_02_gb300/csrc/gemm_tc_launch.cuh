@@ -1,4 +1,5 @@
-// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL, EPI>; included by one .cu file per tile shape.
+// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL, EPI, ZP>; included by one .cu file per tile
+// shape and weight format (zero-point 8, or per-group zero-points).
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -6,19 +7,20 @@ namespace w4a16 {
 
 // Dynamic shared memory, and for clusters the number of clusters the device can
 // hold at once (0 when the query fails).
-template <int TM, int KSUB, int CL, bool EPI>
+template <int TM, int KSUB, int CL, bool EPI, bool ZP>
 cudaError_t setup_tc(int* max_clusters)
 {
-    auto kernel = w4a16_tc_kernel<TM, KSUB, CL, EPI>;
+    using C = TcCfg<TM, KSUB, ZP>;
+    auto kernel = w4a16_tc_kernel<TM, KSUB, CL, EPI, ZP>;
     cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<TM, KSUB>::kSmemBytes);
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     *max_clusters = 0;
     if (CL > 1) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * CL);
-        cfg.blockDim = dim3(TcCfg<TM, KSUB>::kThreads);
-        cfg.dynamicSmemBytes = TcCfg<TM, KSUB>::kSmemBytes;
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = CL;
@@ -34,13 +36,14 @@ cudaError_t setup_tc(int* max_clusters)
     return cudaSuccess;
 }
 
-template <int TM, int KSUB, int CL, bool EPI>
+template <int TM, int KSUB, int CL, bool EPI, bool ZP>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream)
 {
+    using C = TcCfg<TM, KSUB, ZP>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(TcCfg<TM, KSUB>::kThreads);
-    cfg.dynamicSmemBytes = TcCfg<TM, KSUB>::kSmemBytes;
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
     // Programmatic dependent launch: the next kernel may start its prologue and
     // weight stream while this one drains; it waits for this one before reading X.
@@ -57,15 +60,16 @@ cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL, EPI>, tmap, p);
+    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL, EPI, ZP>, tmap, p);
 }
 
 }  // namespace w4a16
 
-#define W4A16_INSTANTIATE_TC(TM, KSUB, CL)                                                                    \
-    namespace w4a16 {                                                                                         \
-    template cudaError_t setup_tc<TM, KSUB, CL, false>(int*);                                                 \
-    template cudaError_t setup_tc<TM, KSUB, CL, true>(int*);                                                  \
-    template cudaError_t launch_tc<TM, KSUB, CL, false>(const CUtensorMap&, const GemmParams&, cudaStream_t); \
-    template cudaError_t launch_tc<TM, KSUB, CL, true>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
+// Both epilogue variants of one tile shape and weight format (ZP = per-group zero-points).
+#define W4A16_INSTANTIATE_TC(TM, KSUB, CL, ZP)                                                                    \
+    namespace w4a16 {                                                                                             \
+    template cudaError_t setup_tc<TM, KSUB, CL, false, ZP>(int*);                                                 \
+    template cudaError_t setup_tc<TM, KSUB, CL, true, ZP>(int*);                                                  \
+    template cudaError_t launch_tc<TM, KSUB, CL, false, ZP>(const CUtensorMap&, const GemmParams&, cudaStream_t); \
+    template cudaError_t launch_tc<TM, KSUB, CL, true, ZP>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
     }

@@ -1,4 +1,5 @@
-// Offline repack of INT4 codes and FP16 group scales into the tile order the
+// Offline repack of INT4 codes, FP16 group scales and (for the asymmetric format)
+// 4-bit group zero-points into the tile order the
 // tcgen05 kernels stream ("quant_marlin_kernel" (aicassindra.com), "The
 // architecture: every piece explained": eight 4-bit values per 32-bit word in a
 // permuted order chosen once, offline, so the inner loop needs no shuffles).
@@ -52,6 +53,36 @@ __global__ void pack_scales_kernel(const uint16_t* __restrict__ scales, uint16_t
         const int n = nt * 128 + n_in;
         out[idx] = n < N ? scales[(size_t)g * N + n] : (uint16_t)0;
     }
+}
+
+// Zero-points: byte (nt*ng + g)*64 + b holds z[g][nt*128 + 2b] (bits 0..3) and
+// z[g][nt*128 + 2b + 1] (bits 4..7); columns past N hold 8.
+__global__ void pack_zeros_kernel(const uint8_t* __restrict__ zeros, uint8_t* __restrict__ out, int N, int ng,
+                                  long long total)
+{
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int b = (int)(idx & 63);
+        const long long rest = idx >> 6;
+        const int g = (int)(rest % ng);
+        const int nt = (int)(rest / ng);
+        const int n = nt * 128 + 2 * b;
+        const uint32_t lo = n < N ? (zeros[(size_t)g * N + n] & 0xFu) : 8u;
+        const uint32_t hi = n + 1 < N ? (zeros[(size_t)g * N + n + 1] & 0xFu) : 8u;
+        out[idx] = (uint8_t)(lo | (hi << 4));
+    }
+}
+
+cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N, int n_tiles, int ng, int sms,
+                              cudaStream_t stream)
+{
+    const long long total = (long long)n_tiles * ng * 64;
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    const long long cap = (long long)sms * 16;
+    if (blocks > cap) blocks = cap;
+    pack_zeros_kernel<<<(unsigned)blocks, threads, 0, stream>>>(zeros, zeros_packed, N, ng, total);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,

@@ -17,7 +17,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = ran
 
 EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error", "w4a16_packed_words",
            "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
-           "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused"]
+           "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
+           "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -63,6 +64,12 @@ def lib():
         L.w4a16_gemm_noalloc.restype = I
         L.w4a16_gemm_fused.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
         L.w4a16_gemm_fused.restype = I
+        L.w4a16_zeros_bytes.argtypes = [I, I, I]
+        L.w4a16_zeros_bytes.restype = Z
+        L.w4a16_pack_zeros.argtypes = [P, P, I, I, I, P]
+        L.w4a16_pack_zeros.restype = I
+        L.w4a16_gemm_zp.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
+        L.w4a16_gemm_zp.restype = I
         _lib = L
     return _lib
 
@@ -182,4 +189,40 @@ def gemm_fused(x, packed, scales_packed, N, group_size, bias=None, residual=None
     _check(lib().w4a16_gemm_fused(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                   _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                   _stream(stream)), "w4a16_gemm_fused")
+    return y
+
+
+def zeros_bytes(K, N, group_size):
+    return lib().w4a16_zeros_bytes(K, N, group_size)
+
+
+def pack_zeros(zeros, K, group_size, stream=None, out=None):
+    """Repack per-group zero-points (uint8 [ceil(K/G)][N], values 0..15) on the GPU
+    into the tile-ordered 4-bit layout; returns a uint8 tensor."""
+    ng, N = zeros.shape
+    assert zeros.dtype == torch.uint8 and zeros.is_cuda and zeros.is_contiguous()
+    nb = zeros_bytes(K, N, group_size)
+    if nb == 0:
+        raise W4A16Error(ERR_INVALID_ARG, "pack_zeros")
+    zp = torch.empty(nb, dtype=torch.uint8, device=zeros.device) if out is None else out
+    _check(lib().w4a16_pack_zeros(_ptr(zeros), _ptr(zp), K, N, group_size, _stream(stream)), "w4a16_pack_zeros")
+    return zp
+
+
+def gemm_zp(x, packed, scales_packed, zeros_packed, N, group_size, bias=None, residual=None, activation="none",
+            y=None, workspace=None, stream=None):
+    """y = act(x @ dequant(W) + bias) + residual with per-group zero-points:
+    dequant(W)[k][n] = (q[k][n] - z[k // G][n]) * s[k // G][n]. Arguments as gemm_fused,
+    plus zeros_packed from pack_zeros."""
+    M, K = x.shape
+    assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
+    for t, shape in ((bias, (N,)), (residual, (M, N))):
+        if t is not None:
+            assert t.dtype == torch.float16 and t.is_cuda and t.is_contiguous() and tuple(t.shape) == shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().w4a16_gemm_zp(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(zeros_packed), _ptr(y), M, N, K,
+                               group_size, _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace),
+                               ws_bytes, _stream(stream)), "w4a16_gemm_zp")
     return y
