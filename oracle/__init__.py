@@ -54,6 +54,16 @@ def _load():
         lib.w4o_unpack_scales.restype = ctypes.c_longlong
         lib.w4o_unpack_zeros.argtypes = [P, I, I, P]
         lib.w4o_unpack_zeros.restype = ctypes.c_longlong
+        lib.w4o_gemm_sample_w8.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
+        lib.w4o_gemm_sample_w8.restype = I
+        lib.w4o_dequant_w8.argtypes = [P, P, I, I, I, P]
+        lib.w4o_packed_bytes_w8.argtypes = [I, I]
+        lib.w4o_packed_bytes_w8.restype = ctypes.c_size_t
+        lib.w4o_locate_w8.argtypes = [I, I, I]
+        lib.w4o_locate_w8.restype = ctypes.c_size_t
+        lib.w4o_unpack_w8.argtypes = [P, I, I, P]
+        lib.w4o_unpack_w8.restype = ctypes.c_longlong
+        lib.w4o_pack_w8.argtypes = [P, I, I, P]
         _lib = lib
     return _lib
 
@@ -178,6 +188,68 @@ def unpack_scales(sp, ng, N):
     s = np.empty((ng, N), np.uint16)
     bad = _load().w4o_unpack_scales(_ptr(sp), ng, N, _ptr(s))
     return s, int(bad)
+
+
+# ------------------------------------------------------------------ W8A16 (8-bit codes, zero-point 128)
+def dequant_w8(q, s, G):
+    """w[k][n] = (q[k][n] - 128) * s[k // G][n] in float64, q 8-bit codes."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _bits16(s)
+    K, N = q.shape
+    assert s.shape == (n_groups(K, G), N)
+    w = np.empty((K, N), np.float64)
+    _load().w4o_dequant_w8(_ptr(q), _ptr(s), K, N, G, _ptr(w))
+    return w
+
+
+def gemm_sample_w8(x, q, s, G, rows, cols, threads=None):
+    """(y, absum) of the W8A16 format restricted to rows x cols."""
+    x = _bits16(x)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = _bits16(s)
+    M, K = x.shape
+    N = q.shape[1]
+    assert q.shape[0] == K and s.shape == (n_groups(K, G), N)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    cols = np.ascontiguousarray(cols, dtype=np.int32)
+    y = np.empty((rows.size, cols.size), np.float64)
+    a = np.empty((rows.size, cols.size), np.float64)
+    rc = _load().w4o_gemm_sample_w8(_ptr(x), _ptr(q), _ptr(s), M, N, K, G, _ptr(rows), rows.size,
+                                    _ptr(cols), cols.size, _ptr(y), _ptr(a), _threads(threads))
+    assert rc == 0
+    return y, a
+
+
+def gemm_w8(x, q, s, G, threads=None):
+    """(y, absum) = x @ dequant_w8(q, s) in float64 (k ascending), all rows and columns."""
+    M, N = np.shape(x)[0], np.shape(q)[1]
+    return gemm_sample_w8(x, q, s, G, np.arange(M), np.arange(N), threads)
+
+
+def packed_bytes_w8(K, N):
+    return int(_load().w4o_packed_bytes_w8(K, N))
+
+
+def locate_w8(K, k, n):
+    """Byte index of weight (k, n) in the 8-bit packed layout."""
+    return int(_load().w4o_locate_w8(K, k, n))
+
+
+def unpack_w8(packed, K, N):
+    """(codes[K][N], number of padding bytes that are not 128)."""
+    p = np.ascontiguousarray(packed).view(np.uint8).ravel()
+    assert p.size == packed_bytes_w8(K, N)
+    codes = np.empty((K, N), np.uint8)
+    bad = _load().w4o_unpack_w8(_ptr(p), K, N, _ptr(codes))
+    return codes, int(bad)
+
+
+def pack_w8(codes):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    K, N = codes.shape
+    out = np.empty(packed_bytes_w8(K, N), np.uint8)
+    _load().w4o_pack_w8(_ptr(codes), K, N, _ptr(out))
+    return out
 
 
 def unpack_zeros(zp, ng, N):

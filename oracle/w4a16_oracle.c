@@ -30,6 +30,14 @@
  * subnormals). Every product x*(q-z)*s has at most 26 significant bits, so it
  * is exact in FP64; only the k-ascending summation rounds.
  *
+ * INT8 codes (the W8A16 format): q in 0..255 with the fixed zero-point 128,
+ *   w[k][n] = (q[k][n] - 128) * s[k / G][n]
+ * ("Low-Precision Quantization Kernels in Production" (llms.blog), section 1 and
+ * its comparison table: the Marlin family serves INT4 and INT8 weights with FP16
+ * activations; 128 is the symmetric zero-point of unsigned 8-bit codes, the
+ * 8-bit counterpart of the 4-bit format's 8). Products have at most 30
+ * significant bits: still exact in FP64.
+ *
  * The packed-layout functions at the end restate the packed word layout that
  * the library's pack entry point documents (the pages fix only "eight 4-bit
  * values per 32-bit word in a permuted order"; the order itself is free), so
@@ -66,14 +74,15 @@ void w4o_decode_halves(const uint16_t* h, double* out, size_t count)
 static int group_of(int k, int G) { return k / G; }
 
 /* Dequantise column n of the weight matrix into w_col[K]. z is [ceil(K/G)][N]
- * integer zero-points, or NULL for the fixed zero-point 8. */
-static void dequant_column(const uint8_t* q, const uint16_t* s, const uint8_t* z, int K, int N, int G,
+ * integer zero-points, or NULL for the fixed zero-point zdef (8 for 4-bit codes,
+ * 128 for 8-bit codes). */
+static void dequant_column(const uint8_t* q, const uint16_t* s, const uint8_t* z, int zdef, int K, int N, int G,
                            int n, double* w_col)
 {
     for (int k = 0; k < K; ++k) {
         int g = group_of(k, G);
         int code = q[(size_t)k * N + n];
-        int zero = z ? z[(size_t)g * N + n] : 8;
+        int zero = z ? z[(size_t)g * N + n] : zdef;
         double scale = w4o_half_to_double(s[(size_t)g * N + n]);
         w_col[k] = (double)(code - zero) * scale;
     }
@@ -84,7 +93,7 @@ void w4o_dequant_zp(const uint8_t* q, const uint16_t* s, const uint8_t* z, int K
 {
     double* col = (double*)malloc(sizeof(double) * (size_t)K);
     for (int n = 0; n < N; ++n) {
-        dequant_column(q, s, z, K, N, G, n, col);
+        dequant_column(q, s, z, 8, K, N, G, n, col);
         for (int k = 0; k < K; ++k) w[(size_t)k * N + n] = col[k];
     }
     free(col);
@@ -96,7 +105,7 @@ void w4o_dequant(const uint8_t* q, const uint16_t* s, int K, int N, int G, doubl
 }
 
 typedef struct {
-    const uint16_t* x; const uint8_t* q; const uint16_t* s; const uint8_t* z;
+    const uint16_t* x; const uint8_t* q; const uint16_t* s; const uint8_t* z; int zdef;
     int M, N, K, G;
     const int* rows; int nrows;      /* rows of y to evaluate           */
     const int* cols; int ncols;      /* columns of y to evaluate        */
@@ -110,7 +119,7 @@ static void* worker(void* arg)
     job_t* j = (job_t*)arg;
     double* w_col = (double*)malloc(sizeof(double) * (size_t)j->K);
     for (int c = j->col_begin; c < j->col_end; ++c) {
-        dequant_column(j->q, j->s, j->z, j->K, j->N, j->G, j->cols[c], w_col);
+        dequant_column(j->q, j->s, j->z, j->zdef, j->K, j->N, j->G, j->cols[c], w_col);
         for (int r = 0; r < j->nrows; ++r) {
             const double* xr = j->xd + (size_t)r * j->K;
             double acc = 0.0, acc_abs = 0.0;
@@ -135,10 +144,10 @@ static void* worker(void* arg)
  * Work is split over `threads` POSIX threads by column; the arithmetic of each
  * element does not depend on the split.
  */
-int w4o_gemm_sample_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, const uint8_t* z,
-                       int M, int N, int K, int G,
-                       const int* rows, int nrows, const int* cols, int ncols,
-                       double* y, double* absum, int threads)
+static int gemm_sample_any(const uint16_t* x, const uint8_t* q, const uint16_t* s, const uint8_t* z, int zdef,
+                           int M, int N, int K, int G,
+                           const int* rows, int nrows, const int* cols, int ncols,
+                           double* y, double* absum, int threads)
 {
     if (M < 0 || N < 0 || K < 0 || G <= 0 || nrows < 0 || ncols < 0) return 1;
     double* xd = (double*)malloc(sizeof(double) * ((size_t)nrows * K + 1));
@@ -154,7 +163,7 @@ int w4o_gemm_sample_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, c
     pthread_t* tid = (pthread_t*)malloc(sizeof(pthread_t) * threads);
     job_t* jobs = (job_t*)malloc(sizeof(job_t) * threads);
     for (int t = 0; t < threads; ++t) {
-        job_t j = {x, q, s, z, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+        job_t j = {x, q, s, z, zdef, M, N, K, G, rows, nrows, cols, ncols, y, absum,
                    (int)((long long)ncols * t / threads),
                    (int)((long long)ncols * (t + 1) / threads), xd};
         jobs[t] = j;
@@ -164,6 +173,33 @@ int w4o_gemm_sample_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, c
     for (int t = 1; t < threads; ++t) pthread_join(tid[t], NULL);
     free(jobs); free(tid); free(xd);
     return 0;
+}
+
+int w4o_gemm_sample_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, const uint8_t* z,
+                       int M, int N, int K, int G,
+                       const int* rows, int nrows, const int* cols, int ncols,
+                       double* y, double* absum, int threads)
+{
+    return gemm_sample_any(x, q, s, z, 8, M, N, K, G, rows, nrows, cols, ncols, y, absum, threads);
+}
+
+/* The W8A16 format: q[K][N] are 8-bit codes 0..255, zero-point 128. */
+int w4o_gemm_sample_w8(const uint16_t* x, const uint8_t* q, const uint16_t* s,
+                       int M, int N, int K, int G,
+                       const int* rows, int nrows, const int* cols, int ncols,
+                       double* y, double* absum, int threads)
+{
+    return gemm_sample_any(x, q, s, NULL, 128, M, N, K, G, rows, nrows, cols, ncols, y, absum, threads);
+}
+
+void w4o_dequant_w8(const uint8_t* q, const uint16_t* s, int K, int N, int G, double* w)
+{
+    double* col = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int n = 0; n < N; ++n) {
+        dequant_column(q, s, NULL, 128, K, N, G, n, col);
+        for (int k = 0; k < K; ++k) w[(size_t)k * N + n] = col[k];
+    }
+    free(col);
 }
 
 int w4o_gemm_sample(const uint16_t* x, const uint8_t* q, const uint16_t* s,
@@ -291,4 +327,53 @@ long long w4o_unpack_zeros(const uint8_t* zp, int ng, int N, uint8_t* z)
                 else if (v != 8) ++bad_pad;
             }
     return bad_pad;
+}
+
+/*
+ * 8-bit packed layout (W8A16), restated for the round-trip check. Column tiles
+ * of 128, reduction chunks of 64 (KC as above), each chunk in four quarters of
+ * 16 values. For tile nt, chunk kc, quarter j4, feature n_in and byte b of the
+ * column's 16 bytes in that quarter:
+ *
+ *   byte index = (((nt * KC + kc) * 4 + j4) * 128 + n_in) * 16 + b,
+ *   word b/4 holds k0 = kc*64 + j4*16 + 4*(b/4) .. k0+3 of column nt*128 + n_in,
+ *   byte b%4 = 0, 1, 2, 3 holds k0 + 0, 2, 1, 3.
+ *
+ * Positions with k >= K or n >= N hold code 128 (weight 0).
+ */
+size_t w4o_packed_bytes_w8(int K, int N) { return (size_t)ceil_div(N, 128) * chunks_per_column(K) * 8192; }
+
+size_t w4o_locate_w8(int K, int k, int n)
+{
+    static const int slot_of_offset[4] = {0, 2, 1, 3};   /* k offset in the word -> byte */
+    int KC = chunks_per_column(K);
+    int nt = n / 128, n_in = n % 128;
+    int kc = k / 64, r = k % 64;
+    int j4 = r / 16, r2 = r % 16;
+    int b = 4 * (r2 / 4) + slot_of_offset[r2 % 4];
+    return ((((size_t)nt * KC + kc) * 4 + j4) * 128 + n_in) * 16 + b;
+}
+
+/* Unpack 8-bit codes[K][N]; returns the number of padding bytes that are not 128. */
+long long w4o_unpack_w8(const uint8_t* packed, int K, int N, uint8_t* codes)
+{
+    int KC = chunks_per_column(K), NT = ceil_div(N, 128);
+    long long bad_pad = 0;
+    for (int nt = 0; nt < NT; ++nt)
+        for (int k = 0; k < KC * 64; ++k)
+            for (int n_in = 0; n_in < 128; ++n_in) {
+                int n = nt * 128 + n_in;
+                uint8_t c = packed[w4o_locate_w8(K, k, n)];
+                if (k < K && n < N) codes[(size_t)k * N + n] = c;
+                else if (c != 128) ++bad_pad;
+            }
+    return bad_pad;
+}
+
+void w4o_pack_w8(const uint8_t* codes, int K, int N, uint8_t* packed)
+{
+    size_t total = w4o_packed_bytes_w8(K, N);
+    memset(packed, 128, total);
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) packed[w4o_locate_w8(K, k, n)] = codes[(size_t)k * N + n];
 }

@@ -10,7 +10,11 @@
 * per-group zero-points: brute force in exact rationals, zero-points of 8 equal
   the symmetric form bit for bit, codes equal to their zero-points give 0, the
   closed form of a unit step in one zero-point, numpy's matmul on the expanded
-  weights, the hand example with zero-point n in column n.
+  weights, the hand example with zero-point n in column n;
+* 8-bit codes (W8A16, zero-point 128): brute force in exact rationals, codes 128
+  give 0, 8-bit codes 16*q equal 16 times the 4-bit result for codes q, numpy's
+  matmul on the expanded weights, the 8-bit layout (bijection, round trip, the
+  pair (k, k+1) in bytes 0 and 2 of a word).
 """
 import os
 import re
@@ -63,9 +67,9 @@ def test_half_decoder_all_patterns(oracle_mod):
         assert oracle_mod.half_to_double(np.array([b], np.uint16))[0] == v
 
 
-def exact_reference(x, q, s, G, z=None):
+def exact_reference(x, q, s, G, z=None, zdef=8):
     """Exact rationals: each FP16 value converts to Fraction without rounding.
-    z: integer zero-points [ceil(K/G)][N], or None for 8."""
+    z: integer zero-points [ceil(K/G)][N], or None for the fixed zdef."""
     M, K = x.shape
     N = q.shape[1]
     xf = [[Fraction(float(v)) for v in row] for row in x.astype(np.float64)]
@@ -76,7 +80,7 @@ def exact_reference(x, q, s, G, z=None):
         for n in range(N):
             acc, acc_abs = Fraction(0), Fraction(0)
             for k in range(K):
-                zero = 8 if z is None else int(z[k // G][n])
+                zero = zdef if z is None else int(z[k // G][n])
                 t = xf[m][k] * (int(q[k][n]) - zero) * sf[k // G][n]
                 acc += t
                 acc_abs += abs(t)
@@ -245,13 +249,15 @@ def test_scales_unpack(oracle_mod):
 
 
 MUTANTS = {
-    "zero_point_7": ("int zero = z ? z[(size_t)g * N + n] : 8;", "int zero = z ? z[(size_t)g * N + n] : 7;"),
-    "zero_points_ignored": ("int zero = z ? z[(size_t)g * N + n] : 8;", "int zero = 8;"),
-    "zero_point_of_first_group": ("int zero = z ? z[(size_t)g * N + n] : 8;",
-                                  "int zero = z ? z[n] : 8;"),
-    "zero_point_of_mirrored_column": ("int zero = z ? z[(size_t)g * N + n] : 8;",
-                                      "int zero = z ? z[(size_t)g * N + (N - 1 - n)] : 8;"),
+    "zero_point_7": ("return gemm_sample_any(x, q, s, z, 8,", "return gemm_sample_any(x, q, s, z, 7,"),
+    "zero_points_ignored": ("int zero = z ? z[(size_t)g * N + n] : zdef;", "int zero = zdef;"),
+    "zero_point_of_first_group": ("int zero = z ? z[(size_t)g * N + n] : zdef;",
+                                  "int zero = z ? z[n] : zdef;"),
+    "zero_point_of_mirrored_column": ("int zero = z ? z[(size_t)g * N + n] : zdef;",
+                                      "int zero = z ? z[(size_t)g * N + (N - 1 - n)] : zdef;"),
     "zero_point_sign": ("(double)(code - zero)", "(double)(zero - code)"),
+    "w8_zero_point_127": ("return gemm_sample_any(x, q, s, NULL, 128,", "return gemm_sample_any(x, q, s, NULL, 127,"),
+    "w8_byte_order": ("slot_of_offset[4] = {0, 2, 1, 3}", "slot_of_offset[4] = {0, 1, 2, 3}"),
     "no_groups": ("static int group_of(int k, int G) { return k / G; }",
                   "static int group_of(int k, int G) { (void)k; (void)G; return 0; }"),
     "transposed_weights": ("int code = q[(size_t)k * N + n];", "int code = q[(size_t)n * N + k];"),
@@ -284,7 +290,9 @@ def test_planted_mistakes_fail_a_pin(oracle_mod, name):
                       test_all_codes_eight_give_zero, test_per_column_group_equals_single_group,
                       lambda o: test_brute_force_exact(o, 0), lambda o: test_brute_force_exact(o, 1),
                       lambda o: test_zero_points_brute_force_exact(o, 0),
-                      lambda o: test_zero_points_brute_force_exact(o, 1)):
+                      lambda o: test_zero_points_brute_force_exact(o, 1),
+                      lambda o: test_w8_brute_force_exact(o, 0),
+                      test_w8_layout_pairs_adjacent_k_in_bytes_0_and_2):
             try:
                 check(mut)
             except AssertionError:
@@ -390,6 +398,84 @@ def test_zeros_unpack(oracle_mod):
     assert bad == 0 and np.array_equal(z2, z)
     zp[-1] = 0   # a padding column that does not hold 8
     assert oracle_mod.unpack_zeros(zp, ng, N)[1] == 2
+
+
+# --------------------------------------------------------------------------- 8-bit codes (W8A16)
+# w = (q - 128) * s with q 0..255: the 8-bit checkpoints that "Low-Precision
+# Quantization Kernels in Production" (llms.blog), section 1, says the Marlin
+# kernel family serves beside the 4-bit ones; 128 is the symmetric zero-point of
+# unsigned 8-bit codes.
+@pytest.mark.parametrize("seed", range(8))
+def test_w8_brute_force_exact(oracle_mod, seed):
+    r = np.random.default_rng(3000 + seed)
+    M, K, N = (int(v) for v in r.integers(1, 9, size=3))
+    G = int(r.choice([1, 2, 3, 4, K]))
+    ng = -(-K // G)
+    x = (r.standard_normal((M, K)) * 4).astype(np.float16)
+    q = r.integers(0, 256, size=(K, N)).astype(np.uint8)
+    s = np.abs(r.standard_normal((ng, N))).astype(np.float16)
+    if seed % 3 == 0:
+        s = (r.integers(1, 1024, size=(ng, N)) * 2.0 ** -24).astype(np.float16)
+    y, a = oracle_mod.gemm_w8(x, q, s, G)
+    ye, ae = exact_reference(x, q, s, G, zdef=128)
+    for m in range(M):
+        for n in range(N):
+            bound = (K * 2.0 ** -53) * float(ae[m][n])
+            assert abs(Fraction(y[m][n]) - ye[m][n]) <= Fraction(bound)
+            assert abs(Fraction(a[m][n]) - ae[m][n]) <= Fraction(bound)
+
+
+def test_w8_codes_128_give_zero(oracle_mod):
+    x, q, s = small_problem()
+    y, a = oracle_mod.gemm_w8(x, np.full_like(q, 128), s, 32)
+    assert np.all(y == 0) and np.all(a == 0)
+
+
+def test_w8_codes_16q_equal_16_times_the_4bit_result(oracle_mod):
+    """(16q - 128) = 16 (q - 8): 8-bit codes 16q give exactly 16 times the 4-bit
+    result for codes q (a power-of-two factor is exact in FP64)."""
+    x, q, s = small_problem()
+    y4, a4 = oracle_mod.gemm(x, q, s, 32)
+    y8, a8 = oracle_mod.gemm_w8(x, (q.astype(np.uint16) * 16).astype(np.uint8), s, 32)
+    assert np.array_equal(y8, 16 * y4) and np.array_equal(a8, 16 * a4)
+
+
+def test_w8_against_numpy_matmul(oracle_mod):
+    x, _, s = inputs.problem(17, 300, 200, 64, seed=9)
+    q = np.random.default_rng(9).integers(0, 256, size=(300, 200)).astype(np.uint8)
+    w = (q.astype(np.float64) - 128) * np.repeat(s.astype(np.float64), 64, axis=0)[:300]
+    ref = x.astype(np.float64) @ w
+    y, a = oracle_mod.gemm_w8(x, q, s, 64)
+    assert np.all(np.abs(y - ref) <= 2 * 300 * 2.0 ** -53 * a)
+    assert np.array_equal(oracle_mod.dequant_w8(q, s, 64), w)
+
+
+@pytest.mark.parametrize("K,N", [(64, 128), (200, 130), (8, 8)])
+def test_w8_layout_is_a_bijection_and_round_trips(oracle_mod, K, N):
+    KC, NT = -(-(-(-K // 64)) // 4) * 4, -(-N // 128)
+    total = oracle_mod.packed_bytes_w8(K, N)
+    assert total == KC * NT * 8192
+    seen = set()
+    for k in range(KC * 64):
+        for n in range(NT * 128):
+            b = oracle_mod.locate_w8(K, k, n)
+            assert 0 <= b < total
+            seen.add(b)
+    assert len(seen) == total
+    q = np.random.default_rng(5).integers(0, 256, size=(K, N)).astype(np.uint8)
+    q2, bad = oracle_mod.unpack_w8(oracle_mod.pack_w8(q), K, N)
+    assert bad == 0 and np.array_equal(q, q2)
+
+
+def test_w8_layout_pairs_adjacent_k_in_bytes_0_and_2(oracle_mod):
+    # a word holds k0 .. k0+3 as bytes (k0, k0+2, k0+1, k0+3): masking bytes 0 and 2
+    # (or 1 and 3) of the word gives the 16-bit pair (k, k+1) of one TMEM column
+    for k0 in range(0, 64, 4):
+        b = [oracle_mod.locate_w8(64, k0 + i, 5) for i in range(4)]
+        assert b[0] % 4 == 0 and b[1] == b[0] + 2 and b[2] == b[0] + 1 and b[3] == b[0] + 3
+    # adjacent columns' 16-byte blocks are adjacent; quarters of 16 k are 2 KB apart
+    assert oracle_mod.locate_w8(64, 0, 1) == oracle_mod.locate_w8(64, 0, 0) + 16
+    assert oracle_mod.locate_w8(64, 16, 0) == oracle_mod.locate_w8(64, 0, 0) + 2048
 
 
 # --------------------------------------------------------------------------- fused epilogue
