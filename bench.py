@@ -466,6 +466,7 @@ def run_ours(args, rank, world):
         out["fused_epilogue"] = fused_epilogue_probe(G)
         out["layer_chain"] = layer_chain_probe(G)
         out["zero_points"] = zero_point_probe(G)
+        out["w8a16"] = w8_probe(G)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
@@ -521,6 +522,38 @@ def zero_point_probe(G):
         rows.append({"case": [M, K, N], "us_symmetric": us_sym, "us_zero_points": us_zp,
                      "tflops_zero_points": flops(M, K, N) / (us_zp * 1e-6) / 1e12,
                      "weight_gbs_zero_points": (weight_bytes(K, N, G) + n_groups(K, G) * N / 2) / (us_zp * 1e-6) / 1e9})
+        del copies
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return rows
+
+
+def w8_probe(G):
+    """The W8A16 format (8-bit codes, 128-value stages): mean time per launch of
+    w4a16_w8_gemm, launched back to back from a CUDA Graph over rotating copies of
+    the packed weights (more bytes than L2), on the gate/up decode layer
+    (16 x 4096 x 22016) and the 18432 x 73728 layer at M = 16; weight bytes are
+    the 8-bit codes plus the FP16 scales."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    rows = []
+    for M, K, N in ((16, 4096, 22016), (16, 18432, 73728)):
+        q = torch.randint(0, 256, (K, N), dtype=torch.uint8, device="cuda",
+                          generator=torch.Generator(device="cuda").manual_seed(0))
+        s = torch.from_numpy(inputs.scales(K, N, G, 0, mult=0.02 / 16)).cuda()
+        packed, sp = w4a16.w8_pack(q, s, G)
+        del q, s
+        n_copies = max(2, int(400e6 // packed.numel()) + 1)
+        copies = [(packed, sp)] + [(packed.clone(), sp.clone()) for _ in range(n_copies - 1)]
+        del packed, sp
+        x = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        us = graph_us_per_launch(
+            lambda c: w4a16.w8_gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream()), copies,
+            reps=40 if K * N < 10 ** 9 else 8)
+        wb = n_groups(K, G) * G * N + n_groups(K, G) * N * 2
+        rows.append({"case": [M, K, N], "us": us, "weight_gbs": wb / (us * 1e-6) / 1e9,
+                     "tflops": flops(M, K, N) / (us * 1e-6) / 1e12})
         del copies
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("a kernel wait timed out")

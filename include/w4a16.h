@@ -113,7 +113,8 @@ w4a16_status w4a16_pack(const uint8_t* codes, const uint16_t* scales,
 w4a16_status w4a16_gemm(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
                         uint16_t* y, int M, int N, int K, int group_size, w4a16_stream_t stream);
 
-/* Bytes of caller workspace w4a16_gemm_ws needs for this shape (0 for invalid sizes). */
+/* Bytes of caller workspace w4a16_gemm_ws needs for this shape, in any weight
+ * format of this library (0 for invalid sizes). */
 size_t w4a16_workspace_bytes(int M, int N, int K, int group_size);
 
 /*
@@ -188,6 +189,46 @@ w4a16_status w4a16_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int K
  */
 w4a16_status w4a16_gemm_zp(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
                            const uint8_t* zeros_packed, uint16_t* y, int M, int N, int K, int group_size,
+                           const uint16_t* bias, const uint16_t* residual, int activation,
+                           void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
+/* ---------------------------------------------------------------- W8A16: 8-bit codes
+ * The same GEMM for 8-bit weights: dequant(Wq)[k][n] = (q[k][n] - 128) * s[k/G][n],
+ * q in 0..255, one FP16 scale per group ("Low-Precision Quantization Kernels in
+ * Production" (llms.blog), section 1: the Marlin family serves 8-bit checkpoints
+ * as well as 4-bit ones; 128 is the symmetric zero-point of unsigned 8-bit codes,
+ * the pages print none). */
+
+/* Bytes of the 8-bit packed codes: ceil(N/128) * KC * 8192, KC as for
+ * w4a16_packed_words. Returns 0 for invalid sizes. */
+size_t w4a16_w8_packed_bytes(int K, int N, int group_size);
+
+/*
+ * Repack 8-bit codes and scales once, offline.
+ *   codes          device, uint8 [K][N], values 0..255
+ *   scales         device, binary16 [ceil(K/G)][N]
+ *   packed         device out, uint8 [w4a16_w8_packed_bytes(K, N, G)], 16-byte aligned
+ *   scales_packed  device out, binary16 [w4a16_scales_elems(K, N, G)] (as w4a16_pack)
+ * Packed layout (8-bit, version 1): column tiles of 128 output features, chunks of
+ * 64 values of k, each in four quarters of 16. Byte
+ * (((nt*KC + kc)*4 + j4)*128 + n_in)*16 + b belongs to word b/4, which holds
+ * k0 = kc*64 + j4*16 + 4*(b/4) .. k0+3 of column nt*128 + n_in; bytes 0, 1, 2, 3 of
+ * the word hold k0, k0+2, k0+1, k0+3. Positions outside K x N hold 128 (weight 0).
+ */
+w4a16_status w4a16_w8_pack(const uint8_t* codes, const uint16_t* scales, uint8_t* packed,
+                           uint16_t* scales_packed, int K, int N, int group_size,
+                           w4a16_stream_t stream);
+
+/*
+ * Y = act(X x dequant(W) + bias) + residual for 8-bit codes. (1024 + q) - 1152 is
+ * q - 128 exactly in FP16; the dequantised weight is rounded once, at the product
+ * with the scale.
+ *   packed         device, output of w4a16_w8_pack for (K, N, G)
+ * bias, residual, activation and workspace as for w4a16_gemm_fused (NULL / 0 for a
+ * plain GEMM); w4a16_workspace_bytes covers this format too.
+ */
+w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_packed,
+                           uint16_t* y, int M, int N, int K, int group_size,
                            const uint16_t* bias, const uint16_t* residual, int activation,
                            void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 

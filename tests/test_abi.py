@@ -51,6 +51,11 @@ def test_sizes(lib):
     assert lib.w4a16_zeros_bytes(4000, 4096, 128) == 32 * 32 * 64
     assert lib.w4a16_zeros_bytes(4096, 200, -1) == 2 * 1 * 64
     assert lib.w4a16_zeros_bytes(4096, 4096, 96) == 0
+    # 8-bit codes: one byte per weight, K padded to a multiple of 256
+    assert lib.w4a16_w8_packed_bytes(4096, 4096, 128) == 4096 * 4096
+    assert lib.w4a16_w8_packed_bytes(4040, 4096, 128) == 4096 * 4096
+    assert lib.w4a16_w8_packed_bytes(8, 8, 8) == 256 * 128
+    assert lib.w4a16_w8_packed_bytes(4096, 4096, 96) == 0
 
 
 @pytest.mark.parametrize("K,N,G", [(0, 8, 8), (8, 0, 8), (12, 8, 12), (8, 12, 8), (4096, 4096, 16),
@@ -83,6 +88,14 @@ def test_invalid_arguments_return_before_any_device_work(lib):
     assert lib.w4a16_pack_zeros(None, p, 64, 64, 64, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_pack_zeros(p, odd, 64, 64, 64, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_pack_zeros(p, p, 64, 60, 64, None) == w.ERR_INVALID_ARG
+    # 8-bit codes
+    assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_w8_gemm(None, p, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_w8_gemm(p, odd, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_w8_gemm(p, p, p, p, 0, 64, 64, 64, None, None, 0, None, 0, None) == w.OK
+    assert lib.w4a16_w8_pack(None, p, p, p, 64, 64, 64, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_w8_pack(p, p, odd, p, 64, 64, 64, None) == w.ERR_INVALID_ARG
     for s in range(6):
         assert lib.w4a16_status_string(s)
 

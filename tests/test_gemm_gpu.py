@@ -148,8 +148,10 @@ def test_workspace_variant_and_graph_capture(w):
     ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device="cuda")
     y = w.gemm_ws(xd, packed, sp, N, G, ws)
     assert torch.equal(y, y_ref)
+    # w4a16_workspace_bytes covers every weight format's plan, so a workspace a little
+    # short of it may still suffice here; one without room for the partials never does
     with pytest.raises(w.W4A16Error) as e:
-        w.gemm_ws(xd, packed, sp, N, G, ws[: nbytes - 1024])
+        w.gemm_ws(xd, packed, sp, N, G, ws[:1024])
     assert e.value.status == w.ERR_WORKSPACE
     # capture into a CUDA graph and replay
     y_g = torch.empty_like(y_ref)

@@ -15,6 +15,8 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* 
                         int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream);
 cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N, int n_tiles, int ng, int sms,
                               cudaStream_t stream);
+cudaError_t launch_pack_w8(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
+                           int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream);
 }
 
 namespace {
@@ -54,7 +56,8 @@ constexpr SplitCost kSplit256 = {0, 0.59, 0.59, 0.0, 0.059};    // 256-row tile 
 struct DeviceState {
     bool ready = false;
     int sms = 0;
-    int max_clusters[3] = {0, 0, 0};  // co-resident 2-CTA clusters for tile heights 64, 128, 256
+    int max_clusters[3] = {0, 0, 0};     // co-resident 2-CTA clusters for tile heights 64, 128, 256 (4-bit)
+    int max_clusters_w8[3] = {0, 0, 0};  // the same for the 8-bit kernels
     void* ws = nullptr;
     size_t ws_bytes = 0;
 };
@@ -92,15 +95,16 @@ struct Plan {
 size_t ws_bytes_for(int grid, int tm) { return kPartialsOff + (size_t)2 * grid * tm * kTileN * sizeof(float); }
 
 // max_clusters: how many 2-CTA clusters of this tile height the device holds at
-// once (0 = unknown).
-Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
+// once (0 = unknown). fmt: the weight format (kFmt*); 8-bit codes run 128-value
+// stages at every tile height (16 KB of codes a stage, as 256 values of 4-bit codes).
+Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0, int fmt = kFmtW4)
 {
     Plan P;
     P.path = 2;
     P.tm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     P.m_tiles = ceil_div(M, P.tm);
     P.n_tiles = ceil_div(N, kTileN);
-    P.ksub = P.tm <= 64 ? 4 : 2;
+    P.ksub = fmt == kFmtW8 ? 2 : P.tm <= 64 ? 4 : 2;
     // From 64 rows of X up, X is the larger operand per stage: two CTAs on
     // adjacent weight tiles load it once, by multicast.
     P.cluster = P.tm >= 64 ? 2 : 1;
@@ -152,37 +156,55 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0)
     return P;
 }
 
-int max_clusters_for(const DeviceState* st, int tm)
+int max_clusters_for(const DeviceState* st, int tm, int fmt = kFmtW4)
 {
-    return tm == 64 ? st->max_clusters[0] : tm == 128 ? st->max_clusters[1] : tm == 256 ? st->max_clusters[2] : 0;
+    const int* mc = fmt == kFmtW8 ? st->max_clusters_w8 : st->max_clusters;
+    return tm == 64 ? mc[0] : tm == 128 ? mc[1] : tm == 256 ? mc[2] : 0;
+}
+
+// The plan of a shape on this device, with the cluster count of its kernel.
+Plan device_plan(const DeviceState* st, int M, int N, int K, int G, int fmt)
+{
+    const int mc = max_clusters_for(st, make_plan(M, N, K, G, st->sms, 0, fmt).tm, fmt);
+    return make_plan(M, N, K, G, st->sms, mc, fmt);
 }
 
 // Shared-memory attributes of every variant of one tile shape (epilogue x weight
-// format); the cluster count kept is the smallest over the variants.
+// format): *mc4 gets the smallest cluster count over the 4-bit variants, *mc8
+// over the 8-bit ones.
 template <int TM, int KSUB, int CL>
-cudaError_t setup_shape(int* max_clusters)
+cudaError_t setup_shape(int* mc4, int* mc8)
 {
-    int mc[4] = {0, 0, 0, 0};
+    int mc[6] = {0, 0, 0, 0, 0, 0};
     cudaError_t e;
-    if ((e = setup_tc<TM, KSUB, CL, false, false>(&mc[0])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, true, false>(&mc[1])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, false, true>(&mc[2])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, true, true>(&mc[3])) != cudaSuccess)
+    if ((e = setup_tc<TM, KSUB, CL, false, kFmtW4>(&mc[0])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, true, kFmtW4>(&mc[1])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, false, kFmtW4Zp>(&mc[2])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, true, kFmtW4Zp>(&mc[3])) != cudaSuccess ||
+        (e = setup_tc<TM, 2, CL, false, kFmtW8>(&mc[4])) != cudaSuccess ||
+        (e = setup_tc<TM, 2, CL, true, kFmtW8>(&mc[5])) != cudaSuccess)
         return e;
     int m = mc[0];
     for (int i = 1; i < 4; ++i) m = mc[i] < m ? mc[i] : m;
-    *max_clusters = m;
+    *mc4 = m;
+    *mc8 = mc[4] < mc[5] ? mc[4] : mc[5];
     return cudaSuccess;
 }
 
 template <int TM, int KSUB, int CL>
-cudaError_t launch_shape(const CUtensorMap& map, const GemmParams& p, bool epi, bool zp, cudaStream_t stream)
+cudaError_t launch_shape(const CUtensorMap& map, const GemmParams& p, bool epi, int fmt, cudaStream_t stream)
 {
-    if (zp)
-        return epi ? launch_tc<TM, KSUB, CL, true, true>(map, p, stream)
-                   : launch_tc<TM, KSUB, CL, false, true>(map, p, stream);
-    return epi ? launch_tc<TM, KSUB, CL, true, false>(map, p, stream)
-               : launch_tc<TM, KSUB, CL, false, false>(map, p, stream);
+    switch (fmt) {
+        case kFmtW4Zp:
+            return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4Zp>(map, p, stream)
+                       : launch_tc<TM, KSUB, CL, false, kFmtW4Zp>(map, p, stream);
+        case kFmtW8:
+            return epi ? launch_tc<TM, 2, CL, true, kFmtW8>(map, p, stream)
+                       : launch_tc<TM, 2, CL, false, kFmtW8>(map, p, stream);
+        default:
+            return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4>(map, p, stream)
+                       : launch_tc<TM, KSUB, CL, false, kFmtW4>(map, p, stream);
+    }
 }
 
 w4a16_status device_state(DeviceState** out)
@@ -201,10 +223,12 @@ w4a16_status device_state(DeviceState** out)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
         int unused = 0;
-        if ((e = setup_shape<16, 4, 1>(&unused)) != cudaSuccess || (e = setup_shape<32, 4, 1>(&unused)) != cudaSuccess ||
-            (e = setup_shape<64, 4, 2>(&st.max_clusters[0])) != cudaSuccess ||
-            (e = setup_shape<128, 2, 2>(&st.max_clusters[1])) != cudaSuccess ||
-            (e = setup_shape<256, 2, 2>(&st.max_clusters[2])) != cudaSuccess)
+        int unused8 = 0;
+        if ((e = setup_shape<16, 4, 1>(&unused, &unused8)) != cudaSuccess ||
+            (e = setup_shape<32, 4, 1>(&unused, &unused8)) != cudaSuccess ||
+            (e = setup_shape<64, 4, 2>(&st.max_clusters[0], &st.max_clusters_w8[0])) != cudaSuccess ||
+            (e = setup_shape<128, 2, 2>(&st.max_clusters[1], &st.max_clusters_w8[1])) != cudaSuccess ||
+            (e = setup_shape<256, 2, 2>(&st.max_clusters[2], &st.max_clusters_w8[2])) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
             void* fn = nullptr;
@@ -275,8 +299,9 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int k
 w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
                        int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
                        const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0,
-                       const uint8_t* zeros_packed = nullptr)
+                       int fmt = kFmtW4, const uint8_t* zeros_packed = nullptr)
 {
+    if ((fmt == kFmtW4Zp) != (zeros_packed != nullptr)) return W4A16_ERR_INVALID_ARG;
     G = norm_group(K, G);
     if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
     if (M == 0) return W4A16_OK;
@@ -288,7 +313,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    const Plan P = make_plan(M, N, K, G, st->sms, max_clusters_for(st, make_plan(M, N, K, G, st->sms).tm));
+    const Plan P = device_plan(st, M, N, K, G, fmt);
     if (own_ws) {
         rc = own_workspace(st, &ws, &ws_bytes);
         if (rc != W4A16_OK) return rc;
@@ -335,13 +360,12 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     const bool epi = bias || residual || act != 0;
-    const bool zp = zeros_packed != nullptr;
     switch (P.tm) {
-        case 16: e = launch_shape<16, 4, 1>(map, p, epi, zp, stream); break;
-        case 32: e = launch_shape<32, 4, 1>(map, p, epi, zp, stream); break;
-        case 64: e = launch_shape<64, 4, 2>(map, p, epi, zp, stream); break;
-        case 128: e = launch_shape<128, 2, 2>(map, p, epi, zp, stream); break;
-        default: e = launch_shape<256, 2, 2>(map, p, epi, zp, stream); break;
+        case 16: e = launch_shape<16, 4, 1>(map, p, epi, fmt, stream); break;
+        case 32: e = launch_shape<32, 4, 1>(map, p, epi, fmt, stream); break;
+        case 64: e = launch_shape<64, 4, 2>(map, p, epi, fmt, stream); break;
+        case 128: e = launch_shape<128, 2, 2>(map, p, epi, fmt, stream); break;
+        default: e = launch_shape<256, 2, 2>(map, p, epi, fmt, stream); break;
     }
     return from_cuda(e);
 }
@@ -411,8 +435,14 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size)
     int sms = kMaxGrid;
     if (device_state(&st) == W4A16_OK) sms = st->sms;
     if (M == 0) return kPartialsOff;
-    const int mc = st ? max_clusters_for(st, make_plan(M, N, K, G, sms).tm) : 0;
-    return make_plan(M, N, K, G, sms, mc).ws_bytes;
+    // enough for every weight format's plan
+    size_t need = 0;
+    for (int fmt : {kFmtW4, kFmtW8}) {
+        const int mc = st ? max_clusters_for(st, make_plan(M, N, K, G, sms, 0, fmt).tm, fmt) : 0;
+        const size_t b = make_plan(M, N, K, G, sms, mc, fmt).ws_bytes;
+        need = b > need ? b : need;
+    }
+    return need;
 }
 
 w4a16_status w4a16_gemm_ws(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y,
@@ -465,7 +495,40 @@ w4a16_status w4a16_gemm_zp(const uint16_t* x, const uint32_t* packed, const uint
     if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
         return W4A16_ERR_INVALID_ARG;
     return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
-                     reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, zeros_packed);
+                     reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, kFmtW4Zp, zeros_packed);
+}
+
+size_t w4a16_w8_packed_bytes(int K, int N, int group_size)
+{
+    if (!valid_sizes(K, N, norm_group(K, group_size))) return 0;
+    return (size_t)ceil_div(N, kTileN) * (ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad) * (2 * kChunkBytes);
+}
+
+w4a16_status w4a16_w8_pack(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
+                           int K, int N, int group_size, w4a16_stream_t stream)
+{
+    const int G = norm_group(K, group_size);
+    if (!valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    if (!codes || !scales || !packed || !scales_packed) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(scales_packed)) return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    return from_cuda(launch_pack_w8(codes, scales, packed, scales_packed, K, N,
+                                    ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad, ceil_div(N, kTileN),
+                                    ceil_div(K, G), st->sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_packed, uint16_t* y,
+                           int M, int N, int K, int group_size, const uint16_t* bias, const uint16_t* residual,
+                           int activation, void* workspace, size_t ws_bytes, w4a16_stream_t stream)
+{
+    if (activation < W4A16_ACT_NONE || activation > W4A16_ACT_RELU) return W4A16_ERR_INVALID_ARG;
+    if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
+        return W4A16_ERR_INVALID_ARG;
+    return gemm_impl(x, reinterpret_cast<const uint32_t*>(packed), scales_packed, y, M, N, K, group_size, workspace,
+                     ws_bytes, workspace == nullptr, reinterpret_cast<cudaStream_t>(stream), bias, residual,
+                     activation, kFmtW8);
 }
 
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream)
@@ -495,7 +558,7 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    const Plan P = make_plan(M, N, K, G, st->sms, max_clusters_for(st, make_plan(M, N, K, G, st->sms).tm));
+    const Plan P = device_plan(st, M, N, K, G, kFmtW4);
     *path = P.path;
     *tile_m = P.tm;
     *grid = P.grid;
@@ -549,8 +612,7 @@ extern "C" w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* pa
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    const int mc = max_clusters_for(st, make_plan(M, N, K, G, st->sms).tm);
-    if (make_plan(M, N, K, G, st->sms, mc).ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
+    if (device_plan(st, M, N, K, G, kFmtW4).ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc != W4A16_OK) return rc;

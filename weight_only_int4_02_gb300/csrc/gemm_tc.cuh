@@ -47,11 +47,18 @@ constexpr int kChunkWords = 1024;  // packed words per (tile, sub-chunk): 128 * 
 constexpr int kChunkBytes = 4096;
 constexpr int kKPad = 4;           // the packed layout pads K to a multiple of 4 sub-chunks
 
+// Weight formats (a template parameter of the kernel): 4-bit codes with the
+// zero-point 8; 4-bit codes with one zero-point per (group, column); 8-bit codes
+// with the zero-point 128 (8 KB per (tile, sub-chunk), bytes of a word in the
+// order k, k+2, k+1, k+3).
+constexpr int kFmtW4 = 0;
+constexpr int kFmtW4Zp = 1;
+constexpr int kFmtW8 = 2;
+
 struct GemmParams {
-    const uint32_t* packed;
+    const uint32_t* packed; // packed codes (4-bit: 1024 words per (tile, sub-chunk); 8-bit: 2048)
     const __half* scales;   // tile-ordered scales [n_tiles][ng][128]
-    const uint8_t* zeros;   // tile-ordered 4-bit zero-points [n_tiles][ng][64 bytes] (kernels built
-                            // for them only; the others use the zero-point 8)
+    const uint8_t* zeros;   // tile-ordered 4-bit zero-points [n_tiles][ng][64 bytes] (kFmtW4Zp only)
     __half* y;
     float* partials;        // [2 * grid][TM][128] FP32
     int* counters;          // [grid], zero between launches (index = cluster * p.cluster + rank)
@@ -95,19 +102,22 @@ __device__ __forceinline__ float epilogue_op(int act, float v, float b, float r)
 
 __device__ __forceinline__ float load_half(const __half* base, size_t i) { return base ? __half2float(base[i]) : 0.f; }
 
-template <int TM, int KSUB, bool ZP = false>
+template <int TM, int KSUB, int FMT = kFmtW4>
 struct TcCfg {
     static constexpr int kStageK = KSUB * kChunkK;
     static constexpr int kXBlock = TM * 128;              // one 64-wide K block of X (TM rows)
     static constexpr int kXBytes = KSUB * kXBlock;
-    static constexpr int kPkBytes = KSUB * kChunkBytes;
+    static constexpr int kPkChunk = FMT == kFmtW8 ? 2 * kChunkBytes : kChunkBytes;  // per (tile, sub-chunk)
+    static constexpr int kPkBytes = KSUB * kPkChunk;
     static constexpr int kScBytes = 2 * KSUB * 256;       // G = 32 puts 2*KSUB groups in a stage
-    static constexpr int kZpBytes = ZP ? 2 * KSUB * 64 : 0;  // 4-bit zero-points of those groups
+    static constexpr int kZpBytes = FMT == kFmtW4Zp ? 2 * KSUB * 64 : 0;  // 4-bit zero-points of those groups
     // Two rings in shared memory: W (packed words + scales [+ zero-points]), freed
     // by the dequant warps once they hold their words, so the HBM stream never
     // waits on the MMA; and X, freed by the MMA's commit.
     static constexpr int kWStageBytes = kPkBytes + kScBytes + kZpBytes;
-    static constexpr int kWStages = (TM <= 32 || KSUB == 2) ? 8 : 6;  // a multiple of the team count
+    // a multiple of the team count; 8-bit stages of 128-row tiles and up are 4 deep
+    // (64 KB of codes in flight, as 8 stages of 4-bit codes) to leave room for X
+    static constexpr int kWStages = FMT == kFmtW8 ? (TM >= 128 ? 4 : 8) : (TM <= 32 || KSUB == 2) ? 8 : 6;
     static constexpr int kXFit = (220 * 1024 - kWStages * kWStageBytes) / kXBytes;
     static constexpr int kXStages = kXFit > 8 ? 8 : kXFit;
     // Dequant teams take stages in turn; a team is KSUB/2 groups of four warps.
@@ -175,6 +185,23 @@ __device__ __forceinline__ int group_of(const GemmParams& p, int k)
 }
 
 __device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
+
+// (q - 128) * s for 8-bit codes as two FP16 pairs (k, k+1), (k+2, k+3) from one
+// word holding k, k+2, k+1, k+3 in bytes 0..3: OR-ing bytes 0 and 2 (or 1 and 3)
+// into the mantissas of 1024.0 gives 1024 + q exactly (the ulp at 1024 is 1).
+__device__ __forceinline__ void dequant_word8(uint32_t w, __half2 s2, uint32_t* out)
+{
+    const uint32_t mask = 0x00FF00FFu, magic = 0x64006400u;
+    const __half2 c1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const uint32_t a = and_or(w, mask, magic);        // bytes 0, 2 -> k, k+1
+    const uint32_t b = and_or(w >> 8, mask, magic);   // bytes 1, 3 -> k+2, k+3
+    __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), c1152);
+    __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), c1152);
+    ha = __hmul2(ha, s2);
+    hb = __hmul2(hb, s2);
+    out[0] = *reinterpret_cast<uint32_t*>(&ha);
+    out[1] = *reinterpret_cast<uint32_t*>(&hb);
+}
 
 // Dequantisation constants for the zero-point z (0..15), duplicated in both halves:
 // lo = 1024 + z (binary16 0x6400 | z) and hi = -(64 + z) (0xD400 | 16z; the ulp at
@@ -300,12 +327,14 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
 
 // EPI: the instantiation with the fused epilogue (bias, activation, residual);
 // the plain one carries none of its code.
-template <int TM, int KSUB, int CL, bool EPI, bool ZP>
-__global__ void __launch_bounds__(TcCfg<TM, KSUB, ZP>::kThreads, 1)
+template <int TM, int KSUB, int CL, bool EPI, int FMT>
+__global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
     static_assert(CL == 1 || (CL == 2 && KSUB % 2 == 0), "cluster of two splits a stage's X blocks");
-    using C = TcCfg<TM, KSUB, ZP>;
+    static_assert(FMT != kFmtW8 || KSUB == 2, "8-bit codes run 128-value stages (16 KB of codes)");
+    constexpr bool ZP = FMT == kFmtW4Zp;
+    using C = TcCfg<TM, KSUB, FMT>;
     constexpr int SW = C::kWStages;
     constexpr int SX = C::kXStages;
     constexpr int A = C::kAStages;
@@ -426,8 +455,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, ZP>::kThreads, 1)
                         const uint32_t zp_bytes = ZP ? (uint32_t)(g1 - g0 + 1) * 64u : 0u;
                         mbar_arrive_expect_tx(wfull_bar(s), C::kPkBytes + sc_bytes + zp_bytes);
                         bulk_load(sbase + C::kOffPk + s * C::kPkBytes,
-                                  p.packed + ((size_t)nt * p.KC + (size_t)kc * KSUB) * kChunkWords, C::kPkBytes,
-                                  wfull_bar(s));
+                                  p.packed + ((size_t)nt * p.KC + (size_t)kc * KSUB) * (C::kPkChunk / 4),
+                                  C::kPkBytes, wfull_bar(s));
                         bulk_load(sbase + C::kOffSc + s * C::kScBytes, p.scales + ((size_t)nt * p.ng + g0) * kTileN,
                                   sc_bytes, wfull_bar(s));
                         if constexpr (ZP)
@@ -537,15 +566,18 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, ZP>::kThreads, 1)
                 const __half* sc = reinterpret_cast<const __half*>(smem + C::kOffSc + s * C::kScBytes) + n_in;
                 const uint8_t* zb = smem + C::kOffZp + s * C::kZpBytes + (n_in >> 1);   // ZP only
                 const int zshift = 4 * (n_in & 1);
-                uint4 w[2][2];
+                // A thread's 16-byte blocks of a sub-chunk sit 2 KB apart: 2 for 4-bit
+                // codes (32 values each), 4 for 8-bit codes (16 values each).
+                constexpr int NB = FMT == kFmtW8 ? 4 : 2;
+                uint4 w[2][NB];
                 __half2 s2[2][2];
                 __half2 clo[2][2], chi[2][2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int j = 2 * gi + h;
-                    const uint8_t* pk = smem + C::kOffPk + s * C::kPkBytes + j * kChunkBytes + n_in * 16;
-                    w[h][0] = *reinterpret_cast<const uint4*>(pk);
-                    w[h][1] = *reinterpret_cast<const uint4*>(pk + kTileN * 16);
+                    const uint8_t* pk = smem + C::kOffPk + s * C::kPkBytes + j * C::kPkChunk + n_in * 16;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) w[h][b] = *reinterpret_cast<const uint4*>(pk + b * kTileN * 16);
                     const int k0 = kc * C::kStageK + j * kChunkK;
                     const __half s_lo = sc[(group_of(p, k0) - gs) * kTileN];
                     const __half s_hi = sc[(group_of(p, k0 + 32) - gs) * kTileN];
@@ -567,15 +599,25 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, ZP>::kThreads, 1)
                 if (lane == 0) mbar_arrive(wempty_bar(s));   // words, scales and zero-points are in registers
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t v[32];
-                    dequant_word(w[h][0].x, s2[h][0], clo[h][0], chi[h][0], v + 0);
-                    dequant_word(w[h][0].y, s2[h][0], clo[h][0], chi[h][0], v + 4);
-                    dequant_word(w[h][0].z, s2[h][0], clo[h][0], chi[h][0], v + 8);
-                    dequant_word(w[h][0].w, s2[h][0], clo[h][0], chi[h][0], v + 12);
-                    dequant_word(w[h][1].x, s2[h][1], clo[h][1], chi[h][1], v + 16);
-                    dequant_word(w[h][1].y, s2[h][1], clo[h][1], chi[h][1], v + 20);
-                    dequant_word(w[h][1].z, s2[h][1], clo[h][1], chi[h][1], v + 24);
-                    dequant_word(w[h][1].w, s2[h][1], clo[h][1], chi[h][1], v + 28);
+                    uint32_t v[32];   // FP16 pairs (k, k+1) of the sub-chunk's 64 values
+                    if constexpr (FMT == kFmtW8) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            dequant_word8(w[h][b].x, s2[h][b >> 1], v + 8 * b + 0);
+                            dequant_word8(w[h][b].y, s2[h][b >> 1], v + 8 * b + 2);
+                            dequant_word8(w[h][b].z, s2[h][b >> 1], v + 8 * b + 4);
+                            dequant_word8(w[h][b].w, s2[h][b >> 1], v + 8 * b + 6);
+                        }
+                    } else {
+                        dequant_word(w[h][0].x, s2[h][0], clo[h][0], chi[h][0], v + 0);
+                        dequant_word(w[h][0].y, s2[h][0], clo[h][0], chi[h][0], v + 4);
+                        dequant_word(w[h][0].z, s2[h][0], clo[h][0], chi[h][0], v + 8);
+                        dequant_word(w[h][0].w, s2[h][0], clo[h][0], chi[h][0], v + 12);
+                        dequant_word(w[h][1].x, s2[h][1], clo[h][1], chi[h][1], v + 16);
+                        dequant_word(w[h][1].y, s2[h][1], clo[h][1], chi[h][1], v + 20);
+                        dequant_word(w[h][1].z, s2[h][1], clo[h][1], chi[h][1], v + 24);
+                        dequant_word(w[h][1].w, s2[h][1], clo[h][1], chi[h][1], v + 28);
+                    }
                     if (h == 0) {
                         // the A slot is free once the MMAs that read it two stages ago completed
                         if (!wait_warp(aempty_bar(a), ((seq / A) & 1) ^ 1, ctl)) { ok = false; break; }
@@ -700,10 +742,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, ZP>::kThreads, 1)
     }
 }
 
-template <int TM, int KSUB, int CL, bool EPI, bool ZP>
+template <int TM, int KSUB, int CL, bool EPI, int FMT>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream);
 
-template <int TM, int KSUB, int CL, bool EPI, bool ZP>
+template <int TM, int KSUB, int CL, bool EPI, int FMT>
 cudaError_t setup_tc(int* max_clusters);
 
 }  // namespace w4a16

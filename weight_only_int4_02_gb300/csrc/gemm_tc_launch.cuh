@@ -1,5 +1,5 @@
-// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL, EPI, ZP>; included by one .cu file per tile
-// shape and weight format (zero-point 8, or per-group zero-points).
+// Host-side launch and set-up of w4a16_tc_kernel<TM, KSUB, CL, EPI, FMT>; included by one .cu file per tile
+// shape and weight format.
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -7,11 +7,11 @@ namespace w4a16 {
 
 // Dynamic shared memory, and for clusters the number of clusters the device can
 // hold at once (0 when the query fails).
-template <int TM, int KSUB, int CL, bool EPI, bool ZP>
+template <int TM, int KSUB, int CL, bool EPI, int FMT>
 cudaError_t setup_tc(int* max_clusters)
 {
-    using C = TcCfg<TM, KSUB, ZP>;
-    auto kernel = w4a16_tc_kernel<TM, KSUB, CL, EPI, ZP>;
+    using C = TcCfg<TM, KSUB, FMT>;
+    auto kernel = w4a16_tc_kernel<TM, KSUB, CL, EPI, FMT>;
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -36,10 +36,10 @@ cudaError_t setup_tc(int* max_clusters)
     return cudaSuccess;
 }
 
-template <int TM, int KSUB, int CL, bool EPI, bool ZP>
+template <int TM, int KSUB, int CL, bool EPI, int FMT>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream)
 {
-    using C = TcCfg<TM, KSUB, ZP>;
+    using C = TcCfg<TM, KSUB, FMT>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(C::kThreads);
@@ -60,16 +60,16 @@ cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL, EPI, ZP>, tmap, p);
+    return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<TM, KSUB, CL, EPI, FMT>, tmap, p);
 }
 
 }  // namespace w4a16
 
-// Both epilogue variants of one tile shape and weight format (ZP = per-group zero-points).
-#define W4A16_INSTANTIATE_TC(TM, KSUB, CL, ZP)                                                                    \
-    namespace w4a16 {                                                                                             \
-    template cudaError_t setup_tc<TM, KSUB, CL, false, ZP>(int*);                                                 \
-    template cudaError_t setup_tc<TM, KSUB, CL, true, ZP>(int*);                                                  \
-    template cudaError_t launch_tc<TM, KSUB, CL, false, ZP>(const CUtensorMap&, const GemmParams&, cudaStream_t); \
-    template cudaError_t launch_tc<TM, KSUB, CL, true, ZP>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
+// Both epilogue variants of one tile shape and weight format (w4a16::kFmt*).
+#define W4A16_INSTANTIATE_TC(TM, KSUB, CL, FMT)                                                                    \
+    namespace w4a16 {                                                                                              \
+    template cudaError_t setup_tc<TM, KSUB, CL, false, FMT>(int*);                                                 \
+    template cudaError_t setup_tc<TM, KSUB, CL, true, FMT>(int*);                                                  \
+    template cudaError_t launch_tc<TM, KSUB, CL, false, FMT>(const CUtensorMap&, const GemmParams&, cudaStream_t); \
+    template cudaError_t launch_tc<TM, KSUB, CL, true, FMT>(const CUtensorMap&, const GemmParams&, cudaStream_t);  \
     }

@@ -85,6 +85,54 @@ cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N
     return cudaGetLastError();
 }
 
+// 8-bit codes (W8A16): byte (((nt*KC + kc)*4 + j4)*128 + n_in)*16 + b holds, for
+// word b/4 with k0 = kc*64 + j4*16 + 4*(b/4), the code of k0 + {0, 2, 1, 3}[b%4] in
+// column nt*128 + n_in: masking bytes 0 and 2 (1 and 3) of a word gives the FP16
+// pair (k, k+1) of one TMEM column; a thread's 16 bytes of a 16-value quarter sit
+// next to its neighbours'. Positions outside K x N hold 128 (weight 0).
+__global__ void pack_codes_w8_kernel(const uint8_t* __restrict__ codes, uint32_t* __restrict__ packed, int K, int N,
+                                     int KC, long long total_words)
+{
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total_words;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int w = (int)(idx & 3);
+        const int n_in = (int)((idx >> 2) & 127);
+        const int j4 = (int)((idx >> 9) & 3);
+        const long long rest = idx >> 11;
+        const int kc = (int)(rest % KC);
+        const int nt = (int)(rest / KC);
+        const int n = nt * 128 + n_in;
+        const int k0 = kc * 64 + j4 * 16 + w * 4;
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int k = k0 + ((b & 1) << 1) + (b >> 1);   // bytes 0..3 hold k0 + 0, 2, 1, 3
+            const uint32_t c = (k < K && n < N) ? (uint32_t)codes[(size_t)k * N + n] : 128u;
+            word |= c << (8 * b);
+        }
+        packed[idx] = word;
+    }
+}
+
+cudaError_t launch_pack_w8(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
+                           int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream)
+{
+    const long long words = (long long)n_tiles * KC * 2048;
+    const long long selems = (long long)n_tiles * ng * 128;
+    const int threads = 256;
+    const long long cap = (long long)sms * 16;
+    long long blocks = (words + threads - 1) / threads;
+    if (blocks > cap) blocks = cap;
+    pack_codes_w8_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, reinterpret_cast<uint32_t*>(packed), K, N,
+                                                                    KC, words);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    blocks = (selems + threads - 1) / threads;
+    if (blocks > cap) blocks = cap;
+    pack_scales_kernel<<<(unsigned)blocks, threads, 0, stream>>>(scales, scales_packed, N, ng, selems);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,
                         int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream)
 {
