@@ -54,6 +54,11 @@ def _load():
         lib.w4o_unpack_scales.restype = ctypes.c_longlong
         lib.w4o_unpack_zeros.argtypes = [P, I, I, P]
         lib.w4o_unpack_zeros.restype = ctypes.c_longlong
+        lib.w4o_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.w4o_bf16_to_double.restype = ctypes.c_double
+        lib.w4o_decode_bf16.argtypes = [P, P, ctypes.c_size_t]
+        lib.w4o_gemm_sample_bf16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
+        lib.w4o_gemm_sample_bf16.restype = I
         lib.w4o_gemm_sample_w8.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
         lib.w4o_gemm_sample_w8.restype = I
         lib.w4o_dequant_w8.argtypes = [P, P, I, I, I, P]
@@ -188,6 +193,38 @@ def unpack_scales(sp, ng, N):
     s = np.empty((ng, N), np.uint16)
     bad = _load().w4o_unpack_scales(_ptr(sp), ng, N, _ptr(s))
     return s, int(bad)
+
+
+# ------------------------------------------------------------------ BF16 activations
+def bf16_to_double(bits):
+    """Decode bfloat16 bit patterns (uint16 array) to float64 with the oracle's decoder."""
+    b = np.ascontiguousarray(np.asarray(bits), dtype=np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().w4o_decode_bf16(_ptr(b), _ptr(out), b.size)
+    return out
+
+
+def gemm_sample_bf16(x, q, s, G, rows, cols, threads=None):
+    """(y, absum) restricted to rows x cols, x and s bfloat16 bit patterns (uint16)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    M, K = x.shape
+    N = q.shape[1]
+    assert q.shape[0] == K and s.shape == (n_groups(K, G), N)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    cols = np.ascontiguousarray(cols, dtype=np.int32)
+    y = np.empty((rows.size, cols.size), np.float64)
+    a = np.empty((rows.size, cols.size), np.float64)
+    rc = _load().w4o_gemm_sample_bf16(_ptr(x), _ptr(q), _ptr(s), M, N, K, G, _ptr(rows), rows.size,
+                                      _ptr(cols), cols.size, _ptr(y), _ptr(a), _threads(threads))
+    assert rc == 0
+    return y, a
+
+
+def gemm_bf16(x, q, s, G, threads=None):
+    """(y, absum) = x @ dequant(q, s) in float64 for bfloat16 x and s (bit patterns)."""
+    return gemm_sample_bf16(x, q, s, G, np.arange(np.shape(x)[0]), np.arange(np.shape(q)[1]), threads)
 
 
 # ------------------------------------------------------------------ W8A16 (8-bit codes, zero-point 128)

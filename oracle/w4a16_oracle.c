@@ -38,6 +38,12 @@
  * 8-bit counterpart of the 4-bit format's 8). Products have at most 30
  * significant bits: still exact in FP64.
  *
+ * BF16 activations (the *_bf16 entry points): x and s arrive as bfloat16 bit
+ * patterns (the upper 16 bits of an IEEE-754 binary32) and are decoded by this
+ * file's own bfloat16 decoder; the arithmetic is the same FP64 definition. The
+ * pages name BF16 beside FP16 as the 16-bit activation type ("Low-Precision
+ * Quantization Kernels in Production" (llms.blog), introduction).
+ *
  * The packed-layout functions at the end restate the packed word layout that
  * the library's pack entry point documents (the pages fix only "eight 4-bit
  * values per 32-bit word in a permuted order"; the order itself is free), so
@@ -65,6 +71,29 @@ double w4o_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* bfloat16 -> double: sign, 8-bit exponent with bias 127, 7-bit fraction. */
+double w4o_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);           /* subnormal: 0.f * 2^-126 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134); /* 1.f * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+void w4o_decode_bf16(const uint16_t* h, double* out, size_t count)
+{
+    for (size_t i = 0; i < count; ++i) out[i] = w4o_bf16_to_double(h[i]);
+}
+
+typedef double (*decode_fn)(uint16_t);
+
 void w4o_decode_halves(const uint16_t* h, double* out, size_t count)
 {
     for (size_t i = 0; i < count; ++i) out[i] = w4o_half_to_double(h[i]);
@@ -76,14 +105,14 @@ static int group_of(int k, int G) { return k / G; }
 /* Dequantise column n of the weight matrix into w_col[K]. z is [ceil(K/G)][N]
  * integer zero-points, or NULL for the fixed zero-point zdef (8 for 4-bit codes,
  * 128 for 8-bit codes). */
-static void dequant_column(const uint8_t* q, const uint16_t* s, const uint8_t* z, int zdef, int K, int N, int G,
-                           int n, double* w_col)
+static void dequant_column(const uint8_t* q, const uint16_t* s, const uint8_t* z, int zdef, decode_fn dec,
+                           int K, int N, int G, int n, double* w_col)
 {
     for (int k = 0; k < K; ++k) {
         int g = group_of(k, G);
         int code = q[(size_t)k * N + n];
         int zero = z ? z[(size_t)g * N + n] : zdef;
-        double scale = w4o_half_to_double(s[(size_t)g * N + n]);
+        double scale = dec(s[(size_t)g * N + n]);
         w_col[k] = (double)(code - zero) * scale;
     }
 }
@@ -93,7 +122,7 @@ void w4o_dequant_zp(const uint8_t* q, const uint16_t* s, const uint8_t* z, int K
 {
     double* col = (double*)malloc(sizeof(double) * (size_t)K);
     for (int n = 0; n < N; ++n) {
-        dequant_column(q, s, z, 8, K, N, G, n, col);
+        dequant_column(q, s, z, 8, w4o_half_to_double, K, N, G, n, col);
         for (int k = 0; k < K; ++k) w[(size_t)k * N + n] = col[k];
     }
     free(col);
@@ -105,7 +134,7 @@ void w4o_dequant(const uint8_t* q, const uint16_t* s, int K, int N, int G, doubl
 }
 
 typedef struct {
-    const uint16_t* x; const uint8_t* q; const uint16_t* s; const uint8_t* z; int zdef;
+    const uint16_t* x; const uint8_t* q; const uint16_t* s; const uint8_t* z; int zdef; decode_fn dec;
     int M, N, K, G;
     const int* rows; int nrows;      /* rows of y to evaluate           */
     const int* cols; int ncols;      /* columns of y to evaluate        */
@@ -119,7 +148,7 @@ static void* worker(void* arg)
     job_t* j = (job_t*)arg;
     double* w_col = (double*)malloc(sizeof(double) * (size_t)j->K);
     for (int c = j->col_begin; c < j->col_end; ++c) {
-        dequant_column(j->q, j->s, j->z, j->zdef, j->K, j->N, j->G, j->cols[c], w_col);
+        dequant_column(j->q, j->s, j->z, j->zdef, j->dec, j->K, j->N, j->G, j->cols[c], w_col);
         for (int r = 0; r < j->nrows; ++r) {
             const double* xr = j->xd + (size_t)r * j->K;
             double acc = 0.0, acc_abs = 0.0;
@@ -145,7 +174,7 @@ static void* worker(void* arg)
  * element does not depend on the split.
  */
 static int gemm_sample_any(const uint16_t* x, const uint8_t* q, const uint16_t* s, const uint8_t* z, int zdef,
-                           int M, int N, int K, int G,
+                           decode_fn dec, int M, int N, int K, int G,
                            const int* rows, int nrows, const int* cols, int ncols,
                            double* y, double* absum, int threads)
 {
@@ -154,7 +183,7 @@ static int gemm_sample_any(const uint16_t* x, const uint8_t* q, const uint16_t* 
     for (int r = 0; r < nrows; ++r) {
         if (rows[r] < 0 || rows[r] >= M) { free(xd); return 1; }
         for (int k = 0; k < K; ++k)
-            xd[(size_t)r * K + k] = w4o_half_to_double(x[(size_t)rows[r] * K + k]);
+            xd[(size_t)r * K + k] = dec(x[(size_t)rows[r] * K + k]);
     }
     for (int c = 0; c < ncols; ++c)
         if (cols[c] < 0 || cols[c] >= N) { free(xd); return 1; }
@@ -163,7 +192,7 @@ static int gemm_sample_any(const uint16_t* x, const uint8_t* q, const uint16_t* 
     pthread_t* tid = (pthread_t*)malloc(sizeof(pthread_t) * threads);
     job_t* jobs = (job_t*)malloc(sizeof(job_t) * threads);
     for (int t = 0; t < threads; ++t) {
-        job_t j = {x, q, s, z, zdef, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+        job_t j = {x, q, s, z, zdef, dec, M, N, K, G, rows, nrows, cols, ncols, y, absum,
                    (int)((long long)ncols * t / threads),
                    (int)((long long)ncols * (t + 1) / threads), xd};
         jobs[t] = j;
@@ -180,7 +209,18 @@ int w4o_gemm_sample_zp(const uint16_t* x, const uint8_t* q, const uint16_t* s, c
                        const int* rows, int nrows, const int* cols, int ncols,
                        double* y, double* absum, int threads)
 {
-    return gemm_sample_any(x, q, s, z, 8, M, N, K, G, rows, nrows, cols, ncols, y, absum, threads);
+    return gemm_sample_any(x, q, s, z, 8, w4o_half_to_double, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+                           threads);
+}
+
+/* BF16 activations and scales (bfloat16 bit patterns), 4-bit codes, zero-point 8. */
+int w4o_gemm_sample_bf16(const uint16_t* x, const uint8_t* q, const uint16_t* s,
+                         int M, int N, int K, int G,
+                         const int* rows, int nrows, const int* cols, int ncols,
+                         double* y, double* absum, int threads)
+{
+    return gemm_sample_any(x, q, s, NULL, 8, w4o_bf16_to_double, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+                           threads);
 }
 
 /* The W8A16 format: q[K][N] are 8-bit codes 0..255, zero-point 128. */
@@ -189,14 +229,15 @@ int w4o_gemm_sample_w8(const uint16_t* x, const uint8_t* q, const uint16_t* s,
                        const int* rows, int nrows, const int* cols, int ncols,
                        double* y, double* absum, int threads)
 {
-    return gemm_sample_any(x, q, s, NULL, 128, M, N, K, G, rows, nrows, cols, ncols, y, absum, threads);
+    return gemm_sample_any(x, q, s, NULL, 128, w4o_half_to_double, M, N, K, G, rows, nrows, cols, ncols, y, absum,
+                           threads);
 }
 
 void w4o_dequant_w8(const uint8_t* q, const uint16_t* s, int K, int N, int G, double* w)
 {
     double* col = (double*)malloc(sizeof(double) * (size_t)K);
     for (int n = 0; n < N; ++n) {
-        dequant_column(q, s, NULL, 128, K, N, G, n, col);
+        dequant_column(q, s, NULL, 128, w4o_half_to_double, K, N, G, n, col);
         for (int k = 0; k < K; ++k) w[(size_t)k * N + n] = col[k];
     }
     free(col);

@@ -14,7 +14,10 @@
 * 8-bit codes (W8A16, zero-point 128): brute force in exact rationals, codes 128
   give 0, 8-bit codes 16*q equal 16 times the 4-bit result for codes q, numpy's
   matmul on the expanded weights, the 8-bit layout (bijection, round trip, the
-  pair (k, k+1) in bytes 0 and 2 of a word).
+  pair (k, k+1) in bytes 0 and 2 of a word);
+* BF16 activations: the bfloat16 decoder against numpy's float32 reading of the
+  same bits over all 65536 patterns, brute force in exact rationals on bfloat16
+  inputs, and equality with the FP16 form on values exact in both formats.
 """
 import os
 import re
@@ -256,6 +259,9 @@ MUTANTS = {
     "zero_point_of_mirrored_column": ("int zero = z ? z[(size_t)g * N + n] : zdef;",
                                       "int zero = z ? z[(size_t)g * N + (N - 1 - n)] : zdef;"),
     "zero_point_sign": ("(double)(code - zero)", "(double)(zero - code)"),
+    "bf16_exponent_bias": ("ldexp((double)(128 + f), e - 134)", "ldexp((double)(128 + f), e - 133)"),
+    "bf16_x_read_as_fp16": ("xd[(size_t)r * K + k] = dec(x[(size_t)rows[r] * K + k]);",
+                            "xd[(size_t)r * K + k] = w4o_half_to_double(x[(size_t)rows[r] * K + k]);"),
     "w8_zero_point_127": ("return gemm_sample_any(x, q, s, NULL, 128,", "return gemm_sample_any(x, q, s, NULL, 127,"),
     "w8_byte_order": ("slot_of_offset[4] = {0, 2, 1, 3}", "slot_of_offset[4] = {0, 1, 2, 3}"),
     "no_groups": ("static int group_of(int k, int G) { return k / G; }",
@@ -292,6 +298,7 @@ def test_planted_mistakes_fail_a_pin(oracle_mod, name):
                       lambda o: test_zero_points_brute_force_exact(o, 0),
                       lambda o: test_zero_points_brute_force_exact(o, 1),
                       lambda o: test_w8_brute_force_exact(o, 0),
+                      test_bf16_decoder_all_patterns, lambda o: test_bf16_brute_force_exact(o, 0),
                       test_w8_layout_pairs_adjacent_k_in_bytes_0_and_2):
             try:
                 check(mut)
@@ -476,6 +483,59 @@ def test_w8_layout_pairs_adjacent_k_in_bytes_0_and_2(oracle_mod):
     # adjacent columns' 16-byte blocks are adjacent; quarters of 16 k are 2 KB apart
     assert oracle_mod.locate_w8(64, 0, 1) == oracle_mod.locate_w8(64, 0, 0) + 16
     assert oracle_mod.locate_w8(64, 16, 0) == oracle_mod.locate_w8(64, 0, 0) + 2048
+
+
+# --------------------------------------------------------------------------- BF16 activations
+# x and s as bfloat16 ("Low-Precision Quantization Kernels in Production"
+# (llms.blog), introduction: FP16 and BF16 are the 16-bit types the weights are
+# quantised from and the tensor cores run).
+def bf16_values(bits):
+    """numpy's reading of bfloat16 bits: the upper half of a float32."""
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
+
+
+def test_bf16_decoder_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle_mod.bf16_to_double(bits)
+    with np.errstate(invalid="ignore"):   # signalling-NaN patterns
+        ref = bf16_values(bits).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    named = {0x3F80: 1.0, 0xC000: -2.0, 0x4300: 128.0, 0x4308: 136.0, 0x0001: 2.0 ** -133,
+             0x0080: 2.0 ** -126, 0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127}
+    for b, v in named.items():
+        assert oracle_mod.bf16_to_double(np.array([b], np.uint16))[0] == v
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bf16_brute_force_exact(oracle_mod, seed):
+    r = np.random.default_rng(4000 + seed)
+    M, K, N = (int(v) for v in r.integers(1, 9, size=3))
+    G = int(r.choice([1, 2, 3, 4, K]))
+    ng = -(-K // G)
+    x = inputs.to_bf16_bits((r.standard_normal((M, K)) * 4).astype(np.float32))
+    q = r.integers(0, 16, size=(K, N)).astype(np.uint8)
+    s = inputs.to_bf16_bits(np.abs(r.standard_normal((ng, N))).astype(np.float32))
+    y, a = oracle_mod.gemm_bf16(x, q, s, G)
+    ye, ae = exact_reference(bf16_values(x), q, bf16_values(s), G)
+    for m in range(M):
+        for n in range(N):
+            bound = (K * 2.0 ** -53) * float(ae[m][n])
+            assert abs(Fraction(y[m][n]) - ye[m][n]) <= Fraction(bound)
+            assert abs(Fraction(a[m][n]) - ae[m][n]) <= Fraction(bound)
+
+
+def test_bf16_equals_fp16_on_values_exact_in_both(oracle_mod):
+    r = np.random.default_rng(6)
+    M, K, N, G = 4, 96, 24, 32
+    xv = (r.integers(-64, 65, size=(M, K)) / 16.0).astype(np.float32)   # 8 significant bits at most
+    sv = (2.0 ** r.integers(-12, 0, size=(3, N))).astype(np.float32)
+    q = inputs.codes(K, N, seed=6)
+    y16, a16 = oracle_mod.gemm(xv.astype(np.float16), q, sv.astype(np.float16), G)
+    yb, ab = oracle_mod.gemm_bf16(inputs.to_bf16_bits(xv), q, inputs.to_bf16_bits(sv), G)
+    assert np.array_equal(bf16_values(inputs.to_bf16_bits(xv)), xv)
+    assert np.array_equal(y16, yb) and np.array_equal(a16, ab)
 
 
 # --------------------------------------------------------------------------- fused epilogue

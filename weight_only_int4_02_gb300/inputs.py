@@ -12,7 +12,9 @@ sizes on Llama-2-like shapes, a 72k x 18k layer, prefill shapes):
   * scales s = FP16(|N(0,1)| * c) per (group, column) with c = 0.02 (0.01 for
     the 72k x 18k layer), or FP16(10^U(-4,-1)) for the edge sweep;
   * zero-points z ~ uniform on {0..15} per (group, column) for the asymmetric
-    format (every value, the extremes 0 and 15 included, is exercised).
+    format (every value, the extremes 0 and 15 included, is exercised);
+  * for BF16 activations, the same x and s distributions rounded to bfloat16
+    (round-to-nearest-even of the float32 draw), passed as bit patterns.
 """
 import numpy as np
 
@@ -30,6 +32,17 @@ def activations(M, K, seed=0, outlier_frac=0.0, outlier_mult=20.0):
         mask = rng(seed, OUTLIER_STREAM).random((M, K), dtype=np.float32) < outlier_frac
         x = np.where(mask, x * np.float32(outlier_mult), x)
     return x.astype(np.float16)
+
+
+def to_bf16_bits(a):
+    """float32 array -> bfloat16 bit patterns (uint16), round to nearest even (finite values)."""
+    b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def activations_bf16(M, K, seed=0):
+    """x[M][K] ~ N(0, 1) as bfloat16 bit patterns (uint16), from the same stream as activations()."""
+    return to_bf16_bits(rng(seed, X_STREAM).standard_normal((M, K), dtype=np.float32))
 
 
 def codes(K, N, seed=0):
@@ -52,6 +65,12 @@ def scales(K, N, group_size, seed=0, kind="halfnormal", mult=0.02):
     else:
         raise ValueError(kind)
     return s.astype(np.float16)
+
+
+def scales_bf16(K, N, group_size, seed=0, mult=0.02):
+    """s[ceil(K/G)][N] = |N(0,1)| * mult as bfloat16 bit patterns (uint16)."""
+    s = np.abs(rng(seed, SCALE_STREAM).standard_normal((n_groups(K, group_size), N), dtype=np.float32))
+    return to_bf16_bits(s * np.float32(mult))
 
 
 def zeros(K, N, group_size, seed=0):
