@@ -467,6 +467,7 @@ def run_ours(args, rank, world):
         out["layer_chain"] = layer_chain_probe(G)
         out["zero_points"] = zero_point_probe(G)
         out["w8a16"] = w8_probe(G)
+        out["bf16_activations"] = bf16_probe(G)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
@@ -554,6 +555,40 @@ def w8_probe(G):
         wb = n_groups(K, G) * G * N + n_groups(K, G) * N * 2
         rows.append({"case": [M, K, N], "us": us, "weight_gbs": wb / (us * 1e-6) / 1e9,
                      "tflops": flops(M, K, N) / (us * 1e-6) / 1e12})
+        del copies
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return rows
+
+
+def bf16_probe(G):
+    """BF16 activations beside FP16 on the same shapes: mean time per launch of
+    w4a16_gemm (FP16) and w4a16_bf16_gemm (BF16 X, scales and Y), launched back to
+    back from a CUDA Graph over rotating copies of the packed weights, on the
+    gate/up decode layer (16 x 4096 x 22016) and a prefill layer (1024 x 5120 x 15360)."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    rows = []
+    for M, K, N in ((16, 4096, 22016), (1024, 5120, 15360)):
+        q = torch.from_numpy(inputs.codes(K, N, 0)).cuda()
+        s16 = torch.from_numpy(inputs.scales(K, N, G, 0)).cuda()
+        packed, sp16 = w4a16.pack(q, s16, G)
+        sbf = torch.from_numpy(inputs.scales_bf16(K, N, G, 0).view(np.int16)).cuda().view(torch.bfloat16)
+        _, spbf = w4a16.pack(q, sbf, G)
+        del q, s16, sbf
+        n_copies = max(2, int(400e6 // (packed.numel() * 4)) + 1)
+        copies = [(packed.clone(), sp16.clone(), spbf.clone()) for _ in range(n_copies)]
+        del packed, sp16, spbf
+        x16 = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
+        xbf = torch.from_numpy(inputs.activations_bf16(M, K, 0).view(np.int16)).cuda().view(torch.bfloat16)
+        y16 = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        ybf = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        us16 = graph_us_per_launch(
+            lambda c: w4a16.gemm(x16, c[0], c[1], N, G, y=y16, stream=torch.cuda.current_stream()), copies)
+        usbf = graph_us_per_launch(
+            lambda c: w4a16.bf16_gemm(xbf, c[0], c[2], N, G, y=ybf, stream=torch.cuda.current_stream()), copies)
+        rows.append({"case": [M, K, N], "us_fp16": us16, "us_bf16": usbf,
+                     "tflops_bf16": flops(M, K, N) / (usbf * 1e-6) / 1e12})
         del copies
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("a kernel wait timed out")

@@ -82,7 +82,8 @@ size_t w4a16_scales_elems(int K, int N, int group_size);
  * Repack codes and scales once, offline ("End-to-end flow": the layout is
  * computed once and exploited on every forward pass).
  *   codes          device, uint8 [K][N], values 0..15 (only the low nibble is read)
- *   scales         device, binary16 [ceil(K/G)][N]
+ *   scales         device, binary16 [ceil(K/G)][N] (or bfloat16 for w4a16_bf16_gemm:
+ *                  the scales are copied as 16-bit patterns)
  *   packed         device out, uint32 [w4a16_packed_words(K, N, G)]
  *   scales_packed  device out, binary16 [w4a16_scales_elems(K, N, G)]
  * Packed layout (version 2): column tiles of 128 output features, reduction
@@ -191,6 +192,25 @@ w4a16_status w4a16_gemm_zp(const uint16_t* x, const uint32_t* packed, const uint
                            const uint8_t* zeros_packed, uint16_t* y, int M, int N, int K, int group_size,
                            const uint16_t* bias, const uint16_t* residual, int activation,
                            void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
+/* ---------------------------------------------------------------- BF16 activations
+ * The 4-bit GEMM (zero-point 8, layout of w4a16_pack) with every 16-bit tensor in
+ * bfloat16 instead of binary16: X, the scales, bias, residual and Y, passed as
+ * bfloat16 bit patterns (uint16_t). Both tensor-core operands are BF16: the weights
+ * are dequantised to BF16, (128 + q) - 136 = q - 8 exactly, then one rounding at
+ * the product with the scale (BF16 keeps 8 significant bits, so each weight
+ * carries up to 2^-8 relative error against 2^-11 in the FP16 form).
+ * ("Low-Precision Quantization Kernels in Production" (llms.blog), introduction:
+ * FP16 and BF16 are the 16-bit types the weights are quantised from and the
+ * tensor cores run.)
+ *   scales_packed  w4a16_pack's scales output for BF16 scales (the repack copies
+ *                  16-bit patterns, so the same call serves both types)
+ * Every other argument, layout and error is that of w4a16_gemm_fused.
+ */
+w4a16_status w4a16_bf16_gemm(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed,
+                             uint16_t* y, int M, int N, int K, int group_size,
+                             const uint16_t* bias, const uint16_t* residual, int activation,
+                             void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
 /* ---------------------------------------------------------------- W8A16: 8-bit codes
  * The same GEMM for 8-bit weights: dequant(Wq)[k][n] = (q[k][n] - 128) * s[k/G][n],

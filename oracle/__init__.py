@@ -299,9 +299,10 @@ def unpack_zeros(zp, ng, N):
     return z, int(bad)
 
 
-def epilogue(z, bias=None, residual=None, activation="none", rows=None, cols=None):
+def epilogue(z, bias=None, residual=None, activation="none", rows=None, cols=None, dtype="f16"):
     """The fused epilogue in float64 on GEMM results z (float64 [M][N], or the
-    sample rows x cols of it): act(z + bias[n]) + residual[m][n].
+    sample rows x cols of it): act(z + bias[n]) + residual[m][n]. dtype "bf16":
+    bias and residual are bfloat16 bit patterns (uint16).
 
     Follows "quant_marlin_kernel", "End-to-end flow" (the output tile flows into a
     bias add, then an activation); the residual add after the activation is the
@@ -309,8 +310,9 @@ def epilogue(z, bias=None, residual=None, activation="none", rows=None, cols=Non
     residual (float16 [M][N]) are decoded with the oracle's own binary16 decoder;
     SiLU(z) = z / (1 + e^-z) with numpy's exp, ReLU(z) = max(z, 0)."""
     z = np.array(z, dtype=np.float64, copy=True)
+    decode = bf16_to_double if dtype == "bf16" else half_to_double
     if bias is not None:
-        b = half_to_double(bias)
+        b = decode(bias)
         z += b if cols is None else b[np.asarray(cols)]
     if activation == "silu":
         with np.errstate(over="ignore"):
@@ -320,6 +322,6 @@ def epilogue(z, bias=None, residual=None, activation="none", rows=None, cols=Non
     else:
         assert activation == "none", activation
     if residual is not None:
-        r = half_to_double(residual)
+        r = decode(residual)
         z += r if rows is None else r[np.ix_(np.asarray(rows), np.asarray(cols))]
     return z

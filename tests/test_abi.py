@@ -88,6 +88,11 @@ def test_invalid_arguments_return_before_any_device_work(lib):
     assert lib.w4a16_pack_zeros(None, p, 64, 64, 64, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_pack_zeros(p, odd, 64, 64, 64, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_pack_zeros(p, p, 64, 60, 64, None) == w.ERR_INVALID_ARG
+    # BF16 activations
+    assert lib.w4a16_bf16_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_bf16_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_bf16_gemm(odd, p, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_bf16_gemm(p, p, p, p, 0, 64, 64, 64, None, None, 0, None, 0, None) == w.OK
     # 8-bit codes
     assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG

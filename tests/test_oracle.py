@@ -582,6 +582,14 @@ def test_epilogue_on_the_hand_example(oracle_mod):
     assert np.array_equal(got, want)
 
 
+def test_epilogue_bf16_decodes_bias_and_residual_as_bfloat16(oracle_mod):
+    z = np.array([[1.0, -2.0, 0.5]])
+    b = np.array([0x3F80, 0xC000, 0x4300], np.uint16)          # 1, -2, 128 in bfloat16
+    r = np.array([[0x3F00, 0x0000, 0xBF80]], np.uint16)        # 0.5, 0, -1
+    got = oracle_mod.epilogue(z, bias=b, residual=r, activation="relu", dtype="bf16")
+    assert np.array_equal(got, np.array([[2.5, 0.0, 127.5]]))
+
+
 def test_epilogue_sampled_matches_full(oracle_mod):
     rng = np.random.default_rng(3)
     z = rng.standard_normal((6, 40))

@@ -175,19 +175,21 @@ Plan device_plan(const DeviceState* st, int M, int N, int K, int G, int fmt)
 template <int TM, int KSUB, int CL>
 cudaError_t setup_shape(int* mc4, int* mc8)
 {
-    int mc[6] = {0, 0, 0, 0, 0, 0};
+    int mc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     cudaError_t e;
     if ((e = setup_tc<TM, KSUB, CL, false, kFmtW4>(&mc[0])) != cudaSuccess ||
         (e = setup_tc<TM, KSUB, CL, true, kFmtW4>(&mc[1])) != cudaSuccess ||
         (e = setup_tc<TM, KSUB, CL, false, kFmtW4Zp>(&mc[2])) != cudaSuccess ||
         (e = setup_tc<TM, KSUB, CL, true, kFmtW4Zp>(&mc[3])) != cudaSuccess ||
-        (e = setup_tc<TM, 2, CL, false, kFmtW8>(&mc[4])) != cudaSuccess ||
-        (e = setup_tc<TM, 2, CL, true, kFmtW8>(&mc[5])) != cudaSuccess)
+        (e = setup_tc<TM, KSUB, CL, false, kFmtW4Bf16>(&mc[4])) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, CL, true, kFmtW4Bf16>(&mc[5])) != cudaSuccess ||
+        (e = setup_tc<TM, 2, CL, false, kFmtW8>(&mc[6])) != cudaSuccess ||
+        (e = setup_tc<TM, 2, CL, true, kFmtW8>(&mc[7])) != cudaSuccess)
         return e;
     int m = mc[0];
-    for (int i = 1; i < 4; ++i) m = mc[i] < m ? mc[i] : m;
+    for (int i = 1; i < 6; ++i) m = mc[i] < m ? mc[i] : m;
     *mc4 = m;
-    *mc8 = mc[4] < mc[5] ? mc[4] : mc[5];
+    *mc8 = mc[6] < mc[7] ? mc[6] : mc[7];
     return cudaSuccess;
 }
 
@@ -201,6 +203,9 @@ cudaError_t launch_shape(const CUtensorMap& map, const GemmParams& p, bool epi, 
         case kFmtW8:
             return epi ? launch_tc<TM, 2, CL, true, kFmtW8>(map, p, stream)
                        : launch_tc<TM, 2, CL, false, kFmtW8>(map, p, stream);
+        case kFmtW4Bf16:
+            return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4Bf16>(map, p, stream)
+                       : launch_tc<TM, KSUB, CL, false, kFmtW4Bf16>(map, p, stream);
         default:
             return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4>(map, p, stream)
                        : launch_tc<TM, KSUB, CL, false, kFmtW4>(map, p, stream);
@@ -271,14 +276,16 @@ w4a16_status own_workspace(DeviceState* st, void** ws, size_t* bytes)
 // X as a 3-D view {64, M, K/64} (strides K*2 and 128 bytes) when K is a multiple of
 // 64, so one TMA brings a stage's KSUB blocks of 64 columns; else the plain 2-D
 // map {K, M}, one TMA per block, with the ragged K edge zero-filled.
-bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int ksub, bool allow_3d, int* is_3d)
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int ksub, bool allow_3d, int* is_3d,
+                  bool bf16 = false)
 {
+    const CUtensorMapDataType dtype = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint32_t estr[3] = {1, 1, 1};
     if (allow_3d && K % kChunkK == 0) {
         cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)M, (cuuint64_t)(K / kChunkK)};
         cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kChunkK * 2};
         cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)rows, (cuuint32_t)ksub};
-        CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), dims, strides, box,
+        CUresult r = g_encode(map, dtype, 3, const_cast<void*>(x), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r == CUDA_SUCCESS) {
@@ -289,7 +296,7 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int k
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)rows};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+    CUresult r = g_encode(map, dtype, 2, const_cast<void*>(x), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     *is_3d = 0;
@@ -357,7 +364,8 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     // enough: MMA rows past M feed only output columns that are never stored.
     p.x_rows = P.m_tiles == 1 ? ((M + 7) / 8) * 8 : P.tm;
     // Clusters split a stage's X blocks between their CTAs: one 2-D TMA per block.
-    if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d)) return W4A16_ERR_INVALID_ARG;
+    if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d, fmt == kFmtW4Bf16))
+        return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     const bool epi = bias || residual || act != 0;
     switch (P.tm) {
@@ -496,6 +504,17 @@ w4a16_status w4a16_gemm_zp(const uint16_t* x, const uint32_t* packed, const uint
         return W4A16_ERR_INVALID_ARG;
     return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
                      reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, kFmtW4Zp, zeros_packed);
+}
+
+w4a16_status w4a16_bf16_gemm(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y,
+                             int M, int N, int K, int group_size, const uint16_t* bias, const uint16_t* residual,
+                             int activation, void* workspace, size_t ws_bytes, w4a16_stream_t stream)
+{
+    if (activation < W4A16_ACT_NONE || activation > W4A16_ACT_RELU) return W4A16_ERR_INVALID_ARG;
+    if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
+        return W4A16_ERR_INVALID_ARG;
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, kFmtW4Bf16);
 }
 
 size_t w4a16_w8_packed_bytes(int K, int N, int group_size)

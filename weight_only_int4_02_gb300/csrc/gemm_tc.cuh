@@ -50,16 +50,17 @@ constexpr int kKPad = 4;           // the packed layout pads K to a multiple of 
 // Weight formats (a template parameter of the kernel): 4-bit codes with the
 // zero-point 8; 4-bit codes with one zero-point per (group, column); 8-bit codes
 // with the zero-point 128 (8 KB per (tile, sub-chunk), bytes of a word in the
-// order k, k+2, k+1, k+3).
+// order k, k+2, k+1, k+3); 4-bit codes with BF16 activations, scales and output.
 constexpr int kFmtW4 = 0;
 constexpr int kFmtW4Zp = 1;
 constexpr int kFmtW8 = 2;
+constexpr int kFmtW4Bf16 = 3;   // 4-bit codes, zero-point 8, BF16 X / scales / bias / residual / Y
 
 struct GemmParams {
     const uint32_t* packed; // packed codes (4-bit: 1024 words per (tile, sub-chunk); 8-bit: 2048)
     const __half* scales;   // tile-ordered scales [n_tiles][ng][128]
     const uint8_t* zeros;   // tile-ordered 4-bit zero-points [n_tiles][ng][64 bytes] (kFmtW4Zp only)
-    __half* y;
+    __half* y;              // 16-bit output (FP16, or BF16 bits for kFmtW4Bf16)
     float* partials;        // [2 * grid][TM][128] FP32
     int* counters;          // [grid], zero between launches (index = cluster * p.cluster + rank)
     int* status;            // error word, bit 0 = a wait timed out
@@ -100,7 +101,25 @@ __device__ __forceinline__ float epilogue_op(int act, float v, float b, float r)
     return v + r;
 }
 
-__device__ __forceinline__ float load_half(const __half* base, size_t i) { return base ? __half2float(base[i]) : 0.f; }
+// 16-bit tensor elements: FP16, or BF16 bit patterns in the same storage (BF).
+template <bool BF>
+__device__ __forceinline__ float ld16(const __half* base, size_t i)
+{
+    if (!base) return 0.f;
+    if constexpr (BF)
+        return __uint_as_float((uint32_t)__half_as_ushort(base[i]) << 16);
+    else
+        return __half2float(base[i]);
+}
+
+template <bool BF>
+__device__ __forceinline__ __half st16(float v)
+{
+    if constexpr (BF)
+        return __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+    else
+        return __float2half_rn(v);
+}
 
 template <int TM, int KSUB, int FMT = kFmtW4>
 struct TcCfg {
@@ -203,6 +222,24 @@ __device__ __forceinline__ void dequant_word8(uint32_t w, __half2 s2, uint32_t* 
     out[1] = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+// (q - 8) * s in BF16 as four pairs (k, k+1) ... (k+6, k+7) from one packed word
+// (nibble i holds k + 2*(i%4) + i/4). BF16 keeps 7 fraction bits, so each nibble
+// pair is shifted down to bits 0..3 of its half and OR-ed into 128.0 (0x4300):
+// 128 + q exactly; (128 + q) - 136 is q - 8 exactly. s2 holds the scale's BF16 bits twice.
+__device__ __forceinline__ void dequant_word_bf16(uint32_t w, uint32_t s2, uint32_t* out)
+{
+    const uint32_t lo = 0x000F000Fu, magic = 0x43004300u;
+    const __nv_bfloat162 c136 = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
+    const __nv_bfloat162 sc = *reinterpret_cast<const __nv_bfloat162*>(&s2);
+    uint32_t u[4] = {and_or(w, lo, magic), and_or(w >> 4, lo, magic), and_or(w >> 8, lo, magic),
+                     and_or(w >> 12, lo, magic)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]), c136), sc);
+        out[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
 // Dequantisation constants for the zero-point z (0..15), duplicated in both halves:
 // lo = 1024 + z (binary16 0x6400 | z) and hi = -(64 + z) (0xD400 | 16z; the ulp at
 // 64 is 1/16). z = 8 gives 1032 and -72.
@@ -258,7 +295,7 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
 // columns j/32, j/32 + 4, j/32 + 8, ... A round issues L4 such loads (L4/NCP
 // columns of NCP contributors) before any is added, so it costs one global
 // round trip. n_base is the tile's first output feature.
-template <int TM, int NCP, int L4, bool EPI>
+template <int TM, int NCP, int L4, bool EPI, bool BF>
 __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
                                            int n_base)
 {
@@ -269,7 +306,7 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
     const int n = n_base + 4 * rg;
     float b4[4] = {0.f, 0.f, 0.f, 0.f};
     if (EPI && p.bias && n < p.N)
-        for (int j = 0; j < 4; ++j) b4[j] = __half2float(p.bias[n + j]);
+        for (int j = 0; j < 4; ++j) b4[j] = ld16<BF>(p.bias, n + j);
     for (int q0 = 0; q0 < ncols; q0 += CPR) {
         float4 acc[CPR];
 #pragma unroll
@@ -308,17 +345,17 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
                 __half* out = p.y + (size_t)m * p.N + n;
                 if constexpr (EPI) {
                     const size_t ri = (size_t)m * p.N + n;
-                    const float r0 = load_half(p.residual, ri), r1 = load_half(p.residual, ri + 1);
-                    const float r2 = load_half(p.residual, ri + 2), r3 = load_half(p.residual, ri + 3);
-                    out[0] = __float2half_rn(epilogue_op(p.act, acc[e].x, b4[0], r0));
-                    out[1] = __float2half_rn(epilogue_op(p.act, acc[e].y, b4[1], r1));
-                    out[2] = __float2half_rn(epilogue_op(p.act, acc[e].z, b4[2], r2));
-                    out[3] = __float2half_rn(epilogue_op(p.act, acc[e].w, b4[3], r3));
+                    const float r0 = ld16<BF>(p.residual, ri), r1 = ld16<BF>(p.residual, ri + 1);
+                    const float r2 = ld16<BF>(p.residual, ri + 2), r3 = ld16<BF>(p.residual, ri + 3);
+                    out[0] = st16<BF>(epilogue_op(p.act, acc[e].x, b4[0], r0));
+                    out[1] = st16<BF>(epilogue_op(p.act, acc[e].y, b4[1], r1));
+                    out[2] = st16<BF>(epilogue_op(p.act, acc[e].z, b4[2], r2));
+                    out[3] = st16<BF>(epilogue_op(p.act, acc[e].w, b4[3], r3));
                 } else {
-                    out[0] = __float2half_rn(acc[e].x);
-                    out[1] = __float2half_rn(acc[e].y);
-                    out[2] = __float2half_rn(acc[e].z);
-                    out[3] = __float2half_rn(acc[e].w);
+                    out[0] = st16<BF>(acc[e].x);
+                    out[1] = st16<BF>(acc[e].y);
+                    out[2] = st16<BF>(acc[e].z);
+                    out[3] = st16<BF>(acc[e].w);
                 }
             }
         }
@@ -334,6 +371,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
     static_assert(CL == 1 || (CL == 2 && KSUB % 2 == 0), "cluster of two splits a stage's X blocks");
     static_assert(FMT != kFmtW8 || KSUB == 2, "8-bit codes run 128-value stages (16 KB of codes)");
     constexpr bool ZP = FMT == kFmtW4Zp;
+    constexpr bool BF = FMT == kFmtW4Bf16;
     using C = TcCfg<TM, KSUB, FMT>;
     constexpr int SW = C::kWStages;
     constexpr int SX = C::kXStages;
@@ -487,7 +525,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16_f32(128, TM);
+        constexpr uint32_t idesc = BF ? idesc_bf16_f32(128, TM) : idesc_f16_f32(128, TM);
         uint32_t seq = 0;
         int d = 0;
         uint32_t dph = 0;
@@ -600,7 +638,16 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t v[32];   // FP16 pairs (k, k+1) of the sub-chunk's 64 values
-                    if constexpr (FMT == kFmtW8) {
+                    if constexpr (BF) {
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const uint32_t sb = *reinterpret_cast<const uint32_t*>(&s2[h][b]);
+                            dequant_word_bf16(w[h][b].x, sb, v + 16 * b + 0);
+                            dequant_word_bf16(w[h][b].y, sb, v + 16 * b + 4);
+                            dequant_word_bf16(w[h][b].z, sb, v + 16 * b + 8);
+                            dequant_word_bf16(w[h][b].w, sb, v + 16 * b + 12);
+                        }
+                    } else if constexpr (FMT == kFmtW8) {
 #pragma unroll
                         for (int b = 0; b < 4; ++b) {
                             dequant_word8(w[h][b].x, s2[h][b >> 1], v + 8 * b + 0);
@@ -647,7 +694,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             const int chunks = (valid + 15) >> 4;
             const bool split = (g.kb != 0 || g.ke != p.iters);
             // The bias of this row is fetched while the MMAs run.
-            const float bias_n = (EPI && n < p.N) ? load_half(p.bias, n) : 0.f;
+            const float bias_n = (EPI && n < p.N) ? ld16<BF>(p.bias, n) : 0.f;
             // All four epilogue warps leave together: they share named barriers.
             const bool ok = wait_warp(dfull_bar(d), dph, ctl);
             if (named_bar_or(1, 128, !ok)) break;
@@ -665,20 +712,20 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int m = m0 + c * 16 + e;
-                                rv[e] = m < p.M ? load_half(p.residual, (size_t)m * p.N + n) : 0.f;
+                                rv[e] = m < p.M ? ld16<BF>(p.residual, (size_t)m * p.N + n) : 0.f;
                             }
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int m = m0 + c * 16 + e;
                                 if (m < p.M)
                                     p.y[(size_t)m * p.N + n] =
-                                        __float2half_rn(epilogue_op(p.act, __uint_as_float(r[e]), bv, rv[e]));
+                                        st16<BF>(epilogue_op(p.act, __uint_as_float(r[e]), bv, rv[e]));
                             }
                         } else {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int m = m0 + c * 16 + e;
-                                if (m < p.M) p.y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(r[e]));
+                                if (m < p.M) p.y[(size_t)m * p.N + n] = st16<BF>(__uint_as_float(r[e]));
                             }
                         }
                     }
@@ -719,11 +766,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
                     constexpr int L4 = KSUB == 4 ? 8 : 16;
                     if (ncontrib <= 2)
-                        fix_reduce<TM, 2, L4, EPI>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                        fix_reduce<TM, 2, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                     else if (ncontrib <= 4)
-                        fix_reduce<TM, 4, L4, EPI>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                        fix_reduce<TM, 4, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                     else
-                        fix_reduce<TM, 8, L4, EPI>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                        fix_reduce<TM, 8, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
                 }
                 named_bar_sync(1, 128);
             }

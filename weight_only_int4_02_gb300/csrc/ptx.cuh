@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace w4a16 {
@@ -339,6 +340,12 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr)
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
 {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with BF16 A and B (A and B formats 1 in bits 7..9 and 10..12).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+{
+    return idesc_f16_f32(M, N) | (1u << 7) | (1u << 10);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)

@@ -19,7 +19,7 @@ EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error
            "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
            "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
            "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp", "w4a16_w8_packed_bytes", "w4a16_w8_pack",
-           "w4a16_w8_gemm"]
+           "w4a16_w8_gemm", "w4a16_bf16_gemm"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -71,6 +71,8 @@ def lib():
         L.w4a16_pack_zeros.restype = I
         L.w4a16_gemm_zp.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
         L.w4a16_gemm_zp.restype = I
+        L.w4a16_bf16_gemm.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
+        L.w4a16_bf16_gemm.restype = I
         L.w4a16_w8_packed_bytes.argtypes = [I, I, I]
         L.w4a16_w8_packed_bytes.restype = Z
         L.w4a16_w8_pack.argtypes = [P, P, P, P, I, I, I, P]
@@ -113,18 +115,18 @@ def workspace_bytes(M, N, K, group_size):
 
 
 def pack(codes, scales, group_size, stream=None, out=None):
-    """Repack codes (uint8 [K][N]) and scales (float16 [ceil(K/G)][N]) on the GPU.
+    """Repack codes (uint8 [K][N]) and scales (float16 or bfloat16 [ceil(K/G)][N]) on the GPU.
 
-    Returns (packed int32 words, packed float16 scales)."""
+    Returns (packed int32 words, packed scales of the scales' dtype)."""
     K, N = codes.shape
-    assert codes.dtype == torch.uint8 and scales.dtype == torch.float16
+    assert codes.dtype == torch.uint8 and scales.dtype in (torch.float16, torch.bfloat16)
     assert codes.is_cuda and scales.is_cuda and codes.is_contiguous() and scales.is_contiguous()
     nw, ns = packed_words(K, N, group_size), scales_elems(K, N, group_size)
     if nw == 0 or ns == 0:
         raise W4A16Error(ERR_INVALID_ARG, "pack")
     if out is None:
         packed = torch.empty(nw, dtype=torch.int32, device=codes.device)
-        sp = torch.empty(ns, dtype=torch.float16, device=codes.device)
+        sp = torch.empty(ns, dtype=scales.dtype, device=codes.device)
     else:
         packed, sp = out
     _check(lib().w4a16_pack(_ptr(codes), _ptr(scales), _ptr(packed), _ptr(sp), K, N, group_size, _stream(stream)),
@@ -271,4 +273,23 @@ def w8_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None, a
     _check(lib().w4a16_w8_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                _stream(stream)), "w4a16_w8_gemm")
+    return y
+
+
+def bf16_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None, activation="none", y=None,
+              workspace=None, stream=None):
+    """y = act(x @ dequant(W) + bias) + residual with bfloat16 x, scales, bias, residual and y
+    (4-bit codes, zero-point 8; packed and scales_packed from pack with bfloat16 scales)."""
+    M, K = x.shape
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    assert scales_packed.dtype == torch.bfloat16
+    for t, shape in ((bias, (N,)), (residual, (M, N))):
+        if t is not None:
+            assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous() and tuple(t.shape) == shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().w4a16_bf16_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
+                                 _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
+                                 _stream(stream)), "w4a16_bf16_gemm")
     return y
