@@ -59,6 +59,12 @@ def _load():
         lib.w4o_decode_bf16.argtypes = [P, P, ctypes.c_size_t]
         lib.w4o_gemm_sample_bf16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
         lib.w4o_gemm_sample_bf16.restype = I
+        lib.w4o_sp_packed_bytes.argtypes = [I, I]
+        lib.w4o_sp_packed_bytes.restype = ctypes.c_size_t
+        lib.w4o_sp_pack.argtypes = [P, I, I, P]
+        lib.w4o_sp_pack.restype = ctypes.c_longlong
+        lib.w4o_sp_unpack.argtypes = [P, I, I, P]
+        lib.w4o_sp_unpack.restype = ctypes.c_longlong
         lib.w4o_gemm_sample_w8.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, I]
         lib.w4o_gemm_sample_w8.restype = I
         lib.w4o_dequant_w8.argtypes = [P, P, I, I, I, P]
@@ -193,6 +199,31 @@ def unpack_scales(sp, ng, N):
     s = np.empty((ng, N), np.uint16)
     bad = _load().w4o_unpack_scales(_ptr(sp), ng, N, _ptr(s))
     return s, int(bad)
+
+
+# ------------------------------------------------------------------ 2:4 sparse 4-bit codes
+# The GEMM of 2:4 sparse codes is the dense definition (gemm, gemm_sample) on the
+# dense codes; these functions restate the sparse packed layout.
+def sp_packed_bytes(K, N):
+    return int(_load().w4o_sp_packed_bytes(K, N))
+
+
+def sp_pack(codes):
+    """(packed uint8 array, number of groups of four with more than two codes other than 8)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    K, N = codes.shape
+    out = np.empty(sp_packed_bytes(K, N), np.uint8)
+    v = _load().w4o_sp_pack(_ptr(codes), K, N, _ptr(out))
+    return out, int(v)
+
+
+def sp_unpack(packed, K, N):
+    """(dense codes[K][N], number of malformed or non-empty padding groups)."""
+    p = np.ascontiguousarray(packed).view(np.uint8).ravel()
+    assert p.size == sp_packed_bytes(K, N)
+    codes = np.empty((K, N), np.uint8)
+    bad = _load().w4o_sp_unpack(_ptr(p), K, N, _ptr(codes))
+    return codes, int(bad)
 
 
 # ------------------------------------------------------------------ BF16 activations

@@ -418,3 +418,112 @@ void w4o_pack_w8(const uint8_t* codes, int K, int N, uint8_t* packed)
     for (int k = 0; k < K; ++k)
         for (int n = 0; n < N; ++n) packed[w4o_locate_w8(K, k, n)] = codes[(size_t)k * N + n];
 }
+
+/*
+ * 2:4 sparse 4-bit layout (sparse layout v1), restated for the round-trip check.
+ * The weights are the dense 4-bit format whose codes are 2:4 sparse along k: in
+ * every aligned group of four k of a column at most two codes differ from 8
+ * (weight 0). Only two codes per group are stored, with their 2-bit positions.
+ * K is padded to a multiple of 256; chunks of 128 k, SC = Kpad / 128 per column.
+ * Chunk (nt, sc) takes 6144 bytes at (nt * SC + sc) * 6144:
+ *   codes, 4096 bytes: word ((b * 128 + n_in) * 4 + wd) holds stored values
+ *     j0 = b*32 + wd*8 .. j0+7 of column nt*128 + n_in, nibble i holding stored
+ *     value j0 + 2*(i mod 4) + i/4;
+ *   positions, 2048 bytes after the codes: word (n_in * 4 + mm) describes the
+ *     groups t = 0..7 of k = sc*128 + mm*32 + 4t .. +3: bits 4t..4t+1 the position
+ *     (0..3) of the group's first stored value, bits 4t+2..4t+3 that of its second,
+ *     first < second.
+ * Stored value j of a chunk is the code at k = sc*128 + 4*(j/2) + (position j%2 of
+ * group j/2). A group's stored positions: those of its codes other than 8 in
+ * increasing order, filled up to two with the smallest positions not taken (their
+ * codes are 8). A group with more than two codes other than 8 (not 2:4) keeps its
+ * first two and counts as a violation. Padding (k >= K or n >= N): code 8,
+ * positions 0 and 1.
+ */
+size_t w4o_sp_packed_bytes(int K, int N) { return (size_t)ceil_div(N, 128) * (chunks_per_column(K) / 2) * 6144; }
+
+/* Stored positions of the group at k = 4T (T-th group) of column n. */
+static int group_positions(const uint8_t* codes, int K, int N, int n, int T, int pos[2])
+{
+    int count = 0, taken[4] = {0, 0, 0, 0};
+    int violation = 0;
+    for (int i = 0; i < 4; ++i) {
+        int k = 4 * T + i;
+        if (k < K && n < N && codes[(size_t)k * N + n] != 8) {
+            if (count < 2) { pos[count++] = i; taken[i] = 1; }
+            else violation = 1;
+        }
+    }
+    for (int i = 0; i < 4 && count < 2; ++i)
+        if (!taken[i]) { pos[count++] = i; taken[i] = 1; }
+    if (pos[0] > pos[1]) { int t = pos[0]; pos[0] = pos[1]; pos[1] = t; }
+    return violation;
+}
+
+long long w4o_sp_pack(const uint8_t* codes, int K, int N, uint8_t* packed)
+{
+    int SC = chunks_per_column(K) / 2, NT = ceil_div(N, 128);
+    long long violations = 0;
+    memset(packed, 0, w4o_sp_packed_bytes(K, N));
+    for (int nt = 0; nt < NT; ++nt)
+        for (int sc = 0; sc < SC; ++sc) {
+            uint8_t* chunk = packed + ((size_t)nt * SC + sc) * 6144;
+            uint32_t* cw = (uint32_t*)chunk;
+            uint32_t* mw = (uint32_t*)(chunk + 4096);
+            for (int n_in = 0; n_in < 128; ++n_in) {
+                int n = nt * 128 + n_in;
+                for (int T = 0; T < 32; ++T) {        /* group within the chunk */
+                    int pos[2];
+                    int Tg = sc * 32 + T;
+                    violations += group_positions(codes, K, N, n, Tg, pos);
+                    int mm = T / 8, t = T % 8;
+                    mw[n_in * 4 + mm] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * t);
+                    for (int s = 0; s < 2; ++s) {
+                        int j = 2 * T + s, k = 4 * Tg + pos[s];
+                        int c = (k < K && n < N) ? codes[(size_t)k * N + n] : 8;
+                        int b = j / 32, wd = (j % 32) / 8, o = j % 8;
+                        int nib = (o % 2) * 4 + o / 2;     /* o = 2*(nib mod 4) + nib/4 */
+                        cw[(b * 128 + n_in) * 4 + wd] |= (uint32_t)(c & 0xF) << (4 * nib);
+                    }
+                }
+            }
+        }
+    return violations;
+}
+
+/* Dense codes[K][N] (8 where nothing is stored) from the sparse layout; returns the
+ * number of malformed groups (positions not increasing) plus padding groups that
+ * do not hold code 8 at positions 0 and 1. */
+long long w4o_sp_unpack(const uint8_t* packed, int K, int N, uint8_t* codes)
+{
+    int SC = chunks_per_column(K) / 2, NT = ceil_div(N, 128);
+    long long bad = 0;
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) codes[(size_t)k * N + n] = 8;
+    for (int nt = 0; nt < NT; ++nt)
+        for (int sc = 0; sc < SC; ++sc) {
+            const uint8_t* chunk = packed + ((size_t)nt * SC + sc) * 6144;
+            const uint32_t* cw = (const uint32_t*)chunk;
+            const uint32_t* mw = (const uint32_t*)(chunk + 4096);
+            for (int n_in = 0; n_in < 128; ++n_in) {
+                int n = nt * 128 + n_in;
+                for (int T = 0; T < 32; ++T) {
+                    int mm = T / 8, t = T % 8;
+                    uint32_t nib4 = (mw[n_in * 4 + mm] >> (4 * t)) & 0xF;
+                    int pos[2] = {(int)(nib4 & 3), (int)(nib4 >> 2)};
+                    int Tg = sc * 32 + T;
+                    int pad = (4 * Tg >= K) || n >= N;
+                    if (pos[0] >= pos[1]) { ++bad; continue; }
+                    for (int s = 0; s < 2; ++s) {
+                        int j = 2 * T + s, k = 4 * Tg + pos[s];
+                        int b = j / 32, wd = (j % 32) / 8, o = j % 8;
+                        int nib = (o % 2) * 4 + o / 2;
+                        int c = (cw[(b * 128 + n_in) * 4 + wd] >> (4 * nib)) & 0xF;
+                        if (pad) { if (c != 8 || pos[0] != 0 || pos[1] != 1) ++bad; }
+                        else codes[(size_t)k * N + n] = (uint8_t)c;
+                    }
+                }
+            }
+        }
+    return bad;
+}

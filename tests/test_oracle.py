@@ -17,7 +17,9 @@
   pair (k, k+1) in bytes 0 and 2 of a word);
 * BF16 activations: the bfloat16 decoder against numpy's float32 reading of the
   same bits over all 65536 patterns, brute force in exact rationals on bfloat16
-  inputs, and equality with the FP16 form on values exact in both formats.
+  inputs, and equality with the FP16 form on values exact in both formats;
+* 2:4 sparse layout: round trip of 2:4 codes, the fill rule and the bits of a
+  hand-worked chunk, violations counted, the generator's 2:4 structure.
 """
 import os
 import re
@@ -262,6 +264,10 @@ MUTANTS = {
     "bf16_exponent_bias": ("ldexp((double)(128 + f), e - 134)", "ldexp((double)(128 + f), e - 133)"),
     "bf16_x_read_as_fp16": ("xd[(size_t)r * K + k] = dec(x[(size_t)rows[r] * K + k]);",
                             "xd[(size_t)r * K + k] = w4o_half_to_double(x[(size_t)rows[r] * K + k]);"),
+    "sp_nibble_order": ("int nib = (o % 2) * 4 + o / 2;     /* o = 2*(nib mod 4) + nib/4 */",
+                        "int nib = o;"),
+    "sp_position_field": ("mw[n_in * 4 + mm] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * t);",
+                          "mw[n_in * 4 + mm] |= (uint32_t)(pos[1] | (pos[0] << 2)) << (4 * t);"),
     "w8_zero_point_127": ("return gemm_sample_any(x, q, s, NULL, 128,", "return gemm_sample_any(x, q, s, NULL, 127,"),
     "w8_byte_order": ("slot_of_offset[4] = {0, 2, 1, 3}", "slot_of_offset[4] = {0, 1, 2, 3}"),
     "no_groups": ("static int group_of(int k, int G) { return k / G; }",
@@ -299,6 +305,7 @@ def test_planted_mistakes_fail_a_pin(oracle_mod, name):
                       lambda o: test_zero_points_brute_force_exact(o, 1),
                       lambda o: test_w8_brute_force_exact(o, 0),
                       test_bf16_decoder_all_patterns, lambda o: test_bf16_brute_force_exact(o, 0),
+                      test_sp_hand_worked_chunk,
                       test_w8_layout_pairs_adjacent_k_in_bytes_0_and_2):
             try:
                 check(mut)
@@ -536,6 +543,52 @@ def test_bf16_equals_fp16_on_values_exact_in_both(oracle_mod):
     yb, ab = oracle_mod.gemm_bf16(inputs.to_bf16_bits(xv), q, inputs.to_bf16_bits(sv), G)
     assert np.array_equal(bf16_values(inputs.to_bf16_bits(xv)), xv)
     assert np.array_equal(y16, yb) and np.array_equal(a16, ab)
+
+
+# --------------------------------------------------------------------------- 2:4 sparse 4-bit layout
+# Sparse-MARLIN ("MARLIN: Mixed-Precision Auto-Regressive Parallel Inference on
+# Large Language Models" note, key results: INT4 with 2:4 sparsity): at most two
+# codes other than 8 in every aligned group of four k; the GEMM is the dense one.
+@pytest.mark.parametrize("K,N", [(256, 8), (200, 130), (512, 256)])
+def test_sp_round_trip(oracle_mod, K, N):
+    q = inputs.codes_2to4(K, N, seed=7)
+    packed, violations = oracle_mod.sp_pack(q)
+    assert violations == 0 and packed.size == oracle_mod.sp_packed_bytes(K, N)
+    q2, bad = oracle_mod.sp_unpack(packed, K, N)
+    assert bad == 0 and np.array_equal(q2, q)
+
+
+def test_sp_generator_is_2to4(oracle_mod):
+    q = inputs.codes_2to4(64, 40, seed=3)
+    nonzero = (q != 8).reshape(16, 4, 40).sum(axis=1)
+    assert nonzero.max() <= 2 and (q != 8).mean() > 0.4
+
+
+def test_sp_hand_worked_chunk(oracle_mod):
+    """Column 0, k 0..3 = [8, 3, 8, 8], k 4..7 = [5, 8, 8, 2], all else 8. Positions:
+    (0, 1) (3 kept, filled with position 0) and (0, 3); stored 8, 3, 5, 2, then 8s.
+    Code word (b 0, column 0, word 0): stored value o in nibble (o%2)*4 + o/2, so
+    nibbles 0..7 = 8, 5, 8, 8, 3, 2, 8, 8 -> 0x88238858. Position word (column 0,
+    MMA 0): groups t = 0..7 -> 0x4, 0xC, then 0x4 -> 0x444444C4."""
+    q = np.full((256, 8), 8, np.uint8)
+    q[1, 0], q[4, 0], q[7, 0] = 3, 5, 2
+    packed, violations = oracle_mod.sp_pack(q)
+    assert violations == 0
+    words = packed.view(np.uint32)
+    assert words[0] == 0x88238858
+    assert words[4096 // 4] == 0x444444C4
+    assert words[4096 // 4 + 1] == 0x44444444      # MMA 1 of column 0: empty groups
+    assert words[4] == 0x88888888                   # column 1, word 0
+
+
+def test_sp_violations_are_counted(oracle_mod):
+    q = np.full((256, 8), 8, np.uint8)
+    q[0:3, 0] = [1, 2, 3]             # three codes other than 8 in one group
+    q[8:12, 5] = [4, 5, 6, 7]         # four
+    packed, violations = oracle_mod.sp_pack(q)
+    assert violations == 2
+    q2, bad = oracle_mod.sp_unpack(packed, 256, 8)
+    assert bad == 0 and list(q2[0:4, 0]) == [1, 2, 8, 8] and list(q2[8:12, 5]) == [4, 5, 8, 8]
 
 
 # --------------------------------------------------------------------------- fused epilogue

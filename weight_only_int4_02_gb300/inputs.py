@@ -2,7 +2,8 @@
 
 Both the CUDA path and the CPU oracle are fed from these generators, so they see
 identical bits. Every tensor draws from its own PCG64 stream keyed by
-(seed, stream id): activations 0, codes 1, scales 2, outlier mask 3, zero-points 4.
+(seed, stream id): activations 0, codes 1, scales 2, outlier mask 3, zero-points 4,
+2:4 sparsity pattern 5.
 
 Distributions follow the workloads the pages measure (a layer sweep over batch
 sizes on Llama-2-like shapes, a 72k x 18k layer, prefill shapes):
@@ -14,11 +15,13 @@ sizes on Llama-2-like shapes, a 72k x 18k layer, prefill shapes):
   * zero-points z ~ uniform on {0..15} per (group, column) for the asymmetric
     format (every value, the extremes 0 and 15 included, is exercised);
   * for BF16 activations, the same x and s distributions rounded to bfloat16
-    (round-to-nearest-even of the float32 draw), passed as bit patterns.
+    (round-to-nearest-even of the float32 draw), passed as bit patterns;
+  * 2:4 sparse codes: in each aligned group of four k of a column one of the six
+    position pairs, uniformly, keeps its uniform code and the other two are 8.
 """
 import numpy as np
 
-X_STREAM, CODE_STREAM, SCALE_STREAM, OUTLIER_STREAM, ZERO_STREAM = 0, 1, 2, 3, 4
+X_STREAM, CODE_STREAM, SCALE_STREAM, OUTLIER_STREAM, ZERO_STREAM, SPARSITY_STREAM = 0, 1, 2, 3, 4, 5
 
 
 def rng(seed, stream):
@@ -48,6 +51,20 @@ def activations_bf16(M, K, seed=0):
 def codes(K, N, seed=0):
     """q[K][N] uniform on 0..15 as uint8."""
     return rng(seed, CODE_STREAM).integers(0, 16, size=(K, N), dtype=np.uint8)
+
+
+def codes_2to4(K, N, seed=0):
+    """q[K][N] 2:4 sparse along k: in every aligned group of four k of a column, two
+    positions (one of the six pairs, uniformly) hold codes uniform on 0..15 and the
+    other two hold 8 (weight 0). K must be a multiple of 4."""
+    assert K % 4 == 0
+    r = rng(seed, SPARSITY_STREAM)
+    pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)])
+    choice = pairs[r.integers(0, 6, size=(K // 4, N))]            # [K/4][N][2]
+    keep = np.zeros((K // 4, N, 4), bool)
+    np.put_along_axis(keep, choice, True, axis=2)
+    keep = keep.transpose(0, 2, 1).reshape(K, N)
+    return np.where(keep, codes(K, N, seed), np.uint8(8)).astype(np.uint8)
 
 
 def n_groups(K, group_size):
