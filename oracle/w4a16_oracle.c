@@ -429,10 +429,12 @@ void w4o_pack_w8(const uint8_t* codes, int K, int N, uint8_t* packed)
  *   codes, 4096 bytes: word ((b * 128 + n_in) * 4 + wd) holds stored values
  *     j0 = b*32 + wd*8 .. j0+7 of column nt*128 + n_in, nibble i holding stored
  *     value j0 + 2*(i mod 4) + i/4;
- *   positions, 2048 bytes after the codes: word (n_in * 4 + mm) describes the
- *     groups t = 0..7 of k = sc*128 + mm*32 + 4t .. +3: bits 4t..4t+1 the position
- *     (0..3) of the group's first stored value, bits 4t+2..4t+3 that of its second,
- *     first < second.
+ *   positions, 2048 bytes after the codes, in the order the sparse tensor-core
+ *     MMA reads them from tensor memory (lane L, one 32-bit word per MMA of 32 k):
+ *     word (L * 4 + mm), nibble u describes group t = 4*((L mod 16)/8) + u mod 4
+ *     (k = sc*128 + mm*32 + 4t .. +3) of column n_in = 16*(L/16) + 8*(u/4) + L mod 8;
+ *     bits 0..1 of the nibble hold the position (0..3) of the group's first stored
+ *     value, bits 2..3 that of its second, first < second.
  * Stored value j of a chunk is the code at k = sc*128 + 4*(j/2) + (position j%2 of
  * group j/2). A group's stored positions: those of its codes other than 8 in
  * increasing order, filled up to two with the smallest positions not taken (their
@@ -441,6 +443,14 @@ void w4o_pack_w8(const uint8_t* codes, int K, int N, uint8_t* packed)
  * positions 0 and 1.
  */
 size_t w4o_sp_packed_bytes(int K, int N) { return (size_t)ceil_div(N, 128) * (chunks_per_column(K) / 2) * 6144; }
+
+/* Word (lane) and nibble of the positions of group t (0..7 within an MMA of 32 k)
+ * of column n_in (0..127) of a chunk. */
+static void sp_position_slot(int n_in, int t, int* lane, int* nibble)
+{
+    *lane = 16 * (n_in / 16) + 8 * (t / 4) + n_in % 8;
+    *nibble = 4 * ((n_in / 8) % 2) + t % 4;
+}
 
 /* Stored positions of the group at k = 4T (T-th group) of column n. */
 static int group_positions(const uint8_t* codes, int K, int N, int n, int T, int pos[2])
@@ -476,8 +486,9 @@ long long w4o_sp_pack(const uint8_t* codes, int K, int N, uint8_t* packed)
                     int pos[2];
                     int Tg = sc * 32 + T;
                     violations += group_positions(codes, K, N, n, Tg, pos);
-                    int mm = T / 8, t = T % 8;
-                    mw[n_in * 4 + mm] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * t);
+                    int mm = T / 8, t = T % 8, L, u;
+                    sp_position_slot(n_in, t, &L, &u);
+                    mw[L * 4 + mm] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * u);
                     for (int s = 0; s < 2; ++s) {
                         int j = 2 * T + s, k = 4 * Tg + pos[s];
                         int c = (k < K && n < N) ? codes[(size_t)k * N + n] : 8;
@@ -508,8 +519,9 @@ long long w4o_sp_unpack(const uint8_t* packed, int K, int N, uint8_t* codes)
             for (int n_in = 0; n_in < 128; ++n_in) {
                 int n = nt * 128 + n_in;
                 for (int T = 0; T < 32; ++T) {
-                    int mm = T / 8, t = T % 8;
-                    uint32_t nib4 = (mw[n_in * 4 + mm] >> (4 * t)) & 0xF;
+                    int mm = T / 8, t = T % 8, L, u;
+                    sp_position_slot(n_in, t, &L, &u);
+                    uint32_t nib4 = (mw[L * 4 + mm] >> (4 * u)) & 0xF;
                     int pos[2] = {(int)(nib4 & 3), (int)(nib4 >> 2)};
                     int Tg = sc * 32 + T;
                     int pad = (4 * Tg >= K) || n >= N;

@@ -266,8 +266,9 @@ MUTANTS = {
                             "xd[(size_t)r * K + k] = w4o_half_to_double(x[(size_t)rows[r] * K + k]);"),
     "sp_nibble_order": ("int nib = (o % 2) * 4 + o / 2;     /* o = 2*(nib mod 4) + nib/4 */",
                         "int nib = o;"),
-    "sp_position_field": ("mw[n_in * 4 + mm] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * t);",
-                          "mw[n_in * 4 + mm] |= (uint32_t)(pos[1] | (pos[0] << 2)) << (4 * t);"),
+    "sp_position_field": ("mw[L * 4 + mm] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * u);",
+                          "mw[L * 4 + mm] |= (uint32_t)(pos[1] | (pos[0] << 2)) << (4 * u);"),
+    "sp_position_lane": ("*lane = 16 * (n_in / 16) + 8 * (t / 4) + n_in % 8;", "*lane = n_in;"),
     "w8_zero_point_127": ("return gemm_sample_any(x, q, s, NULL, 128,", "return gemm_sample_any(x, q, s, NULL, 127,"),
     "w8_byte_order": ("slot_of_offset[4] = {0, 2, 1, 3}", "slot_of_offset[4] = {0, 1, 2, 3}"),
     "no_groups": ("static int group_of(int k, int G) { return k / G; }",
@@ -305,7 +306,7 @@ def test_planted_mistakes_fail_a_pin(oracle_mod, name):
                       lambda o: test_zero_points_brute_force_exact(o, 1),
                       lambda o: test_w8_brute_force_exact(o, 0),
                       test_bf16_decoder_all_patterns, lambda o: test_bf16_brute_force_exact(o, 0),
-                      test_sp_hand_worked_chunk,
+                      test_sp_hand_worked_chunk, lambda o: test_sp_round_trip(o, 512, 256),
                       test_w8_layout_pairs_adjacent_k_in_bytes_0_and_2):
             try:
                 check(mut)
@@ -565,20 +566,27 @@ def test_sp_generator_is_2to4(oracle_mod):
 
 
 def test_sp_hand_worked_chunk(oracle_mod):
-    """Column 0, k 0..3 = [8, 3, 8, 8], k 4..7 = [5, 8, 8, 2], all else 8. Positions:
-    (0, 1) (3 kept, filled with position 0) and (0, 3); stored 8, 3, 5, 2, then 8s.
+    """Column 0, k 0..3 = [8, 3, 8, 8], k 4..7 = [5, 8, 8, 2]; column 8, k 0..3 =
+    [8, 8, 6, 7]; column 0, k 16..19 = [9, 8, 8, 1]; all else 8.
+    Positions: (0, 1) (3 kept, filled with position 0), (0, 3), (2, 3), (0, 3).
     Code word (b 0, column 0, word 0): stored value o in nibble (o%2)*4 + o/2, so
-    nibbles 0..7 = 8, 5, 8, 8, 3, 2, 8, 8 -> 0x88238858. Position word (column 0,
-    MMA 0): groups t = 0..7 -> 0x4, 0xC, then 0x4 -> 0x444444C4."""
-    q = np.full((256, 8), 8, np.uint8)
+    nibbles 0..7 = 8, 5, 8, 8, 3, 2, 8, 8 -> 0x88238858.
+    Position words in tensor-memory lane order: lane 0 holds groups 0..3 of column 0
+    in nibbles 0..3 and of column 8 in nibbles 4..7 -> 0x444E44C4; lane 8 holds
+    groups 4..7 of column 0 (nibble 0: group 4 = (0, 3) -> 0xC) -> 0x4444444C."""
+    q = np.full((256, 16), 8, np.uint8)
     q[1, 0], q[4, 0], q[7, 0] = 3, 5, 2
+    q[2, 8], q[3, 8] = 6, 7
+    q[16, 0], q[19, 0] = 9, 1
     packed, violations = oracle_mod.sp_pack(q)
     assert violations == 0
     words = packed.view(np.uint32)
+    meta = words[4096 // 4:]
     assert words[0] == 0x88238858
-    assert words[4096 // 4] == 0x444444C4
-    assert words[4096 // 4 + 1] == 0x44444444      # MMA 1 of column 0: empty groups
-    assert words[4] == 0x88888888                   # column 1, word 0
+    assert meta[0 * 4 + 0] == 0x444E44C4
+    assert meta[8 * 4 + 0] == 0x4444444C
+    assert meta[0 * 4 + 1] == 0x44444444      # MMA 1 (k 32..63): empty groups
+    assert words[4] == 0x88888888             # column 1, word 0
 
 
 def test_sp_violations_are_counted(oracle_mod):
