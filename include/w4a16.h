@@ -212,6 +212,58 @@ w4a16_status w4a16_bf16_gemm(const uint16_t* x, const uint32_t* packed, const ui
                              const uint16_t* bias, const uint16_t* residual, int activation,
                              void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
+/* ---------------------------------------------------------------- 2:4 sparse 4-bit codes
+ * Sparse-MARLIN ("MARLIN: Mixed-Precision Auto-Regressive Parallel Inference on
+ * Large Language Models" note, key results: INT4 weights with 2:4 sparsity): the
+ * 4-bit GEMM (zero-point 8, FP16) on codes that are 2:4 sparse along k, i.e. at
+ * most two codes other than 8 (weight 0) in every aligned group of four k of a
+ * column. Only two codes per group are stored, with their 2-bit positions, and
+ * the sparse tensor-core MMA skips the other two: half the MMAs and 3/4 of the
+ * weight bytes of the dense format. The result is that of w4a16_gemm_fused on the
+ * same codes (exactly the same products, in another order of summation). */
+
+/* Bytes of the sparse packed weights: ceil(N/128) * (KC/2) * 6144, KC as for
+ * w4a16_packed_words. Returns 0 for invalid sizes. */
+size_t w4a16_sp_packed_bytes(int K, int N, int group_size);
+
+/*
+ * Repack 2:4 sparse codes and scales once, offline.
+ *   codes          device, uint8 [K][N], values 0..15, at most two codes other than 8
+ *                  in every aligned group of four k of a column
+ *   scales         device, binary16 [ceil(K/G)][N]
+ *   packed         device out, uint8 [w4a16_sp_packed_bytes(K, N, G)], 16-byte aligned
+ *   scales_packed  device out, binary16 [w4a16_scales_elems(K, N, G)] (as w4a16_pack)
+ *   violations     device, 8-byte aligned counter, or NULL: the kernel adds the number
+ *                  of groups that hold more than two codes other than 8 (those keep
+ *                  their first two, so their results differ from the dense GEMM)
+ * Sparse layout (version 1): chunks of 128 values of k (KC/2 per column), 6144
+ * bytes per (column tile nt, chunk sc) at (nt*(KC/2) + sc)*6144:
+ *   4096 bytes of stored codes: word ((b*128 + n_in)*4 + wd) holds stored values
+ *     j0 = b*32 + wd*8 .. j0+7 of column nt*128 + n_in, nibble i holding stored
+ *     value j0 + 2*(i%4) + i/4; stored value j is the code at k = 128*sc + 4*(j/2) +
+ *     (position j%2 of group j/2);
+ *   2048 bytes of position words, in the order the sparse MMA reads them from
+ *     tensor memory: word (L*4 + mm), nibble u describes group t = 4*((L%16)/8) +
+ *     u%4 of k = 128*sc + 32*mm + 4t .. +3 of column nt*128 + 16*(L/16) + 8*(u/4) +
+ *     L%8: bits 0..1 the position (0..3) of the group's first stored code, bits
+ *     2..3 that of its second (first < second).
+ * A group stores the positions of its codes other than 8 in increasing order,
+ * filled up to two with the smallest free positions (code 8). Padding (k >= K,
+ * n >= N): code 8 at positions 0 and 1.
+ */
+w4a16_status w4a16_sp_pack(const uint8_t* codes, const uint16_t* scales, uint8_t* packed,
+                           uint16_t* scales_packed, int K, int N, int group_size,
+                           unsigned long long* violations, w4a16_stream_t stream);
+
+/*
+ * Y = act(X x dequant(W) + bias) + residual for 2:4 sparse codes packed by
+ * w4a16_sp_pack. Arguments, epilogue and workspace as for w4a16_gemm_fused.
+ */
+w4a16_status w4a16_sp_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_packed,
+                           uint16_t* y, int M, int N, int K, int group_size,
+                           const uint16_t* bias, const uint16_t* residual, int activation,
+                           void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
 /* ---------------------------------------------------------------- W8A16: 8-bit codes
  * The same GEMM for 8-bit weights: dequant(Wq)[k][n] = (q[k][n] - 128) * s[k/G][n],
  * q in 0..255, one FP16 scale per group ("Low-Precision Quantization Kernels in

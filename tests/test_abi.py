@@ -51,6 +51,10 @@ def test_sizes(lib):
     assert lib.w4a16_zeros_bytes(4000, 4096, 128) == 32 * 32 * 64
     assert lib.w4a16_zeros_bytes(4096, 200, -1) == 2 * 1 * 64
     assert lib.w4a16_zeros_bytes(4096, 4096, 96) == 0
+    # 2:4 sparse codes: 6144 bytes per (column tile, 128 values of k)
+    assert lib.w4a16_sp_packed_bytes(4096, 4096, 128) == 32 * 32 * 6144
+    assert lib.w4a16_sp_packed_bytes(4040, 4096, 128) == 32 * 32 * 6144
+    assert lib.w4a16_sp_packed_bytes(4096, 4096, 96) == 0
     # 8-bit codes: one byte per weight, K padded to a multiple of 256
     assert lib.w4a16_w8_packed_bytes(4096, 4096, 128) == 4096 * 4096
     assert lib.w4a16_w8_packed_bytes(4040, 4096, 128) == 4096 * 4096
@@ -93,6 +97,13 @@ def test_invalid_arguments_return_before_any_device_work(lib):
     assert lib.w4a16_bf16_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_bf16_gemm(odd, p, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_bf16_gemm(p, p, p, p, 0, 64, 64, 64, None, None, 0, None, 0, None) == w.OK
+    # 2:4 sparse codes
+    assert lib.w4a16_sp_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_sp_gemm(p, odd, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_sp_gemm(p, p, p, p, 0, 64, 64, 64, None, None, 0, None, 0, None) == w.OK
+    assert lib.w4a16_sp_pack(None, p, p, p, 64, 64, 64, None, None) == w.ERR_INVALID_ARG
+    four = ctypes.c_void_p(ctypes.addressof(buf) + 4)
+    assert lib.w4a16_sp_pack(p, p, p, p, 64, 64, 64, four, None) == w.ERR_INVALID_ARG
     # 8-bit codes
     assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG

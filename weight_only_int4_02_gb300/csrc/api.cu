@@ -15,6 +15,9 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* 
                         int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream);
 cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N, int n_tiles, int ng, int sms,
                               cudaStream_t stream);
+cudaError_t launch_pack_sp(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
+                           int K, int N, int SC, int n_tiles, int ng, int sms, unsigned long long* violations,
+                           cudaStream_t stream);
 cudaError_t launch_pack_w8(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
                            int K, int N, int KC, int n_tiles, int ng, int sms, cudaStream_t stream);
 }
@@ -58,6 +61,7 @@ struct DeviceState {
     int sms = 0;
     int max_clusters[3] = {0, 0, 0};     // co-resident 2-CTA clusters for tile heights 64, 128, 256 (4-bit)
     int max_clusters_w8[3] = {0, 0, 0};  // the same for the 8-bit kernels
+    int max_clusters_sp[2] = {0, 0};     // and for the 2:4 sparse kernels (tile heights 64, 128)
     void* ws = nullptr;
     size_t ws_bytes = 0;
 };
@@ -83,7 +87,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 struct Plan {
     int path;     // 2 = per-weight scaling tcgen05 kernel
     int tm;       // rows of X per tile (MMA N)
-    int ksub;     // 64-value sub-chunks per pipeline stage
+    int ksub;     // sub-chunks per pipeline stage (64 values of k; 128 for 2:4 sparse codes)
+    int xblocks;  // 64-wide blocks of X per stage (the X tensor map's box depth)
     int cluster;  // CTAs per cluster; 2 share each X tile by TMA multicast
     int m_tiles, n_tiles, n_blocks, KC, ng, iters;
     long long total;
@@ -102,15 +107,17 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0, int fm
     Plan P;
     P.path = 2;
     P.tm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    if (fmt == kFmtW4Sp && P.tm > 128) P.tm = 128;   // sparse stages leave no room for 256-row X tiles
     P.m_tiles = ceil_div(M, P.tm);
     P.n_tiles = ceil_div(N, kTileN);
-    P.ksub = fmt == kFmtW8 ? 2 : P.tm <= 64 ? 4 : 2;
+    P.ksub = (fmt == kFmtW8 || fmt == kFmtW4Sp) ? 2 : P.tm <= 64 ? 4 : 2;
+    P.xblocks = fmt == kFmtW4Sp ? 4 : P.ksub;
     // From 64 rows of X up, X is the larger operand per stage: two CTAs on
     // adjacent weight tiles load it once, by multicast.
     P.cluster = P.tm >= 64 ? 2 : 1;
     P.n_blocks = ceil_div(P.n_tiles, P.cluster);
     P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
-    P.iters = P.KC / P.ksub;
+    P.iters = P.KC / P.xblocks;
     P.ng = ceil_div(K, G);
     P.total = (long long)P.n_blocks * P.m_tiles * P.iters;
     long long units = (sms < kMaxGrid ? sms : kMaxGrid) / P.cluster;
@@ -158,6 +165,7 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0, int fm
 
 int max_clusters_for(const DeviceState* st, int tm, int fmt = kFmtW4)
 {
+    if (fmt == kFmtW4Sp) return tm == 64 ? st->max_clusters_sp[0] : tm == 128 ? st->max_clusters_sp[1] : 0;
     const int* mc = fmt == kFmtW8 ? st->max_clusters_w8 : st->max_clusters;
     return tm == 64 ? mc[0] : tm == 128 ? mc[1] : tm == 256 ? mc[2] : 0;
 }
@@ -173,7 +181,7 @@ Plan device_plan(const DeviceState* st, int M, int N, int K, int G, int fmt)
 // format): *mc4 gets the smallest cluster count over the 4-bit variants, *mc8
 // over the 8-bit ones.
 template <int TM, int KSUB, int CL>
-cudaError_t setup_shape(int* mc4, int* mc8)
+cudaError_t setup_shape(int* mc4, int* mc8, int* mcsp = nullptr)
 {
     int mc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     cudaError_t e;
@@ -190,6 +198,13 @@ cudaError_t setup_shape(int* mc4, int* mc8)
     for (int i = 1; i < 6; ++i) m = mc[i] < m ? mc[i] : m;
     *mc4 = m;
     *mc8 = mc[6] < mc[7] ? mc[6] : mc[7];
+    if constexpr (TM <= 128) {
+        int a = 0, b = 0;
+        if ((e = setup_tc<TM, 2, CL, false, kFmtW4Sp>(&a)) != cudaSuccess ||
+            (e = setup_tc<TM, 2, CL, true, kFmtW4Sp>(&b)) != cudaSuccess)
+            return e;
+        if (mcsp) *mcsp = a < b ? a : b;
+    }
     return cudaSuccess;
 }
 
@@ -206,6 +221,12 @@ cudaError_t launch_shape(const CUtensorMap& map, const GemmParams& p, bool epi, 
         case kFmtW4Bf16:
             return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4Bf16>(map, p, stream)
                        : launch_tc<TM, KSUB, CL, false, kFmtW4Bf16>(map, p, stream);
+        case kFmtW4Sp:
+            if constexpr (TM <= 128)
+                return epi ? launch_tc<TM, 2, CL, true, kFmtW4Sp>(map, p, stream)
+                           : launch_tc<TM, 2, CL, false, kFmtW4Sp>(map, p, stream);
+            else
+                return cudaErrorInvalidValue;   // the plan never picks 256-row tiles for sparse codes
         default:
             return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4>(map, p, stream)
                        : launch_tc<TM, KSUB, CL, false, kFmtW4>(map, p, stream);
@@ -231,8 +252,10 @@ w4a16_status device_state(DeviceState** out)
         int unused8 = 0;
         if ((e = setup_shape<16, 4, 1>(&unused, &unused8)) != cudaSuccess ||
             (e = setup_shape<32, 4, 1>(&unused, &unused8)) != cudaSuccess ||
-            (e = setup_shape<64, 4, 2>(&st.max_clusters[0], &st.max_clusters_w8[0])) != cudaSuccess ||
-            (e = setup_shape<128, 2, 2>(&st.max_clusters[1], &st.max_clusters_w8[1])) != cudaSuccess ||
+            (e = setup_shape<64, 4, 2>(&st.max_clusters[0], &st.max_clusters_w8[0], &st.max_clusters_sp[0])) !=
+                cudaSuccess ||
+            (e = setup_shape<128, 2, 2>(&st.max_clusters[1], &st.max_clusters_w8[1], &st.max_clusters_sp[1])) !=
+                cudaSuccess ||
             (e = setup_shape<256, 2, 2>(&st.max_clusters[2], &st.max_clusters_w8[2])) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
@@ -347,7 +370,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     }
     p.n_tiles = P.n_tiles;
     p.m_tiles = P.m_tiles;
-    p.KC = P.KC;
+    p.KC = fmt == kFmtW4Sp ? P.KC / 2 : P.KC;   // packed chunks per column (128 values of k when sparse)
     p.iters = P.iters;
     p.total_iters = P.total;
     p.grid = P.grid;
@@ -364,7 +387,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     // enough: MMA rows past M feed only output columns that are never stored.
     p.x_rows = P.m_tiles == 1 ? ((M + 7) / 8) * 8 : P.tm;
     // Clusters split a stage's X blocks between their CTAs: one 2-D TMA per block.
-    if (!encode_x_map(&map, x, M, K, p.x_rows, P.ksub, P.cluster == 1, &p.x_3d, fmt == kFmtW4Bf16))
+    if (!encode_x_map(&map, x, M, K, p.x_rows, P.xblocks, P.cluster == 1, &p.x_3d, fmt == kFmtW4Bf16))
         return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     const bool epi = bias || residual || act != 0;
@@ -445,7 +468,7 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size)
     if (M == 0) return kPartialsOff;
     // enough for every weight format's plan
     size_t need = 0;
-    for (int fmt : {kFmtW4, kFmtW8}) {
+    for (int fmt : {kFmtW4, kFmtW8, kFmtW4Sp}) {
         const int mc = st ? max_clusters_for(st, make_plan(M, N, K, G, sms, 0, fmt).tm, fmt) : 0;
         const size_t b = make_plan(M, N, K, G, sms, mc, fmt).ws_bytes;
         need = b > need ? b : need;
@@ -515,6 +538,40 @@ w4a16_status w4a16_bf16_gemm(const uint16_t* x, const uint32_t* packed, const ui
         return W4A16_ERR_INVALID_ARG;
     return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
                      reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, kFmtW4Bf16);
+}
+
+size_t w4a16_sp_packed_bytes(int K, int N, int group_size)
+{
+    if (!valid_sizes(K, N, norm_group(K, group_size))) return 0;
+    return (size_t)ceil_div(N, kTileN) * (ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad / 2) * (kChunkBytes + 2048);
+}
+
+w4a16_status w4a16_sp_pack(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
+                           int K, int N, int group_size, unsigned long long* violations, w4a16_stream_t stream)
+{
+    const int G = norm_group(K, group_size);
+    if (!valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    if (!codes || !scales || !packed || !scales_packed) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(scales_packed) || (reinterpret_cast<uintptr_t>(violations) & 7))
+        return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    return from_cuda(launch_pack_sp(codes, scales, packed, scales_packed, K, N,
+                                    ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad / 2, ceil_div(N, kTileN),
+                                    ceil_div(K, G), st->sms, violations, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_sp_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_packed, uint16_t* y,
+                           int M, int N, int K, int group_size, const uint16_t* bias, const uint16_t* residual,
+                           int activation, void* workspace, size_t ws_bytes, w4a16_stream_t stream)
+{
+    if (activation < W4A16_ACT_NONE || activation > W4A16_ACT_RELU) return W4A16_ERR_INVALID_ARG;
+    if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
+        return W4A16_ERR_INVALID_ARG;
+    return gemm_impl(x, reinterpret_cast<const uint32_t*>(packed), scales_packed, y, M, N, K, group_size, workspace,
+                     ws_bytes, workspace == nullptr, reinterpret_cast<cudaStream_t>(stream), bias, residual,
+                     activation, kFmtW4Sp);
 }
 
 size_t w4a16_w8_packed_bytes(int K, int N, int group_size)

@@ -50,11 +50,14 @@ constexpr int kKPad = 4;           // the packed layout pads K to a multiple of 
 // Weight formats (a template parameter of the kernel): 4-bit codes with the
 // zero-point 8; 4-bit codes with one zero-point per (group, column); 8-bit codes
 // with the zero-point 128 (8 KB per (tile, sub-chunk), bytes of a word in the
-// order k, k+2, k+1, k+3); 4-bit codes with BF16 activations, scales and output.
+// order k, k+2, k+1, k+3); 4-bit codes with BF16 activations, scales and output;
+// 2:4 sparse 4-bit codes (sub-chunks of 128 k: 4 KB of stored codes then 2 KB of
+// position words in tensor-memory lane order, fed to the sparse MMA).
 constexpr int kFmtW4 = 0;
 constexpr int kFmtW4Zp = 1;
 constexpr int kFmtW8 = 2;
 constexpr int kFmtW4Bf16 = 3;   // 4-bit codes, zero-point 8, BF16 X / scales / bias / residual / Y
+constexpr int kFmtW4Sp = 4;     // 4-bit codes, zero-point 8, 2:4 sparse along k (two stored per four)
 
 struct GemmParams {
     const uint32_t* packed; // packed codes (4-bit: 1024 words per (tile, sub-chunk); 8-bit: 2048)
@@ -123,20 +126,26 @@ __device__ __forceinline__ __half st16(float v)
 
 template <int TM, int KSUB, int FMT = kFmtW4>
 struct TcCfg {
-    static constexpr int kStageK = KSUB * kChunkK;
+    static constexpr bool kSp = FMT == kFmtW4Sp;
+    static constexpr int kSubK = kSp ? 2 * kChunkK : kChunkK;   // values of k per sub-chunk
+    static constexpr int kStageK = KSUB * kSubK;
+    static constexpr int kXBlocks = kStageK / kChunkK;      // 64-wide K blocks of X per stage
     static constexpr int kXBlock = TM * 128;              // one 64-wide K block of X (TM rows)
-    static constexpr int kXBytes = KSUB * kXBlock;
-    static constexpr int kPkChunk = FMT == kFmtW8 ? 2 * kChunkBytes : kChunkBytes;  // per (tile, sub-chunk)
+    static constexpr int kXBytes = kXBlocks * kXBlock;
+    // packed bytes per (tile, sub-chunk): 4-bit codes 4 KB, 8-bit codes 8 KB, 2:4
+    // sparse 4 KB of stored codes + 2 KB of position words
+    static constexpr int kPkChunk = FMT == kFmtW8 ? 2 * kChunkBytes : kSp ? kChunkBytes + 2048 : kChunkBytes;
     static constexpr int kPkBytes = KSUB * kPkChunk;
-    static constexpr int kScBytes = 2 * KSUB * 256;       // G = 32 puts 2*KSUB groups in a stage
-    static constexpr int kZpBytes = FMT == kFmtW4Zp ? 2 * KSUB * 64 : 0;  // 4-bit zero-points of those groups
+    static constexpr int kScBytes = (kStageK / 32) * 256;   // G = 32 puts kStageK/32 groups in a stage
+    static constexpr int kZpBytes = FMT == kFmtW4Zp ? (kStageK / 32) * 64 : 0;  // 4-bit zero-points of those groups
     // Two rings in shared memory: W (packed words + scales [+ zero-points]), freed
     // by the dequant warps once they hold their words, so the HBM stream never
     // waits on the MMA; and X, freed by the MMA's commit.
     static constexpr int kWStageBytes = kPkBytes + kScBytes + kZpBytes;
     // a multiple of the team count; 8-bit stages of 128-row tiles and up are 4 deep
     // (64 KB of codes in flight, as 8 stages of 4-bit codes) to leave room for X
-    static constexpr int kWStages = FMT == kFmtW8 ? (TM >= 128 ? 4 : 8) : (TM <= 32 || KSUB == 2) ? 8 : 6;
+    static constexpr int kWStages =
+        (FMT == kFmtW8 || kSp) ? (TM >= 128 ? 4 : 8) : (TM <= 32 || KSUB == 2) ? 8 : 6;
     static constexpr int kXFit = (220 * 1024 - kWStages * kWStageBytes) / kXBytes;
     static constexpr int kXStages = kXFit > 8 ? 8 : kXFit;
     // Dequant teams take stages in turn; a team is KSUB/2 groups of four warps.
@@ -148,7 +157,11 @@ struct TcCfg {
     static constexpr int kMmaWarp = kProdWWarp + 1;
     static constexpr int kThreads = 32 * (kMmaWarp + 1);
     static constexpr int kDBufs = TM <= 128 ? 2 : 1;
-    static constexpr int kASlotCols = KSUB * 32;          // 16-bit A values, two per column
+    // sparse: one position column per MMA, each at an 8-column boundary (the alignment
+    // the MMA's A operand uses; a tighter packing has not been measured)
+    static constexpr int kMetaStride = 8;
+    static constexpr int kMetaCols = kSp ? KSUB * 4 * kMetaStride : 0;
+    static constexpr int kASlotCols = KSUB * 32 + kMetaCols;  // 16-bit A values, two per column
     static constexpr int kAFit = (512 - kDBufs * TM) / kASlotCols;
     static constexpr int kAStages = kAFit >= 4 ? 4 : 2;               // a multiple of the team count
     static constexpr int kACol = 0;
@@ -171,7 +184,8 @@ struct TcCfg {
     static_assert(KSUB % 2 == 0, "a dequant warp unpacks two sub-chunks");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert(kDCol + kDBufs * TM <= 512, "tensor memory");
-    static_assert(kKPad % KSUB == 0, "stages must tile the padded K");
+    static_assert((kKPad * kChunkK) % kStageK == 0, "stages must tile the padded K");
+    static_assert(!kSp || KSUB == 2, "sparse stages are two 128-value sub-chunks");
 };
 
 // First iteration of work unit (cluster) c.
@@ -468,19 +482,19 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     const int k0 = kc * C::kStageK;
                     if (is_x && CL > 1) {
                         // each CTA brings its share of the stage's X blocks into both CTAs
-                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(KSUB * p.x_rows * 128));
+                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(C::kXBlocks * p.x_rows * 128));
 #pragma unroll
-                        for (int j = rank; j < KSUB; j += CL)
+                        for (int j = rank; j < C::kXBlocks; j += CL)
                             tma_load_2d_mc(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
                                            xfull_bar(s), k0 + j * kChunkK, mt * TM, (uint16_t)((1u << CL) - 1));
                     } else if (is_x) {
-                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(KSUB * p.x_rows * 128));
+                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(C::kXBlocks * p.x_rows * 128));
                         if (p.x_3d) {
                             tma_load_3d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, xfull_bar(s), 0, mt * TM,
-                                        kc * KSUB);
+                                        kc * C::kXBlocks);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < KSUB; ++j)
+                            for (int j = 0; j < C::kXBlocks; ++j)
                                 tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
                                             xfull_bar(s), k0 + j * kChunkK, mt * TM);
                         }
@@ -525,7 +539,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = BF ? idesc_bf16_f32(128, TM) : idesc_f16_f32(128, TM);
+        constexpr uint32_t idesc =
+            (BF ? idesc_bf16_f32(128, TM) : idesc_f16_f32(128, TM)) | (C::kSp ? kIdescSparse : 0u);
         uint32_t seq = 0;
         int d = 0;
         uint32_t dph = 0;
@@ -549,13 +564,28 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     // The descriptor's start address counts 16-byte units: +2 per 16 K values
                     // inside a 128-byte row, +x_rows*128/16 per 64-wide K block (blocks of
                     // x_rows rows sit back to back, each 1024-byte aligned).
+                    if constexpr (C::kSp) {
+                        // sub-chunk j: 4 sparse MMAs of 32 values of k, each reading 8 A columns
+                        // (16 stored values), one position column, and half an X block (+4 per 32 k)
 #pragma unroll
-                    for (int j = 0; j < KSUB; ++j) {
+                        for (int j = 0; j < KSUB; ++j) {
 #pragma unroll
-                        for (int kk = 0; kk < kChunkK / 16; ++kk) {
-                            const uint64_t bd = b0 + (uint64_t)(j * p.x_rows * 8 + kk * 2);
-                            mma_f16_ts(d_tmem, a0 + j * 32 + kk * 8, bd, idesc,
-                                       (kc > g.kb || j > 0 || kk > 0) ? 1u : 0u);
+                            for (int mm = 0; mm < 4; ++mm) {
+                                const uint64_t bd = b0 + (uint64_t)((2 * j + mm / 2) * p.x_rows * 8 + (mm % 2) * 4);
+                                mma_f16_sp_ts(d_tmem, a0 + j * 32 + mm * 8, bd,
+                                              a0 + KSUB * 32 + (j * 4 + mm) * C::kMetaStride, idesc,
+                                              (kc > g.kb || j > 0 || mm > 0) ? 1u : 0u);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < KSUB; ++j) {
+#pragma unroll
+                            for (int kk = 0; kk < kChunkK / 16; ++kk) {
+                                const uint64_t bd = b0 + (uint64_t)(j * p.x_rows * 8 + kk * 2);
+                                mma_f16_ts(d_tmem, a0 + j * 32 + kk * 8, bd, idesc,
+                                           (kc > g.kb || j > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
                     }
                     if constexpr (CL > 1)
@@ -605,10 +635,14 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                 const uint8_t* zb = smem + C::kOffZp + s * C::kZpBytes + (n_in >> 1);   // ZP only
                 const int zshift = 4 * (n_in & 1);
                 // A thread's 16-byte blocks of a sub-chunk sit 2 KB apart: 2 for 4-bit
-                // codes (32 values each), 4 for 8-bit codes (16 values each).
+                // codes (32 values each; 32 stored values of 64 k when sparse), 4 for
+                // 8-bit codes (16 values each). Sparse sub-chunks then hold the
+                // thread's lane of position words (16 bytes per lane).
                 constexpr int NB = FMT == kFmtW8 ? 4 : 2;
+                constexpr int NS = C::kSubK / 32;   // scales per sub-chunk (one per 32 k; G >= 32)
                 uint4 w[2][NB];
-                __half2 s2[2][2];
+                uint4 meta[2];
+                __half2 s2[2][NS];
                 __half2 clo[2][2], chi[2][2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -616,11 +650,13 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     const uint8_t* pk = smem + C::kOffPk + s * C::kPkBytes + j * C::kPkChunk + n_in * 16;
 #pragma unroll
                     for (int b = 0; b < NB; ++b) w[h][b] = *reinterpret_cast<const uint4*>(pk + b * kTileN * 16);
-                    const int k0 = kc * C::kStageK + j * kChunkK;
-                    const __half s_lo = sc[(group_of(p, k0) - gs) * kTileN];
-                    const __half s_hi = sc[(group_of(p, k0 + 32) - gs) * kTileN];
-                    s2[h][0] = __halves2half2(s_lo, s_lo);
-                    s2[h][1] = __halves2half2(s_hi, s_hi);
+                    if constexpr (C::kSp) meta[h] = *reinterpret_cast<const uint4*>(pk + kChunkBytes);
+                    const int k0 = kc * C::kStageK + j * C::kSubK;
+#pragma unroll
+                    for (int q = 0; q < NS; ++q) {
+                        const __half sq = sc[(group_of(p, k0 + 32 * q) - gs) * kTileN];
+                        s2[h][q] = __halves2half2(sq, sq);
+                    }
                     if constexpr (ZP) {
                         const uint32_t z_lo = (zb[(group_of(p, k0) - gs) * 64] >> zshift) & 0xFu;
                         const uint32_t z_hi = (zb[(group_of(p, k0 + 32) - gs) * 64] >> zshift) & 0xFu;
@@ -647,6 +683,15 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                             dequant_word_bf16(w[h][b].z, sb, v + 16 * b + 8);
                             dequant_word_bf16(w[h][b].w, sb, v + 16 * b + 12);
                         }
+                    } else if constexpr (C::kSp) {
+                        // stored values: word (b, wd) holds 8 of groups covering k b*64 + wd*16 .. +15
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            dequant_word(w[h][b].x, s2[h][2 * b], clo[h][0], chi[h][0], v + 16 * b + 0);
+                            dequant_word(w[h][b].y, s2[h][2 * b], clo[h][0], chi[h][0], v + 16 * b + 4);
+                            dequant_word(w[h][b].z, s2[h][2 * b + 1], clo[h][0], chi[h][0], v + 16 * b + 8);
+                            dequant_word(w[h][b].w, s2[h][2 * b + 1], clo[h][0], chi[h][0], v + 16 * b + 12);
+                        }
                     } else if constexpr (FMT == kFmtW8) {
 #pragma unroll
                         for (int b = 0; b < 4; ++b) {
@@ -671,6 +716,15 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                         tc_fence_after();
                     }
                     tmem_st32(tmem + lane_base + C::kACol + a * C::kASlotCols + (2 * gi + h) * 32, v);
+                    if constexpr (C::kSp) {
+                        const uint32_t mcol = tmem + lane_base + C::kACol + a * C::kASlotCols + KSUB * 32 +
+                                              (2 * gi + h) * 4 * C::kMetaStride;
+                        tmem_st1(mcol + 0 * C::kMetaStride, meta[h].x);
+                        tmem_st1(mcol + 1 * C::kMetaStride, meta[h].y);
+                        tmem_st1(mcol + 2 * C::kMetaStride, meta[h].z);
+                        tmem_st1(mcol + 3 * C::kMetaStride, meta[h].w);
+                        tmem_wait_st();
+                    }
                 }
                 if (!ok) break;
                 tc_fence_before();

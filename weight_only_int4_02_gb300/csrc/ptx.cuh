@@ -224,6 +224,22 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// The 2:4 sparse form: A holds two stored values of every four along K (K = 32
+// per instruction, 8 TMEM columns of A), their positions in tensor memory at
+// meta_tmem (one 32-bit column: lane L, nibble u describes group
+// 4*((L mod 16)/8) + u mod 4 of row 16*(L/16) + 8*(u/4) + L mod 8), and the
+// instruction descriptor's sparsity bit set.
+__device__ __forceinline__ void mma_f16_sp_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t meta_tmem,
+                                              uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.sp.cta_group::1.kind::f16 [%0], [%1], %2, [%3], %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
@@ -296,6 +312,15 @@ __device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float (&v)[N])
     for (int e = 0; e < N; ++e) v[e] = __uint_as_float(r[e]);
 }
 
+// Each lane of the warp writes one 32-bit column of its own TMEM lane (the wait for
+// completion is left to the caller's next tcgen05.wait::st or fence).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Each lane of the warp writes 16 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
@@ -347,6 +372,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {
     return idesc_f16_f32(M, N) | (1u << 7) | (1u << 10);
 }
+
+// Sparse flag (bit 2) of the instruction descriptor: A is 2:4 sparse along K.
+constexpr uint32_t kIdescSparse = 1u << 2;
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {

@@ -19,7 +19,7 @@ EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error
            "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
            "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
            "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp", "w4a16_w8_packed_bytes", "w4a16_w8_pack",
-           "w4a16_w8_gemm", "w4a16_bf16_gemm"]
+           "w4a16_w8_gemm", "w4a16_bf16_gemm", "w4a16_sp_packed_bytes", "w4a16_sp_pack", "w4a16_sp_gemm"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -71,6 +71,12 @@ def lib():
         L.w4a16_pack_zeros.restype = I
         L.w4a16_gemm_zp.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
         L.w4a16_gemm_zp.restype = I
+        L.w4a16_sp_packed_bytes.argtypes = [I, I, I]
+        L.w4a16_sp_packed_bytes.restype = Z
+        L.w4a16_sp_pack.argtypes = [P, P, P, P, I, I, I, P, P]
+        L.w4a16_sp_pack.restype = I
+        L.w4a16_sp_gemm.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
+        L.w4a16_sp_gemm.restype = I
         L.w4a16_bf16_gemm.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
         L.w4a16_bf16_gemm.restype = I
         L.w4a16_w8_packed_bytes.argtypes = [I, I, I]
@@ -292,4 +298,47 @@ def bf16_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None,
     _check(lib().w4a16_bf16_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                  _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                  _stream(stream)), "w4a16_bf16_gemm")
+    return y
+
+
+def sp_packed_bytes(K, N, group_size):
+    return lib().w4a16_sp_packed_bytes(K, N, group_size)
+
+
+def sp_pack(codes, scales, group_size, stream=None, violations=None):
+    """Repack 2:4 sparse codes (uint8 [K][N]: at most two codes other than 8 in every
+    aligned group of four k) and scales (float16 [ceil(K/G)][N]).
+
+    Returns (packed uint8, packed float16 scales). violations: an int64 CUDA tensor
+    of one element to which the number of groups that are not 2:4 is added, or None."""
+    K, N = codes.shape
+    assert codes.dtype == torch.uint8 and scales.dtype == torch.float16
+    assert codes.is_cuda and scales.is_cuda and codes.is_contiguous() and scales.is_contiguous()
+    nb, ns = sp_packed_bytes(K, N, group_size), scales_elems(K, N, group_size)
+    if nb == 0 or ns == 0:
+        raise W4A16Error(ERR_INVALID_ARG, "sp_pack")
+    if violations is not None:
+        assert violations.dtype == torch.int64 and violations.is_cuda and violations.numel() == 1
+    packed = torch.empty(nb, dtype=torch.uint8, device=codes.device)
+    sp = torch.empty(ns, dtype=torch.float16, device=codes.device)
+    _check(lib().w4a16_sp_pack(_ptr(codes), _ptr(scales), _ptr(packed), _ptr(sp), K, N, group_size,
+                               _ptr(violations), _stream(stream)), "w4a16_sp_pack")
+    return packed, sp
+
+
+def sp_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None, activation="none", y=None,
+            workspace=None, stream=None):
+    """y = act(x @ dequant(W) + bias) + residual for 2:4 sparse codes packed by sp_pack.
+    Arguments as gemm_fused."""
+    M, K = x.shape
+    assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
+    for t, shape in ((bias, (N,)), (residual, (M, N))):
+        if t is not None:
+            assert t.dtype == torch.float16 and t.is_cuda and t.is_contiguous() and tuple(t.shape) == shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().w4a16_sp_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
+                               _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
+                               _stream(stream)), "w4a16_sp_gemm")
     return y
