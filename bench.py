@@ -468,6 +468,7 @@ def run_ours(args, rank, world):
         out["zero_points"] = zero_point_probe(G)
         out["w8a16"] = w8_probe(G)
         out["bf16_activations"] = bf16_probe(G)
+        out["sparse_2to4"] = sparse_probe(G)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
@@ -590,6 +591,57 @@ def bf16_probe(G):
         rows.append({"case": [M, K, N], "us_fp16": us16, "us_bf16": usbf,
                      "tflops_bf16": flops(M, K, N) / (usbf * 1e-6) / 1e12})
         del copies
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return rows
+
+
+def sparse_probe(G):
+    """2:4 sparse INT4 beside dense INT4 on the same 2:4 codes: mean time per launch of
+    w4a16_gemm and w4a16_sp_gemm, launched back to back from a CUDA Graph over
+    rotating copies of the packed weights (more bytes than L2), on the gate/up decode
+    layer (16 x 4096 x 22016) and the 18432 x 73728 layer at M = 1, 16 and 128. The
+    codes are drawn on the GPU: uniform on 0..15, two of every four k kept (one of
+    the six position pairs, uniformly), the rest 8. Sparse weight bytes: stored
+    codes (K*N/4) + position words (K*N/8) + FP16 scales."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    rows = []
+    pairs = torch.tensor([[1, 1, 0, 0], [1, 0, 1, 0], [1, 0, 0, 1], [0, 1, 1, 0], [0, 1, 0, 1], [0, 0, 1, 1]],
+                         dtype=torch.bool, device="cuda")
+    for K, N, Ms in ((4096, 22016, (16,)), (18432, 73728, (1, 16, 128))):
+        gen = torch.Generator(device="cuda").manual_seed(0)
+        q = torch.randint(0, 16, (K, N), dtype=torch.uint8, device="cuda", generator=gen)
+        choice = torch.randint(0, 6, (K // 4, N), dtype=torch.int64, device="cuda", generator=gen)
+        keep = pairs[choice]                               # [K/4][N][4]
+        del choice
+        q = torch.where(keep.permute(0, 2, 1).reshape(K, N), q, torch.full_like(q, 8))
+        del keep
+        s = torch.from_numpy(inputs.scales(K, N, G, 0)).cuda()
+        dense = w4a16.pack(q, s, G)
+        viol = torch.zeros(1, dtype=torch.int64, device="cuda")
+        sparse = w4a16.sp_pack(q, s, G, violations=viol)
+        del q
+        if int(viol.item()) != 0:
+            raise RuntimeError("sparse probe codes are not 2:4")
+        n_copies = max(2, int(400e6 // (dense[0].numel() * 4)) + 1)
+        dcopies = [dense] + [(dense[0].clone(), dense[1].clone()) for _ in range(n_copies - 1)]
+        scopies = [sparse] + [(sparse[0].clone(), sparse[1].clone()) for _ in range(n_copies - 1)]
+        del dense, sparse
+        for M in Ms:
+            x = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
+            y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+            reps = 40 if K * N < 10 ** 9 else 8
+            us_d = graph_us_per_launch(
+                lambda c: w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream()), dcopies, reps)
+            us_s = graph_us_per_launch(
+                lambda c: w4a16.sp_gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream()), scopies, reps)
+            sb = K * N // 4 + K * N // 8 + n_groups(K, G) * N * 2
+            rows.append({"case": [M, K, N], "us_dense": us_d, "us_sparse": us_s, "speedup": us_d / us_s,
+                         "sparse_gbs": sb / (us_s * 1e-6) / 1e9,
+                         "dense_gbs": weight_bytes(K, N, G) / (us_d * 1e-6) / 1e9,
+                         "tflops_sparse": flops(M, K, N) / (us_s * 1e-6) / 1e12})
+        del dcopies, scopies
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("a kernel wait timed out")
     return rows
