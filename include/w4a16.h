@@ -312,9 +312,10 @@ w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint1
  */
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
 
-/* Which kernel path and tile the dispatcher picks for a shape on the current
- * device: *path = 1 (small-M, group scaling on FP32 accumulators) or
- * 2 (large-M, per-weight scaling); *tile_m = rows of X per tile; *grid = CTAs. */
+/* Which kernel and tile the dispatcher picks for a shape of the 4-bit FP16 format
+ * (w4a16_gemm and w4a16_gemm_fused) on the current device: *path = 2 (the one
+ * kernel built: per-weight scaling, dequantised weights in tensor memory; the
+ * value 1 is retired); *tile_m = rows of X per tile; *grid = CTAs. */
 w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid);
 
 /*
