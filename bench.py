@@ -780,22 +780,38 @@ def fp16_baseline(per_case, dev, reps):
 
 
 def run_e2e(per_case, G, dev, K, W, world):
-    """Same metric through the public API with host buffers: per step, pinned X -> device,
-    the GEMMs, device Y -> pinned host, all inside the timed region (one graph per step)."""
+    """Same metric through the public API with host buffers: per step, every GEMM's X from
+    pinned host memory to the device (one copy of the step's X, gathered in one pinned
+    buffer), the GEMMs, and every Y back to pinned host memory (one copy), all inside the
+    timed region (one graph per step). Gathering the copies keeps the GEMMs back to back,
+    so each launch still overlaps the next (programmatic dependent launch)."""
     import torch
     from weight_only_int4_02_gb300 import w4a16
-    xs_h = [c["x"].cpu().pin_memory() for c in per_case]
-    ys_h = [torch.empty((c["M"], c["N"]), dtype=torch.float16).pin_memory() for c in per_case]
-    h2d = sum(x.numel() * 2 for x in xs_h)
-    d2h = sum(y.numel() * 2 for y in ys_h)
+    x_sizes = [c["M"] * c["K"] for c in per_case]     # multiples of 8 elements: 16-byte aligned views
+    y_sizes = [c["M"] * c["N"] for c in per_case]
+    x_dev = torch.empty(sum(x_sizes), dtype=torch.float16, device="cuda")
+    y_dev = torch.empty(sum(y_sizes), dtype=torch.float16, device="cuda")
+    x_host = torch.empty(sum(x_sizes), dtype=torch.float16).pin_memory()
+    y_host = torch.empty(sum(y_sizes), dtype=torch.float16).pin_memory()
+    xs, ys, ys_h = [], [], []
+    ox = oy = 0
+    for c, nx, ny in zip(per_case, x_sizes, y_sizes):
+        x_host[ox:ox + nx].copy_(c["x"].reshape(-1).cpu())
+        xs.append(x_dev[ox:ox + nx].view(c["M"], c["K"]))
+        ys.append(y_dev[oy:oy + ny].view(c["M"], c["N"]))
+        ys_h.append(y_host[oy:oy + ny].view(c["M"], c["N"]))
+        ox += nx
+        oy += ny
+    h2d = x_host.numel() * 2
+    d2h = y_host.numel() * 2
     cap = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):
         st = torch.cuda.current_stream()
-        for c, xh, yh in zip(per_case, xs_h, ys_h):
-            c["x"].copy_(xh, non_blocking=True)
-            w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
-            yh.copy_(c["y"], non_blocking=True)
+        x_dev.copy_(x_host, non_blocking=True)
+        for c, x, y in zip(per_case, xs, ys):
+            w4a16.gemm(x, c["packed"], c["sp"], c["N"], G, y=y, stream=st)
+        y_host.copy_(y_dev, non_blocking=True)
     for _ in range(max(W, 1)):
         g.replay()
     torch.cuda.synchronize()
@@ -809,7 +825,7 @@ def run_e2e(per_case, G, dev, K, W, world):
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b) / K, world, dev)
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
-    ok = all(torch.equal(yh, c["y"].cpu()) for c, yh in zip(per_case, ys_h))
+    ok = all(torch.equal(yh, c["y"].cpu()) for c, yh in zip(per_case, ys_h))   # the device-timed run's Y
     return {"value": step_flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "outputs_match_device": ok}
 
@@ -857,21 +873,34 @@ def run_case(args):
     from weight_only_int4_02_gb300 import w4a16
     M, K, N = (int(v) for v in args.case.split(","))
     G = 128
-    q = inputs.codes(K, N, 0)
-    s = inputs.scales(K, N, G, 0)
-    packed, sp = w4a16.pack(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), G)
-    wbytes = packed.numel() * 4 + sp.numel() * 2
-    copies = [(packed.clone(), sp.clone()) for _ in range(max(2, int(400e6 // wbytes) + 1))]
+    s = torch.from_numpy(inputs.scales(K, N, G, 0)).cuda()
     x = torch.from_numpy(inputs.activations(M, K, 0)).cuda()
     y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    if args.format == "w8":
+        q = inputs.rng(0, inputs.CODE_STREAM).integers(0, 256, size=(K, N), dtype=np.uint8)
+        weights = w4a16.w8_pack(torch.from_numpy(q).cuda(), s, G)
+
+        def call(c, stream=None):
+            w4a16.w8_gemm(x, c[0], c[1], N, G, y=y, stream=stream)
+    elif args.format == "sparse":
+        weights = w4a16.sp_pack(torch.from_numpy(inputs.codes_2to4(K, N, 0)).cuda(), s, G)
+
+        def call(c, stream=None):
+            w4a16.sp_gemm(x, c[0], c[1], N, G, y=y, stream=stream)
+    else:
+        weights = w4a16.pack(torch.from_numpy(inputs.codes(K, N, 0)).cuda(), s, G)
+
+        def call(c, stream=None):
+            w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=stream)
+    wbytes = weights[0].numel() * weights[0].element_size() + weights[1].numel() * 2
+    copies = [(weights[0].clone(), weights[1].clone()) for _ in range(max(2, int(400e6 // wbytes) + 1))]
     for c in copies:
-        w4a16.gemm(x, c[0], c[1], N, G, y=y)
+        call(c)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=torch.cuda.Stream()):
         for r in range(args.reps):
-            c = copies[r % len(copies)]
-            w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream())
+            call(copies[r % len(copies)], stream=torch.cuda.current_stream())
     g.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -882,7 +911,7 @@ def run_case(args):
     us = a.elapsed_time(b) * 1e3 / args.reps
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("a kernel wait timed out")
-    print(json.dumps({"case": [M, K, N], "us_per_launch": us, "weight_gbs": wbytes / us / 1e3,
+    print(json.dumps({"case": [M, K, N], "format": args.format, "us_per_launch": us, "weight_gbs": wbytes / us / 1e3,
                       "tflops": flops(M, K, N) / us / 1e6, "plan": w4a16.plan(M, N, K, G),
                       "launches_before_timed": len(copies) + args.reps}), flush=True)
 
@@ -897,6 +926,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None, help="M,K,N: time one GEMM shape (profiling aid)")
     ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--format", default="int4", choices=["int4", "w8", "sparse"],
+                    help="weight format of --case: 4-bit codes, 8-bit codes, or 2:4 sparse 4-bit codes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
