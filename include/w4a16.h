@@ -312,6 +312,16 @@ w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint1
  */
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
 
+/*
+ * Self-test of failure detection (no counterpart in the pages): launches one warp
+ * that waits, with the kernels' own bounded wait, on a barrier that nothing ever
+ * completes. After limit_ns (1 .. 10^10) the wait gives up, sets the error word of
+ * `workspace` (NULL = the library's own workspace of the current device) and the
+ * kernel returns; w4a16_check_device_status then reports W4A16_ERR_TIMEOUT and
+ * clears it. The context stays usable. Nothing faults, traps or hangs.
+ */
+w4a16_status w4a16_selftest_wait_timeout(void* workspace, long long limit_ns, w4a16_stream_t stream);
+
 /* Which kernel and tile the dispatcher picks for a shape of the 4-bit FP16 format
  * (w4a16_gemm and w4a16_gemm_fused) on the current device: *path = 2 (the one
  * kernel built: per-weight scaling, dequantised weights in tensor memory; the

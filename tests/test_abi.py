@@ -97,6 +97,10 @@ def test_invalid_arguments_return_before_any_device_work(lib):
     assert lib.w4a16_bf16_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_bf16_gemm(odd, p, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_bf16_gemm(p, p, p, p, 0, 64, 64, 64, None, None, 0, None, 0, None) == w.OK
+    # failure-detection self-test: the limit must be in 1 .. 10^10 ns, the workspace 256-byte aligned
+    assert lib.w4a16_selftest_wait_timeout(None, 0, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_selftest_wait_timeout(None, 10 ** 11, None) == w.ERR_INVALID_ARG
+    assert lib.w4a16_selftest_wait_timeout(odd, 1000, None) == w.ERR_INVALID_ARG
     # 2:4 sparse codes
     assert lib.w4a16_sp_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_sp_gemm(p, odd, p, p, 4, 64, 64, 64, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG

@@ -26,6 +26,29 @@ namespace {
 
 using namespace w4a16;
 
+// Self-test of the bounded waits: one warp waits, with the GEMM kernels' own
+// wait_warp, on phase 0 of an mbarrier that nothing arrives on; after limit_ns the
+// wait gives up, sets the error word and the kernel returns.
+__global__ void wait_selftest_kernel(int* status, long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitCtl ctl{&abort_flag, status, limit_ns};
+    wait_warp(smem_addr(&bar), 0, ctl);
+}
+
+cudaError_t launch_wait_selftest(int* status, long long limit_ns, cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 thread_local int t_last_cuda_error = 0;
 
 w4a16_status from_cuda(cudaError_t e)
@@ -605,6 +628,21 @@ w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint1
     return gemm_impl(x, reinterpret_cast<const uint32_t*>(packed), scales_packed, y, M, N, K, group_size, workspace,
                      ws_bytes, workspace == nullptr, reinterpret_cast<cudaStream_t>(stream), bias, residual,
                      activation, kFmtW8);
+}
+
+w4a16_status w4a16_selftest_wait_timeout(void* workspace, long long limit_ns, w4a16_stream_t stream)
+{
+    if (limit_ns <= 0 || limit_ns > 10000000000LL) return W4A16_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return W4A16_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    w4a16_status rc = device_state(&st);
+    if (rc != W4A16_OK) return rc;
+    if (!workspace) {
+        size_t bytes = 0;
+        if ((rc = own_workspace(st, &workspace, &bytes)) != W4A16_OK) return rc;
+    }
+    return from_cuda(launch_wait_selftest(reinterpret_cast<int*>(workspace), limit_ns,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream)

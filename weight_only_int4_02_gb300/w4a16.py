@@ -19,7 +19,8 @@ EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error
            "w4a16_scales_elems", "w4a16_pack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_gemm_ws",
            "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
            "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp", "w4a16_w8_packed_bytes", "w4a16_w8_pack",
-           "w4a16_w8_gemm", "w4a16_bf16_gemm", "w4a16_sp_packed_bytes", "w4a16_sp_pack", "w4a16_sp_gemm"]
+           "w4a16_w8_gemm", "w4a16_bf16_gemm", "w4a16_sp_packed_bytes", "w4a16_sp_pack", "w4a16_sp_gemm",
+           "w4a16_selftest_wait_timeout"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -71,6 +72,8 @@ def lib():
         L.w4a16_pack_zeros.restype = I
         L.w4a16_gemm_zp.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
         L.w4a16_gemm_zp.restype = I
+        L.w4a16_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P]
+        L.w4a16_selftest_wait_timeout.restype = I
         L.w4a16_sp_packed_bytes.argtypes = [I, I, I]
         L.w4a16_sp_packed_bytes.restype = Z
         L.w4a16_sp_pack.argtypes = [P, P, P, P, I, I, I, P, P]
@@ -160,6 +163,13 @@ def gemm_ws(x, packed, scales_packed, N, group_size, workspace, y=None, stream=N
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "w4a16_gemm_ws")
     return y
+
+
+def selftest_wait_timeout(limit_ns, workspace=None, stream=None):
+    """Launch one warp whose bounded wait on a barrier that nothing completes gives up
+    after limit_ns and sets the workspace's error word (see check_device_status)."""
+    _check(lib().w4a16_selftest_wait_timeout(_ptr(workspace), int(limit_ns), _stream(stream)),
+           "w4a16_selftest_wait_timeout")
 
 
 def check_device_status(workspace=None, stream=None):
