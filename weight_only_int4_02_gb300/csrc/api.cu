@@ -74,9 +74,11 @@ constexpr int kMinItersPerCta = 4;
 struct SplitCost {
     double ring, prefetched_us, streamed_us, fixup_us, fixup_row_us;
 };
-constexpr SplitCost kSplit16 = {8, 0.15, 0.40, 1.4, 0.03};      // 16- and 32-row tiles, 16 KB stages
-constexpr SplitCost kSplit64 = {0, 0.525, 0.525, 2.6, 0.04};    // 64-row tile pairs, 16 KB stages
-constexpr SplitCost kSplit128 = {0, 0.375, 0.375, 2.9, 0.02};   // 128-row tile pairs, 8 KB stages
+// The per-row fix-up costs are the fitted ones divided by the ratio of warps that now
+// reduce a unit's last tile (the whole CTA, 15 or 23 warps, against the 4 epilogue warps).
+constexpr SplitCost kSplit16 = {8, 0.15, 0.40, 1.4, 0.006};     // 16- and 32-row tiles, 16 KB stages
+constexpr SplitCost kSplit64 = {0, 0.525, 0.525, 2.6, 0.008};   // 64-row tile pairs, 16 KB stages
+constexpr SplitCost kSplit128 = {0, 0.375, 0.375, 2.9, 0.006};  // 128-row tile pairs, 8 KB stages
 constexpr SplitCost kSplit256 = {0, 0.59, 0.59, 0.0, 0.059};    // 256-row tile pairs, 8 KB stages (prefill)
 
 struct DeviceState {

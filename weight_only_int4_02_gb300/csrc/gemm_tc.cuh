@@ -305,18 +305,19 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
 // Split-K fix-up of a tile by its last contributor: Y = the sum of every
 // contributor's FP32 partial, added in contributor (CTA) order. Partials are
 // column-major ([TM][128] per slot), so one 16-byte load brings four rows of a
-// column: thread j of the four epilogue warps takes rows 4(j mod 32) .. +3 of
-// columns j/32, j/32 + 4, j/32 + 8, ... A round issues L4 such loads (L4/NCP
-// columns of NCP contributors) before any is added, so it costs one global
-// round trip. n_base is the tile's first output feature.
+// column: thread j of the nw participating warps (the four epilogue warps, or the
+// whole CTA for its last tile) takes rows 4(j mod 32) .. +3 of columns j/32,
+// j/32 + nw, j/32 + 2nw, ... A round issues L4 such loads (L4/NCP columns of NCP
+// contributors) before any is added, so it costs one global round trip. n_base is
+// the tile's first output feature.
 template <int TM, int NCP, int L4, bool EPI, bool BF>
 __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
-                                           int n_base)
+                                           int n_base, int nw)
 {
     constexpr int CPR = L4 / NCP;
     const int rg = threadIdx.x & 31;
     const int m_first = threadIdx.x >> 5;
-    const int ncols = valid > m_first ? (valid - m_first + 3) >> 2 : 0;   // columns m_first + 4q, q < ncols
+    const int ncols = valid > m_first ? (valid - m_first + nw - 1) / nw : 0;   // columns m_first + nw*q, q < ncols
     const int n = n_base + 4 * rg;
     float b4[4] = {0.f, 0.f, 0.f, 0.f};
     if (EPI && p.bias && n < p.N)
@@ -333,7 +334,7 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
                 const float* base = p.partials + (size_t)slot_of(p, min(cc, c_hi), t, rank) * TM * kTileN + 4 * rg;
 #pragma unroll
                 for (int e = 0; e < CPR; ++e) {
-                    const int m = m_first + 4 * (q0 + e);
+                    const int m = m_first + nw * (q0 + e);
                     v[u][e] = (cc <= c_hi && q0 + e < ncols)
                                   ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)m * kTileN))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -355,7 +356,7 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
 #pragma unroll
             for (int e = 0; e < CPR; ++e) {
                 if (q0 + e >= ncols) continue;
-                const int m = m0 + m_first + 4 * (q0 + e);
+                const int m = m0 + m_first + nw * (q0 + e);
                 __half* out = p.y + (size_t)m * p.N + n;
                 if constexpr (EPI) {
                     const size_t ri = (size_t)m * p.N + n;
@@ -374,6 +375,22 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
             }
         }
     }
+}
+
+// fix_reduce with the contributor batch chosen by the contributor count.
+template <int TM, int KSUB, bool EPI, bool BF>
+__device__ __forceinline__ void fix_tile(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
+                                         int n_base, int nw)
+{
+    // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
+    constexpr int L4 = KSUB == 4 ? 8 : 16;
+    const int ncontrib = c_hi - c_lo + 1;
+    if (ncontrib <= 2)
+        fix_reduce<TM, 2, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base, nw);
+    else if (ncontrib <= 4)
+        fix_reduce<TM, 4, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base, nw);
+    else
+        fix_reduce<TM, 8, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base, nw);
 }
 
 // EPI: the instantiation with the fused epilogue (bias, activation, residual);
@@ -434,6 +451,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         }
         mbar_init(teardown_bar, 1);
         *abort_flag = 0;
+        reinterpret_cast<int*>(smem + C::kOffMisc + 24)[0] = 0;   // no deferred fix-up yet
         fence_mbar_init();
     }
     if (warp == C::kProdXWarp && lane == 0) prefetch_tmap(&tmap_x);
@@ -813,18 +831,15 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                 }
                 named_bar_sync(1, 128);
                 const int last = *last_flag;
-                if (last) {
+                if (last && i >= it_end) {
+                    // the CTA's final tile: every warp reduces it once all roles are done
+                    if (threadIdx.x == 0) {
+                        int* dfr = reinterpret_cast<int*>(smem + C::kOffMisc + 24);
+                        dfr[0] = 1; dfr[1] = t; dfr[2] = c_lo; dfr[3] = c_hi;
+                    }
+                } else if (last) {
                     __threadfence();
-                    const int ncontrib = c_hi - c_lo + 1;
-                    const int n_base = n - n_in;
-                    // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
-                    constexpr int L4 = KSUB == 4 ? 8 : 16;
-                    if (ncontrib <= 2)
-                        fix_reduce<TM, 2, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
-                    else if (ncontrib <= 4)
-                        fix_reduce<TM, 4, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
-                    else
-                        fix_reduce<TM, 8, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base);
+                    fix_tile<TM, KSUB, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n - n_in, 4);
                 }
                 named_bar_sync(1, 128);
             }
@@ -833,6 +848,18 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    {
+        // the split-K fix-up of the CTA's final tile, if it arrived last, by all warps
+        const int* dfr = reinterpret_cast<const int*>(smem + C::kOffMisc + 24);
+        if (dfr[0]) {
+            __threadfence();
+            const int t = dfr[1];
+            const int nb = t / p.m_tiles, mt = t - nb * p.m_tiles;
+            const int m0 = mt * TM;
+            fix_tile<TM, KSUB, EPI, BF>(p, t, rank, dfr[2], dfr[3], min(TM, p.M - m0), m0,
+                                        (nb * CL + rank) * kTileN, C::kThreads / 32);
+        }
+    }
     // No CTA may leave while its peer can still write into its X ring or arrive on
     // its barriers.
     if constexpr (CL > 1) cluster_sync();
