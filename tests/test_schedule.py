@@ -206,11 +206,10 @@ def test_shared_memory_and_tmem_layout_fits():
 
 def test_small_layer_splits_are_tile_aligned():
     """With fewer tiles than SMs, every tile has the same number of contributors
-    and unit boundaries fall on tile boundaries; the measured best splits of the
-    decode layers are chosen (quarters up to M = 8 and halves at M = 16 and 32 for
-    4096x4096; whole tiles for 12288x4096; quarters for 4096x11008 up to M = 32;
-    whole tile pairs, halves, thirds or quarters at M = 64 and 128; whole tile
-    pairs or halves for the 256-row prefill tiles)."""
+    and unit boundaries fall on tile boundaries; the cost model's splits of the
+    decode layers (measured against the alternatives on GB300): quarters for
+    4096x4096 and 4096x11008 from M = 1 to 128, whole tiles for 12288x4096, whole
+    tile pairs or halves for the 256-row prefill tiles."""
     expect = {(1, 4096, 4096): 4, (8, 4096, 4096): 4, (16, 4096, 4096): 4, (32, 4096, 4096): 4,
               (1, 12288, 4096): 1, (16, 12288, 4096): 1, (1, 4096, 11008): 4, (16, 4096, 11008): 4,
               (32, 4096, 11008): 4, (64, 4096, 4096): 4, (64, 12288, 4096): 1, (64, 4096, 11008): 4,
