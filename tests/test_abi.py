@@ -33,6 +33,29 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in names
 
 
+def declared_arities():
+    """{function: number of parameters} from the header's declarations."""
+    text = open(os.path.join(ROOT, "include", "w4a16.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(w4a16_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    from weight_only_int4_02_gb300 import w4a16
+    arity = declared_arities()
+    assert len(arity) >= 20
+    for name in w4a16.EXPORTS:
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            assert arity[name] == 0, name
+        else:
+            assert len(fn.argtypes) == arity[name], (name, len(fn.argtypes), arity[name])
+
+
 def test_sizes(lib):
     assert lib.w4a16_layout_version() == 2
     assert lib.w4a16_packed_words(4096, 4096, 128) == 32 * 64 * 1024
