@@ -150,3 +150,32 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith(".py"):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+
+
+def test_binding_rejects_short_or_strided_buffers_before_any_launch(lib):
+    torch = pytest.importorskip("torch")
+    from weight_only_int4_02_gb300 import w4a16 as w
+    M, N, K, G = 4, 256, 512, 128
+    x = torch.zeros((M, K), dtype=torch.float16)
+    y = torch.zeros((M, N), dtype=torch.float16)
+    packed = torch.zeros(w.packed_words(K, N, G), dtype=torch.int32)
+    sp = torch.zeros(w.scales_elems(K, N, G), dtype=torch.float16)
+    w.check_buffers(x, packed, sp, N, G, y)                                  # exact sizes pass
+    for bad in [dict(packed=packed[:-1]), dict(scales_packed=sp[:-8]), dict(y=y[:, :-8]),
+                dict(y=torch.zeros((N, M), dtype=torch.float16).t()), dict(y=torch.zeros((M, N), dtype=torch.float32))]:
+        args = dict(packed=packed, scales_packed=sp, y=y)
+        args.update(bad)
+        with pytest.raises(w.W4A16Error) as e:
+            w.check_buffers(x, args["packed"], args["scales_packed"], N, G, args["y"])
+        assert e.value.status == w.ERR_INVALID_ARG
+    # the other formats' weight sizes
+    w.check_buffers(x, torch.zeros(w.w8_packed_bytes(K, N, G), dtype=torch.uint8), sp, N, G, y, "w8")
+    with pytest.raises(w.W4A16Error):
+        w.check_buffers(x, packed, sp, N, G, y, "w8")                       # 4-bit buffer for 8-bit codes
+    w.check_buffers(x, torch.zeros(w.sp_packed_bytes(K, N, G), dtype=torch.uint8), sp, N, G, y, "sparse")
+    zp = torch.zeros(w.zeros_bytes(K, N, G), dtype=torch.uint8)
+    w.check_buffers(x, packed, sp, N, G, y, "int4", zp)
+    with pytest.raises(w.W4A16Error):
+        w.check_buffers(x, packed, sp, N, G, y, "int4", zp[:-16])
+    # sizes the library rejects itself are left to it
+    w.check_buffers(x, packed[:1], sp[:1], N, 48, y)

@@ -107,6 +107,32 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def check_buffers(x, packed, scales_packed, N, group_size, y, weight_format="int4", zeros_packed=None):
+    """Raise W4A16Error(ERR_INVALID_ARG) before any launch when a buffer is smaller than
+    its shape needs or not contiguous (the C ABI sees only pointers). Sizes the
+    library rejects anyway (invalid K, N or group size) are left to it."""
+    M, K = x.shape
+    need_w = {"int4": packed_words(K, N, group_size) * 4, "w8": w8_packed_bytes(K, N, group_size),
+              "sparse": sp_packed_bytes(K, N, group_size)}[weight_format]
+    need_s = scales_elems(K, N, group_size) * 2
+    if need_w == 0 or need_s == 0:
+        return
+    checks = [(packed, need_w, "packed weights"), (scales_packed, need_s, "packed scales"), (y, M * N * 2, "y")]
+    if zeros_packed is not None:
+        checks.append((zeros_packed, zeros_bytes(K, N, group_size), "packed zero-points"))
+    for t, need, what in checks:
+        if not t.is_contiguous():
+            raise W4A16Error(ERR_INVALID_ARG, "%s is not contiguous" % what)
+        if _nbytes(t) < need:
+            raise W4A16Error(ERR_INVALID_ARG, "%s hold %d bytes, the shape needs %d" % (what, _nbytes(t), need))
+    if tuple(y.shape) != (M, N) or y.element_size() != 2:
+        raise W4A16Error(ERR_INVALID_ARG, "y must be a 16-bit [M][N] tensor")
+
+
 def layout_version():
     return lib().w4a16_layout_version()
 
@@ -149,6 +175,7 @@ def gemm(x, packed, scales_packed, N, group_size, y=None, stream=None):
     assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'int4')
     _check(lib().w4a16_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                             _stream(stream)), "w4a16_gemm")
     return y
@@ -159,6 +186,7 @@ def gemm_ws(x, packed, scales_packed, N, group_size, workspace, y=None, stream=N
     M, K = x.shape
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'int4')
     _check(lib().w4a16_gemm_ws(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "w4a16_gemm_ws")
@@ -191,6 +219,7 @@ def gemm_noalloc(x, packed, scales_packed, N, group_size, y=None, stream=None):
     assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'int4')
     _check(lib().w4a16_gemm_noalloc(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                     _stream(stream)), "w4a16_gemm_noalloc")
     return y
@@ -211,6 +240,7 @@ def gemm_fused(x, packed, scales_packed, N, group_size, bias=None, residual=None
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'int4')
     _check(lib().w4a16_gemm_fused(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                   _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                   _stream(stream)), "w4a16_gemm_fused")
@@ -247,6 +277,7 @@ def gemm_zp(x, packed, scales_packed, zeros_packed, N, group_size, bias=None, re
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'int4', zeros_packed)
     _check(lib().w4a16_gemm_zp(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(zeros_packed), _ptr(y), M, N, K,
                                group_size, _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace),
                                ws_bytes, _stream(stream)), "w4a16_gemm_zp")
@@ -286,6 +317,7 @@ def w8_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None, a
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'w8')
     _check(lib().w4a16_w8_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                _stream(stream)), "w4a16_w8_gemm")
@@ -305,6 +337,7 @@ def bf16_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None,
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'int4')
     _check(lib().w4a16_bf16_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                  _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                  _stream(stream)), "w4a16_bf16_gemm")
@@ -348,6 +381,7 @@ def sp_gemm(x, packed, scales_packed, N, group_size, bias=None, residual=None, a
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check_buffers(x, packed, scales_packed, N, group_size, y, 'sparse')
     _check(lib().w4a16_sp_gemm(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                _stream(stream)), "w4a16_sp_gemm")
