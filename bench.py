@@ -938,8 +938,11 @@ def main():
         run_case(args)
         return
     if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; the other ranks exit without work
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            line = run_reference(args)
+            line["n_gpus"] = world
+            print(json.dumps(line), flush=True)
         return
 
     import torch
