@@ -30,14 +30,22 @@ def tile_m_for(M):
     return 256
 
 
-def plan(M, N, K, G, sms=SMS):
+# weight formats: 4-bit (also per-group zero-points and BF16 activations, same stages),
+# 8-bit codes, 2:4 sparse 4-bit codes
+FORMATS = ("int4", "w8", "sparse")
+
+
+def plan(M, N, K, G, sms=SMS, fmt="int4"):
     tm = tile_m_for(M)
-    ksub = 4 if tm <= 64 else 2
+    if fmt == "sparse":
+        tm = min(tm, 128)
+    ksub = 2 if fmt in ("w8", "sparse") else (4 if tm <= 64 else 2)
+    xblocks = 4 if fmt == "sparse" else ksub
     cl = 2 if tm >= 64 else 1
     m_tiles, n_tiles, ng = ceil_div(M, tm), ceil_div(N, 128), ceil_div(K, G)
     n_blocks = ceil_div(n_tiles, cl)
     KC = ceil_div(ceil_div(K, 64), 4) * 4
-    iters = KC // ksub
+    iters = KC // xblocks
     total = n_blocks * m_tiles * iters
     units = min(sms, MAX_GRID) // cl
     work_tiles = n_blocks * m_tiles
@@ -62,8 +70,8 @@ def plan(M, N, K, G, sms=SMS):
         min_iters = max(4, iters // 2 if tm >= 64 else (iters // 4 if tm == 32 else 0))
         units = min(units, -(-total // min_iters))
     units = max(1, units)
-    return dict(tm=tm, ksub=ksub, cl=cl, m_tiles=m_tiles, n_tiles=n_tiles, n_blocks=n_blocks, KC=KC,
-                iters=iters, ng=ng, total=total, units=units, grid=units * cl)
+    return dict(tm=tm, ksub=ksub, xblocks=xblocks, fmt=fmt, cl=cl, m_tiles=m_tiles, n_tiles=n_tiles,
+                n_blocks=n_blocks, KC=KC, iters=iters, ng=ng, total=total, units=units, grid=units * cl)
 
 
 def cta_begin(P, c):
@@ -94,13 +102,17 @@ def segments(P, c):
         i += ke - kb
 
 
-def check_shape(M, N, K, G, sms=SMS):
+def check_shape(M, N, K, G, sms=SMS, fmt="int4"):
     """Every (weight tile, stage) is computed once; every global access of the
     producers, the partial slots and the counters stays inside its buffer; the
     reducer of a split tile reads exactly the slots its contributors wrote."""
-    P = plan(M, N, K, G, sms)
+    P = plan(M, N, K, G, sms, fmt)
     KC, ng, tm, ks, iters, cl = P["KC"], P["ng"], P["tm"], P["ksub"], P["iters"], P["cl"]
-    packed_words = P["n_tiles"] * KC * 1024
+    # packed words per (tile, sub-chunk) and sub-chunks per column, per format
+    chunk_words = {"int4": 1024, "w8": 2048, "sparse": 1536}[fmt]
+    sub_k = 128 if fmt == "sparse" else 64
+    KCp = KC * 64 // sub_k
+    packed_words = P["n_tiles"] * KCp * chunk_words
     scales_elems = P["n_tiles"] * ng * 128
     partial_floats = 2 * P["grid"] * tm * 128
     assert P["grid"] <= MAX_GRID
@@ -114,19 +126,20 @@ def check_shape(M, N, K, G, sms=SMS):
                 nt = nb * cl + rank
                 phantom = nt >= P["n_tiles"]
                 for st in range(kb, ke):
-                    k0 = st * ks * 64
+                    k0 = st * ks * sub_k
                     if not phantom:
                         key = (nt, mt, st)
                         assert key not in covered
                         covered[key] = (c, rank)
-                        w0 = (nt * KC + st * ks) * 1024            # one bulk copy of ks sub-chunks
-                        assert 0 <= w0 and w0 + ks * 1024 <= packed_words
+                        w0 = (nt * KCp + st * ks) * chunk_words    # one bulk copy of ks sub-chunks
+                        assert 0 <= w0 and w0 + ks * chunk_words <= packed_words
+                        assert (w0 * 4) % 16 == 0                  # bulk-copy source alignment
                         g0 = min(k0 // G, ng - 1)
-                        g1 = min((k0 + ks * 64 - 1) // G, ng - 1)
-                        assert 1 <= g1 - g0 + 1 <= 2 * ks          # fits the scale slot
+                        g1 = min((k0 + ks * sub_k - 1) // G, ng - 1)
+                        assert 1 <= g1 - g0 + 1 <= ks * sub_k // 32  # fits the scale slot
                         e0 = (nt * ng + g0) * 128
                         assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
-                    for j in range(ks):
+                    for j in range(P["xblocks"]):
                         assert ((k0 + j * 64) * 2) % 16 == 0    # TMA inner coordinate, 16-byte aligned
                     assert mt * tm < M
                 split = kb != 0 or ke != iters
@@ -167,6 +180,12 @@ def test_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
     check_shape(M, N, K, G)
 
 
+@pytest.mark.parametrize("fmt", ["w8", "sparse"])
+@pytest.mark.parametrize("M,N,K,G", [s for s in SHAPES if s[0] <= 1024])
+def test_schedule_of_other_weight_formats(M, N, K, G, fmt):
+    check_shape(M, N, K, G, fmt=fmt)
+
+
 @pytest.mark.parametrize("sms", [1, 7, 148, 160])
 def test_schedule_other_sm_counts(sms):
     for shp in [(16, 4096, 4096, 128), (1, 256, 16384, 128), (4096, 5120, 13824, 128), (3, 136, 200, 200)]:
@@ -178,30 +197,61 @@ def _constexpr(src, name):
     return m.group(1)
 
 
-def test_shared_memory_and_tmem_layout_fits():
-    """Mirror of TcCfg: stage rings, barriers, alignment and TMEM columns."""
+def tc_cfg(tm, ks, fmt):
+    """Mirror of TcCfg<TM, KSUB, FMT> (fmt: int4, zp, bf16, w8, sparse)."""
+    sp, w8, zp = fmt == "sparse", fmt == "w8", fmt == "zp"
+    sub_k = 128 if sp else 64
+    stage_k = ks * sub_k
+    xblocks = stage_k // 64
+    xblock = tm * 128
+    xbytes = xblocks * xblock
+    pk = ks * (8192 if w8 else 6144 if sp else 4096)
+    sc = (stage_k // 32) * 256
+    zpb = (stage_k // 32) * 64 if zp else 0
+    SW = (4 if tm >= 128 else 8) if (w8 or sp) else (8 if (tm <= 32 or ks == 2) else 6)
+    SX = min(8, (220 * 1024 - SW * (pk + sc + zpb)) // xbytes)
+    dbufs = 2 if tm <= 128 else 1
+    slot = ks * 32 + (ks * 4 * 8 if sp else 0)
+    A = 4 if (512 - dbufs * tm) // slot >= 4 else 2
+    off_pk = SX * xbytes
+    off_sc = off_pk + SW * pk
+    off_zp = off_sc + SW * sc
+    off_bar = off_zp + SW * zpb
+    nbars = 2 * SW + 2 * SX + 2 * A + 4 + 1
+    smem = off_bar + nbars * 8 + 64 + 1024
+    return dict(SW=SW, SX=SX, A=A, slot=slot, dbufs=dbufs, xblock=xblock, off_pk=off_pk, off_sc=off_sc,
+                off_zp=off_zp, off_bar=off_bar, smem=smem, dcol=A * slot, threads=32 * (4 + 4 * ks + 3))
+
+
+CONFIGS = ([(tm, ks, f) for (tm, ks) in ((16, 4), (32, 4), (64, 4), (128, 2), (256, 2)) for f in ("int4", "zp", "bf16")]
+           + [(tm, 2, "w8") for tm in (16, 32, 64, 128, 256)] + [(tm, 2, "sparse") for tm in (16, 32, 64, 128)])
+
+
+@pytest.mark.parametrize("tm,ks,fmt", CONFIGS)
+def test_shared_memory_and_tmem_layout_fits(tm, ks, fmt):
+    """Mirror of TcCfg for every instantiated kernel: stage rings, barriers,
+    alignment, TMEM columns, threads."""
     src = open(os.path.join(CSRC, "gemm_tc.cuh")).read()
     assert _constexpr(src, "kChunkBytes") == "4096" and _constexpr(src, "kKPad") == "4"
-    for tm, ks in ((16, 4), (32, 4), (64, 4), (128, 2), (256, 2)):
-        xblock = tm * 128
-        xb, pk, sc = ks * xblock, ks * 4096, 2 * ks * 256
-        SW = 8 if (tm <= 32 or ks == 2) else 6
-        SX = min(8, (220 * 1024 - SW * (pk + sc)) // xb)
-        dbufs = 2 if tm <= 128 else 1
-        A = 4 if (512 - dbufs * tm) // (ks * 32) >= 4 else 2
-        assert SW % 2 == 0 and A % 2 == 0
-        assert SW >= 2 and SX >= 2 and A >= 2, (tm, SW, SX, A)
-        off_pk = SX * xb
-        off_sc = off_pk + SW * pk
-        off_bar = off_sc + SW * sc
-        nbars = 2 * SW + 2 * SX + 2 * A + 4 + 1
-        smem = off_bar + nbars * 8 + 64 + 1024
-        assert smem <= 227 * 1024, (tm, smem)
-        assert xblock % 1024 == 0 and off_pk % 16 == 0 and off_sc % 16 == 0 and off_bar % 8 == 0
-        assert A * ks * 32 + dbufs * tm <= 512
-        assert SW % 2 == 0 and A % 2 == 0
-        threads = 32 * (4 + 4 * ks + 3)
-        assert threads <= 1024
+    c = tc_cfg(tm, ks, fmt)
+    assert c["SW"] % 2 == 0 and c["A"] % 2 == 0                     # rings shared by two teams in turn
+    assert c["SW"] >= 2 and c["SX"] >= 2 and c["A"] >= 2, c
+    assert c["smem"] <= 227 * 1024, c
+    assert c["xblock"] % 1024 == 0                                  # 128-byte swizzle atoms
+    assert c["off_pk"] % 16 == 0 and c["off_sc"] % 16 == 0 and c["off_zp"] % 16 == 0 and c["off_bar"] % 8 == 0
+    assert c["dcol"] + c["dbufs"] * tm <= 512
+    assert c["threads"] <= 1024
+
+
+def test_layout_mirror_matches_the_compiled_sizes():
+    """Shared-memory bytes of a few configurations as the compiled TcCfg reports them."""
+    assert tc_cfg(16, 4, "int4")["smem"] == 214408
+    assert tc_cfg(64, 4, "int4")["smem"] == 210200
+    assert tc_cfg(128, 2, "int4")["smem"] == 206184
+    assert tc_cfg(16, 2, "w8")["smem"] == 173480
+    assert tc_cfg(256, 2, "w8")["smem"] == 201992
+    assert tc_cfg(16, 2, "sparse")["smem"] == 181640
+    assert tc_cfg(128, 2, "sparse")["smem"] == 189672
 
 
 def test_small_layer_splits_are_tile_aligned():
