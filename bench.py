@@ -832,30 +832,38 @@ def run_e2e(per_case, G, dev, K, W, world):
 
 # --------------------------------------------------------------------------- reference arm (oracle)
 def run_reference(args):
+    """The oracle on the host cores. Each step is one case of the workload in turn (all
+    rows, every s-th output column, s sized so that the whole run takes about 90 s of
+    oracle time whatever --steps is), so that the driver's full step count still ends
+    within a few minutes."""
     import oracle
     oracle.build()
     wl = inputs.WORKLOADS[args.workload]
     threads = os.cpu_count() or 1
     cache = {}
     cases = wl["cases"]
+    G, mult, outl = wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0)
     total = sum(flops(*c) for c in cases)
-    t, done = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), 1024,
-                                threads, cache)
+    t, done = oracle_sample_run(cases, G, mult, outl, 1024, threads, cache)   # calibration
     rate = done / max(t, 1e-9)
-    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))   # whole run within a few minutes
-    stride = max(1, int(total / max(rate * budget, 1.0)))
-    for _ in range(args.warmup):
-        oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride, threads,
-                          cache)
+    budget = min(10.0, 90.0 / max(1, args.steps + args.warmup))             # oracle seconds per step
+    strides = {c: max(1, int(flops(*c) / max(rate * budget, 1.0))) for c in cases}
+
+    def step(i):
+        c = cases[i % len(cases)]
+        return oracle_sample_run([c], G, mult, outl, strides[c], threads, cache)
+
+    for i in range(args.warmup):
+        step(i)
     t_all, d_all = 0.0, 0
-    for _ in range(args.steps):
-        t, d = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride,
-                                 threads, cache)
+    for i in range(args.steps):
+        t, d = step(args.warmup + i)
         t_all += t
         d_all += d
     v = d_all / t_all / 1e12
-    sample = ("CPU oracle (FP64 C, %d threads): per step every case of the workload, all rows, every %d-th "
-              "output column (%.3g of the workload's flops)" % (threads, stride, d_all / args.steps / total))
+    sample = ("CPU oracle (FP64 C, %d threads): per step one of the workload's %d cases in turn, all rows, every "
+              "s-th output column (s = %d .. %d; %.3g of the workload's flops over the run)"
+              % (threads, len(cases), min(strides.values()), max(strides.values()), d_all / total))
     return {"impl": "reference", "metric": "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM/tensor roofline",
             "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_all / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
