@@ -340,8 +340,9 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
  *   fixed device array of W4A16_NOALLOC_MAX_BYTES inside the library, held by
  *   every GPU that loads the library until the process exits. A shape whose
  *   scratch would exceed it returns W4A16_ERR_WORKSPACE with nothing launched
- *   (on a 152-SM GB300 this admits every shape with M <= 32, and larger M
- *   where the dispatcher uses few CTAs, such as 4096x4096 up to M = 128).
+ *   (on a 152-SM GB300 this admits every shape with M <= 32; at larger M only
+ *   shapes the dispatcher gives few split tiles, such as 4096x12288 at M = 64;
+ *   4096x4096 at M = 64 needs 8 MiB + 4352 bytes and is rejected).
  *   The first call on each device looks the array's device address up; make
  *   that first call before any stream capture.
  *   Each call enqueues a clear of the array's error word and counters, then the

@@ -271,3 +271,23 @@ def test_small_layer_splits_are_tile_aligned():
         assert P["units"] == work_tiles * s, (M, N, K, P["units"])
         for t in range(work_tiles):
             assert cta_begin(P, t * s) == t * P["iters"]
+
+
+def test_no_alloc_scratch_admission():
+    """The fixed 8 MiB scratch of the no-allocation entry point holds the error word,
+    the counters and two FP32 partial slots per CTA of the plan: on 152 SMs every
+    decode layer fits up to M = 32; at M = 64 only the 12288-wide layer (whole tiles,
+    no split); at M = 128 none (the rejected shapes return a workspace error)."""
+    limit, partials_off = 8 << 20, 256 + 4 * MAX_GRID
+
+    def need(M, N, K):
+        P = plan(M, N, K, 128)
+        return partials_off + 2 * P["grid"] * P["tm"] * 128 * 4
+
+    layers = sorted(set((n, k) for (_, k, n) in inputs.WORKLOADS["llama2_7b_decode_sweep"]["cases"]))
+    for M in (1, 16, 32, 64, 128):
+        for (N, K) in layers:
+            fits = need(M, N, K) <= limit
+            assert fits == (M <= 32 or (M == 64 and N == 12288)), (M, N, K, need(M, N, K))
+    assert need(64, 4096, 4096) == limit + partials_off
+    assert need(128, 22016, 4096) > limit and need(16, 4096, 4096) <= limit
