@@ -53,7 +53,7 @@ typedef struct CUstream_st* w4a16_stream_t;
 typedef enum {
     W4A16_OK = 0,
     W4A16_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or group size is invalid */
-    W4A16_ERR_UNSUPPORTED = 2,  /* the device is not sm_103 / sm_100 class             */
+    W4A16_ERR_UNSUPPORTED = 2,  /* the device is not compute capability 10.3 (sm_103)  */
     W4A16_ERR_CUDA = 3,         /* a CUDA runtime call failed; code in w4a16_last_cuda_error() */
     W4A16_ERR_TIMEOUT = 4,      /* a kernel gave up waiting on one of its own pipeline barriers */
     W4A16_ERR_WORKSPACE = 5     /* the caller's workspace is smaller than w4a16_workspace_bytes() */
