@@ -1,5 +1,5 @@
 #!/usr/bin/env python3
-"""Benchmark of the W4A16 matmul on one GB300 (or N replicas under torchrun).
+"""Benchmark of the W4A16 matmul on one GB300.
 
 One step = one pass of the workload's GEMMs (default: the Llama-2-7B-like
 decode sweep, M in {1..128} x the four layer shapes, group 128), each reading
@@ -8,10 +8,14 @@ than L2 holds. Steps are replayed from CUDA Graphs with an event node around
 every launch, so per-kernel durations come from CUDA events on the launching
 stream. Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+  python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
---impl reference times the CPU oracle (test infrastructure) on the host cores
-on a bounded sample of the same workload.
+The GPU arm runs on one GPU only: with --gpus above 1, or under a launcher that
+sets WORLD_SIZE above 1, it exits with an error before any CUDA work (the 2-CTA
+cluster kernels load X by TMA multicast within one GPU's memory, and nothing here
+is written for several GPUs). --impl reference times the CPU oracle (test
+infrastructure) on the host cores on a bounded sample of the same workload; it
+touches no GPU, and under a multi-process launcher rank 0 alone runs it.
 """
 import argparse
 import ctypes
@@ -248,30 +252,21 @@ def cpu_baseline(wl, budget_s=15.0):
 
 
 # --------------------------------------------------------------------------- our arm
-def max_over_ranks(value, world, device):
-    """The largest value over the replicas (the slowest one sets the job's time);
-    the value itself when there is one rank. device: where the all-reduce tensor
-    lives (the GPU for NCCL, "cpu" for gloo)."""
-    if world <= 1:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
+def single_gpu_refusal(gpus, env):
+    """The error text when the GPU arm is asked for more than one GPU, else None."""
+    world = int(env.get("WORLD_SIZE", "1") or "1")
+    if gpus > 1 or world > 1:
+        return ("bench.py runs the W4A16 kernels on one GPU only (asked for --gpus %d, WORLD_SIZE %d); "
+                "run it without a multi-process launcher and with --gpus 1" % (gpus, world))
+    return None
 
 
-def job_throughput(units_per_replica, world, seconds):
-    """Whole-job throughput: every replica processes its own units (weak scaling)."""
-    return units_per_replica * world / seconds
-
-
-def run_ours(args, rank, world):
+def run_ours(args):
     import torch
     from weight_only_int4_02_gb300 import w4a16
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     wl = inputs.WORKLOADS[args.workload]
     G = wl["group_size"]
     cases = wl["cases"]
@@ -333,10 +328,8 @@ def run_ours(args, rank, world):
         graphs[i % pool].replay()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
@@ -346,11 +339,8 @@ def run_ours(args, rank, world):
     t1.record()
     torch.cuda.synchronize()
     wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
     clocks = sampler.stop(wall0, wall1)
-    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    ms_step = ms_total / K
+    ms_step = t0.elapsed_time(t1) / K
     status = w4a16.check_device_status()
     if status != w4a16.OK:
         raise RuntimeError("a kernel wait timed out in the timed region")
@@ -362,7 +352,7 @@ def run_ours(args, rank, world):
             grp_ms[gi, b] = cud.elapsed_ms(evs[gi][b], evs[gi][b + 1])
     grp_mean = grp_ms.mean(axis=0)
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
-    value = job_throughput(step_flops, world, ms_step * 1e-3) / 1e12
+    value = step_flops / (ms_step * 1e-3) / 1e12
 
     # ---- per kernel instance (all launches of one M use one instance) and per M
     kernels = {}
@@ -433,17 +423,17 @@ def run_ours(args, rank, world):
         per_m_out.append(entry)
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(per_case, G, dev, K, args.warmup, world)
+    e2e = run_e2e(per_case, G, dev, K, args.warmup)
 
     out = {
         "metric": "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM/tensor roofline",
-        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
         "config": {"workload": args.workload, "gemms_per_step": len(per_case),
                    "shapes": "M in %s x (K,N) in %s, group %d" % (
                        sorted(set(c["M"] for c in per_case)), sorted(set((c["K"], c["N"]) for c in per_case)), G),
-                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "parallelism": "single-gpu",
                    "l2": "inputs larger than L2: every GEMM reads its own copy of the packed weights "
                          "(%.0f MB distinct per step vs 129 MB L2)" % (distinct_bytes / 1e6),
                    "timing": "CUDA Graph per step with an event node at every change of M; per-kernel "
@@ -469,7 +459,7 @@ def run_ours(args, rank, world):
         out["w8a16"] = w8_probe(G)
         out["bf16_activations"] = bf16_probe(G)
         out["sparse_2to4"] = sparse_probe(G)
-    if rank == 0 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
 
@@ -779,7 +769,7 @@ def fp16_baseline(per_case, dev, reps):
         return None
 
 
-def run_e2e(per_case, G, dev, K, W, world):
+def run_e2e(per_case, G, dev, K, W):
     """Same metric through the public API with host buffers: per step, every GEMM's X from
     pinned host memory to the device (one copy of the step's X, gathered in one pinned
     buffer), the GEMMs, and every Y back to pinned host memory (one copy), all inside the
@@ -815,18 +805,16 @@ def run_e2e(per_case, G, dev, K, W, world):
     for _ in range(max(W, 1)):
         g.replay()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(K):
         g.replay()
     b.record()
     torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b) / K, world, dev)
+    ms = a.elapsed_time(b) / K
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
     ok = all(torch.equal(yh, c["y"].cpu()) for c, yh in zip(per_case, ys_h))   # the device-timed run's Y
-    return {"value": step_flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+    return {"value": step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "outputs_match_device": ok}
 
 
@@ -938,11 +926,15 @@ def main():
                     help="weight format of --case: 4-bit codes, 8-bit codes, or 2:4 sparse 4-bit codes")
     args = ap.parse_args()
     if args.warmup < 3:
-        args.warmup = 3
+        ap.error("--warmup must be at least 3 steps (asked for %d)" % args.warmup)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 
     if args.case:
+        refusal = single_gpu_refusal(args.gpus, os.environ)
+        if refusal:
+            print(refusal, file=sys.stderr, flush=True)
+            sys.exit(2)
         run_case(args)
         return
     if args.impl == "reference":
@@ -953,15 +945,12 @@ def main():
             print(json.dumps(line), flush=True)
         return
 
-    import torch
-    if world > 1:
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        torch.distributed.init_process_group("nccl")
-    out = run_ours(args, rank, world)
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    refusal = single_gpu_refusal(args.gpus, os.environ)
+    if refusal:
+        print(refusal, file=sys.stderr, flush=True)
+        sys.exit(2)
+    out = run_ours(args)
+    print(json.dumps(out), flush=True)
 
 
 if __name__ == "__main__":

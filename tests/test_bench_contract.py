@@ -74,3 +74,25 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_gpu_arm_refuses_more_than_one_gpu():
+    """The GPU arm is single-GPU: asked for several GPUs (by flag or by a launcher's
+    WORLD_SIZE) it exits non-zero with a plain message, before any CUDA work."""
+    assert bench.single_gpu_refusal(1, {}) is None
+    assert bench.single_gpu_refusal(1, {"WORLD_SIZE": "1"}) is None
+    assert "one GPU" in bench.single_gpu_refusal(2, {})
+    assert "one GPU" in bench.single_gpu_refusal(1, {"WORLD_SIZE": "2"})
+    for argv, env in ((["--gpus", "2"], {}), ([], {"WORLD_SIZE": "2", "RANK": "0"})):
+        out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + argv + ["--steps", "1"],
+                             capture_output=True, text=True, timeout=300, cwd=ROOT,
+                             env=dict(os.environ, CUDA_VISIBLE_DEVICES="", **env))
+        assert out.returncode != 0
+        assert "one GPU only" in out.stderr
+        assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def test_warmup_below_three_is_an_error():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode != 0 and "at least 3" in out.stderr
