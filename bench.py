@@ -453,6 +453,8 @@ def run_ours(args):
         "byte_ratio_fp16_over_w4g128": fp16_over_int4_byte_ratio(G),
     }
     if args.workload == DEFAULT_WORKLOAD:
+        out["fp16_peak"] = fp16_peak_probe()
+        out["workloads"] = workloads_probe(G, peaks)
         out["fused_epilogue"] = fused_epilogue_probe(G)
         out["layer_chain"] = layer_chain_probe(G)
         out["zero_points"] = zero_point_probe(G)
@@ -740,6 +742,115 @@ def layer_chain_probe(G):
     return out
 
 
+def _gpu_codes_scales(K, N, G, seed, mult):
+    """Codes uniform on 0..15 and scales FP16(|N(0,1)| * mult), drawn on the GPU (the
+    distributions of the workloads; the 18432 x 73728 layer would take long on the host)."""
+    import torch
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    q = torch.randint(0, 16, (K, N), dtype=torch.uint8, device="cuda", generator=gen)
+    s = (torch.randn((n_groups(K, G), N), device="cuda", generator=gen).abs() * mult).half()
+    return q, s
+
+
+def _gpu_activations(M, K, seed, outlier_frac):
+    import torch
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    x = torch.randn((M, K), device="cuda", generator=gen)
+    if outlier_frac > 0.0:
+        x = torch.where(torch.rand((M, K), device="cuda", generator=gen) < outlier_frac, x * 20.0, x)
+    return x.half()
+
+
+def fp16_us_per_launch(x, weights, y, reps):
+    """torch.matmul(x, w) with FP16 weights, back to back over the weight copies: from a
+    CUDA Graph when cuBLAS can be captured, else launched eagerly between two events."""
+    import torch
+    try:
+        return graph_us_per_launch(lambda wt: torch.matmul(x, wt, out=y), weights, reps)
+    except RuntimeError:
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for r in range(reps):
+            torch.matmul(x, weights[r % len(weights)], out=y)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+
+def fp16_peak_probe(reps=10):
+    """FP16 dense tensor throughput of torch.matmul (cuBLAS) on 8192^3, best of reps:
+    the FP16 peak measured on this GPU in this run (the BF16 one is in MEASURED_PEAKS.json)."""
+    import torch
+    n = 8192
+    a = torch.randn((n, n), dtype=torch.float16, device="cuda")
+    b = torch.randn((n, n), dtype=torch.float16, device="cuda")
+    c = torch.empty((n, n), dtype=torch.float16, device="cuda")
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b, c
+    return {"tflops": 2 * n ** 3 / (best * 1e-3) / 1e12, "shape": [n, n, n], "ms": best, "of": "best of %d" % reps}
+
+
+def workloads_probe(G, peaks):
+    """Every other workload's headline shapes, each timed as a CUDA Graph of launches
+    back to back over rotating weight copies (more bytes than L2 unless one copy
+    already is): the single 16 x 4096 x 4096 GEMM, the 18432 x 73728 layer at
+    M = 1, 16, 128, and the four Llama-2-13B-like prefill layers at M = 1024 and 4096
+    (X with 1% outliers x20). Each entry: microseconds per launch, TFLOP/s, weight
+    GB/s, the roofline fraction (algorithmic bytes over the measured HBM copy rate,
+    or flops over the measured BF16 burst peak, whichever binds), the kernel the
+    dispatcher picked, and torch.matmul with FP16 weights of the same shape under
+    the same protocol."""
+    import torch
+    from weight_only_int4_02_gb300 import w4a16
+    groups = [("single_m16_4096x4096", 4096, 4096, 0.02, 0.0, (16,)),
+              ("large_layer_18432x73728", 18432, 73728, 0.01, 0.0, (1, 16, 128))]
+    groups += [("llama2_13b_prefill", k, n, 0.02, 0.01, (1024, 4096)) for (k, n) in inputs.LLAMA2_13B_LAYERS]
+    rows = []
+    for wi, (name, K, N, mult, outl, Ms) in enumerate(groups):
+        q, s = _gpu_codes_scales(K, N, G, 100 + wi, mult)
+        packed, sp = w4a16.pack(q, s, G)
+        del q, s
+        wb = packed.numel() * 4 + sp.numel() * 2
+        n_copies = max(1, int(-(-400e6 // wb)))
+        copies = [(packed, sp)] + [(packed.clone(), sp.clone()) for _ in range(n_copies - 1)]
+        del packed, sp
+        fb = K * N * 2
+        f_copies = max(1, int(-(-400e6 // fb)))
+        wf = [torch.randn((K, N), dtype=torch.float16, device="cuda") for _ in range(f_copies)]
+        for M in Ms:
+            x = _gpu_activations(M, K, 200 + M, outl)
+            y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+            fl = flops(M, K, N)
+            reps = max(2, min(40, int(2e12 // max(fl, 1)), int(4e9 // wb)))
+            us = graph_us_per_launch(
+                lambda c: w4a16.gemm(x, c[0], c[1], N, G, y=y, stream=torch.cuda.current_stream()), copies, reps)
+            us16 = fp16_us_per_launch(x, wf, y, reps)
+            path, tile, grid = w4a16.plan(M, N, K, G)
+            roof_s = roofline_seconds(M, K, N, G, peaks)
+            hbm_s = algorithmic_bytes(M, K, N, G) / (peaks["hbm_gbs"] * 1e9)
+            rows.append({"workload": name, "M": M, "K": K, "N": N, "us": us, "tflops": fl / (us * 1e-6) / 1e12,
+                         "weight_gbs": weight_bytes(K, N, G) / (us * 1e-6) / 1e9,
+                         "roofline_frac": roof_s / (us * 1e-6), "bound": "hbm" if hbm_s >= roof_s else "tensor",
+                         "kernel": ("w4a16_gemv_kernel<%d>" if path == 1 else "w4a16_tc_kernel<%d>") % tile,
+                         "fp16_us": us16, "speedup_vs_fp16": us16 / us, "launches_timed": reps})
+            del x, y
+        del copies, wf
+        torch.cuda.empty_cache()
+    if w4a16.check_device_status() != w4a16.OK:
+        raise RuntimeError("a kernel wait timed out")
+    return rows
+
+
 def fp16_baseline(per_case, dev, reps):
     """Mean time per M of torch.matmul with FP16 weights of the same shapes (own copy per case)."""
     import torch
@@ -770,38 +881,75 @@ def fp16_baseline(per_case, dev, reps):
 
 
 def run_e2e(per_case, G, dev, K, W):
-    """Same metric through the public API with host buffers: per step, every GEMM's X from
-    pinned host memory to the device (one copy of the step's X, gathered in one pinned
-    buffer), the GEMMs, and every Y back to pinned host memory (one copy), all inside the
-    timed region (one graph per step). Gathering the copies keeps the GEMMs back to back,
-    so each launch still overlaps the next (programmatic dependent launch)."""
+    """Same metric through the public API with host buffers: per step, every GEMM's X
+    from pinned host memory to the device, the GEMMs, and every Y back to pinned host
+    memory, all inside the timed region (one CUDA Graph per step). The copies run on
+    two side streams so that they overlap the GEMMs: the GEMMs go by groups of equal M,
+    largest M first; the first group's X is uploaded GEMM by GEMM and every later
+    group's X in one copy while earlier groups compute; each group's Y is downloaded in
+    one copy once its GEMMs are done, while later groups compute. What stays exposed
+    is the first GEMM's X and the last group's (smallest) Y."""
     import torch
     from weight_only_int4_02_gb300 import w4a16
-    x_sizes = [c["M"] * c["K"] for c in per_case]     # multiples of 8 elements: 16-byte aligned views
-    y_sizes = [c["M"] * c["N"] for c in per_case]
-    x_dev = torch.empty(sum(x_sizes), dtype=torch.float16, device="cuda")
-    y_dev = torch.empty(sum(y_sizes), dtype=torch.float16, device="cuda")
-    x_host = torch.empty(sum(x_sizes), dtype=torch.float16).pin_memory()
-    y_host = torch.empty(sum(y_sizes), dtype=torch.float16).pin_memory()
-    xs, ys, ys_h = [], [], []
+    order = sorted(range(len(per_case)), key=lambda i: (-per_case[i]["M"], i))
+    groups = []
+    for i in order:
+        if groups and per_case[groups[-1][0]]["M"] == per_case[i]["M"]:
+            groups[-1].append(i)
+        else:
+            groups.append([i])
+    x_sizes = {i: per_case[i]["M"] * per_case[i]["K"] for i in order}   # multiples of 8: 16-byte aligned views
+    y_sizes = {i: per_case[i]["M"] * per_case[i]["N"] for i in order}
+    x_dev = torch.empty(sum(x_sizes.values()), dtype=torch.float16, device="cuda")
+    y_dev = torch.empty(sum(y_sizes.values()), dtype=torch.float16, device="cuda")
+    x_host = torch.empty(sum(x_sizes.values()), dtype=torch.float16).pin_memory()
+    y_host = torch.empty(sum(y_sizes.values()), dtype=torch.float16).pin_memory()
+    xs, ys, ys_h, x_rng, y_rng = {}, {}, {}, {}, {}
     ox = oy = 0
-    for c, nx, ny in zip(per_case, x_sizes, y_sizes):
+    for i in order:
+        c, nx, ny = per_case[i], x_sizes[i], y_sizes[i]
         x_host[ox:ox + nx].copy_(c["x"].reshape(-1).cpu())
-        xs.append(x_dev[ox:ox + nx].view(c["M"], c["K"]))
-        ys.append(y_dev[oy:oy + ny].view(c["M"], c["N"]))
-        ys_h.append(y_host[oy:oy + ny].view(c["M"], c["N"]))
+        xs[i] = x_dev[ox:ox + nx].view(c["M"], c["K"])
+        ys[i] = y_dev[oy:oy + ny].view(c["M"], c["N"])
+        ys_h[i] = y_host[oy:oy + ny].view(c["M"], c["N"])
+        x_rng[i], y_rng[i] = (ox, ox + nx), (oy, oy + ny)
         ox += nx
         oy += ny
     h2d = x_host.numel() * 2
     d2h = y_host.numel() * 2
-    cap = torch.cuda.Stream()
+    # X copies: one per GEMM of the first group, one per later group; Y copies: one per group
+    x_chunks = [[i] for i in groups[0]] + groups[1:]
+    cap, up, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):
-        st = torch.cuda.current_stream()
-        x_dev.copy_(x_host, non_blocking=True)
-        for c, x, y in zip(per_case, xs, ys):
-            w4a16.gemm(x, c["packed"], c["sp"], c["N"], G, y=y, stream=st)
-        y_host.copy_(y_dev, non_blocking=True)
+        main = torch.cuda.current_stream()
+        up.wait_stream(main)
+        down.wait_stream(main)
+        ready = {}
+        with torch.cuda.stream(up):
+            for ch in x_chunks:
+                a, b = x_rng[ch[0]][0], x_rng[ch[-1]][1]
+                x_dev[a:b].copy_(x_host[a:b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(up)
+                for i in ch:
+                    ready[i] = ev
+        waited = set()
+        for grp in groups:
+            for i in grp:
+                if id(ready[i]) not in waited:
+                    main.wait_event(ready[i])
+                    waited.add(id(ready[i]))
+                c = per_case[i]
+                w4a16.gemm(xs[i], c["packed"], c["sp"], c["N"], G, y=ys[i], stream=main)
+            done = torch.cuda.Event()
+            done.record(main)
+            down.wait_event(done)
+            with torch.cuda.stream(down):
+                a, b = y_rng[grp[0]][0], y_rng[grp[-1]][1]
+                y_host[a:b].copy_(y_dev[a:b], non_blocking=True)
+        main.wait_stream(up)
+        main.wait_stream(down)
     for _ in range(max(W, 1)):
         g.replay()
     torch.cuda.synchronize()
@@ -813,9 +961,10 @@ def run_e2e(per_case, G, dev, K, W):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / K
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
-    ok = all(torch.equal(yh, c["y"].cpu()) for c, yh in zip(per_case, ys_h))   # the device-timed run's Y
+    ok = all(torch.equal(ys_h[i], per_case[i]["y"].cpu()) for i in order)   # the device-timed run's Y
     return {"value": step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "outputs_match_device": ok}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "outputs_match_device": ok,
+            "copies_per_step": {"h2d": len(x_chunks), "d2h": len(groups)}}
 
 
 # --------------------------------------------------------------------------- reference arm (oracle)

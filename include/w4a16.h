@@ -35,6 +35,17 @@
  *  - Group size G must be 32, 64 or 128, or equal to K (one scale per column);
  *    G = -1 is accepted as "equal to K". K must be a multiple of 8 (16-byte X
  *    rows) and N a multiple of 8 (16-byte Y rows).
+ *  - The GEMM kernels are launched with programmatic dependent launch: a GEMM
+ *    may start, and start streaming its packed weights, scales and zero-points,
+ *    before the kernel enqueued just ahead of it on the stream has finished; it
+ *    waits for that kernel before it reads x, bias or residual and before it
+ *    writes y. So the kernel enqueued immediately before a GEMM on the same
+ *    stream must not write that GEMM's packed weights, scales or zero-points.
+ *    The repack calls (w4a16_pack, w4a16_pack_zeros, w4a16_sp_pack,
+ *    w4a16_w8_pack) end with a kernel that writes nothing for this reason, so a
+ *    GEMM may follow them directly. After writing packed buffers with a kernel
+ *    of your own, enqueue another ordinary kernel (one launched without
+ *    programmatic serialization) or synchronise before the GEMM.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -307,8 +318,10 @@ w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint1
 /*
  * Synchronises `stream`, then reads and clears the error word that the kernels
  * set when one of their bounded waits gave up (W4A16_ERR_TIMEOUT), for the
- * given workspace (NULL = the library's own workspace of the current device).
- * After a timeout the workspace's split-K counters are reset as well.
+ * given workspace. NULL covers the library's own workspace of the current device
+ * and, once a w4a16_gemm_noalloc call has run on that device, the fixed array
+ * that call uses. After a timeout the split-K counters of the workspace (or
+ * array) are reset as well.
  */
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
 
@@ -322,11 +335,28 @@ w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
  */
 w4a16_status w4a16_selftest_wait_timeout(void* workspace, long long limit_ns, w4a16_stream_t stream);
 
-/* Which kernel and tile the dispatcher picks for a shape of the 4-bit FP16 format
- * (w4a16_gemm and w4a16_gemm_fused) on the current device: *path = 2 (the one
- * kernel built: per-weight scaling, dequantised weights in tensor memory; the
- * value 1 is retired); *tile_m = rows of X per tile; *grid = CTAs. */
+/* Which kernel the dispatcher picks for a shape of the 4-bit FP16 format
+ * (w4a16_gemm, w4a16_gemm_ws, w4a16_gemm_fused) on the current device. It picks
+ * path 1 by itself for one row of X and at most 4096 x 4096 weights (where it
+ * measured faster on GB300), path 2 otherwise:
+ *   *path = 1: the CUDA-core kernel for one to four rows of X ("Low-Precision
+ *              Quantization Kernels in Production" (llms.blog), section 2: the
+ *              activation vector held on chip, weights streamed, unpacked in
+ *              registers, group-scaled and reduced across a warp; section 5: at
+ *              batch 1 the matmul is a memory-bound GEMV). *tile_m = the rows of X
+ *              it is built for (1, 2 or 4); *grid = CTAs, one per block of 8, 16 or
+ *              32 output columns, each over the whole of K (no workspace is used).
+ *   *path = 2: the tensor-core kernel (dequantised weights in tensor memory,
+ *              tcgen05 MMA); *tile_m = rows of X per tile; *grid = CTAs.
+ * The other weight formats always run path 2. */
 w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid);
+
+/* Forces the dispatcher's choice for the 4-bit FP16 format, for tests and
+ * ablations (no counterpart in the pages): 0 = automatic (the default), 1 = the
+ * CUDA-core kernel for every shape it serves (M <= 4), 2 = the tensor-core kernel
+ * for every M. Applies to every later call in the process, on every device and host
+ * thread. Returns the previous setting, or -1 (nothing changed) for another value. */
+int w4a16_force_path(int path);
 
 /*
  * w4a16_gemm without any device allocation by the library or the caller. The
@@ -336,21 +366,24 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
  * implicit device-wide synchronisation.
  *   Arguments, layouts and results are those of w4a16_gemm; the caller still
  *   passes x, packed, scales_packed and y.
- *   The split-K scratch (error word, tile counters, FP32 partials) lives in one
- *   fixed device array of W4A16_NOALLOC_MAX_BYTES inside the library, held by
- *   every GPU that loads the library until the process exits. A shape whose
- *   scratch would exceed it returns W4A16_ERR_WORKSPACE with nothing launched
- *   (on a 152-SM GB300 this admits every shape with M <= 32; at larger M only
- *   shapes the dispatcher gives few split tiles, such as 4096x12288 at M = 64;
- *   4096x4096 at M = 64 needs 8 MiB + 4352 bytes and is rejected).
+ *   The split-K scratch of the tensor-core kernel (error word, tile counters,
+ *   FP32 partials) lives in one fixed device array of W4A16_NOALLOC_MAX_BYTES
+ *   inside the library, held by every GPU that loads the library until the
+ *   process exits. A shape whose scratch would exceed it returns
+ *   W4A16_ERR_WORKSPACE with nothing launched (on a 152-SM GB300 this admits
+ *   every shape with M <= 32; at larger M only shapes the dispatcher gives few
+ *   split tiles, such as 4096x12288 at M = 64; 4096x4096 at M = 64 needs
+ *   8 MiB + 4352 bytes and is rejected). Shapes the CUDA-core kernel takes
+ *   (M <= 4) use no scratch at all.
  *   The first call on each device looks the array's device address up; make
  *   that first call before any stream capture.
- *   Each call enqueues a clear of the array's error word and counters, then the
- *   GEMM. Every call on a device shares the one array: calls whose work overlaps
- *   on the GPU (different streams, no ordering between them) race and give
- *   wrong results; order them on one stream or with events.
+ *   A call that uses the scratch enqueues a clear of its tile counters, then the
+ *   GEMM; the error word is left for w4a16_check_device_status(NULL, ...), which
+ *   reads and clears it. Arguments are checked before anything is enqueued: a
+ *   refused call touches nothing. Every call on a device shares the one array:
+ *   calls whose work overlaps on the GPU (different streams, no ordering between
+ *   them) race and give wrong results; order them on one stream or with events.
  *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
- *   w4a16_check_device_status(NULL, ...) does not cover this array.
  */
 #define W4A16_NOALLOC_MAX_BYTES ((size_t)8 << 20)
 w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* packed,

@@ -52,3 +52,18 @@ def check_within_fused(y_gpu, y_ref, z_ref, absum, bias_abs, resid_abs, what="",
                              % (what, int(bad.sum()), bad.size, worst, idx.tolist(),
                                 [y[tuple(i)] for i in idx], [y_ref[tuple(i)] for i in idx]))
     return float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+
+
+class forced_path:
+    """Run a block with the library's dispatcher forced to one path (1: the CUDA-core
+    kernel where it applies, 2: the tensor-core kernel); the previous setting is
+    restored on exit."""
+
+    def __init__(self, w, path):
+        self.w, self.path = w, path
+
+    def __enter__(self):
+        self.prev = self.w.force_path(self.path)
+
+    def __exit__(self, *exc):
+        self.w.force_path(self.prev)

@@ -236,14 +236,24 @@ def test_edge_sweep(w, oracle_mod):
 def test_device_plan_matches_host_mirror(w):
     """The dispatcher on the device picks the grid that the schedule mirror (whose
     coverage and bounds the CPU tests check) computes for the same SM count."""
-    from tests.test_schedule import plan as mirror_plan
+    from tests.test_schedule import dispatch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shapes = [(m, n, k) for (m, k, n) in inputs.WORKLOADS["llama2_7b_decode_sweep"]["cases"] if m <= 32]
-    shapes += [(1, 256, 16384), (3, 136, 200), (17, 4096, 4000), (1, 73728, 18432), (16, 73728, 18432)]
-    for (M, N, K) in shapes:
-        path, tm, grid = w.plan(M, N, K, 128)
-        P = mirror_plan(M, N, K, 128, sms)
-        assert (tm, grid) == (P["tm"], P["grid"]), (M, N, K, tm, grid, P["tm"], P["grid"])
+    shapes += [(1, 256, 16384), (3, 136, 200), (17, 4096, 4000), (1, 73728, 18432), (16, 73728, 18432),
+               (2, 8192, 4096)]
+    for force in (0, 2):
+        prev = w.force_path(force)
+        try:
+            for (M, N, K) in shapes:
+                path, tm, grid = w.plan(M, N, K, 128)
+                P = dispatch(M, N, K, 128, sms, force=force)
+                assert (path, tm) == (P["path"], P["tm"]), (M, N, K, force, path, tm, grid)
+                if path == 1:   # persistent grid: at most one CTA per block, at least one per SM or block
+                    assert min(P["blocks"], sms) <= grid <= P["blocks"], (M, N, K, grid, P["blocks"])
+                else:
+                    assert grid == P["grid"], (M, N, K, force, grid, P["grid"])
+        finally:
+            w.force_path(prev)
 
 
 def _chain(w, x_d, layers, G, stream_sync):

@@ -35,20 +35,88 @@ def tile_m_for(M):
 FORMATS = ("int4", "w8", "sparse")
 
 
+GEMV_MAX_M = 4
+
+
+def gemv_plan(M, N, K, G, sms=SMS):
+    """Mirror of make_gemv_plan: the CUDA-core kernel for one to four rows of X,
+    one CTA per block of cw output columns over the whole of K."""
+    mr = 1 if M <= 1 else 2 if M <= 2 else 4
+    cw = 32 if ceil_div(N, 32) >= sms else 16
+    blocks = ceil_div(N, cw)
+    KC = ceil_div(ceil_div(K, 64), 4) * 4
+    return dict(path=1, tm=mr, mr=mr, cw=cw, blocks=blocks, grid=blocks, KC=KC, ng=ceil_div(K, G),
+                n_tiles=ceil_div(N, 128), rows=ceil_div(K, 32), tile_rows=2 * KC)
+
+
+GEMV_AUTO_MAX_WEIGHTS = 4096 * 4096
+
+
+def dispatch(M, N, K, G, sms=SMS, fmt="int4", force=0):
+    """Mirror of device_plan for the 4-bit FP16 format: path 1 when forced (up to
+    four rows of X) or, by itself, for one row of X and at most 4096 x 4096
+    weights; else the tensor-core plan."""
+    if fmt == "int4" and M <= GEMV_MAX_M and force != 2:
+        if force == 1 or (M == 1 and K * N <= GEMV_AUTO_MAX_WEIGHTS):
+            return gemv_plan(M, N, K, G, sms)
+    return plan(M, N, K, G, sms, fmt)
+
+
+def check_gemv_shape(M, N, K, G, sms=SMS):
+    """Every (output column, row of 32 k) is read by exactly one thread of one CTA,
+    every packed unit and scale it reads lies inside its buffer and holds that
+    column's codes, and no two threads write the same Y element."""
+    P = gemv_plan(M, N, K, G, sms)
+    cw = P["cw"]
+    cpt = cw // 8
+    units = P["n_tiles"] * P["tile_rows"] * 128
+    scales = P["n_tiles"] * P["ng"] * 128
+    seen = set()
+    writes = set()
+    assert 128 % cw == 0                     # a block never straddles a tile
+    for b in range(P["blocks"]):             # one CTA per block (grid = blocks)
+        for warp in range(8):
+            for lane in range(32):
+                n0 = b * cw + (lane & 7)
+                nt, n_in0 = n0 >> 7, n0 & 127
+                r = warp * 4 + (lane >> 3)
+                while r < P["rows"]:
+                    g = min((r * 32) // G, P["ng"] - 1)
+                    for j in range(cpt):
+                        n, n_in = n0 + 8 * j, n_in0 + 8 * j
+                        assert n >> 7 == nt
+                        u = (nt * P["tile_rows"] + r) * 128 + n_in
+                        assert 0 <= u < units
+                        assert 0 <= (nt * P["ng"] + g) * 128 + n_in < scales
+                        # the unit holds k = 32r .. 32r+31 of column n (layout v2: kc = r // 2, j = r % 2)
+                        kc, jj = divmod(r, 2)
+                        assert u * 4 == (((nt * P["KC"] + kc) * 2 + jj) * 128 + n_in) * 4
+                        if n < N:
+                            assert (n, r) not in seen
+                            seen.add((n, r))
+                    r += 32
+        for t in range(min(256, P["mr"] * cw)):
+            m, c = divmod(t, cw)
+            if m < M and b * cw + c < N:
+                assert (m, b * cw + c) not in writes
+                writes.add((m, b * cw + c))
+    assert len(seen) == N * P["rows"]
+    assert len(writes) == M * N
+    return P
+
+
 def plan(M, N, K, G, sms=SMS, fmt="int4"):
     tm = tile_m_for(M)
     if fmt == "sparse":
         tm = min(tm, 128)
     ksub = 2 if fmt in ("w8", "sparse") else (4 if tm <= 64 else 2)
     xblocks = 4 if fmt == "sparse" else ksub
-    cl = 2 if tm >= 64 else 1
     m_tiles, n_tiles, ng = ceil_div(M, tm), ceil_div(N, 128), ceil_div(K, G)
-    n_blocks = ceil_div(n_tiles, cl)
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     iters = KC // xblocks
-    total = n_blocks * m_tiles * iters
-    units = min(sms, MAX_GRID) // cl
-    work_tiles = n_blocks * m_tiles
+    total = n_tiles * m_tiles * iters
+    units = min(sms, MAX_GRID)           # one work unit per CTA; every CTA loads its own X
+    work_tiles = n_tiles * m_tiles
     if work_tiles < units:
         # tile-aligned split: s parts per tile, chosen by the measured cost model
         ring, pre_us, str_us, fix_us, row_us = ((8.0, 0.15, 0.40, 1.4, 0.006) if tm <= 32 else
@@ -70,26 +138,25 @@ def plan(M, N, K, G, sms=SMS, fmt="int4"):
         min_iters = max(4, iters // 2 if tm >= 64 else (iters // 4 if tm == 32 else 0))
         units = min(units, -(-total // min_iters))
     units = max(1, units)
-    return dict(tm=tm, ksub=ksub, xblocks=xblocks, fmt=fmt, cl=cl, m_tiles=m_tiles, n_tiles=n_tiles,
-                n_blocks=n_blocks, KC=KC, iters=iters, ng=ng, total=total, units=units, grid=units * cl)
+    return dict(path=2, tm=tm, ksub=ksub, xblocks=xblocks, fmt=fmt, m_tiles=m_tiles, n_tiles=n_tiles,
+                KC=KC, iters=iters, ng=ng, total=total, grid=units)
 
 
 def cta_begin(P, c):
-    return c * P["total"] // P["units"]
+    return c * P["total"] // P["grid"]
 
 
 def cta_of(P, i):
-    c = (i * P["units"]) // P["total"]
-    while c + 1 < P["units"] and cta_begin(P, c + 1) <= i:
+    c = (i * P["grid"]) // P["total"]
+    while c + 1 < P["grid"] and cta_begin(P, c + 1) <= i:
         c += 1
     while c > 0 and cta_begin(P, c) > i:
         c -= 1
     return c
 
 
-def slot_of(P, c, t, rank):
-    cta = c * P["cl"] + rank
-    return 2 * cta if cta_begin(P, c) >= t * P["iters"] else 2 * cta + 1
+def slot_of(P, c, t):
+    return 2 * c if cta_begin(P, c) >= t * P["iters"] else 2 * c + 1
 
 
 def segments(P, c):
@@ -107,7 +174,7 @@ def check_shape(M, N, K, G, sms=SMS, fmt="int4"):
     producers, the partial slots and the counters stays inside its buffer; the
     reducer of a split tile reads exactly the slots its contributors wrote."""
     P = plan(M, N, K, G, sms, fmt)
-    KC, ng, tm, ks, iters, cl = P["KC"], P["ng"], P["tm"], P["ksub"], P["iters"], P["cl"]
+    KC, ng, tm, ks, iters = P["KC"], P["ng"], P["tm"], P["ksub"], P["iters"]
     # packed words per (tile, sub-chunk) and sub-chunks per column, per format
     chunk_words = {"int4": 1024, "w8": 2048, "sparse": 1536}[fmt]
     sub_k = 128 if fmt == "sparse" else 64
@@ -118,44 +185,40 @@ def check_shape(M, N, K, G, sms=SMS, fmt="int4"):
     assert P["grid"] <= MAX_GRID
     covered = {}
     writers = {}
-    for c in range(P["units"]):
-        for rank in range(cl):
-            for (t, kb, ke) in segments(P, c):
-                assert 0 <= t < P["n_blocks"] * P["m_tiles"] and 0 <= kb < ke <= iters
-                nb, mt = divmod(t, P["m_tiles"])
-                nt = nb * cl + rank
-                phantom = nt >= P["n_tiles"]
-                for st in range(kb, ke):
-                    k0 = st * ks * sub_k
-                    if not phantom:
-                        key = (nt, mt, st)
-                        assert key not in covered
-                        covered[key] = (c, rank)
-                        w0 = (nt * KCp + st * ks) * chunk_words    # one bulk copy of ks sub-chunks
-                        assert 0 <= w0 and w0 + ks * chunk_words <= packed_words
-                        assert (w0 * 4) % 16 == 0                  # bulk-copy source alignment
-                        g0 = min(k0 // G, ng - 1)
-                        g1 = min((k0 + ks * sub_k - 1) // G, ng - 1)
-                        assert 1 <= g1 - g0 + 1 <= ks * sub_k // 32  # fits the scale slot
-                        e0 = (nt * ng + g0) * 128
-                        assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
-                    for j in range(P["xblocks"]):
-                        assert ((k0 + j * 64) * 2) % 16 == 0    # TMA inner coordinate, 16-byte aligned
-                    assert mt * tm < M
-                split = kb != 0 or ke != iters
-                if split:
-                    slot = slot_of(P, c, t, rank)
-                    assert 0 <= slot < 2 * P["grid"]
-                    assert (slot + 1) * tm * 128 <= partial_floats
-                    writers.setdefault((t, rank), []).append((c, slot))
+    for c in range(P["grid"]):
+        for (t, kb, ke) in segments(P, c):
+            assert 0 <= t < P["n_tiles"] * P["m_tiles"] and 0 <= kb < ke <= iters
+            nt, mt = divmod(t, P["m_tiles"])
+            for st in range(kb, ke):
+                k0 = st * ks * sub_k
+                key = (nt, mt, st)
+                assert key not in covered
+                covered[key] = c
+                w0 = (nt * KCp + st * ks) * chunk_words    # one bulk copy of ks sub-chunks
+                assert 0 <= w0 and w0 + ks * chunk_words <= packed_words
+                assert (w0 * 4) % 16 == 0                  # bulk-copy source alignment
+                g0 = min(k0 // G, ng - 1)
+                g1 = min((k0 + ks * sub_k - 1) // G, ng - 1)
+                assert 1 <= g1 - g0 + 1 <= ks * sub_k // 32  # fits the scale slot
+                e0 = (nt * ng + g0) * 128
+                assert e0 >= 0 and e0 + (g1 - g0 + 1) * 128 <= scales_elems
+                for j in range(P["xblocks"]):
+                    assert ((k0 + j * 64) * 2) % 16 == 0    # TMA inner coordinate, 16-byte aligned
+                assert mt * tm < M
+            split = kb != 0 or ke != iters
+            if split:
+                slot = slot_of(P, c, t)
+                assert 0 <= slot < 2 * P["grid"]
+                assert (slot + 1) * tm * 128 <= partial_floats
+                writers.setdefault(t, []).append((c, slot))
     assert len(covered) == P["n_tiles"] * P["m_tiles"] * iters
     counter_ids = set()
-    for (t, rank), ws in writers.items():
+    for t, ws in writers.items():
         c_lo, c_hi = cta_of(P, t * iters), cta_of(P, t * iters + iters - 1)
-        counter = c_lo * cl + rank
+        counter = c_lo
         assert counter < P["grid"] and counter not in counter_ids
         counter_ids.add(counter)
-        read = [(cc, slot_of(P, cc, t, rank)) for cc in range(c_lo, c_hi + 1)]
+        read = [(cc, slot_of(P, cc, t)) for cc in range(c_lo, c_hi + 1)]
         assert sorted(read) == sorted(ws), (t, read, ws)
         assert len(set(s for _, s in ws)) == len(ws)
     # a slot is written by one tile only
@@ -178,6 +241,33 @@ SHAPES = sorted(set(
 @pytest.mark.parametrize("M,N,K,G", SHAPES)
 def test_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
     check_shape(M, N, K, G)
+
+
+GEMV_SHAPES = sorted(set((m, n, k, g) for (m, n, k, g) in SHAPES if m <= GEMV_MAX_M and n * k <= 12288 * 4096)
+                     | {(2, 8192, 4096, 128), (4, 4096, 11008, 128), (3, 1032, 4040, 32), (2, 8, 8, 8)})
+
+
+@pytest.mark.parametrize("M,N,K,G", GEMV_SHAPES)
+def test_gemv_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
+    check_gemv_shape(M, N, K, G)
+
+
+def test_gemv_column_block_widths():
+    """Blocks of 32 columns when that still gives one block per SM, else 16: 16
+    for the 4096-wide layers, 32 for 8192 and wider."""
+    assert gemv_plan(1, 4096, 4096, 128)["cw"] == 16
+    assert gemv_plan(1, 4864, 4096, 128)["cw"] == 32
+    assert gemv_plan(1, 8192, 4096, 128)["cw"] == 32
+    assert gemv_plan(1, 12288, 4096, 128)["cw"] == 32
+    assert gemv_plan(4, 22016, 4096, 128)["cw"] == 32
+    assert gemv_plan(3, 4096, 4096, 128)["mr"] == 4 and gemv_plan(2, 4096, 4096, 128)["mr"] == 2
+    assert dispatch(5, 4096, 4096, 128)["path"] != 1
+    assert dispatch(4, 4096, 4096, 128, fmt="w8")["tm"] == 16
+    assert dispatch(1, 4096, 4096, 128, force=2)["tm"] == 16
+    # the automatic choice: one row of X and at most 4096 x 4096 weights
+    assert dispatch(1, 4096, 4096, 128)["path"] == 1
+    assert dispatch(1, 12288, 4096, 128)["path"] == 2 and dispatch(2, 4096, 4096, 128)["path"] == 2
+    assert dispatch(4, 12288, 4096, 128, force=1)["path"] == 1
 
 
 @pytest.mark.parametrize("fmt", ["w8", "sparse"])
@@ -267,8 +357,8 @@ def test_small_layer_splits_are_tile_aligned():
               (256, 15360, 5120): 1, (256, 5120, 5120): 1, (256, 5120, 13824): 2, (512, 5120, 5120): 1}
     for (M, N, K), s in expect.items():
         P = plan(M, N, K, 128)
-        work_tiles = P["n_blocks"] * P["m_tiles"]
-        assert P["units"] == work_tiles * s, (M, N, K, P["units"])
+        work_tiles = P["n_tiles"] * P["m_tiles"]
+        assert P["grid"] == work_tiles * s, (M, N, K, P["grid"])
         for t in range(work_tiles):
             assert cta_begin(P, t * s) == t * P["iters"]
 

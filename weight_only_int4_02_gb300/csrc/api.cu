@@ -4,10 +4,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
 #include "gemm_tc.cuh"
+#include "gemv.cuh"
 #include "w4a16.h"
 
 namespace w4a16 {
@@ -84,12 +86,14 @@ constexpr SplitCost kSplit256 = {0, 0.59, 0.59, 0.0, 0.059};    // 256-row tile 
 struct DeviceState {
     bool ready = false;
     int sms = 0;
-    int max_clusters[3] = {0, 0, 0};     // co-resident 2-CTA clusters for tile heights 64, 128, 256 (4-bit)
-    int max_clusters_w8[3] = {0, 0, 0};  // the same for the 8-bit kernels
-    int max_clusters_sp[2] = {0, 0};     // and for the 2:4 sparse kernels (tile heights 64, 128)
     void* ws = nullptr;
     size_t ws_bytes = 0;
+    int* gemv_status = nullptr;   // device address of the CUDA-core kernel's error word
 };
+
+// Error word of the CUDA-core kernel when it runs without a workspace (it needs
+// none): a timeout of one of its bounded waits sets bit 0.
+__device__ int g_gemv_status;
 
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -109,25 +113,47 @@ bool valid_sizes(int K, int N, int G)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// log2(G) for G a power of two; 30 (every k in group 0) otherwise, where G = K.
+int group_shift(int G)
+{
+    if ((G & (G - 1)) != 0) return 30;
+    int sh = 0;
+    while ((1 << sh) < G) ++sh;
+    return sh;
+}
+
+// The CUDA-core kernel (path 1) serves the 4-bit FP16 format (plain or with the
+// fused epilogue) for up to this many rows of X when it is forced; the dispatcher
+// picks it by itself where it measured faster than the tensor-core kernel on
+// GB300: one row of X and at most 4096 x 4096 weights (7.0 against 7.8 us per
+// launch). It is ALU-bound (about 3.5 instructions per weight at 55% issue), so
+// on larger layers and from two rows up the tensor-core kernel wins.
+constexpr int kGemvMaxM = 4;
+constexpr long long kGemvAutoMaxWeights = 4096LL * 4096;
+// Forced path (0 = the dispatcher's choice, 1 = CUDA-core kernel where it applies,
+// 2 = tensor-core kernel), for tests and ablations.
+std::atomic<int> g_force_path{0};
+
 struct Plan {
-    int path;     // 2 = per-weight scaling tcgen05 kernel
+    int path;     // 1 = CUDA-core kernel (one to four rows of X), 2 = tcgen05 kernel
     int tm;       // rows of X per tile (MMA N)
     int ksub;     // sub-chunks per pipeline stage (64 values of k; 128 for 2:4 sparse codes)
     int xblocks;  // 64-wide blocks of X per stage (the X tensor map's box depth)
-    int cluster;  // CTAs per cluster; 2 share each X tile by TMA multicast
-    int m_tiles, n_tiles, n_blocks, KC, ng, iters;
+    int m_tiles, n_tiles, KC, ng, iters;
     long long total;
-    int units;    // work units (clusters)
-    int grid;     // CTAs
+    int grid;     // CTAs, one work unit each
     size_t ws_bytes;
+    int gemv_mr;  // path 1: rows of X the kernel is built for (1, 2, 4)
+    int gemv_cw;  // path 1: output columns per block (8, 16, 32)
+    int gemv_blocks;
 };
 
 size_t ws_bytes_for(int grid, int tm) { return kPartialsOff + (size_t)2 * grid * tm * kTileN * sizeof(float); }
 
-// max_clusters: how many 2-CTA clusters of this tile height the device holds at
-// once (0 = unknown). fmt: the weight format (kFmt*); 8-bit codes run 128-value
-// stages at every tile height (16 KB of codes a stage, as 256 values of 4-bit codes).
-Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0, int fmt = kFmtW4)
+// fmt: the weight format (kFmt*); 8-bit codes run 128-value stages at every tile
+// height (16 KB of codes a stage, as 256 values of 4-bit codes). Every CTA loads
+// its own X tiles: no clusters, no multicast between CTAs.
+Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
 {
     Plan P;
     P.path = 2;
@@ -137,19 +163,14 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0, int fm
     P.n_tiles = ceil_div(N, kTileN);
     P.ksub = (fmt == kFmtW8 || fmt == kFmtW4Sp) ? 2 : P.tm <= 64 ? 4 : 2;
     P.xblocks = fmt == kFmtW4Sp ? 4 : P.ksub;
-    // From 64 rows of X up, X is the larger operand per stage: two CTAs on
-    // adjacent weight tiles load it once, by multicast.
-    P.cluster = P.tm >= 64 ? 2 : 1;
-    P.n_blocks = ceil_div(P.n_tiles, P.cluster);
     P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
     P.iters = P.KC / P.xblocks;
     P.ng = ceil_div(K, G);
-    P.total = (long long)P.n_blocks * P.m_tiles * P.iters;
-    long long units = (sms < kMaxGrid ? sms : kMaxGrid) / P.cluster;
-    if (P.cluster > 1 && max_clusters > 0 && units > max_clusters) units = max_clusters;
-    const long long work_tiles = (long long)P.n_blocks * P.m_tiles;
+    P.total = (long long)P.n_tiles * P.m_tiles * P.iters;
+    long long units = sms < kMaxGrid ? sms : kMaxGrid;
+    const long long work_tiles = (long long)P.n_tiles * P.m_tiles;
     if (work_tiles < units) {
-        // Fewer tiles (or tile pairs) than work units: every tile is cut into the
+        // Fewer tiles than work units (CTAs): every tile is cut into the
         // same number s of parts, so that unit boundaries fall on tile boundaries
         // and each split tile has exactly s contributors. s trades the stages a
         // unit runs against the split-K fix-up, whose last contributor reads every
@@ -182,79 +203,90 @@ Plan make_plan(int M, int N, int K, int G, int sms, int max_clusters = 0, int fm
         if (units > by_work) units = by_work;
     }
     if (units < 1) units = 1;
-    P.units = (int)units;
-    P.grid = P.units * P.cluster;
+    P.grid = (int)units;
     P.ws_bytes = ws_bytes_for(P.grid, P.tm);
     return P;
 }
 
-int max_clusters_for(const DeviceState* st, int tm, int fmt = kFmtW4)
+// Path 1 (CUDA-core kernel) for a shape: blocks of 32 columns when that gives at
+// least one block per SM, else of 16, one CTA per block.
+Plan make_gemv_plan(int M, int N, int K, int G, int sms)
 {
-    if (fmt == kFmtW4Sp) return tm == 64 ? st->max_clusters_sp[0] : tm == 128 ? st->max_clusters_sp[1] : 0;
-    const int* mc = fmt == kFmtW8 ? st->max_clusters_w8 : st->max_clusters;
-    return tm == 64 ? mc[0] : tm == 128 ? mc[1] : tm == 256 ? mc[2] : 0;
+    Plan P = {};
+    P.path = 1;
+    P.gemv_mr = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+    P.gemv_cw = ceil_div(N, 32) >= sms ? 32 : 16;
+    P.gemv_blocks = ceil_div(N, P.gemv_cw);
+    P.grid = P.gemv_blocks;
+    P.n_tiles = ceil_div(N, kTileN);
+    P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
+    P.ng = ceil_div(K, G);
+    P.ws_bytes = 0;   // no workspace: no partial sum leaves a CTA
+    return P;
 }
 
-// The plan of a shape on this device, with the cluster count of its kernel.
+bool gemv_applies(int M, int N, int K, int fmt, int force)
+{
+    if (fmt != kFmtW4 || M > kGemvMaxM || force == 2) return false;
+    return force == 1 || (M == 1 && (long long)K * N <= kGemvAutoMaxWeights);
+}
+
+// The plan of a shape on this device.
 Plan device_plan(const DeviceState* st, int M, int N, int K, int G, int fmt)
 {
-    const int mc = max_clusters_for(st, make_plan(M, N, K, G, st->sms, 0, fmt).tm, fmt);
-    return make_plan(M, N, K, G, st->sms, mc, fmt);
+    if (gemv_applies(M, N, K, fmt, g_force_path.load())) {
+        Plan P = make_gemv_plan(M, N, K, G, st->sms);
+        // persistent: no more CTAs than the SMs hold at once
+        const long long slots = (long long)st->sms * gemv_resident_ctas(P.gemv_mr, P.gemv_cw, false);
+        if (P.grid > slots) P.grid = (int)slots;
+        return P;
+    }
+    return make_plan(M, N, K, G, st->sms, fmt);
 }
 
-// Shared-memory attributes of every variant of one tile shape (epilogue x weight
-// format): *mc4 gets the smallest cluster count over the 4-bit variants, *mc8
-// over the 8-bit ones.
-template <int TM, int KSUB, int CL>
-cudaError_t setup_shape(int* mc4, int* mc8, int* mcsp = nullptr)
+// Shared-memory attributes of every variant of one tile shape (epilogue x weight format).
+template <int TM, int KSUB>
+cudaError_t setup_shape()
 {
-    int mc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     cudaError_t e;
-    if ((e = setup_tc<TM, KSUB, CL, false, kFmtW4>(&mc[0])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, true, kFmtW4>(&mc[1])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, false, kFmtW4Zp>(&mc[2])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, true, kFmtW4Zp>(&mc[3])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, false, kFmtW4Bf16>(&mc[4])) != cudaSuccess ||
-        (e = setup_tc<TM, KSUB, CL, true, kFmtW4Bf16>(&mc[5])) != cudaSuccess ||
-        (e = setup_tc<TM, 2, CL, false, kFmtW8>(&mc[6])) != cudaSuccess ||
-        (e = setup_tc<TM, 2, CL, true, kFmtW8>(&mc[7])) != cudaSuccess)
+    if ((e = setup_tc<TM, KSUB, false, kFmtW4>()) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, true, kFmtW4>()) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, false, kFmtW4Zp>()) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, true, kFmtW4Zp>()) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, false, kFmtW4Bf16>()) != cudaSuccess ||
+        (e = setup_tc<TM, KSUB, true, kFmtW4Bf16>()) != cudaSuccess ||
+        (e = setup_tc<TM, 2, false, kFmtW8>()) != cudaSuccess || (e = setup_tc<TM, 2, true, kFmtW8>()) != cudaSuccess)
         return e;
-    int m = mc[0];
-    for (int i = 1; i < 6; ++i) m = mc[i] < m ? mc[i] : m;
-    *mc4 = m;
-    *mc8 = mc[6] < mc[7] ? mc[6] : mc[7];
     if constexpr (TM <= 128) {
-        int a = 0, b = 0;
-        if ((e = setup_tc<TM, 2, CL, false, kFmtW4Sp>(&a)) != cudaSuccess ||
-            (e = setup_tc<TM, 2, CL, true, kFmtW4Sp>(&b)) != cudaSuccess)
+        if ((e = setup_tc<TM, 2, false, kFmtW4Sp>()) != cudaSuccess ||
+            (e = setup_tc<TM, 2, true, kFmtW4Sp>()) != cudaSuccess)
             return e;
-        if (mcsp) *mcsp = a < b ? a : b;
     }
     return cudaSuccess;
 }
 
-template <int TM, int KSUB, int CL>
+template <int TM, int KSUB>
 cudaError_t launch_shape(const CUtensorMap& map, const GemmParams& p, bool epi, int fmt, cudaStream_t stream)
 {
     switch (fmt) {
         case kFmtW4Zp:
-            return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4Zp>(map, p, stream)
-                       : launch_tc<TM, KSUB, CL, false, kFmtW4Zp>(map, p, stream);
+            return epi ? launch_tc<TM, KSUB, true, kFmtW4Zp>(map, p, stream)
+                       : launch_tc<TM, KSUB, false, kFmtW4Zp>(map, p, stream);
         case kFmtW8:
-            return epi ? launch_tc<TM, 2, CL, true, kFmtW8>(map, p, stream)
-                       : launch_tc<TM, 2, CL, false, kFmtW8>(map, p, stream);
+            return epi ? launch_tc<TM, 2, true, kFmtW8>(map, p, stream)
+                       : launch_tc<TM, 2, false, kFmtW8>(map, p, stream);
         case kFmtW4Bf16:
-            return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4Bf16>(map, p, stream)
-                       : launch_tc<TM, KSUB, CL, false, kFmtW4Bf16>(map, p, stream);
+            return epi ? launch_tc<TM, KSUB, true, kFmtW4Bf16>(map, p, stream)
+                       : launch_tc<TM, KSUB, false, kFmtW4Bf16>(map, p, stream);
         case kFmtW4Sp:
             if constexpr (TM <= 128)
-                return epi ? launch_tc<TM, 2, CL, true, kFmtW4Sp>(map, p, stream)
-                           : launch_tc<TM, 2, CL, false, kFmtW4Sp>(map, p, stream);
+                return epi ? launch_tc<TM, 2, true, kFmtW4Sp>(map, p, stream)
+                           : launch_tc<TM, 2, false, kFmtW4Sp>(map, p, stream);
             else
                 return cudaErrorInvalidValue;   // the plan never picks 256-row tiles for sparse codes
         default:
-            return epi ? launch_tc<TM, KSUB, CL, true, kFmtW4>(map, p, stream)
-                       : launch_tc<TM, KSUB, CL, false, kFmtW4>(map, p, stream);
+            return epi ? launch_tc<TM, KSUB, true, kFmtW4>(map, p, stream)
+                       : launch_tc<TM, KSUB, false, kFmtW4>(map, p, stream);
     }
 }
 
@@ -273,15 +305,13 @@ w4a16_status device_state(DeviceState** out)
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
-        int unused = 0;
-        int unused8 = 0;
-        if ((e = setup_shape<16, 4, 1>(&unused, &unused8)) != cudaSuccess ||
-            (e = setup_shape<32, 4, 1>(&unused, &unused8)) != cudaSuccess ||
-            (e = setup_shape<64, 4, 2>(&st.max_clusters[0], &st.max_clusters_w8[0], &st.max_clusters_sp[0])) !=
-                cudaSuccess ||
-            (e = setup_shape<128, 2, 2>(&st.max_clusters[1], &st.max_clusters_w8[1], &st.max_clusters_sp[1])) !=
-                cudaSuccess ||
-            (e = setup_shape<256, 2, 2>(&st.max_clusters[2], &st.max_clusters_w8[2])) != cudaSuccess)
+        if ((e = setup_gemv()) != cudaSuccess) return from_cuda(e);
+        void* gs = nullptr;
+        if ((e = cudaGetSymbolAddress(&gs, g_gemv_status)) != cudaSuccess) return from_cuda(e);
+        st.gemv_status = static_cast<int*>(gs);
+        if ((e = setup_shape<16, 4>()) != cudaSuccess || (e = setup_shape<32, 4>()) != cudaSuccess ||
+            (e = setup_shape<64, 4>()) != cudaSuccess || (e = setup_shape<128, 2>()) != cudaSuccess ||
+            (e = setup_shape<256, 2>()) != cudaSuccess)
             return from_cuda(e);
         if (!g_encode) {
             void* fn = nullptr;
@@ -351,6 +381,30 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int k
     return r == CUDA_SUCCESS;
 }
 
+// Tensor maps of the CUDA-core kernel: the packed words as uint32
+// [n_tiles * tile_rows][512] (one row = 32 values of k for a tile's 128 columns),
+// boxes of 32 rows x cb columns; the tile-ordered scales as 16-bit
+// [n_tiles * ng][128], boxes of scale_rows groups x cb columns.
+bool encode_gemv_maps(CUtensorMap* tw, CUtensorMap* ts, const void* packed, const void* scales, int n_tiles,
+                      int tile_rows, int ng, int cb, int scale_rows)
+{
+    cuuint32_t estr[2] = {1, 1};
+    cuuint64_t wdims[2] = {512, (cuuint64_t)n_tiles * tile_rows};
+    cuuint64_t wstrides[1] = {2048};
+    cuuint32_t wbox[2] = {(cuuint32_t)cb * 4, (cuuint32_t)(kGemvStageK / 32)};
+    CUresult r = g_encode(tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(packed), wdims, wstrides, wbox,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    cuuint64_t sdims[2] = {128, (cuuint64_t)n_tiles * ng};
+    cuuint64_t sstrides[1] = {256};
+    cuuint32_t sbox[2] = {(cuuint32_t)cb, (cuuint32_t)scale_rows};
+    r = g_encode(ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(scales), sdims, sstrides, sbox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
                        int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
                        const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0,
@@ -369,6 +423,36 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
     const Plan P = device_plan(st, M, N, K, G, fmt);
+    if (P.path == 1) {
+        GemvParams g;
+        g.x = reinterpret_cast<const __half*>(x);
+        g.y = reinterpret_cast<__half*>(y);
+        g.bias = reinterpret_cast<const __half*>(bias);
+        g.residual = reinterpret_cast<const __half*>(residual);
+        // a timeout is reported in the caller's workspace (or the no-allocation
+        // array) when one is given, else in the library's own word for this kernel
+        g.status = own_ws ? st->gemv_status : reinterpret_cast<int*>(ws);
+        g.wait_limit_ns = g_wait_limit_ns;
+        g.act = act;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.ng = P.ng;
+        g.g_shift = group_shift(G);
+        g.tile_rows = 2 * P.KC;
+        g.rows = ceil_div(K, 32);
+        g.stages = ceil_div(g.rows, kGemvStageK / 32);
+        g.scale_rows = ((G & (G - 1)) == 0 && G <= kGemvStageK) ? kGemvStageK / G : 1;
+        g.blocks = P.gemv_blocks;
+        CUtensorMap tw, ts;
+        if (!encode_gemv_maps(&tw, &ts, packed, scales_packed, P.n_tiles, g.tile_rows, P.ng, P.gemv_cw, g.scale_rows))
+            return W4A16_ERR_INVALID_ARG;
+        const bool epi = bias || residual || act != 0;
+        // persistent: no more CTAs than the SMs hold at once; CTAs take blocks in turn
+        const long long slots = (long long)st->sms * gemv_resident_ctas(P.gemv_mr, P.gemv_cw, epi);
+        const int grid = (int)(P.gemv_blocks < slots ? P.gemv_blocks : slots);
+        return from_cuda(launch_gemv(tw, ts, g, P.gemv_mr, P.gemv_cw, epi, grid, stream));
+    }
     if (own_ws) {
         rc = own_workspace(st, &ws, &ws_bytes);
         if (rc != W4A16_OK) return rc;
@@ -388,20 +472,13 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.K = K;
     p.G = G;
     p.ng = P.ng;
-    p.g_shift = 30;
-    if ((G & (G - 1)) == 0) {
-        p.g_shift = 0;
-        while ((1 << p.g_shift) < G) ++p.g_shift;
-    }
+    p.g_shift = group_shift(G);
     p.n_tiles = P.n_tiles;
     p.m_tiles = P.m_tiles;
     p.KC = fmt == kFmtW4Sp ? P.KC / 2 : P.KC;   // packed chunks per column (128 values of k when sparse)
     p.iters = P.iters;
     p.total_iters = P.total;
     p.grid = P.grid;
-    p.cluster = P.cluster;
-    p.units = P.units;
-    p.n_blocks = P.n_blocks;
     p.wait_limit_ns = g_wait_limit_ns;
     p.bias = reinterpret_cast<const __half*>(bias);
     p.residual = reinterpret_cast<const __half*>(residual);
@@ -411,20 +488,23 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     // With one row tile, a box of M rows rounded up to the 8-row swizzle atom is
     // enough: MMA rows past M feed only output columns that are never stored.
     p.x_rows = P.m_tiles == 1 ? ((M + 7) / 8) * 8 : P.tm;
-    // Clusters split a stage's X blocks between their CTAs: one 2-D TMA per block.
-    if (!encode_x_map(&map, x, M, K, p.x_rows, P.xblocks, P.cluster == 1, &p.x_3d, fmt == kFmtW4Bf16))
+    if (!encode_x_map(&map, x, M, K, p.x_rows, P.xblocks, true, &p.x_3d, fmt == kFmtW4Bf16))
         return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     const bool epi = bias || residual || act != 0;
     switch (P.tm) {
-        case 16: e = launch_shape<16, 4, 1>(map, p, epi, fmt, stream); break;
-        case 32: e = launch_shape<32, 4, 1>(map, p, epi, fmt, stream); break;
-        case 64: e = launch_shape<64, 4, 2>(map, p, epi, fmt, stream); break;
-        case 128: e = launch_shape<128, 2, 2>(map, p, epi, fmt, stream); break;
-        default: e = launch_shape<256, 2, 2>(map, p, epi, fmt, stream); break;
+        case 16: e = launch_shape<16, 4>(map, p, epi, fmt, stream); break;
+        case 32: e = launch_shape<32, 4>(map, p, epi, fmt, stream); break;
+        case 64: e = launch_shape<64, 4>(map, p, epi, fmt, stream); break;
+        case 128: e = launch_shape<128, 2>(map, p, epi, fmt, stream); break;
+        default: e = launch_shape<256, 2>(map, p, epi, fmt, stream); break;
     }
     return from_cuda(e);
 }
+
+// The no-allocation array's device address on the current device, or null if no
+// no-allocation call has looked it up yet (defined with that entry point below).
+void* noalloc_scratch_if_set();
 
 }  // namespace
 
@@ -494,8 +574,7 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size)
     // enough for every weight format's plan
     size_t need = 0;
     for (int fmt : {kFmtW4, kFmtW8, kFmtW4Sp}) {
-        const int mc = st ? max_clusters_for(st, make_plan(M, N, K, G, sms, 0, fmt).tm, fmt) : 0;
-        const size_t b = make_plan(M, N, K, G, sms, mc, fmt).ws_bytes;
+        const size_t b = make_plan(M, N, K, G, sms, fmt).ws_bytes;
         need = b > need ? b : need;
     }
     return need;
@@ -647,24 +726,53 @@ w4a16_status w4a16_selftest_wait_timeout(void* workspace, long long limit_ns, w4
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Reads the error word at the start of a workspace (or of the no-allocation
+// array); after a timeout clears the word and the split-K counters.
+w4a16_status read_and_clear_status(void* ws, bool* timed_out)
+{
+    int word = 0;
+    cudaError_t e = cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (word == 0) return W4A16_OK;
+    *timed_out = true;
+    if ((e = cudaMemset(ws, 0, kPartialsOff)) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess)
+        return from_cuda(e);
+    return W4A16_OK;
+}
+
+// Reads and clears one error word (no counters beside it).
+w4a16_status read_and_clear_word(int* word_dev, bool* timed_out)
+{
+    int word = 0;
+    cudaError_t e = cudaMemcpy(&word, word_dev, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (word == 0) return W4A16_OK;
+    *timed_out = true;
+    if ((e = cudaMemset(word_dev, 0, sizeof(int))) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess)
+        return from_cuda(e);
+    return W4A16_OK;
+}
+
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream)
 {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return from_cuda(e);
-    if (!workspace) {
+    bool timed_out = false;
+    w4a16_status rc = W4A16_OK;
+    if (workspace) {
+        rc = read_and_clear_status(workspace, &timed_out);
+    } else {
         DeviceState* st = nullptr;
-        w4a16_status rc = device_state(&st);
-        if (rc != W4A16_OK) return rc;
-        workspace = st->ws;
-        if (!workspace) return W4A16_OK;
+        if ((rc = device_state(&st)) != W4A16_OK) return rc;
+        // the library's own workspace, the CUDA-core kernel's word, and the
+        // no-allocation array once it is in use
+        if (st->ws) rc = read_and_clear_status(st->ws, &timed_out);
+        if (rc == W4A16_OK) rc = read_and_clear_word(st->gemv_status, &timed_out);
+        void* na = noalloc_scratch_if_set();
+        if (rc == W4A16_OK && na) rc = read_and_clear_status(na, &timed_out);
     }
-    int word = 0;
-    if ((e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return from_cuda(e);
-    if (word == 0) return W4A16_OK;
-    if ((e = cudaMemset(workspace, 0, kPartialsOff)) != cudaSuccess ||
-        (e = cudaDeviceSynchronize()) != cudaSuccess)
-        return from_cuda(e);
-    return W4A16_ERR_TIMEOUT;
+    if (rc != W4A16_OK) return rc;
+    return timed_out ? W4A16_ERR_TIMEOUT : W4A16_OK;
 }
 
 w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid)
@@ -676,9 +784,15 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
     if (rc != W4A16_OK) return rc;
     const Plan P = device_plan(st, M, N, K, G, kFmtW4);
     *path = P.path;
-    *tile_m = P.tm;
+    *tile_m = P.path == 1 ? P.gemv_mr : P.tm;
     *grid = P.grid;
     return W4A16_OK;
+}
+
+int w4a16_force_path(int path)
+{
+    if (path < 0 || path > 2) return -1;
+    return g_force_path.exchange(path);
 }
 
 
@@ -716,6 +830,14 @@ w4a16_status noalloc_scratch(void** out)
     return W4A16_OK;
 }
 
+void* noalloc_scratch_if_set()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_noalloc_ptr[dev];
+}
+
 }  // namespace
 
 extern "C" w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* packed,
@@ -725,17 +847,26 @@ extern "C" w4a16_status w4a16_gemm_noalloc(const uint16_t* x, const uint32_t* pa
     const int G = norm_group(K, group_size);
     if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
     if (M == 0) return W4A16_OK;
+    // Every check that can refuse the call comes before anything is enqueued.
+    if (!x || !packed || !scales_packed || !y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales_packed) || !aligned16(y))
+        return W4A16_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
-    if (device_plan(st, M, N, K, G, kFmtW4).ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
+    const Plan P = device_plan(st, M, N, K, G, kFmtW4);
+    if (P.ws_bytes > kNoAllocBytes) return W4A16_ERR_WORKSPACE;
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc != W4A16_OK) return rc;
-    // The error word and the split-K counters must start at zero; the array keeps
-    // whatever the previous call left there.
-    cudaError_t e = cudaMemsetAsync(scratch, 0, kPartialsOff, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return from_cuda(e);
+    if (P.path == 2) {
+        // The split-K counters must start at zero; the array keeps whatever the
+        // previous call left there. The error word (bytes 0..3) is left alone: it
+        // holds a timeout until w4a16_check_device_status(NULL) reads and clears it.
+        cudaError_t e = cudaMemsetAsync(static_cast<char*>(scratch) + kCountersOff, 0, kPartialsOff - kCountersOff,
+                                        reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     return gemm_impl(x, packed, scales_packed, y, M, N, K, G, scratch, kNoAllocBytes, false,
                      reinterpret_cast<cudaStream_t>(stream));
 }

@@ -65,18 +65,15 @@ struct GemmParams {
     const uint8_t* zeros;   // tile-ordered 4-bit zero-points [n_tiles][ng][64 bytes] (kFmtW4Zp only)
     __half* y;              // 16-bit output (FP16, or BF16 bits for kFmtW4Bf16)
     float* partials;        // [2 * grid][TM][128] FP32
-    int* counters;          // [grid], zero between launches (index = cluster * p.cluster + rank)
+    int* counters;          // [grid], zero between launches (index = the tile's first contributor)
     int* status;            // error word, bit 0 = a wait timed out
     int M, N, K, G, ng;
     int g_shift;            // log2(G) for G a power of two; 30 when there is one group
     int n_tiles, m_tiles;
     int KC;                 // 64-value sub-chunks per weight column in the packed layout
     int iters;              // stages per tile = KC / KSUB
-    long long total_iters;  // n_blocks * m_tiles * iters
-    int grid;               // CTAs
-    int cluster;            // CTAs per cluster (1, or 2 sharing each X tile by multicast)
-    int units;              // grid / cluster: the work split is over clusters
-    int n_blocks;           // ceil(n_tiles / cluster): a cluster takes `cluster` adjacent weight tiles
+    long long total_iters;  // n_tiles * m_tiles * iters
+    int grid;               // CTAs: one work unit each
     int x_3d;               // X tensor map is 3-D {64, M, K/64}: one TMA per stage
     int x_rows;             // rows of X each TMA box brings (<= TM, a multiple of 8); the
                             // MMA's B rows past them feed only output columns >= M
@@ -188,27 +185,25 @@ struct TcCfg {
     static_assert(!kSp || KSUB == 2, "sparse stages are two 128-value sub-chunks");
 };
 
-// First iteration of work unit (cluster) c.
+// First iteration of CTA c.
 __device__ __forceinline__ long long cta_begin(const GemmParams& p, int c)
 {
-    return (long long)c * p.total_iters / p.units;
+    return (long long)c * p.total_iters / p.grid;
 }
 
-// The work unit whose range holds iteration i.
+// The CTA whose range holds iteration i.
 __device__ __forceinline__ int cta_of(const GemmParams& p, long long i)
 {
-    int c = (int)((i * p.units) / p.total_iters);
-    while (c + 1 < p.units && cta_begin(p, c + 1) <= i) ++c;
+    int c = (int)((i * p.grid) / p.total_iters);
+    while (c + 1 < p.grid && cta_begin(p, c + 1) <= i) ++c;
     while (c > 0 && cta_begin(p, c) > i) --c;
     return c;
 }
 
-// Partial slot of the CTA of rank `rank` in unit c for tile t: 2*cta if t holds
-// the unit's first iteration, else 2*cta + 1 (cta = c * cluster + rank).
-__device__ __forceinline__ int slot_of(const GemmParams& p, int c, int t, int rank)
+// Partial slot of CTA c for tile t: 2c if t holds the CTA's first iteration, else 2c + 1.
+__device__ __forceinline__ int slot_of(const GemmParams& p, int c, int t)
 {
-    const int cta = c * p.cluster + rank;
-    return cta_begin(p, c) >= (long long)t * p.iters ? 2 * cta : 2 * cta + 1;
+    return cta_begin(p, c) >= (long long)t * p.iters ? 2 * c : 2 * c + 1;
 }
 
 // Group of reduction index k, clamped to the last group (padding past K holds code 8).
@@ -311,7 +306,7 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
 // contributors) before any is added, so it costs one global round trip. n_base is
 // the tile's first output feature.
 template <int TM, int NCP, int L4, bool EPI, bool BF>
-__device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
+__device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0,
                                            int n_base, int nw)
 {
     constexpr int CPR = L4 / NCP;
@@ -331,7 +326,7 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
 #pragma unroll
             for (int u = 0; u < NCP; ++u) {
                 const int cc = cc0 + u;
-                const float* base = p.partials + (size_t)slot_of(p, min(cc, c_hi), t, rank) * TM * kTileN + 4 * rg;
+                const float* base = p.partials + (size_t)slot_of(p, min(cc, c_hi), t) * TM * kTileN + 4 * rg;
 #pragma unroll
                 for (int e = 0; e < CPR; ++e) {
                     const int m = m_first + nw * (q0 + e);
@@ -379,27 +374,26 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int rank,
 
 // fix_reduce with the contributor batch chosen by the contributor count.
 template <int TM, int KSUB, bool EPI, bool BF>
-__device__ __forceinline__ void fix_tile(const GemmParams& p, int t, int rank, int c_lo, int c_hi, int valid, int m0,
-                                         int n_base, int nw)
+__device__ __forceinline__ void fix_tile(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0, int n_base,
+                                         int nw)
 {
     // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
     constexpr int L4 = KSUB == 4 ? 8 : 16;
     const int ncontrib = c_hi - c_lo + 1;
     if (ncontrib <= 2)
-        fix_reduce<TM, 2, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base, nw);
+        fix_reduce<TM, 2, L4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n_base, nw);
     else if (ncontrib <= 4)
-        fix_reduce<TM, 4, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base, nw);
+        fix_reduce<TM, 4, L4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n_base, nw);
     else
-        fix_reduce<TM, 8, L4, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n_base, nw);
+        fix_reduce<TM, 8, L4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n_base, nw);
 }
 
 // EPI: the instantiation with the fused epilogue (bias, activation, residual);
 // the plain one carries none of its code.
-template <int TM, int KSUB, int CL, bool EPI, int FMT>
+template <int TM, int KSUB, bool EPI, int FMT>
 __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p)
 {
-    static_assert(CL == 1 || (CL == 2 && KSUB % 2 == 0), "cluster of two splits a stage's X blocks");
     static_assert(FMT != kFmtW8 || KSUB == 2, "8-bit codes run 128-value stages (16 KB of codes)");
     constexpr bool ZP = FMT == kFmtW4Zp;
     constexpr bool BF = FMT == kFmtW4Bf16;
@@ -439,7 +433,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         }
         for (int s = 0; s < SX; ++s) {
             mbar_init(xfull_bar(s), 1);
-            mbar_init(xempty_bar(s), CL);            // the MMA commit of every CTA of the cluster
+            mbar_init(xempty_bar(s), 1);             // the MMA commit
         }
         for (int a = 0; a < A; ++a) {
             mbar_init(afull_bar(a), 2 * KSUB);       // the stage's dequant team
@@ -461,15 +455,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    // The cluster's CTAs write into each other's X ring and barriers: all of them
-    // must be initialised first.
-    if constexpr (CL > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (threadIdx.x == 0) launch_dependents();
 
-    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
-    const int cta = blockIdx.x / CL;                 // work unit (cluster) index
+    const int cta = blockIdx.x;
     const long long it_begin = cta_begin(p, cta);
     const long long it_end = cta_begin(p, cta + 1);
 
@@ -489,23 +479,14 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         bool ok = true;
         for (long long i = it_begin; ok && i < it_end;) {
             const Segment g = segment_at(p, i, it_end);
-            const int nb = g.t / p.m_tiles, mt = g.t - nb * p.m_tiles;
-            const int nt = nb * CL + rank;
-            const bool phantom = nt >= p.n_tiles;   // odd tile count: the last cluster's second tile
+            const int nt = g.t / p.m_tiles, mt = g.t - nt * p.m_tiles;
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
                 const int s = (int)(seq % S);
                 const uint32_t empty = is_x ? xempty_bar(s) : wempty_bar(s);
                 if (!wait_warp(empty, ((seq / S) & 1) ^ 1, ctl)) { ok = false; break; }
                 if (lane == 0) {
                     const int k0 = kc * C::kStageK;
-                    if (is_x && CL > 1) {
-                        // each CTA brings its share of the stage's X blocks into both CTAs
-                        mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(C::kXBlocks * p.x_rows * 128));
-#pragma unroll
-                        for (int j = rank; j < C::kXBlocks; j += CL)
-                            tma_load_2d_mc(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
-                                           xfull_bar(s), k0 + j * kChunkK, mt * TM, (uint16_t)((1u << CL) - 1));
-                    } else if (is_x) {
+                    if (is_x) {
                         mbar_arrive_expect_tx(xfull_bar(s), (uint32_t)(C::kXBlocks * p.x_rows * 128));
                         if (p.x_3d) {
                             tma_load_3d(sbase + C::kOffX + s * C::kXBytes, &tmap_x, xfull_bar(s), 0, mt * TM,
@@ -516,8 +497,6 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                                 tma_load_2d(sbase + C::kOffX + s * C::kXBytes + j * p.x_rows * 128, &tmap_x,
                                             xfull_bar(s), k0 + j * kChunkK, mt * TM);
                         }
-                    } else if (phantom) {
-                        mbar_arrive(wfull_bar(s));   // no weights to stream; the output is never stored
                     } else {
                         const int g0 = group_of(p, k0);
                         const int g1 = group_of(p, k0 + C::kStageK - 1);
@@ -544,15 +523,6 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             for (uint32_t k = 1; k <= inflight; ++k) {
                 const uint32_t q = seq - k;
                 wait_drain(is_x ? xfull_bar((int)(q % S)) : wfull_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
-            }
-            // In a cluster, the peer's MMA commits arrive on this CTA's X ring: wait
-            // until the last use of every slot has received all of them, so that no
-            // arrival can land after this CTA (and reach whatever runs here next).
-            if (is_x && CL > 1) {
-                for (uint32_t k = 1; k <= inflight; ++k) {
-                    const uint32_t q = seq - k;
-                    wait_drain(xempty_bar((int)(q % S)), (q / S) & 1, 1000000000LL);
-                }
             }
         }
     } else if (warp == C::kMmaWarp) {
@@ -606,10 +576,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                             }
                         }
                     }
-                    if constexpr (CL > 1)
-                        mma_commit_mc(xempty_bar(s), (uint16_t)((1u << CL) - 1));
-                    else
-                        mma_commit(xempty_bar(s));
+                    mma_commit(xempty_bar(s));
                     mma_commit(aempty_bar(a));
                 }
                 __syncwarp();
@@ -759,8 +726,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         for (long long i = it_begin; i < it_end;) {
             const Segment g = segment_at(p, i, it_end);
             const int t = g.t;
-            const int nb = t / p.m_tiles, mt = t - nb * p.m_tiles;
-            const int n = (nb * CL + rank) * kTileN + n_in;   // n >= N for a phantom tile: nothing stored
+            const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
+            const int n = nt * kTileN + n_in;
             const int m0 = mt * TM;
             const int valid = min(TM, p.M - m0);
             const int chunks = (valid + 15) >> 4;
@@ -772,7 +739,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             if (named_bar_or(1, 128, !ok)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + ((uint32_t)(warp * 32) << 16) + C::kDCol + d * TM;
-            float* part = p.partials + (size_t)slot_of(p, cta, t, rank) * TM * kTileN + n_in;
+            float* part = p.partials + (size_t)slot_of(p, cta, t) * TM * kTileN + n_in;
             for (int c = 0; c < chunks; ++c) {
                 uint32_t r[16];
                 tmem_ld16(d_tmem + c * 16, r);
@@ -823,7 +790,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                 const int c_lo = cta_of(p, (long long)t * p.iters);
                 const int c_hi = cta_of(p, (long long)t * p.iters + p.iters - 1);
                 if (threadIdx.x == 0) {
-                    int* counter = p.counters + c_lo * CL + rank;
+                    int* counter = p.counters + c_lo;
                     const int prev = atomicAdd(counter, 1);
                     const int last = (prev == c_hi - c_lo);
                     if (last) *counter = 0;
@@ -839,7 +806,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     }
                 } else if (last) {
                     __threadfence();
-                    fix_tile<TM, KSUB, EPI, BF>(p, t, rank, c_lo, c_hi, valid, m0, n - n_in, 4);
+                    fix_tile<TM, KSUB, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n - n_in, 4);
                 }
                 named_bar_sync(1, 128);
             }
@@ -854,15 +821,11 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         if (dfr[0]) {
             __threadfence();
             const int t = dfr[1];
-            const int nb = t / p.m_tiles, mt = t - nb * p.m_tiles;
+            const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
             const int m0 = mt * TM;
-            fix_tile<TM, KSUB, EPI, BF>(p, t, rank, dfr[2], dfr[3], min(TM, p.M - m0), m0,
-                                        (nb * CL + rank) * kTileN, C::kThreads / 32);
+            fix_tile<TM, KSUB, EPI, BF>(p, t, dfr[2], dfr[3], min(TM, p.M - m0), m0, nt * kTileN, C::kThreads / 32);
         }
     }
-    // No CTA may leave while its peer can still write into its X ring or arrive on
-    // its barriers.
-    if constexpr (CL > 1) cluster_sync();
     if (warp == C::kMmaWarp) {
         __syncwarp();
         tc_fence_after();
@@ -870,10 +833,10 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
     }
 }
 
-template <int TM, int KSUB, int CL, bool EPI, int FMT>
+template <int TM, int KSUB, bool EPI, int FMT>
 cudaError_t launch_tc(const CUtensorMap& tmap, const GemmParams& p, cudaStream_t stream);
 
-template <int TM, int KSUB, int CL, bool EPI, int FMT>
-cudaError_t setup_tc(int* max_clusters);
+template <int TM, int KSUB, bool EPI, int FMT>
+cudaError_t setup_tc();
 
 }  // namespace w4a16

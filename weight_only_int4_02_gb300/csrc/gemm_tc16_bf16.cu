@@ -1,3 +1,3 @@
 // Instantiation of the tcgen05 W4A16 kernel for 16 rows of X per tile, BF16 activations.
 #include "gemm_tc_launch.cuh"
-W4A16_INSTANTIATE_TC(16, 4, 1, kFmtW4Bf16)
+W4A16_INSTANTIATE_TC(16, 4, kFmtW4Bf16)

@@ -1,3 +1,3 @@
 // Instantiation of the tcgen05 W4A16 kernel for 32 rows of X per tile.
 #include "gemm_tc_launch.cuh"
-W4A16_INSTANTIATE_TC(32, 4, 1, kFmtW4)
+W4A16_INSTANTIATE_TC(32, 4, kFmtW4)

@@ -1,3 +1,3 @@
 // Instantiation of the tcgen05 kernel for 2:4 sparse 4-bit codes, 32 rows of X per tile.
 #include "gemm_tc_launch.cuh"
-W4A16_INSTANTIATE_TC(32, 2, 1, kFmtW4Sp)
+W4A16_INSTANTIATE_TC(32, 2, kFmtW4Sp)

@@ -1,3 +1,3 @@
 // Instantiation of the tcgen05 kernel for 8-bit codes (W8A16), 32 rows of X per tile.
 #include "gemm_tc_launch.cuh"
-W4A16_INSTANTIATE_TC(32, 2, 1, kFmtW8)
+W4A16_INSTANTIATE_TC(32, 2, kFmtW8)

@@ -1,3 +1,3 @@
 // Instantiation of the tcgen05 W4A16 kernel for 64 rows of X per tile, per-group zero-points.
 #include "gemm_tc_launch.cuh"
-W4A16_INSTANTIATE_TC(64, 4, 2, kFmtW4Zp)
+W4A16_INSTANTIATE_TC(64, 4, kFmtW4Zp)

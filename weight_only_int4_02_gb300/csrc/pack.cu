@@ -73,6 +73,20 @@ __global__ void pack_zeros_kernel(const uint8_t* __restrict__ zeros, uint8_t* __
     }
 }
 
+// The GEMM kernels start streaming their packed weights before the kernel ahead
+// of them in the stream has finished (programmatic dependent launch; they wait
+// for it only before they read X). So the kernel just ahead of a GEMM must not
+// write its weights. Each repack therefore ends with this kernel, launched in the
+// ordinary way: it starts only once the repack has completed and its writes are
+// visible, writes nothing, and is the one a following GEMM may overlap.
+__global__ void pack_done_kernel() {}
+
+cudaError_t launch_pack_done(cudaStream_t stream)
+{
+    pack_done_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N, int n_tiles, int ng, int sms,
                               cudaStream_t stream)
 {
@@ -82,7 +96,9 @@ cudaError_t launch_pack_zeros(const uint8_t* zeros, uint8_t* zeros_packed, int N
     const long long cap = (long long)sms * 16;
     if (blocks > cap) blocks = cap;
     pack_zeros_kernel<<<(unsigned)blocks, threads, 0, stream>>>(zeros, zeros_packed, N, ng, total);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pack_done(stream);
 }
 
 // 8-bit codes (W8A16): byte (((nt*KC + kc)*4 + j4)*128 + n_in)*16 + b holds, for
@@ -218,7 +234,9 @@ cudaError_t launch_pack_sp(const uint8_t* codes, const uint16_t* scales, uint8_t
     blocks = (selems + 255) / 256;
     if (blocks > cap) blocks = cap;
     pack_scales_kernel<<<(unsigned)blocks, 256, 0, stream>>>(scales, scales_packed, N, ng, selems);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pack_done(stream);
 }
 
 cudaError_t launch_pack_w8(const uint8_t* codes, const uint16_t* scales, uint8_t* packed, uint16_t* scales_packed,
@@ -237,7 +255,9 @@ cudaError_t launch_pack_w8(const uint8_t* codes, const uint16_t* scales, uint8_t
     blocks = (selems + threads - 1) / threads;
     if (blocks > cap) blocks = cap;
     pack_scales_kernel<<<(unsigned)blocks, threads, 0, stream>>>(scales, scales_packed, N, ng, selems);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pack_done(stream);
 }
 
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* packed, uint16_t* scales_packed,
@@ -255,7 +275,9 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, uint32_t* 
     blocks = (selems + threads - 1) / threads;
     if (blocks > cap) blocks = cap;
     pack_scales_kernel<<<(unsigned)blocks, threads, 0, stream>>>(scales, scales_packed, N, ng, selems);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pack_done(stream);
 }
 
 }  // namespace w4a16

@@ -20,7 +20,7 @@ EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error
            "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
            "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp", "w4a16_w8_packed_bytes", "w4a16_w8_pack",
            "w4a16_w8_gemm", "w4a16_bf16_gemm", "w4a16_sp_packed_bytes", "w4a16_sp_pack", "w4a16_sp_gemm",
-           "w4a16_selftest_wait_timeout"]
+           "w4a16_selftest_wait_timeout", "w4a16_force_path"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -62,6 +62,8 @@ def lib():
         L.w4a16_check_device_status.restype = I
         L.w4a16_plan.argtypes = [I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]
         L.w4a16_plan.restype = I
+        L.w4a16_force_path.argtypes = [I]
+        L.w4a16_force_path.restype = I
         L.w4a16_gemm_noalloc.argtypes = [P, P, P, P, I, I, I, I, P]
         L.w4a16_gemm_noalloc.restype = I
         L.w4a16_gemm_fused.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
@@ -210,6 +212,16 @@ def plan(M, N, K, group_size):
     p, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     _check(lib().w4a16_plan(M, N, K, group_size, ctypes.byref(p), ctypes.byref(t), ctypes.byref(g)), "w4a16_plan")
     return p.value, t.value, g.value
+
+
+def force_path(path):
+    """Force the dispatcher's choice for the 4-bit FP16 format: 0 automatic, 1 the
+    CUDA-core kernel wherever it applies (M <= 4), 2 the tensor-core kernel.
+    Returns the previous setting."""
+    prev = lib().w4a16_force_path(int(path))
+    if prev < 0:
+        raise W4A16Error(ERR_INVALID_ARG, "w4a16_force_path(%r)" % (path,))
+    return prev
 
 
 def gemm_noalloc(x, packed, scales_packed, N, group_size, y=None, stream=None):
