@@ -77,6 +77,12 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def kernel_name(plan):
+    """The kernel instance a plan (path, tile or rows, grid) of w4a16_plan launches."""
+    path, tile, _ = plan
+    return ("w4a16_gemv_kernel<%d>" if path == 1 else "w4a16_tc_kernel<%d>") % tile
+
+
 def roofline_seconds(M, K, N, G, peaks):
     return max(algorithmic_bytes(M, K, N, G) / (peaks["hbm_gbs"] * 1e9),
                flops(M, K, N) / (peaks["bf16_tflops"] * 1e12))
@@ -354,19 +360,41 @@ def run_ours(args):
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
     value = step_flops / (ms_step * 1e-3) / 1e12
 
-    # ---- per kernel instance (all launches of one M use one instance) and per M
+    # ---- diagnostic, outside the timed region: every launch between two event nodes
+    diag = torch.cuda.CUDAGraph()
+    diag_ev = [cud.event() for _ in range(len(per_case) + 1)]
+    with torch.cuda.graph(diag, stream=cap):
+        st = torch.cuda.current_stream()
+        cud.record_external(diag_ev[0], st)
+        for ci, c in enumerate(per_case):
+            w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
+            cud.record_external(diag_ev[ci + 1], st)
+    mean_ms = np.zeros(len(per_case))
+    for r in range(8):
+        diag.replay()
+        torch.cuda.synchronize()
+        if r >= 3:
+            mean_ms += np.array([cud.elapsed_ms(diag_ev[ci], diag_ev[ci + 1]) for ci in range(len(per_case))]) / 5
+
+    mean_ms_by_case = {id(c): mean_ms[ci] for ci, c in enumerate(per_case)}
+
+    # ---- per kernel instance and per M
     kernels = {}
     per_m = {}
     for b in range(len(bounds) - 1):
         group = per_case[bounds[b]:bounds[b + 1]]
         M = group[0]["M"]
-        path, tile_m, grid = w4a16.plan(M, group[0]["N"], group[0]["K"], G)
-        name = "w4a16_tc_kernel<%d>" % tile_m
-        k = kernels.setdefault(name, dict(ms=0.0, bytes=0, flops=0, launches=0))
-        k["ms"] += grp_mean[b]
-        k["bytes"] += sum(algorithmic_bytes(c["M"], c["K"], c["N"], G) for c in group)
-        k["flops"] += sum(flops(c["M"], c["K"], c["N"]) for c in group)
-        k["launches"] += len(group)
+        # a group of one M may mix kernels (the CUDA-core one for its smallest layer):
+        # its measured time is shared among them in proportion to their isolated times
+        # (diagnostic run above), every launch counted under its own kernel
+        grp_names = [kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G)) for c in group]
+        iso = [float(mean_ms_by_case[id(c)]) for c in group]
+        for c, name, t_iso in zip(group, grp_names, iso):
+            k = kernels.setdefault(name, dict(ms=0.0, bytes=0, flops=0, launches=0))
+            k["ms"] += grp_mean[b] * (t_iso / sum(iso))
+            k["bytes"] += algorithmic_bytes(c["M"], c["K"], c["N"], G)
+            k["flops"] += flops(c["M"], c["K"], c["N"])
+            k["launches"] += 1
         d = per_m.setdefault(M, dict(ms=0.0, fl=0, wb=0, roof_s=0.0))
         d["ms"] += grp_mean[b]
         d["fl"] += sum(flops(c["M"], c["K"], c["N"]) for c in group)
@@ -390,22 +418,6 @@ def run_ours(args):
     roof["algorithmic_bytes_per_launch"] = dom["bytes"] / dom["launches"]
     roof["avg_launch_us"] = dom["ms"] * 1e3 / dom["launches"]
     roof["peak_source"] = peaks["source"] + (" (HBM copy)" if roof["bound"] == "hbm" else " (bf16 burst)")
-
-    # ---- diagnostic, outside the timed region: every launch between two event nodes
-    diag = torch.cuda.CUDAGraph()
-    diag_ev = [cud.event() for _ in range(len(per_case) + 1)]
-    with torch.cuda.graph(diag, stream=cap):
-        st = torch.cuda.current_stream()
-        cud.record_external(diag_ev[0], st)
-        for ci, c in enumerate(per_case):
-            w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
-            cud.record_external(diag_ev[ci + 1], st)
-    mean_ms = np.zeros(len(per_case))
-    for r in range(8):
-        diag.replay()
-        torch.cuda.synchronize()
-        if r >= 3:
-            mean_ms += np.array([cud.elapsed_ms(diag_ev[ci], diag_ev[ci + 1]) for ci in range(len(per_case))]) / 5
 
     # ---- FP16-weight GEMM of the same shapes (cuBLAS through torch.matmul), same protocol
     fp16 = fp16_baseline(per_case, dev, reps=max(3, min(K, 50)))
@@ -446,6 +458,7 @@ def run_ours(args):
         "e2e": e2e,
         "per_M": per_m_out,
         "per_case_isolated": [{"M": c["M"], "K": c["K"], "N": c["N"], "us": float(mean_ms[ci] * 1e3),
+                      "kernel": kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G)),
                       "weight_gbs": weight_bytes(c["K"], c["N"], G) / (mean_ms[ci] * 1e-3) / 1e9,
                       "roofline_frac": roofline_seconds(c["M"], c["K"], c["N"], G, peaks) / (mean_ms[ci] * 1e-3)}
                      for ci, c in enumerate(per_case)],
@@ -841,7 +854,7 @@ def workloads_probe(G, peaks):
             rows.append({"workload": name, "M": M, "K": K, "N": N, "us": us, "tflops": fl / (us * 1e-6) / 1e12,
                          "weight_gbs": weight_bytes(K, N, G) / (us * 1e-6) / 1e9,
                          "roofline_frac": roof_s / (us * 1e-6), "bound": "hbm" if hbm_s >= roof_s else "tensor",
-                         "kernel": ("w4a16_gemv_kernel<%d>" if path == 1 else "w4a16_tc_kernel<%d>") % tile,
+                         "kernel": kernel_name((path, tile, grid)),
                          "fp16_us": us16, "speedup_vs_fp16": us16 / us, "launches_timed": reps})
             del x, y
         del copies, wf

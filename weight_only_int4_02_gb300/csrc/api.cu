@@ -79,9 +79,9 @@ struct SplitCost {
 // The per-row fix-up costs are the fitted ones divided by the ratio of warps that now
 // reduce a unit's last tile (the whole CTA, 15 or 23 warps, against the 4 epilogue warps).
 constexpr SplitCost kSplit16 = {8, 0.15, 0.40, 1.4, 0.006};     // 16- and 32-row tiles, 16 KB stages
-constexpr SplitCost kSplit64 = {0, 0.525, 0.525, 2.6, 0.008};   // 64-row tile pairs, 16 KB stages
-constexpr SplitCost kSplit128 = {0, 0.375, 0.375, 2.9, 0.006};  // 128-row tile pairs, 8 KB stages
-constexpr SplitCost kSplit256 = {0, 0.59, 0.59, 0.0, 0.059};    // 256-row tile pairs, 8 KB stages (prefill)
+constexpr SplitCost kSplit64 = {0, 0.525, 0.525, 2.6, 0.008};   // 64-row tiles, 16 KB stages
+constexpr SplitCost kSplit128 = {0, 0.375, 0.375, 2.9, 0.006};  // 128-row tiles, 8 KB stages
+constexpr SplitCost kSplit256 = {0, 0.70, 0.70, 3.0, 0.0043};   // 256-row tiles, 8 KB stages (prefill)
 
 struct DeviceState {
     bool ready = false;
@@ -100,6 +100,12 @@ DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 long long g_wait_limit_ns = 1000000000LL;
+// Ablation knobs, read once from the environment: W4A16_SPLIT forces the number of
+// parts every tile is cut into when there are fewer tiles than SMs (clamped to what
+// the shape allows); W4A16_MIN_ITERS forces the fewest stages a CTA takes when
+// there are more. 0 keeps the dispatcher's own choice.
+int g_force_split = 0;
+int g_force_min_iters = 0;
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -190,6 +196,8 @@ Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
                 best_s = s;
             }
         }
+        if (g_force_split > 0) best_s = g_force_split < s_max ? (g_force_split < P.iters ? g_force_split : P.iters) : s_max;
+        if (best_s < 1) best_s = 1;
         units = work_tiles * best_s;
     } else {
         // Stream-K over every SM, but a work unit takes at least kMinItersPerCta
@@ -199,6 +207,7 @@ Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
         // round trip per 16 rows.
         int min_iters = P.tm >= 64 ? P.iters / 2 : P.tm == 32 ? P.iters / 4 : 0;
         if (min_iters < kMinItersPerCta) min_iters = kMinItersPerCta;
+        if (g_force_min_iters > 0) min_iters = g_force_min_iters;
         const long long by_work = (P.total + min_iters - 1) / min_iters;
         if (units > by_work) units = by_work;
     }
@@ -321,6 +330,8 @@ w4a16_status device_state(DeviceState** out)
             if (q != cudaDriverEntryPointSuccess || !fn) return W4A16_ERR_UNSUPPORTED;
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
             if (const char* s = std::getenv("W4A16_WAIT_LIMIT_NS")) g_wait_limit_ns = std::atoll(s);
+            if (const char* s = std::getenv("W4A16_SPLIT")) g_force_split = std::atoi(s);
+            if (const char* s = std::getenv("W4A16_MIN_ITERS")) g_force_min_iters = std::atoi(s);
         }
         st.sms = sms;
         st.ready = true;
