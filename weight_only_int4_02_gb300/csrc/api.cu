@@ -106,6 +106,7 @@ long long g_wait_limit_ns = 1000000000LL;
 // there are more. 0 keeps the dispatcher's own choice.
 int g_force_split = 0;
 int g_force_min_iters = 0;
+int g_force_tm = 0;   // W4A16_TILE_M: rows of X per tile (16, 32, 64, 128 or 256) for the tensor-core kernel
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -164,6 +165,8 @@ Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
     Plan P;
     P.path = 2;
     P.tm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    if (g_force_tm == 16 || g_force_tm == 32 || g_force_tm == 64 || g_force_tm == 128 || g_force_tm == 256)
+        P.tm = g_force_tm;
     if (fmt == kFmtW4Sp && P.tm > 128) P.tm = 128;   // sparse stages leave no room for 256-row X tiles
     P.m_tiles = ceil_div(M, P.tm);
     P.n_tiles = ceil_div(N, kTileN);
@@ -332,6 +335,7 @@ w4a16_status device_state(DeviceState** out)
             if (const char* s = std::getenv("W4A16_WAIT_LIMIT_NS")) g_wait_limit_ns = std::atoll(s);
             if (const char* s = std::getenv("W4A16_SPLIT")) g_force_split = std::atoi(s);
             if (const char* s = std::getenv("W4A16_MIN_ITERS")) g_force_min_iters = std::atoi(s);
+            if (const char* s = std::getenv("W4A16_TILE_M")) g_force_tm = std::atoi(s);
         }
         st.sms = sms;
         st.ready = true;
