@@ -335,6 +335,18 @@ w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
  */
 w4a16_status w4a16_selftest_wait_timeout(void* workspace, long long limit_ns, w4a16_stream_t stream);
 
+/*
+ * Sets the limit of every bounded wait in the kernels launched after this call
+ * (default 1 s, or W4A16_WAIT_LIMIT_NS read at the first call on a device), for
+ * tests of failure detection; no counterpart in the pages. A wait that runs out
+ * makes its CTA give up: it stops issuing, waits (with a fixed 1 s bound) for the
+ * copies and MMAs it already issued, frees its tensor memory and returns, and the
+ * error word reports W4A16_ERR_TIMEOUT (w4a16_check_device_status); the results of
+ * that launch are not valid. limit_ns <= 0 changes nothing. Returns the previous
+ * limit. Applies to every device and host thread of the process.
+ */
+long long w4a16_set_wait_limit_ns(long long limit_ns);
+
 /* Which kernel the dispatcher picks for a shape of the 4-bit FP16 format
  * (w4a16_gemm, w4a16_gemm_ws, w4a16_gemm_fused) on the current device. It picks
  * path 1 by itself for one row of X and at most 4096 x 4096 weights (where it

@@ -55,3 +55,53 @@ def test_timeout_takes_about_its_limit(w):
     ms = a.elapsed_time(b)
     assert 19.0 <= ms <= 200.0, ms
     assert w.check_device_status(ws) == w.ERR_TIMEOUT
+
+
+def test_gemm_waits_run_out_in_every_kernel_then_the_context_recovers(w, oracle_mod):
+    """The GEMM kernels' own bounded waits, made to run out: with the wait limit at
+    1 ns, a wait that is not satisfied at once gives up; its CTA stops issuing, waits
+    (with a fixed bound) for the copies and MMAs it has in flight, frees its tensor
+    memory and returns, and the host reads W4A16_ERR_TIMEOUT. Every kernel is one
+    CTA (no clusters, no writes between CTAs), so this path touches nothing another
+    CTA still uses. A long-K layer (18432 deep, one 128-column tile per SM) keeps
+    waits of microseconds in every kernel: the tensor-core tiles of 16 to 256 rows
+    and the CUDA-core kernel. With the limit restored, the same context and
+    workspace compute the same GEMMs correctly (checked against the oracle on
+    sampled rows and columns)."""
+    K, N, G = 18432, 19456, 128
+    q = inputs.codes(K, N, 7)
+    s = inputs.scales(K, N, G, 7, "halfnormal", 0.01)
+    packed, sp = w.pack(to_dev(q), to_dev(s), G)
+    runs = [(1, 1), (16, 2), (32, 2), (64, 2), (128, 2), (256, 2)]   # (M, forced path)
+    xs = {M: inputs.activations(M, K, 70 + M) for M, _ in runs}
+    assert w.check_device_status() == w.OK
+    prev = w.set_wait_limit_ns(1)
+    try:
+        for M, path in runs:
+            prev_path = w.force_path(path)
+            try:
+                for attempt in range(3):
+                    w.gemm(to_dev(xs[M]), packed, sp, N, G)
+                    torch.cuda.synchronize()
+                    status = w.check_device_status()
+                    if status == w.ERR_TIMEOUT:
+                        break
+                assert status == w.ERR_TIMEOUT, (M, path, status)
+                assert w.check_device_status() == w.OK          # read once, then cleared
+            finally:
+                w.force_path(prev_path)
+    finally:
+        w.set_wait_limit_ns(prev)
+    rs = np.random.default_rng(8)
+    cols = np.sort(rs.choice(N, 192, replace=False))
+    for M, path in runs:
+        prev_path = w.force_path(path)
+        try:
+            y = w.gemm(to_dev(xs[M]), packed, sp, N, G)
+            torch.cuda.synchronize()
+        finally:
+            w.force_path(prev_path)
+        assert w.check_device_status() == w.OK
+        rows = np.unique(rs.integers(0, M, size=6))
+        y_ref, absum = oracle_mod.gemm_sample(xs[M], q, s, G, rows, cols)
+        check_within(y.cpu().numpy()[np.ix_(rows, cols)], y_ref, absum, "M=%d path %d after timeouts" % (M, path))

@@ -804,6 +804,16 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
     return W4A16_OK;
 }
 
+long long w4a16_set_wait_limit_ns(long long limit_ns)
+{
+    DeviceState* st = nullptr;
+    device_state(&st);   // the first device set-up reads W4A16_WAIT_LIMIT_NS; set after it
+    std::lock_guard<std::mutex> lock(g_mu);
+    const long long prev = g_wait_limit_ns;
+    if (limit_ns > 0) g_wait_limit_ns = limit_ns;
+    return prev;
+}
+
 int w4a16_force_path(int path)
 {
     if (path < 0 || path > 2) return -1;

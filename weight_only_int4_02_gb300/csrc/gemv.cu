@@ -79,7 +79,7 @@ struct GemvCfg {
     static constexpr int kOffS = kStages * kWBytes;
     static constexpr int kOffX = kOffS + kStages * kSBytes;
     static constexpr int kOffBar = kOffX + kStages * kXBytes;
-    static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+    static constexpr int kOffMisc = kOffBar + 3 * kStages * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 128;    // + alignment slack
 };
 
@@ -129,15 +129,19 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
     const uint32_t sbase = smem_addr(smem);
+    // full: the stage's copies landed (one arrival, with their bytes); xready: the
+    // converter wrote the stage's X; empty: every consumer warp is done with the slot
     auto full_bar = [&](int s) { return sbase + C::kOffBar + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + C::kOffBar + 8u * (kStages + s); };
+    auto xready_bar = [&](int s) { return sbase + C::kOffBar + 8u * (2 * kStages + s); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc);
     __shared__ float red[kConsumerWarps][MR][CB];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 2);                 // producer (with the copies' bytes) + converter
+            mbar_init(full_bar(s), 1);                 // producer, with the copies' bytes
+            mbar_init(xready_bar(s), 1);               // converter
             mbar_init(empty_bar(s), kConsumerWarps);
         }
         *abort_flag = 0;
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
             const int nt = n0 >> 7;
             for (int st = 0; st < p.stages; ++st, ++seq) {
                 const int s = (int)(seq % kStages);
-                if (*abort_flag || !wait_warp(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) {
+                if (*abort_flag || !wait_warp<true>(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) {
                     ok = false;
                     break;
                 }
@@ -179,7 +183,8 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
                 __syncwarp();
             }
         }
-        // Wind down: let the copies in flight land before the CTA can exit.
+        // Wind down: let the copies in flight land before the CTA can exit (the full
+        // barriers depend on the copies alone).
         if (lane == 0) {
             const uint32_t inflight = seq < (uint32_t)kStages ? seq : (uint32_t)kStages;
             for (uint32_t k = 1; k <= inflight; ++k) {
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
         for (int b = blockIdx.x; b < p.blocks; b += gridDim.x) {
             for (int st = 0; st < p.stages; ++st, ++seq) {
                 const int s = (int)(seq % kStages);
-                if (*abort_flag || !wait_warp(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) break;
+                if (*abort_flag || !wait_warp<true>(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) break;
                 float* xs = reinterpret_cast<float*>(smem + C::kOffX + s * C::kXBytes);
 #pragma unroll
                 for (int m = 0; m < MR; ++m) {
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_bar(s));   // release: the writes above precede the arrival
+                if (lane == 0) mbar_arrive(xready_bar(s));   // release: the writes above precede the arrival
             }
             if (*abort_flag) break;
         }
@@ -239,7 +244,8 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
             for (int st = 0; st < p.stages; ++st, ++seq) {
                 if (!ok) continue;
                 const int s = (int)(seq % kStages);
-                if (!wait_warp(full_bar(s), (seq / kStages) & 1, ctl)) {
+                if (!wait_warp<true>(full_bar(s), (seq / kStages) & 1, ctl) ||
+                    !wait_warp<true>(xready_bar(s), (seq / kStages) & 1, ctl)) {
                     ok = false;
                     continue;
                 }

@@ -54,8 +54,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test for completion of phase `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Test for completion of phase `parity`; a thread whose phase is not complete
 // yet is suspended (not spinning) for up to `hint_ns` or until the phase completes.
+// The bounded waits below sleep in steps of at most their limit (and 20 us).
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
     uint32_t ok;
@@ -85,8 +100,9 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Wa
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint32_t hint = c.limit_ns < kSleepHintNs ? (uint32_t)c.limit_ns : kSleepHintNs;
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*c.abort_flag) return false;
         if ((long long)(global_timer_ns() - t0) > c.limit_ns) {
             *c.abort_flag = 1;
@@ -96,13 +112,19 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Wa
     }
 }
 
-// All 32 lanes of a warp wait; the outcome is uniform across the warp.
+// All 32 lanes of a warp wait; the outcome is uniform across the warp. The first
+// check is the potentially blocking try_wait (measured cheaper in the tensor-core
+// kernels, whose waits are mostly about to complete), or with TEST_FIRST the
+// non-blocking test, so that a limit shorter than the hardware's own blocking time
+// applies from the first check (the CUDA-core kernel, whose waits are all short).
+template <bool TEST_FIRST = false>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c)
 {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, TEST_FIRST ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint32_t hint = c.limit_ns < kSleepHintNs ? (uint32_t)c.limit_ns : kSleepHintNs;
     for (;;) {
-        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSleepHintNs))) return true;
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, hint))) return true;
         int stop = 0;
         if ((threadIdx.x & 31) == 0) {
             if (*c.abort_flag) {

@@ -20,7 +20,7 @@ EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error
            "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
            "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp", "w4a16_w8_packed_bytes", "w4a16_w8_pack",
            "w4a16_w8_gemm", "w4a16_bf16_gemm", "w4a16_sp_packed_bytes", "w4a16_sp_pack", "w4a16_sp_gemm",
-           "w4a16_selftest_wait_timeout", "w4a16_force_path"]
+           "w4a16_selftest_wait_timeout", "w4a16_force_path", "w4a16_set_wait_limit_ns"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -64,6 +64,8 @@ def lib():
         L.w4a16_plan.restype = I
         L.w4a16_force_path.argtypes = [I]
         L.w4a16_force_path.restype = I
+        L.w4a16_set_wait_limit_ns.argtypes = [ctypes.c_longlong]
+        L.w4a16_set_wait_limit_ns.restype = ctypes.c_longlong
         L.w4a16_gemm_noalloc.argtypes = [P, P, P, P, I, I, I, I, P]
         L.w4a16_gemm_noalloc.restype = I
         L.w4a16_gemm_fused.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
@@ -212,6 +214,12 @@ def plan(M, N, K, group_size):
     p, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     _check(lib().w4a16_plan(M, N, K, group_size, ctypes.byref(p), ctypes.byref(t), ctypes.byref(g)), "w4a16_plan")
     return p.value, t.value, g.value
+
+
+def set_wait_limit_ns(limit_ns):
+    """Set the limit of the kernels' bounded waits (for tests of failure detection);
+    returns the previous limit. limit_ns <= 0 only reads it."""
+    return lib().w4a16_set_wait_limit_ns(int(limit_ns))
 
 
 def force_path(path):
