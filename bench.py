@@ -77,9 +77,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_name(plan):
-    """The kernel instance a plan (path, tile or rows, grid) of w4a16_plan launches."""
-    path, tile, _ = plan
+def kernel_name(plan, N):
+    """The kernel instance a plan (path, tile or rows, grid) of w4a16_plan launches for
+    N output columns: the decode kernel by rows of X and columns per block (one CTA
+    per block of 16 or 64), the others by rows of X."""
+    path, tile, grid = plan
+    if path == 3:
+        return "w4a16_decode_kernel<%d,%d>" % (tile, 64 if grid == -(-N // 64) else 16)
     return ("w4a16_gemv_kernel<%d>" if path == 1 else "w4a16_tc_kernel<%d>") % tile
 
 
@@ -387,7 +391,7 @@ def run_ours(args):
         # a group of one M may mix kernels (the CUDA-core one for its smallest layer):
         # its measured time is shared among them in proportion to their isolated times
         # (diagnostic run above), every launch counted under its own kernel
-        grp_names = [kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G)) for c in group]
+        grp_names = [kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G), c["N"]) for c in group]
         iso = [float(mean_ms_by_case[id(c)]) for c in group]
         for c, name, t_iso in zip(group, grp_names, iso):
             k = kernels.setdefault(name, dict(ms=0.0, bytes=0, flops=0, launches=0))
@@ -458,7 +462,7 @@ def run_ours(args):
         "e2e": e2e,
         "per_M": per_m_out,
         "per_case_isolated": [{"M": c["M"], "K": c["K"], "N": c["N"], "us": float(mean_ms[ci] * 1e3),
-                      "kernel": kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G)),
+                      "kernel": kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G), c["N"]),
                       "weight_gbs": weight_bytes(c["K"], c["N"], G) / (mean_ms[ci] * 1e-3) / 1e9,
                       "roofline_frac": roofline_seconds(c["M"], c["K"], c["N"], G, peaks) / (mean_ms[ci] * 1e-3)}
                      for ci, c in enumerate(per_case)],
@@ -854,7 +858,7 @@ def workloads_probe(G, peaks):
             rows.append({"workload": name, "M": M, "K": K, "N": N, "us": us, "tflops": fl / (us * 1e-6) / 1e12,
                          "weight_gbs": weight_bytes(K, N, G) / (us * 1e-6) / 1e9,
                          "roofline_frac": roof_s / (us * 1e-6), "bound": "hbm" if hbm_s >= roof_s else "tensor",
-                         "kernel": kernel_name((path, tile, grid)),
+                         "kernel": kernel_name((path, tile, grid), N),
                          "fp16_us": us16, "speedup_vs_fp16": us16 / us, "launches_timed": reps})
             del x, y
         del copies, wf

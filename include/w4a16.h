@@ -318,9 +318,10 @@ w4a16_status w4a16_w8_gemm(const uint16_t* x, const uint8_t* packed, const uint1
 /*
  * Synchronises `stream`, then reads and clears the error word that the kernels
  * set when one of their bounded waits gave up (W4A16_ERR_TIMEOUT), for the
- * given workspace. NULL covers the library's own workspace of the current device
- * and, once a w4a16_gemm_noalloc call has run on that device, the fixed array
- * that call uses. After a timeout the split-K counters of the workspace (or
+ * given workspace. NULL covers the library's own workspace of the current device,
+ * the error word of the kernels that run without a workspace (the decode and the
+ * CUDA-core kernel) and, once a w4a16_gemm_noalloc call has run on that device,
+ * the fixed array that call uses. After a timeout the split-K counters of the workspace (or
  * array) are reset as well.
  */
 w4a16_status w4a16_check_device_status(void* workspace, w4a16_stream_t stream);
@@ -349,25 +350,32 @@ long long w4a16_set_wait_limit_ns(long long limit_ns);
 
 /* Which kernel the dispatcher picks for a shape of the 4-bit FP16 format
  * (w4a16_gemm, w4a16_gemm_ws, w4a16_gemm_fused) on the current device. It picks
- * path 1 by itself for one row of X and at most 4096 x 4096 weights (where it
- * measured faster on GB300), path 2 otherwise:
+ * path 3 by itself for up to eight rows of X when K is a multiple of 32 (where it
+ * measured faster on GB300), path 2 otherwise; path 1 only when forced:
  *   *path = 1: the CUDA-core kernel for one to four rows of X ("Low-Precision
  *              Quantization Kernels in Production" (llms.blog), section 2: the
  *              activation vector held on chip, weights streamed, unpacked in
  *              registers, group-scaled and reduced across a warp; section 5: at
  *              batch 1 the matmul is a memory-bound GEMV). *tile_m = the rows of X
- *              it is built for (1, 2 or 4); *grid = CTAs, one per block of 8, 16 or
+ *              it is built for (1, 2 or 4); *grid = CTAs, one per block of 16 or
  *              32 output columns, each over the whole of K (no workspace is used).
  *   *path = 2: the tensor-core kernel (dequantised weights in tensor memory,
  *              tcgen05 MMA); *tile_m = rows of X per tile; *grid = CTAs.
+ *   *path = 3: the decode kernel for one to sixteen rows of X ("quant_marlin_kernel",
+ *              "The architecture": register-level unpack feeding the tensor-core
+ *              MMA from registers; here warp-level MMAs). *tile_m = the rows of X
+ *              it is built for (8 or 16); *grid = CTAs, one per block of 16 or 64
+ *              output columns, each over the whole of K (no workspace is used).
  * The other weight formats always run path 2. */
 w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid);
 
 /* Forces the dispatcher's choice for the 4-bit FP16 format, for tests and
  * ablations (no counterpart in the pages): 0 = automatic (the default), 1 = the
  * CUDA-core kernel for every shape it serves (M <= 4), 2 = the tensor-core kernel
- * for every M. Applies to every later call in the process, on every device and host
- * thread. Returns the previous setting, or -1 (nothing changed) for another value. */
+ * for every M, 3 = the decode kernel for every shape it serves (M <= 16, K a
+ * multiple of 32). Shapes a forced path does not serve run path 2. Applies to every
+ * later call in the process, on every device and host thread. Returns the previous
+ * setting, or -1 (nothing changed) for another value. */
 int w4a16_force_path(int path);
 
 /*
@@ -385,8 +393,8 @@ int w4a16_force_path(int path);
  *   W4A16_ERR_WORKSPACE with nothing launched (on a 152-SM GB300 this admits
  *   every shape with M <= 32; at larger M only shapes the dispatcher gives few
  *   split tiles, such as 4096x12288 at M = 64; 4096x4096 at M = 64 needs
- *   8 MiB + 4352 bytes and is rejected). Shapes the CUDA-core kernel takes
- *   (M <= 4) use no scratch at all.
+ *   8 MiB + 4352 bytes and is rejected). Shapes the decode kernel takes
+ *   (M <= 8, K a multiple of 32) use no scratch at all, only its error word.
  *   The first call on each device looks the array's device address up; make
  *   that first call before any stream capture.
  *   A call that uses the scratch enqueues a clear of its tile counters, then the

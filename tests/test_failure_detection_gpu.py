@@ -64,15 +64,15 @@ def test_gemm_waits_run_out_in_every_kernel_then_the_context_recovers(w, oracle_
     memory and returns, and the host reads W4A16_ERR_TIMEOUT. Every kernel is one
     CTA (no clusters, no writes between CTAs), so this path touches nothing another
     CTA still uses. A long-K layer (18432 deep, one 128-column tile per SM) keeps
-    waits of microseconds in every kernel: the tensor-core tiles of 16 to 256 rows
-    and the CUDA-core kernel. With the limit restored, the same context and
+    waits of microseconds in every kernel: the tensor-core tiles of 16 to 256 rows,
+    the CUDA-core kernel and the decode kernel (8 and 16 rows of X). With the limit restored, the same context and
     workspace compute the same GEMMs correctly (checked against the oracle on
     sampled rows and columns)."""
     K, N, G = 18432, 19456, 128
     q = inputs.codes(K, N, 7)
     s = inputs.scales(K, N, G, 7, "halfnormal", 0.01)
     packed, sp = w.pack(to_dev(q), to_dev(s), G)
-    runs = [(1, 1), (16, 2), (32, 2), (64, 2), (128, 2), (256, 2)]   # (M, forced path)
+    runs = [(1, 1), (16, 2), (32, 2), (64, 2), (128, 2), (256, 2), (1, 3), (16, 3)]   # (M, forced path)
     xs = {M: inputs.activations(M, K, 70 + M) for M, _ in runs}
     assert w.check_device_status() == w.OK
     prev = w.set_wait_limit_ns(1)

@@ -241,7 +241,7 @@ def test_device_plan_matches_host_mirror(w):
     shapes = [(m, n, k) for (m, k, n) in inputs.WORKLOADS["llama2_7b_decode_sweep"]["cases"] if m <= 32]
     shapes += [(1, 256, 16384), (3, 136, 200), (17, 4096, 4000), (1, 73728, 18432), (16, 73728, 18432),
                (2, 8192, 4096)]
-    for force in (0, 2):
+    for force in (0, 1, 2, 3):
         prev = w.force_path(force)
         try:
             for (M, N, K) in shapes:

@@ -1,8 +1,8 @@
 """GPU parity of the CUDA-core kernel for one to four rows of X (path 1) against the
 CPU oracle, beside the tensor-core kernel (path 2) forced on the same inputs.
 
-The dispatcher picks path 1 by itself only for one row of X on layers of at most
-4096 x 4096 weights (where it measured faster); here both paths are forced in turn
+The dispatcher does not pick path 1 by itself (the decode kernel measured faster on
+every decode layer); here both paths are forced in turn
 on the same shapes, each against the oracle: small and ragged shapes spanning several column
 blocks of both widths (16, 32), the edge sweep (group = K and group 32, N = 256
 with K = 16384, K = 4000 and 4040), and the four full-size decode layers at
@@ -193,12 +193,12 @@ def test_chained_launches_read_the_previous_output(w1):
 def test_gemm_right_after_its_repack(w, oracle_mod):
     """A GEMM enqueued directly after the repack of its weights, with no
     synchronisation in between, reads the repacked weights (each repack ends with a
-    kernel that writes nothing, which is all the GEMM may overlap). Both paths; the
-    weight buffers are reused with new codes on every round."""
+    kernel that writes nothing, which is all the GEMM may overlap). All three paths;
+    the weight buffers are reused with new codes on every round."""
     N, K, G = 4096, 4096, 128
     packed = torch.empty(w.packed_words(K, N, G), dtype=torch.int32, device="cuda")
     sp = torch.empty(w.scales_elems(K, N, G), dtype=torch.float16, device="cuda")
-    for rnd, (M, path) in enumerate(((1, 1), (4, 1), (16, 2), (1, 2))):
+    for rnd, (M, path) in enumerate(((1, 1), (4, 1), (16, 2), (1, 2), (1, 3), (8, 3), (16, 3))):
         x, q, s = inputs.problem(M, K, N, G, seed=90 + rnd)
         qd, sd, xd = to_dev(q), to_dev(s), to_dev(x)
         torch.cuda.synchronize()

@@ -49,17 +49,112 @@ def gemv_plan(M, N, K, G, sms=SMS):
                 n_tiles=ceil_div(N, 128), rows=ceil_div(K, 32), tile_rows=2 * KC)
 
 
-GEMV_AUTO_MAX_WEIGHTS = 4096 * 4096
+DECODE_MAX_M = 16
+DECODE_AUTO_MAX_M = 8
+DEC_STAGE_ROWS = 16
+DEC_MAX_RING = 16
+DEC_SMEM_BUDGET = 104 * 1024
+DEC_WORDS_IN_FLIGHT = 64 * 1024
+
+
+def decode_plan(M, N, K, G, sms=SMS):
+    """Mirror of make_decode_plan and of the launch's ring sizing: the decode kernel
+    for one to sixteen rows of X, one CTA per block of cb output columns (64 when
+    that gives at least one block per SM, else 16) over the whole of K."""
+    mr = 8 if M <= 8 else 16
+    cb = 64 if ceil_div(N, 64) >= sms else 16
+    blocks = ceil_div(N, cb)
+    KC = ceil_div(ceil_div(K, 64), 4) * 4
+    rows = K // 32
+    slot = DEC_STAGE_ROWS * (cb * 16 + cb * 2 + M * 64)
+    ring = min(DEC_WORDS_IN_FLIGHT // (DEC_STAGE_ROWS * cb * 16), DEC_SMEM_BUDGET // slot, DEC_MAX_RING)
+    sh = group_shift(G)
+    return dict(path=3, tm=mr, mr=mr, cb=cb, blocks=blocks, grid=blocks, KC=KC, ng=ceil_div(K, G),
+                n_tiles=ceil_div(N, 128), rows=rows, tile_rows=2 * KC, stages=ceil_div(rows, DEC_STAGE_ROWS),
+                slot=slot, ring=ring, smem=ring * slot + 3 * DEC_MAX_RING * 8 + 16 + 128, g_shift=sh,
+                scale_rows=(DEC_STAGE_ROWS * 32 // G) if (G & (G - 1)) == 0 and G <= DEC_STAGE_ROWS * 32 else 1)
+
+
+def group_shift(G):
+    if G & (G - 1):
+        return 30
+    return G.bit_length() - 1
 
 
 def dispatch(M, N, K, G, sms=SMS, fmt="int4", force=0):
-    """Mirror of device_plan for the 4-bit FP16 format: path 1 when forced (up to
-    four rows of X) or, by itself, for one row of X and at most 4096 x 4096
-    weights; else the tensor-core plan."""
-    if fmt == "int4" and M <= GEMV_MAX_M and force != 2:
-        if force == 1 or (M == 1 and K * N <= GEMV_AUTO_MAX_WEIGHTS):
-            return gemv_plan(M, N, K, G, sms)
+    """Mirror of device_plan for the 4-bit FP16 format: path 3 (decode kernel) when
+    forced or, by itself, for up to eight rows of X, where K is a multiple of 32;
+    path 1 (CUDA-core kernel) only when forced; else the tensor-core plan."""
+    if fmt == "int4" and M <= DECODE_MAX_M and K % 32 == 0:
+        if force == 3 or (force == 0 and M <= DECODE_AUTO_MAX_M):
+            return decode_plan(M, N, K, G, sms)
+    if fmt == "int4" and M <= GEMV_MAX_M and force == 1:
+        return gemv_plan(M, N, K, G, sms)
     return plan(M, N, K, G, sms, fmt)
+
+
+def check_decode_shape(M, N, K, G, sms=SMS):
+    """Mirror of the decode kernel's indexing. In one column block every (column,
+    row of 32 k, word) is unpacked by exactly one lane of one warp of one team, and
+    the shared-memory word it reads is the global word of layout v2 that holds that
+    column's codes; the X it reads lies inside X; every block's copies stay inside
+    its own tile of the packed words and scales; every Y element is written once;
+    the ring, the reduction and the shared memory fit."""
+    P = decode_plan(M, N, K, G, sms)
+    cb, mr, rows = P["cb"], P["mr"], P["rows"]
+    assert K % 32 == 0 and M <= DECODE_MAX_M
+    assert 2 <= P["ring"] <= DEC_MAX_RING
+    assert 8 * mr * cb * 4 <= P["ring"] * DEC_STAGE_ROWS * cb * 16      # warps' sums fit the weight ring
+    assert 2 * (P["smem"] + 1024) <= 228 * 1024                          # two CTAs per SM
+    assert 128 % cb == 0
+    # one block, every lane's reads
+    seen = set()
+    for st in range(P["stages"]):
+        team = st % 2
+        g0 = min((st * DEC_STAGE_ROWS * 32) >> P["g_shift"], P["ng"] - 1)
+        for wl in range(4):
+            for rr in range(4):
+                rl = 4 * wl + rr
+                row = st * DEC_STAGE_ROWS + rl
+                if row >= rows:
+                    continue
+                gl = min((row * 32) >> P["g_shift"], P["ng"] - 1) - g0
+                assert 0 <= gl < P["scale_rows"]
+                for lane in range(32):
+                    g, t = lane >> 2, lane & 3
+                    for h in range(mr // 8):
+                        m = min(8 * h + g, M - 1)
+                        assert 0 <= m < M and row * 32 + 8 * t + 7 < K
+                    for sb in range(cb // 16):
+                        for off in (0, 8):
+                            nl = 16 * sb + g + off
+                            smem_word = (rl * cb + nl) * 4 + t               # in the slot's [16][cb][4] words
+                            assert smem_word < DEC_STAGE_ROWS * cb * 4
+                            key = (nl, row, t)
+                            assert key not in seen
+                            seen.add(key)
+                            # the box starts at word (n0 & 127) * 4 of map row nt * tile_rows + st * 16
+                            box_row, box_col = divmod(smem_word, cb * 4)
+                            map_row = st * DEC_STAGE_ROWS + box_row              # within the tile
+                            kc, jj = divmod(map_row, 2)
+                            word_in_row = box_col                                # + (n0 & 127) * 4
+                            assert (map_row, word_in_row) == (row, nl * 4 + t)
+                            # layout v2: word (kc, jj, n_in, wd) holds k = 64 kc + 32 jj + 8 wd .. +7
+                            assert 64 * kc + 32 * jj + 8 * t == row * 32 + 8 * t
+    assert len(seen) == cb * rows * 4
+    # every block: copies inside its tile, Y written once
+    cols = set()
+    for b in range(P["blocks"]):
+        n0 = b * cb
+        nt = n0 >> 7
+        assert nt < P["n_tiles"] and (n0 & 127) + cb <= 128
+        assert (n0 & 127) * 4 + cb * 4 <= 512
+        for c in range(cb):
+            if n0 + c < N:
+                assert n0 + c not in cols
+                cols.add(n0 + c)
+    assert len(cols) == N
+    return P
 
 
 def check_gemv_shape(M, N, K, G, sms=SMS):
@@ -261,13 +356,41 @@ def test_gemv_column_block_widths():
     assert gemv_plan(1, 12288, 4096, 128)["cw"] == 32
     assert gemv_plan(4, 22016, 4096, 128)["cw"] == 32
     assert gemv_plan(3, 4096, 4096, 128)["mr"] == 4 and gemv_plan(2, 4096, 4096, 128)["mr"] == 2
-    assert dispatch(5, 4096, 4096, 128)["path"] != 1
+    assert dispatch(4, 12288, 4096, 128, force=1)["path"] == 1
+    assert dispatch(5, 4096, 4096, 128, force=1)["path"] == 2
+
+
+DECODE_SHAPES = sorted(set((m, n, k, g) for (m, n, k, g) in SHAPES if m <= DECODE_MAX_M and k % 32 == 0
+                           and n * k <= 22016 * 4096)
+                       | {(1, 73728, 18432, 128), (8, 73728, 18432, 128), (16, 12288, 4096, 128),
+                          (9, 1024, 2048, 64), (2, 264, 544, 32), (13, 4104, 1024, 128), (1, 4096, 4000, 4000)})
+
+
+@pytest.mark.parametrize("M,N,K,G", DECODE_SHAPES)
+def test_decode_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
+    check_decode_shape(M, N, K, G)
+
+
+def test_dispatch_rule():
+    """The automatic choice for the 4-bit FP16 format: the decode kernel (path 3) for
+    up to eight rows of X where K is a multiple of 32, the tensor-core kernel
+    otherwise; blocks of 64 columns for the layers 12288 wide and wider, 16 for the
+    4096-wide ones (measured on GB300)."""
+    for (N, K) in [(4096, 4096), (12288, 4096), (22016, 4096), (4096, 11008), (73728, 18432)]:
+        for M in (1, 2, 4, 8):
+            P = dispatch(M, N, K, 128)
+            assert P["path"] == 3 and P["tm"] == 8
+            assert P["cb"] == (16 if N == 4096 else 64)
+        assert dispatch(9, N, K, 128)["path"] == 2
+        assert dispatch(16, N, K, 128, force=3)["path"] == 3 and dispatch(16, N, K, 128, force=3)["tm"] == 16
+        assert dispatch(17, N, K, 128, force=3)["path"] == 2
+        assert dispatch(1, N, K, 128, force=2)["path"] == 2
+    assert dispatch(1, 4096, 4040, 128)["path"] == 2          # K not a multiple of 32
     assert dispatch(4, 4096, 4096, 128, fmt="w8")["tm"] == 16
     assert dispatch(1, 4096, 4096, 128, force=2)["tm"] == 16
-    # the automatic choice: one row of X and at most 4096 x 4096 weights
-    assert dispatch(1, 4096, 4096, 128)["path"] == 1
-    assert dispatch(1, 12288, 4096, 128)["path"] == 2 and dispatch(2, 4096, 4096, 128)["path"] == 2
-    assert dispatch(4, 12288, 4096, 128, force=1)["path"] == 1
+    # ring depth: about 64 KB of packed words in flight, fewer where shared memory says so
+    assert decode_plan(1, 4096, 4096, 128)["ring"] == 16 and decode_plan(1, 22016, 4096, 128)["ring"] == 4
+    assert decode_plan(16, 22016, 4096, 128)["ring"] == 3
 
 
 @pytest.mark.parametrize("fmt", ["w8", "sparse"])

@@ -21,8 +21,8 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("M,N,K", [
     (16, 4096, 4096),    # 16-row tensor-core tiles, every tile split across CTAs: the scratch is used
     (17, 4096, 4096),    # 32-row tiles with a 17-row tail, split tiles
-    (3, 4096, 4096),     # three rows: the 16-row tensor-core tiles
-    (1, 4096, 4096),     # one row on a 4096 x 4096 layer: the CUDA-core kernel, no scratch at all
+    (3, 4096, 4096),     # three rows: the decode kernel, no scratch at all
+    (1, 4096, 4096),     # one row: the decode kernel
 ])
 def test_no_alloc_matches_the_oracle_on_two_calls(oracle_mod, M, N, K):
     if not torch.cuda.is_available():

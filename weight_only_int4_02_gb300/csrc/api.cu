@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "gemm_tc.cuh"
+#include "decode.cuh"
 #include "gemv.cuh"
 #include "w4a16.h"
 
@@ -88,11 +89,11 @@ struct DeviceState {
     int sms = 0;
     void* ws = nullptr;
     size_t ws_bytes = 0;
-    int* gemv_status = nullptr;   // device address of the CUDA-core kernel's error word
+    int* gemv_status = nullptr;   // device address of the error word of the kernels without a workspace
 };
 
-// Error word of the CUDA-core kernel when it runs without a workspace (it needs
-// none): a timeout of one of its bounded waits sets bit 0.
+// Error word of the kernels that need no workspace (the CUDA-core kernel and the
+// decode kernel) when the caller passes none: a timeout of a bounded wait sets bit 0.
 __device__ int g_gemv_status;
 
 constexpr int kMaxDevices = 64;
@@ -107,6 +108,7 @@ long long g_wait_limit_ns = 1000000000LL;
 int g_force_split = 0;
 int g_force_min_iters = 0;
 int g_force_tm = 0;   // W4A16_TILE_M: rows of X per tile (16, 32, 64, 128 or 256) for the tensor-core kernel
+int g_force_cb = 0;   // W4A16_DECODE_CB: columns per block (16, 32 or 64) for the decode kernel
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -130,19 +132,25 @@ int group_shift(int G)
 }
 
 // The CUDA-core kernel (path 1) serves the 4-bit FP16 format (plain or with the
-// fused epilogue) for up to this many rows of X when it is forced; the dispatcher
-// picks it by itself where it measured faster than the tensor-core kernel on
-// GB300: one row of X and at most 4096 x 4096 weights (7.0 against 7.8 us per
-// launch). It is ALU-bound (about 3.5 instructions per weight at 55% issue), so
-// on larger layers and from two rows up the tensor-core kernel wins.
+// fused epilogue) for up to this many rows of X when it is forced. The dispatcher
+// does not pick it by itself: it is ALU-bound (about 3.5 instructions per weight at
+// 55% issue) and measured slower than the decode kernel on every decode layer
+// (4096 x 4096 at one row of X: 8.0 against 5.3 us per launch).
 constexpr int kGemvMaxM = 4;
-constexpr long long kGemvAutoMaxWeights = 4096LL * 4096;
-// Forced path (0 = the dispatcher's choice, 1 = CUDA-core kernel where it applies,
-// 2 = tensor-core kernel), for tests and ablations.
+// The decode kernel (path 3) serves the 4-bit FP16 format (plain or with the fused
+// epilogue) for up to sixteen rows of X when K is a multiple of 32; the dispatcher
+// picks it by itself for up to eight, where it measured faster than the tensor-core
+// kernel on every decode layer (4096 x 4096: 5.3 against 7.9 us; 18432 x 73728:
+// 121 against 138 us). From nine rows on the second half of X doubles its MMAs and
+// the tensor-core kernel wins on all but the smallest layers.
+constexpr int kDecodeMaxM = 16;
+constexpr int kDecodeAutoMaxM = 8;
+// Forced path (0 = the dispatcher's choice, 1 = CUDA-core kernel, 2 = tensor-core
+// kernel, 3 = decode kernel, each where it applies), for tests and ablations.
 std::atomic<int> g_force_path{0};
 
 struct Plan {
-    int path;     // 1 = CUDA-core kernel (one to four rows of X), 2 = tcgen05 kernel
+    int path;     // 1 = CUDA-core kernel (one to four rows of X), 2 = tcgen05 kernel, 3 = decode kernel
     int tm;       // rows of X per tile (MMA N)
     int ksub;     // sub-chunks per pipeline stage (64 values of k; 128 for 2:4 sparse codes)
     int xblocks;  // 64-wide blocks of X per stage (the X tensor map's box depth)
@@ -153,6 +161,8 @@ struct Plan {
     int gemv_mr;  // path 1: rows of X the kernel is built for (1, 2, 4)
     int gemv_cw;  // path 1: output columns per block (8, 16, 32)
     int gemv_blocks;
+    int dec_mr;   // path 3: rows of X the kernel is built for (8, 16)
+    int dec_cb;   // path 3: output columns per block (16, 32, 64)
 };
 
 size_t ws_bytes_for(int grid, int tm) { return kPartialsOff + (size_t)2 * grid * tm * kTileN * sizeof(float); }
@@ -237,16 +247,43 @@ Plan make_gemv_plan(int M, int N, int K, int G, int sms)
     return P;
 }
 
-bool gemv_applies(int M, int N, int K, int fmt, int force)
+bool gemv_applies(int M, int fmt, int force)
 {
-    if (fmt != kFmtW4 || M > kGemvMaxM || force == 2) return false;
-    return force == 1 || (M == 1 && (long long)K * N <= kGemvAutoMaxWeights);
+    return fmt == kFmtW4 && M <= kGemvMaxM && force == 1;
+}
+
+// Path 3 (decode kernel) for a shape: blocks of 64 columns where that gives at least
+// one block per SM (each row of a block is then 1 KB of contiguous packed words),
+// else of 16 (more CTAs for narrow layers); one CTA per block. Measured on the
+// decode layers: N = 4096 is fastest with 16, N >= 12288 with 64; 32 was never best.
+Plan make_decode_plan(int M, int N, int K, int G, int sms)
+{
+    Plan P = {};
+    P.path = 3;
+    P.dec_mr = M <= 8 ? 8 : 16;
+    int cb = ceil_div(N, 64) >= sms ? 64 : 16;
+    if (g_force_cb == 16 || g_force_cb == 32 || g_force_cb == 64) cb = g_force_cb;
+    P.dec_cb = cb;
+    P.grid = ceil_div(N, cb);
+    P.n_tiles = ceil_div(N, kTileN);
+    P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
+    P.ng = ceil_div(K, G);
+    P.ws_bytes = 0;   // no workspace: no partial sum leaves a CTA
+    return P;
+}
+
+bool decode_applies(int M, int K, int fmt, int force)
+{
+    if (fmt != kFmtW4 || M > kDecodeMaxM || K % 32 != 0) return false;
+    return force == 3 || (force == 0 && M <= kDecodeAutoMaxM);
 }
 
 // The plan of a shape on this device.
 Plan device_plan(const DeviceState* st, int M, int N, int K, int G, int fmt)
 {
-    if (gemv_applies(M, N, K, fmt, g_force_path.load())) {
+    const int force = g_force_path.load();
+    if (decode_applies(M, K, fmt, force)) return make_decode_plan(M, N, K, G, st->sms);
+    if (gemv_applies(M, fmt, force)) {
         Plan P = make_gemv_plan(M, N, K, G, st->sms);
         // persistent: no more CTAs than the SMs hold at once
         const long long slots = (long long)st->sms * gemv_resident_ctas(P.gemv_mr, P.gemv_cw, false);
@@ -317,7 +354,7 @@ w4a16_status device_state(DeviceState** out)
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return from_cuda(e);
         if (major != 10 || minor != 3) return W4A16_ERR_UNSUPPORTED;  // built for sm_103a only
-        if ((e = setup_gemv()) != cudaSuccess) return from_cuda(e);
+        if ((e = setup_gemv()) != cudaSuccess || (e = setup_decode()) != cudaSuccess) return from_cuda(e);
         void* gs = nullptr;
         if ((e = cudaGetSymbolAddress(&gs, g_gemv_status)) != cudaSuccess) return from_cuda(e);
         st.gemv_status = static_cast<int*>(gs);
@@ -336,6 +373,7 @@ w4a16_status device_state(DeviceState** out)
             if (const char* s = std::getenv("W4A16_SPLIT")) g_force_split = std::atoi(s);
             if (const char* s = std::getenv("W4A16_MIN_ITERS")) g_force_min_iters = std::atoi(s);
             if (const char* s = std::getenv("W4A16_TILE_M")) g_force_tm = std::atoi(s);
+            if (const char* s = std::getenv("W4A16_DECODE_CB")) g_force_cb = std::atoi(s);
         }
         st.sms = sms;
         st.ready = true;
@@ -420,6 +458,38 @@ bool encode_gemv_maps(CUtensorMap* tw, CUtensorMap* ts, const void* packed, cons
     return r == CUDA_SUCCESS;
 }
 
+// Tensor maps of the decode kernel: the packed words as uint32 [n_tiles * tile_rows][512],
+// boxes of 16 rows x cb columns; the tile-ordered scales as 16-bit [n_tiles * ng][128],
+// boxes of scale_rows groups x cb columns; X as the 3-D view {32, M, K/32} (strides
+// 2K and 64 bytes; K is a multiple of 32), boxes of 32 values x M rows x 16 (every
+// box in bounds: out-of-bounds rows measured slow to fill).
+bool encode_decode_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tx, const void* packed, const void* scales,
+                        const void* x, int n_tiles, int tile_rows, int ng, int cb, int scale_rows, int M, int K)
+{
+    cuuint32_t estr[3] = {1, 1, 1};
+    cuuint64_t wdims[2] = {512, (cuuint64_t)n_tiles * tile_rows};
+    cuuint64_t wstrides[1] = {2048};
+    cuuint32_t wbox[2] = {(cuuint32_t)cb * 4, (cuuint32_t)kDecStageRows};
+    CUresult r = g_encode(tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(packed), wdims, wstrides, wbox,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    cuuint64_t sdims[2] = {128, (cuuint64_t)n_tiles * ng};
+    cuuint64_t sstrides[1] = {256};
+    cuuint32_t sbox[2] = {(cuuint32_t)cb, (cuuint32_t)scale_rows};
+    r = g_encode(ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(scales), sdims, sstrides, sbox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    cuuint64_t xdims[3] = {32, (cuuint64_t)M, (cuuint64_t)(K / 32)};
+    cuuint64_t xstrides[2] = {(cuuint64_t)K * 2, 64};
+    cuuint32_t xbox[3] = {32, (cuuint32_t)M, (cuuint32_t)kDecStageRows};
+    r = g_encode(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), xdims, xstrides, xbox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
                        int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
                        const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0,
@@ -438,6 +508,37 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
     const Plan P = device_plan(st, M, N, K, G, fmt);
+    if (P.path == 3) {
+        DecodeParams d;
+        d.y = reinterpret_cast<__half*>(y);
+        d.bias = reinterpret_cast<const __half*>(bias);
+        d.residual = reinterpret_cast<const __half*>(residual);
+        // a timeout is reported in the caller's workspace (or the no-allocation
+        // array) when one is given, else in the library's own word for these kernels
+        d.status = own_ws ? st->gemv_status : reinterpret_cast<int*>(ws);
+        d.wait_limit_ns = g_wait_limit_ns;
+        d.act = act;
+        d.M = M;
+        d.N = N;
+        d.ng = P.ng;
+        d.g_shift = group_shift(G);
+        d.tile_rows = 2 * P.KC;
+        d.rows = K / 32;
+        d.stages = ceil_div(d.rows, kDecStageRows);
+        d.scale_rows = ((G & (G - 1)) == 0 && G <= kDecStageRows * 32) ? kDecStageRows * 32 / G : 1;
+        d.x_rows = M;
+        // slots for about 64 KB of packed words in flight, within the shared-memory budget
+        d.ring = kDecWordsInFlight / (kDecStageRows * P.dec_cb * 16);
+        if (d.ring > kDecSmemBudget / decode_slot_bytes(P.dec_cb, M)) d.ring = kDecSmemBudget / decode_slot_bytes(P.dec_cb, M);
+        if (d.ring > kDecMaxRing) d.ring = kDecMaxRing;
+        if (d.ring < 2) return W4A16_ERR_INVALID_ARG;   // cannot happen for M <= 16
+        CUtensorMap tw, ts, tx;
+        if (!encode_decode_maps(&tw, &ts, &tx, packed, scales_packed, x, P.n_tiles, d.tile_rows, P.ng, P.dec_cb,
+                                d.scale_rows, M, K))
+            return W4A16_ERR_INVALID_ARG;
+        const bool epi = bias || residual || act != 0;
+        return from_cuda(launch_decode(tw, ts, tx, d, P.dec_mr, P.dec_cb, epi, P.grid, stream));
+    }
     if (P.path == 1) {
         GemvParams g;
         g.x = reinterpret_cast<const __half*>(x);
@@ -799,7 +900,7 @@ w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* til
     if (rc != W4A16_OK) return rc;
     const Plan P = device_plan(st, M, N, K, G, kFmtW4);
     *path = P.path;
-    *tile_m = P.path == 1 ? P.gemv_mr : P.tm;
+    *tile_m = P.path == 1 ? P.gemv_mr : P.path == 3 ? P.dec_mr : P.tm;
     *grid = P.grid;
     return W4A16_OK;
 }
@@ -816,7 +917,7 @@ long long w4a16_set_wait_limit_ns(long long limit_ns)
 
 int w4a16_force_path(int path)
 {
-    if (path < 0 || path > 2) return -1;
+    if (path < 0 || path > 3) return -1;
     return g_force_path.exchange(path);
 }
 

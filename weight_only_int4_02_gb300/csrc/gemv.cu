@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
             const int nt = n0 >> 7;
             for (int st = 0; st < p.stages; ++st, ++seq) {
                 const int s = (int)(seq % kStages);
-                if (*abort_flag || !wait_warp<true>(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) {
+                if (__any_sync(0xffffffffu, *abort_flag != 0) || !wait_warp<true>(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) {
                     ok = false;
                     break;
                 }
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
         for (int b = blockIdx.x; b < p.blocks; b += gridDim.x) {
             for (int st = 0; st < p.stages; ++st, ++seq) {
                 const int s = (int)(seq % kStages);
-                if (*abort_flag || !wait_warp<true>(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) break;
+                if (__any_sync(0xffffffffu, *abort_flag != 0) || !wait_warp<true>(empty_bar(s), ((seq / kStages) & 1) ^ 1, ctl)) break;
                 float* xs = reinterpret_cast<float*>(smem + C::kOffX + s * C::kXBytes);
 #pragma unroll
                 for (int m = 0; m < MR; ++m) {
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xready_bar(s));   // release: the writes above precede the arrival
             }
-            if (*abort_flag) break;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
         }
     } else {
         // ------------------------------------------------------------ consumers

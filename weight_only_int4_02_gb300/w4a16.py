@@ -224,7 +224,8 @@ def set_wait_limit_ns(limit_ns):
 
 def force_path(path):
     """Force the dispatcher's choice for the 4-bit FP16 format: 0 automatic, 1 the
-    CUDA-core kernel wherever it applies (M <= 4), 2 the tensor-core kernel.
+    CUDA-core kernel wherever it applies (M <= 4), 2 the tensor-core kernel, 3 the
+    decode kernel wherever it applies (M <= 16, K a multiple of 32).
     Returns the previous setting."""
     prev = lib().w4a16_force_path(int(path))
     if prev < 0:
