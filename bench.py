@@ -310,12 +310,16 @@ def run_ours(args):
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("kernel wait timed out during warm-up")
 
-    # ---- a pool of graphs, one step each, with an event node at every change of M
-    # (launches of one M overlap through programmatic dependent launch; an event
-    # node between two launches would serialise them)
+    # ---- a pool of graphs, one step each, with an event node at every change of M.
+    # The event nodes hang off a side branch (forked after the group's last launch,
+    # joined at the end of the step): every launch follows the previous one directly,
+    # so launches overlap through programmatic dependent launch across the changes of
+    # M as well (an event node between two launches would serialise them). An event
+    # node records when every launch before it has completed.
     bounds = [0] + [ci for ci in range(1, len(per_case)) if per_case[ci]["M"] != per_case[ci - 1]["M"]]
     bounds.append(len(per_case))
     cap = torch.cuda.Stream()
+    side = torch.cuda.Stream()
     K = args.steps
     pool = min(K, 64)
     graphs, evs = [], []
@@ -329,7 +333,13 @@ def run_ours(args):
                 for ci in range(bounds[b], bounds[b + 1]):
                     c = per_case[ci]
                     w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
-                cud.record_external(ev[b + 1], st)
+                fork = torch.cuda.Event()
+                fork.record(st)
+                side.wait_event(fork)
+                cud.record_external(ev[b + 1], side)
+            join = torch.cuda.Event()
+            join.record(side)
+            st.wait_event(join)
         graphs.append(g)
         evs.append(ev)
     torch.cuda.synchronize()
@@ -452,7 +462,8 @@ def run_ours(args):
                    "parallelism": "single-gpu",
                    "l2": "inputs larger than L2: every GEMM reads its own copy of the packed weights "
                          "(%.0f MB distinct per step vs 129 MB L2)" % (distinct_bytes / 1e6),
-                   "timing": "CUDA Graph per step with an event node at every change of M; per-kernel "
+                   "timing": "CUDA Graph per step with an event node at every change of M, on a side "
+                             "branch (every launch follows the previous one directly); per-kernel "
                              "durations are the mean over the last %d steps of the timed region; "
                              "per_case_isolated has an event node after every launch (outside the timed "
                              "region), which removes the overlap of consecutive launches" % pool},
@@ -903,8 +914,8 @@ def run_e2e(per_case, G, dev, K, W):
     memory, all inside the timed region (one CUDA Graph per step). The copies run on
     two side streams so that they overlap the GEMMs: the GEMMs go by groups of equal M,
     largest M first; the first group's X is uploaded GEMM by GEMM and every later
-    group's X in one copy while earlier groups compute; each group's Y is downloaded in
-    one copy once its GEMMs are done, while later groups compute. What stays exposed
+    group's X in one copy while the first group computes; each group's Y is downloaded
+    in one copy once its GEMMs are done, while later groups compute. What stays exposed
     is the first GEMM's X and the last group's (smallest) Y."""
     import torch
     from weight_only_int4_02_gb300 import w4a16
@@ -951,12 +962,20 @@ def run_e2e(per_case, G, dev, K, W):
                 ev.record(up)
                 for i in ch:
                     ready[i] = ev
+        # Every launch follows the previous one directly (programmatic dependent
+        # launch) except where it waits for an upload: the first group's GEMMs each wait
+        # for their own X, and its last GEMM also for every later group's X (uploaded
+        # long before), so the later groups start without a wait.
         waited = set()
-        for grp in groups:
+        for gi, grp in enumerate(groups):
             for i in grp:
-                if id(ready[i]) not in waited:
-                    main.wait_event(ready[i])
-                    waited.add(id(ready[i]))
+                need = [ready[i]]
+                if gi == 0 and i == grp[-1]:
+                    need += [ready[j] for g2 in groups[1:] for j in g2]
+                for ev in need:
+                    if id(ev) not in waited:
+                        main.wait_event(ev)
+                        waited.add(id(ev))
                 c = per_case[i]
                 w4a16.gemm(xs[i], c["packed"], c["sp"], c["N"], G, y=ys[i], stream=main)
             done = torch.cuda.Event()
