@@ -708,12 +708,13 @@ def fused_epilogue_probe(G):
 def layer_chain_probe(G):
     """A Llama-2-7B-like decode layer as a chain of dependent GEMMs (each X is the
     previous output, so every launch waits for its predecessor before reading X):
-    QKV (4096 -> 12288), O (the first 4096 columns -> 4096, residual add fused),
-    gate/up (4096 -> 22016, SiLU fused), down (the first 11008 columns -> 4096,
-    residual add fused); the two column slices are torch copies (attention and the
-    gate product, which are not W4A16 work, would produce fresh tensors there).
-    Mean time per chain from a CUDA Graph of back-to-back chains over rotating
-    copies of the packed weights, at M = 1 and 16."""
+    QKV (4096 -> 12288), O (the first 4096 columns of QKV's output, read in place
+    through the row stride -> 4096, plus the layer input as residual), gate/up
+    (4096 -> 22016, SiLU fused), down (the first 11008 columns of gate/up's output ->
+    4096, plus O's output as residual). Four launches, nothing between them (attention
+    and the gate product, which are not W4A16 work, would sit where the column slices
+    are read). Mean time per chain from a CUDA Graph of back-to-back chains over
+    rotating copies of the packed weights, at M = 1 and 16."""
     import torch
     from weight_only_int4_02_gb300 import w4a16
     dims = [(4096, 12288), (4096, 4096), (4096, 22016), (11008, 4096)]
@@ -726,28 +727,23 @@ def layer_chain_probe(G):
     layer_bytes = sum(p[0].numel() * 4 + p[1].numel() * 2 for p in packs)
     rot = max(2, int(500e6 // layer_bytes) + 1)
     sets = [[(p[0].clone(), p[1].clone()) for p in packs] for _ in range(rot)]
-    out = {"layers": "QKV 4096x12288, O 4096x4096 (+residual), gate/up 4096x22016 (SiLU), down 11008x4096 (+residual)",
+    out = {"layers": "QKV 4096x12288, O 4096x4096 (+residual), gate/up 4096x22016 (SiLU), down 11008x4096 "
+                     "(+residual); slices read in place",
            "weight_bytes_per_chain": layer_bytes}
     reps = 20
     for M in (1, 16):
         x = torch.from_numpy(inputs.activations(M, 4096, 7)).cuda()
         h_qkv = torch.empty((M, 12288), dtype=torch.float16, device="cuda")
-        a_in = torch.empty((M, 4096), dtype=torch.float16, device="cuda")
         h_o = torch.empty((M, 4096), dtype=torch.float16, device="cuda")
         h_gu = torch.empty((M, 22016), dtype=torch.float16, device="cuda")
-        d_in = torch.empty((M, 11008), dtype=torch.float16, device="cuda")
         h_out = torch.empty((M, 4096), dtype=torch.float16, device="cuda")
 
         def chain(ws):
             st = torch.cuda.current_stream()
             w4a16.gemm(x, ws[0][0], ws[0][1], 12288, G, y=h_qkv, stream=st)
-            a_in.copy_(h_qkv[:, :4096])
-            h_o.copy_(x)
-            w4a16.gemm_fused(a_in, ws[1][0], ws[1][1], 4096, G, residual=h_o, y=h_o, stream=st)
-            w4a16.gemm_fused(h_o, ws[2][0], ws[2][1], 22016, G, activation="silu", y=h_gu, stream=st)
-            d_in.copy_(h_gu[:, :11008])
-            h_out.copy_(h_o)
-            w4a16.gemm_fused(d_in, ws[3][0], ws[3][1], 4096, G, residual=h_out, y=h_out, stream=st)
+            w4a16.gemm_strided(h_qkv[:, :4096], ws[1][0], ws[1][1], 4096, G, residual=x, y=h_o, stream=st)
+            w4a16.gemm_strided(h_o, ws[2][0], ws[2][1], 22016, G, activation="silu", y=h_gu, stream=st)
+            w4a16.gemm_strided(h_gu[:, :11008], ws[3][0], ws[3][1], 4096, G, residual=h_o, y=h_out, stream=st)
 
         for ws in sets:
             chain(ws)

@@ -172,6 +172,25 @@ w4a16_status w4a16_gemm_fused(const uint16_t* x, const uint32_t* packed,
                               const uint16_t* bias, const uint16_t* residual, int activation,
                               void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
+/*
+ * w4a16_gemm_fused on row-strided activations, outputs and residual: X row m
+ * starts at x + m * ldx, Y row m at y + m * ldy, residual row m at residual +
+ * m * ldr (elements). A layer can read the leading K columns of a wider output
+ * (the first 4096 of a fused QKV projection, the first 11008 of a gate/up
+ * projection) and write into a slice of a wider buffer without a copy; the pages
+ * have no counterpart (their kernels read contiguous activations).
+ *   ldx  >= K, a multiple of 8 (rows start on 16-byte boundaries)
+ *   ldy  >= N;   ldr >= N when residual is given (ignored otherwise)
+ * Every other argument, layout and error is that of w4a16_gemm_fused; the rows of
+ * Y must not overlap X or the residual (other than residual == y, same stride).
+ * Returns W4A16_ERR_INVALID_ARG for strides outside these bounds.
+ */
+w4a16_status w4a16_gemm_strided(const uint16_t* x, int ldx, const uint32_t* packed,
+                                const uint16_t* scales_packed, uint16_t* y, int ldy,
+                                int M, int N, int K, int group_size,
+                                const uint16_t* bias, const uint16_t* residual, int ldr, int activation,
+                                void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
 /* Bytes of the packed zero-points: ceil(N/128) * ceil(K/G) * 64 (two 4-bit
  * zero-points a byte). Returns 0 for invalid sizes. */
 size_t w4a16_zeros_bytes(int K, int N, int group_size);

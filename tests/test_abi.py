@@ -131,6 +131,15 @@ def test_invalid_arguments_return_before_any_device_work(lib):
     assert lib.w4a16_sp_pack(None, p, p, p, 64, 64, 64, None, None) == w.ERR_INVALID_ARG
     four = ctypes.c_void_p(ctypes.addressof(buf) + 4)
     assert lib.w4a16_sp_pack(p, p, p, p, 64, 64, 64, four, None) == w.ERR_INVALID_ARG
+    # row strides: ldx >= K and a multiple of 8, ldy >= N, ldr >= N with a residual
+    sg = lib.w4a16_gemm_strided   # (x, ldx, packed, scales, y, ldy, M, N, K, G, bias, residual, ldr, act, ws, n, s)
+    assert sg(p, 56, p, p, p, 64, 4, 64, 64, 64, None, None, 0, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert sg(p, 68, p, p, p, 64, 4, 64, 64, 64, None, None, 0, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert sg(p, 64, p, p, p, 60, 4, 64, 64, 64, None, None, 0, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert sg(p, 64, p, p, p, 64, 4, 64, 64, 64, None, p, 32, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert sg(p, 64, p, p, p, 64, 4, 64, 64, 64, None, p, 0, 0, None, 0, None) == w.ERR_INVALID_ARG
+    assert sg(p, 64, p, p, p, 64, 4, 64, 64, 64, None, None, 0, 3, None, 0, None) == w.ERR_INVALID_ARG
+    assert sg(p, 72, p, p, p, 80, 0, 64, 64, 64, None, None, 0, 0, None, 0, None) == w.OK   # M = 0
     # 8-bit codes
     assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 64, None, None, 3, None, 0, None) == w.ERR_INVALID_ARG
     assert lib.w4a16_w8_gemm(p, p, p, p, 4, 64, 64, 48, None, None, 0, None, 0, None) == w.ERR_INVALID_ARG

@@ -404,17 +404,18 @@ w4a16_status own_workspace(DeviceState* st, void** ws, size_t* bytes)
     return W4A16_OK;
 }
 
-// X as a 3-D view {64, M, K/64} (strides K*2 and 128 bytes) when K is a multiple of
-// 64, so one TMA brings a stage's KSUB blocks of 64 columns; else the plain 2-D
-// map {K, M}, one TMA per block, with the ragged K edge zero-filled.
-bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int ksub, bool allow_3d, int* is_3d,
-                  bool bf16 = false)
+// X (rows ldx elements apart) as a 3-D view {64, M, K/64} (strides 2 ldx and 128
+// bytes) when K is a multiple of 64, so one TMA brings a stage's KSUB blocks of 64
+// columns; else the plain 2-D map {K, M}, one TMA per block, with the ragged K edge
+// zero-filled.
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int ldx, int rows, int ksub, bool allow_3d,
+                  int* is_3d, bool bf16 = false)
 {
     const CUtensorMapDataType dtype = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint32_t estr[3] = {1, 1, 1};
     if (allow_3d && K % kChunkK == 0) {
         cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)M, (cuuint64_t)(K / kChunkK)};
-        cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kChunkK * 2};
+        cuuint64_t strides[2] = {(cuuint64_t)ldx * 2, (cuuint64_t)kChunkK * 2};
         cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)rows, (cuuint32_t)ksub};
         CUresult r = g_encode(map, dtype, 3, const_cast<void*>(x), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -425,7 +426,7 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int rows, int k
         }
     }
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
     cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)rows};
     CUresult r = g_encode(map, dtype, 2, const_cast<void*>(x), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -461,10 +462,11 @@ bool encode_gemv_maps(CUtensorMap* tw, CUtensorMap* ts, const void* packed, cons
 // Tensor maps of the decode kernel: the packed words as uint32 [n_tiles * tile_rows][512],
 // boxes of 16 rows x cb columns; the tile-ordered scales as 16-bit [n_tiles * ng][128],
 // boxes of scale_rows groups x cb columns; X as the 3-D view {32, M, K/32} (strides
-// 2K and 64 bytes; K is a multiple of 32), boxes of 32 values x M rows x 16 (every
+// 2 ldx and 64 bytes; K is a multiple of 32), boxes of 32 values x M rows x 16 (every
 // box in bounds: out-of-bounds rows measured slow to fill).
 bool encode_decode_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tx, const void* packed, const void* scales,
-                        const void* x, int n_tiles, int tile_rows, int ng, int cb, int scale_rows, int M, int K)
+                        const void* x, int n_tiles, int tile_rows, int ng, int cb, int scale_rows, int M, int K,
+                        int ldx)
 {
     cuuint32_t estr[3] = {1, 1, 1};
     cuuint64_t wdims[2] = {512, (cuuint64_t)n_tiles * tile_rows};
@@ -482,7 +484,7 @@ bool encode_decode_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tx, const
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     cuuint64_t xdims[3] = {32, (cuuint64_t)M, (cuuint64_t)(K / 32)};
-    cuuint64_t xstrides[2] = {(cuuint64_t)K * 2, 64};
+    cuuint64_t xstrides[2] = {(cuuint64_t)ldx * 2, 64};
     cuuint32_t xbox[3] = {32, (cuuint32_t)M, (cuuint32_t)kDecStageRows};
     r = g_encode(tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), xdims, xstrides, xbox, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -493,11 +495,18 @@ bool encode_decode_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tx, const
 w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t* scales_packed, uint16_t* y, int M,
                        int N, int K, int G, void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream,
                        const uint16_t* bias = nullptr, const uint16_t* residual = nullptr, int act = 0,
-                       int fmt = kFmtW4, const uint8_t* zeros_packed = nullptr)
+                       int fmt = kFmtW4, const uint8_t* zeros_packed = nullptr, int ldx = 0, int ldy = 0,
+                       int ldr = 0)
 {
     if ((fmt == kFmtW4Zp) != (zeros_packed != nullptr)) return W4A16_ERR_INVALID_ARG;
     G = norm_group(K, G);
     if (M < 0 || !valid_sizes(K, N, G)) return W4A16_ERR_INVALID_ARG;
+    // Row strides in elements (0: the dense [M][K] and [M][N] layouts). X rows start on
+    // 16-byte boundaries (the TMA maps' strides): ldx is a multiple of 8.
+    if (ldx == 0) ldx = K;
+    if (ldy == 0) ldy = N;
+    if (ldr == 0) ldr = N;
+    if (ldx < K || ldx % 8 != 0 || ldy < N || ldr < N) return W4A16_ERR_INVALID_ARG;
     if (M == 0) return W4A16_OK;
     if (!x || !packed || !scales_packed || !y) return W4A16_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(packed) || !aligned16(scales_packed) || !aligned16(y) ||
@@ -513,6 +522,8 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
         d.y = reinterpret_cast<__half*>(y);
         d.bias = reinterpret_cast<const __half*>(bias);
         d.residual = reinterpret_cast<const __half*>(residual);
+        d.ldy = ldy;
+        d.ldr = ldr;
         // a timeout is reported in the caller's workspace (or the no-allocation
         // array) when one is given, else in the library's own word for these kernels
         d.status = own_ws ? st->gemv_status : reinterpret_cast<int*>(ws);
@@ -534,7 +545,7 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
         if (d.ring < 2) return W4A16_ERR_INVALID_ARG;   // cannot happen for M <= 16
         CUtensorMap tw, ts, tx;
         if (!encode_decode_maps(&tw, &ts, &tx, packed, scales_packed, x, P.n_tiles, d.tile_rows, P.ng, P.dec_cb,
-                                d.scale_rows, M, K))
+                                d.scale_rows, M, K, ldx))
             return W4A16_ERR_INVALID_ARG;
         const bool epi = bias || residual || act != 0;
         return from_cuda(launch_decode(tw, ts, tx, d, P.dec_mr, P.dec_cb, epi, P.grid, stream));
@@ -543,6 +554,9 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
         GemvParams g;
         g.x = reinterpret_cast<const __half*>(x);
         g.y = reinterpret_cast<__half*>(y);
+        g.ldx = ldx;
+        g.ldy = ldy;
+        g.ldr = ldr;
         g.bias = reinterpret_cast<const __half*>(bias);
         g.residual = reinterpret_cast<const __half*>(residual);
         // a timeout is reported in the caller's workspace (or the no-allocation
@@ -599,12 +613,14 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.bias = reinterpret_cast<const __half*>(bias);
     p.residual = reinterpret_cast<const __half*>(residual);
     p.act = act;
+    p.ldy = ldy;
+    p.ldr = ldr;
 
     CUtensorMap map;
     // With one row tile, a box of M rows rounded up to the 8-row swizzle atom is
     // enough: MMA rows past M feed only output columns that are never stored.
     p.x_rows = P.m_tiles == 1 ? ((M + 7) / 8) * 8 : P.tm;
-    if (!encode_x_map(&map, x, M, K, p.x_rows, P.xblocks, true, &p.x_3d, fmt == kFmtW4Bf16))
+    if (!encode_x_map(&map, x, M, K, ldx, p.x_rows, P.xblocks, true, &p.x_3d, fmt == kFmtW4Bf16))
         return W4A16_ERR_INVALID_ARG;
     cudaError_t e;
     const bool epi = bias || residual || act != 0;
@@ -714,6 +730,20 @@ w4a16_status w4a16_gemm_fused(const uint16_t* x, const uint32_t* packed, const u
         return W4A16_ERR_INVALID_ARG;
     return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
                      reinterpret_cast<cudaStream_t>(stream), bias, residual, activation);
+}
+
+w4a16_status w4a16_gemm_strided(const uint16_t* x, int ldx, const uint32_t* packed, const uint16_t* scales_packed,
+                                uint16_t* y, int ldy, int M, int N, int K, int group_size, const uint16_t* bias,
+                                const uint16_t* residual, int ldr, int activation, void* workspace, size_t ws_bytes,
+                                w4a16_stream_t stream)
+{
+    if (activation < W4A16_ACT_NONE || activation > W4A16_ACT_RELU) return W4A16_ERR_INVALID_ARG;
+    if ((bias && (reinterpret_cast<uintptr_t>(bias) & 1)) || (residual && (reinterpret_cast<uintptr_t>(residual) & 1)))
+        return W4A16_ERR_INVALID_ARG;
+    if (ldx <= 0 || ldy <= 0 || (residual && ldr <= 0)) return W4A16_ERR_INVALID_ARG;
+    return gemm_impl(x, packed, scales_packed, y, M, N, K, group_size, workspace, ws_bytes, workspace == nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), bias, residual, activation, kFmtW4, nullptr, ldx, ldy,
+                     residual ? ldr : N);
 }
 
 size_t w4a16_zeros_bytes(int K, int N, int group_size)

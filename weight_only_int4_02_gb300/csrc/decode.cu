@@ -329,9 +329,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                     float v = 0.f;
 #pragma unroll
                     for (int w = 0; w < kConsumers; ++w) v += red[(w * MR + m) * CB + c];
-                    const size_t yi = (size_t)m * p.N + n;
-                    if constexpr (EPI) v = epilogue_op(p.act, v, ld16<false>(p.bias, n), ld16<false>(p.residual, yi));
-                    p.y[yi] = __float2half_rn(v);
+                    if constexpr (EPI)
+                        v = epilogue_op(p.act, v, ld16<false>(p.bias, n), ld16<false>(p.residual, (size_t)m * p.ldr + n));
+                    p.y[(size_t)m * p.ldy + n] = __float2half_rn(v);
                 }
             }
         }

@@ -16,10 +16,11 @@ constexpr int kDecStageRows = 16;   // rows of 32 values of k per pipeline stage
 struct DecodeParams {
     __half* y;               // [M][N]
     const __half* bias;      // [N] or null (fused epilogue)
-    const __half* residual;  // [M][N] or null (may be y itself)
+    const __half* residual;  // [M][ldr] or null (may be y itself)
     int* status;             // error word: bit 0 = a wait timed out
     long long wait_limit_ns;
     int act;                 // 0 none, 1 SiLU, 2 ReLU
+    int ldy, ldr;            // row strides (elements) of y and the residual: >= N
     int M, N, ng;
     int g_shift;             // log2(G) for G a power of two; 30 for one group
     int tile_rows;           // rows of 32 k per column tile in the packed layout: 2 * KC
@@ -45,7 +46,7 @@ constexpr int decode_smem_bytes(int cb, int x_rows, int ring)
 // Tensor maps (built on the host):
 //   tmap_w: the packed words as uint32 [n_tiles * tile_rows][512], box {cb * 4, 16};
 //   tmap_s: the tile-ordered scales as 16-bit [n_tiles * ng][128], box {cb, scale_rows};
-//   tmap_x: X as 16-bit {32, M, K / 32} with strides {2K, 64} bytes, box {32, M, 16},
+//   tmap_x: X as 16-bit {32, M, K / 32} with strides {2 ldx, 64} bytes, box {32, M, 16},
 //           so a stage lands as [16 rows of k][M rows of X][32 values].
 // mr: 8 or 16 (rows of X the kernel is built for, >= M); cb: 16, 32 or 64; grid = ceil(N / cb);
 // the dynamic shared memory is decode_smem_bytes(cb, M, p.ring).

@@ -81,8 +81,9 @@ struct GemmParams {
     // Fused epilogue, applied to every FP32 result before its rounding to FP16:
     // y = act(v + bias[n]) + residual[m][n]. Null pointers and act 0 leave v as is.
     const __half* bias;      // [N] or null
-    const __half* residual;  // [M][N] or null (may be y itself)
+    const __half* residual;  // [M][ldr] or null (may be y itself)
     int act;                 // 0 none, 1 SiLU, 2 ReLU
+    int ldy, ldr;            // row strides (elements) of y and the residual: >= N
 };
 
 // The fused epilogue on the FP32 result v: act(v + b) + r, with b and r already
@@ -352,9 +353,9 @@ __device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo,
             for (int e = 0; e < CPR; ++e) {
                 if (q0 + e >= ncols) continue;
                 const int m = m0 + m_first + nw * (q0 + e);
-                __half* out = p.y + (size_t)m * p.N + n;
+                __half* out = p.y + (size_t)m * p.ldy + n;
                 if constexpr (EPI) {
-                    const size_t ri = (size_t)m * p.N + n;
+                    const size_t ri = (size_t)m * p.ldr + n;
                     const float r0 = ld16<BF>(p.residual, ri), r1 = ld16<BF>(p.residual, ri + 1);
                     const float r2 = ld16<BF>(p.residual, ri + 2), r3 = ld16<BF>(p.residual, ri + 3);
                     out[0] = st16<BF>(epilogue_op(p.act, acc[e].x, b4[0], r0));
@@ -751,20 +752,20 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int m = m0 + c * 16 + e;
-                                rv[e] = m < p.M ? ld16<BF>(p.residual, (size_t)m * p.N + n) : 0.f;
+                                rv[e] = m < p.M ? ld16<BF>(p.residual, (size_t)m * p.ldr + n) : 0.f;
                             }
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int m = m0 + c * 16 + e;
                                 if (m < p.M)
-                                    p.y[(size_t)m * p.N + n] =
+                                    p.y[(size_t)m * p.ldy + n] =
                                         st16<BF>(epilogue_op(p.act, __uint_as_float(r[e]), bv, rv[e]));
                             }
                         } else {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int m = m0 + c * 16 + e;
-                                if (m < p.M) p.y[(size_t)m * p.N + n] = st16<BF>(__uint_as_float(r[e]));
+                                if (m < p.M) p.y[(size_t)m * p.ldy + n] = st16<BF>(__uint_as_float(r[e]));
                             }
                         }
                     }

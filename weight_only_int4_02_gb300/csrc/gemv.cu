@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
                         const int k = st * kGemvStageK + kl;
                         float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
                         if (m < p.M && k < p.K) {
-                            const uint4 xv = ld_x16(p.x + (size_t)m * p.K + k);
+                            const uint4 xv = ld_x16(p.x + (size_t)m * p.ldx + k);
                             const float2 a = __half22float2(u32_as_half2(xv.x)), b2 = __half22float2(u32_as_half2(xv.y));
                             const float2 c = __half22float2(u32_as_half2(xv.z)), d = __half22float2(u32_as_half2(xv.w));
                             lo = make_float4(a.x, a.y, b2.x, b2.y);
@@ -322,10 +322,9 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) v += red[w][m][c];
                 if (m < p.M && nn < p.N) {
-                    const size_t i = (size_t)m * p.N + nn;
                     if constexpr (EPI)
-                        v = epilogue_op(p.act, v, ld16<false>(p.bias, nn), ld16<false>(p.residual, i));
-                    p.y[i] = __float2half_rn(v);
+                        v = epilogue_op(p.act, v, ld16<false>(p.bias, nn), ld16<false>(p.residual, (size_t)m * p.ldr + nn));
+                    p.y[(size_t)m * p.ldy + nn] = __float2half_rn(v);
                 }
             }
             named_bar_sync(1, 32 * kConsumerWarps);

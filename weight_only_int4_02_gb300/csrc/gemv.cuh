@@ -14,10 +14,11 @@ constexpr int kGemvThreads = 320;     // 8 consumer warps, 1 producer warp, 1 X 
 constexpr int kGemvStageK = 1024;     // values of k per pipeline stage (32 rows of 32)
 
 struct GemvParams {
-    const __half* x;         // [M][K]
-    __half* y;               // [M][N]
+    const __half* x;         // [M][ldx]
+    __half* y;               // [M][ldy]
     const __half* bias;      // [N] or null (fused epilogue)
-    const __half* residual;  // [M][N] or null (may be y itself)
+    const __half* residual;  // [M][ldr] or null (may be y itself)
+    int ldx, ldy, ldr;       // row strides (elements): ldx >= K, ldy and ldr >= N
     int* status;             // error word: bit 0 = a wait timed out
     long long wait_limit_ns;
     int act;                 // 0 none, 1 SiLU, 2 ReLU

@@ -20,7 +20,7 @@ EXPORTS = ["w4a16_layout_version", "w4a16_status_string", "w4a16_last_cuda_error
            "w4a16_check_device_status", "w4a16_plan", "w4a16_gemm_noalloc", "w4a16_gemm_fused",
            "w4a16_zeros_bytes", "w4a16_pack_zeros", "w4a16_gemm_zp", "w4a16_w8_packed_bytes", "w4a16_w8_pack",
            "w4a16_w8_gemm", "w4a16_bf16_gemm", "w4a16_sp_packed_bytes", "w4a16_sp_pack", "w4a16_sp_gemm",
-           "w4a16_selftest_wait_timeout", "w4a16_force_path", "w4a16_set_wait_limit_ns"]
+           "w4a16_selftest_wait_timeout", "w4a16_force_path", "w4a16_set_wait_limit_ns", "w4a16_gemm_strided"]
 
 ACTIVATIONS = {"none": 0, "silu": 1, "relu": 2}
 
@@ -70,6 +70,8 @@ def lib():
         L.w4a16_gemm_noalloc.restype = I
         L.w4a16_gemm_fused.argtypes = [P, P, P, P, I, I, I, I, P, P, I, P, Z, P]
         L.w4a16_gemm_fused.restype = I
+        L.w4a16_gemm_strided.argtypes = [P, I, P, P, P, I, I, I, I, I, P, P, I, I, P, Z, P]
+        L.w4a16_gemm_strided.restype = I
         L.w4a16_zeros_bytes.argtypes = [I, I, I]
         L.w4a16_zeros_bytes.restype = Z
         L.w4a16_pack_zeros.argtypes = [P, P, I, I, I, P]
@@ -135,6 +137,18 @@ def check_buffers(x, packed, scales_packed, N, group_size, y, weight_format="int
             raise W4A16Error(ERR_INVALID_ARG, "%s hold %d bytes, the shape needs %d" % (what, _nbytes(t), need))
     if tuple(y.shape) != (M, N) or y.element_size() != 2:
         raise W4A16Error(ERR_INVALID_ARG, "y must be a 16-bit [M][N] tensor")
+
+
+def check_buffers_weights(packed, scales_packed, K, N, group_size):
+    """check_buffers for the weights alone (the activations may be strided views)."""
+    need_w, need_s = packed_words(K, N, group_size) * 4, scales_elems(K, N, group_size) * 2
+    if need_w == 0 or need_s == 0:
+        return
+    for t, need, what in ((packed, need_w, "packed weights"), (scales_packed, need_s, "packed scales")):
+        if not t.is_contiguous():
+            raise W4A16Error(ERR_INVALID_ARG, "%s is not contiguous" % what)
+        if _nbytes(t) < need:
+            raise W4A16Error(ERR_INVALID_ARG, "%s hold %d bytes, the shape needs %d" % (what, _nbytes(t), need))
 
 
 def layout_version():
@@ -265,6 +279,34 @@ def gemm_fused(x, packed, scales_packed, N, group_size, bias=None, residual=None
     _check(lib().w4a16_gemm_fused(_ptr(x), _ptr(packed), _ptr(scales_packed), _ptr(y), M, N, K, group_size,
                                   _ptr(bias), _ptr(residual), ACTIVATIONS[activation], _ptr(workspace), ws_bytes,
                                   _stream(stream)), "w4a16_gemm_fused")
+    return y
+
+
+def _row_stride(t, cols, name):
+    """Elements between rows of a 2-D float16 CUDA view whose rows are contiguous."""
+    assert t.dtype == torch.float16 and t.is_cuda and t.dim() == 2, name
+    assert t.shape[1] == cols and (t.stride(1) == 1 or t.shape[1] == 1), name
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), cols)
+
+
+def gemm_strided(x, packed, scales_packed, N, group_size, bias=None, residual=None, activation="none", y=None,
+                 workspace=None, stream=None):
+    """gemm_fused on row-strided 2-D views (rows contiguous, rows any distance apart):
+    x may be the leading K columns of a wider tensor, y and residual slices of wider
+    buffers; the strides are taken from the views."""
+    M, K = x.shape
+    ldx = _row_stride(x, K, "x")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    ldy = _row_stride(y, N, "y")
+    ldr = _row_stride(residual, N, "residual") if residual is not None else 0
+    if bias is not None:
+        assert bias.dtype == torch.float16 and bias.is_cuda and bias.is_contiguous() and tuple(bias.shape) == (N,)
+    check_buffers_weights(packed, scales_packed, K, N, group_size)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().w4a16_gemm_strided(_ptr(x), ldx, _ptr(packed), _ptr(scales_packed), _ptr(y), ldy, M, N, K,
+                                    group_size, _ptr(bias), _ptr(residual), ldr, ACTIVATIONS[activation],
+                                    _ptr(workspace), ws_bytes, _stream(stream)), "w4a16_gemm_strided")
     return y
 
 
