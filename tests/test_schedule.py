@@ -62,7 +62,7 @@ def decode_plan(M, N, K, G, sms=SMS):
     for one to sixteen rows of X, one CTA per block of cb output columns (64 when
     that gives at least one block per SM, else 16) over the whole of K."""
     mr = 8 if M <= 8 else 16
-    cb = 64 if ceil_div(N, 64) >= sms else 16
+    cb = 128 if ceil_div(N, 128) >= 2 * sms else 64 if ceil_div(N, 64) >= sms else 16
     blocks = ceil_div(N, cb)
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     rows = K // 32
@@ -95,52 +95,62 @@ def dispatch(M, N, K, G, sms=SMS, fmt="int4", force=0):
 
 def check_decode_shape(M, N, K, G, sms=SMS):
     """Mirror of the decode kernel's indexing. In one column block every (column,
-    row of 32 k, word) is unpacked by exactly one lane of one warp of one team, and
-    the shared-memory word it reads is the global word of layout v2 that holds that
-    column's codes; the X it reads lies inside X; every block's copies stay inside
-    its own tile of the packed words and scales; every Y element is written once;
-    the ring, the reduction and the shared memory fit."""
+    row of 32 k, word) is unpacked by exactly one lane of one warp (the stage's team
+    for blocks of 16 to 64 columns; with 128 columns both teams take every stage, each
+    its own 64), and the shared-memory word it reads (one TMA box per 64 columns) is the
+    global word of layout v2 that holds that column's codes; the X it reads lies inside
+    X; every block's copies stay inside its own tile of the packed words and scales;
+    every Y element is written once; the ring, the reduction and the shared memory fit."""
     P = decode_plan(M, N, K, G, sms)
     cb, mr, rows = P["cb"], P["mr"], P["rows"]
+    col_teams = cb == 128
+    warp_cols = 64 if col_teams else cb
+    box_cols = min(cb, 64)
     assert K % 32 == 0 and M <= DECODE_MAX_M
     assert 2 <= P["ring"] <= DEC_MAX_RING
-    assert 8 * mr * cb * 4 <= P["ring"] * DEC_STAGE_ROWS * cb * 16      # warps' sums fit the weight ring
-    assert 2 * (P["smem"] + 1024) <= 228 * 1024                          # two CTAs per SM
-    assert 128 % cb == 0
+    assert 8 * mr * warp_cols * 4 <= P["ring"] * DEC_STAGE_ROWS * cb * 16    # warps' sums fit the weight ring
+    assert 2 * (P["smem"] + 1024) <= 228 * 1024                              # two CTAs per SM
+    assert 128 % cb == 0 and box_cols * 4 <= 256                             # TMA boxes of at most 256 words
     # one block, every lane's reads
     seen = set()
     for st in range(P["stages"]):
-        team = st % 2
+        teams = (0, 1) if col_teams else (st % 2,)
         g0 = min((st * DEC_STAGE_ROWS * 32) >> P["g_shift"], P["ng"] - 1)
-        for wl in range(4):
-            for rr in range(4):
-                rl = 4 * wl + rr
-                row = st * DEC_STAGE_ROWS + rl
-                if row >= rows:
-                    continue
-                gl = min((row * 32) >> P["g_shift"], P["ng"] - 1) - g0
-                assert 0 <= gl < P["scale_rows"]
-                for lane in range(32):
-                    g, t = lane >> 2, lane & 3
-                    for h in range(mr // 8):
-                        m = min(8 * h + g, M - 1)
-                        assert 0 <= m < M and row * 32 + 8 * t + 7 < K
-                    for sb in range(cb // 16):
-                        for off in (0, 8):
-                            nl = 16 * sb + g + off
-                            smem_word = (rl * cb + nl) * 4 + t               # in the slot's [16][cb][4] words
-                            assert smem_word < DEC_STAGE_ROWS * cb * 4
-                            key = (nl, row, t)
-                            assert key not in seen
-                            seen.add(key)
-                            # the box starts at word (n0 & 127) * 4 of map row nt * tile_rows + st * 16
-                            box_row, box_col = divmod(smem_word, cb * 4)
-                            map_row = st * DEC_STAGE_ROWS + box_row              # within the tile
-                            kc, jj = divmod(map_row, 2)
-                            word_in_row = box_col                                # + (n0 & 127) * 4
-                            assert (map_row, word_in_row) == (row, nl * 4 + t)
-                            # layout v2: word (kc, jj, n_in, wd) holds k = 64 kc + 32 jj + 8 wd .. +7
-                            assert 64 * kc + 32 * jj + 8 * t == row * 32 + 8 * t
+        for team in teams:
+            cbase = 64 * team if col_teams else 0
+            for wl in range(4):
+                for rr in range(4):
+                    rl = 4 * wl + rr
+                    row = st * DEC_STAGE_ROWS + rl
+                    if row >= rows:
+                        continue
+                    gl = min((row * 32) >> P["g_shift"], P["ng"] - 1) - g0
+                    assert 0 <= gl < P["scale_rows"]
+                    assert gl * cb + cbase + 7 + 16 * (warp_cols // 16 - 1) + 8 < DEC_STAGE_ROWS * cb   # scales
+                    for lane in range(32):
+                        g, t = lane >> 2, lane & 3
+                        for h in range(mr // 8):
+                            m = min(8 * h + g, M - 1)
+                            assert 0 <= m < M and row * 32 + 8 * t + 7 < K
+                        for sb in range(warp_cols // 16):
+                            for off in (0, 8):
+                                nl = cbase + 16 * sb + g + off
+                                bx, nb = divmod(nl, box_cols)
+                                smem_word = bx * DEC_STAGE_ROWS * box_cols * 4 + (rl * box_cols + nb) * 4 + t
+                                assert smem_word < DEC_STAGE_ROWS * cb * 4
+                                key = (nl, row, t)
+                                assert key not in seen
+                                seen.add(key)
+                                # box bx starts at word ((n0 & 127) + 64 bx) * 4 of map row
+                                # nt * tile_rows + st * 16
+                                within = smem_word - bx * DEC_STAGE_ROWS * box_cols * 4
+                                box_row, box_col = divmod(within, box_cols * 4)
+                                map_row = st * DEC_STAGE_ROWS + box_row              # within the tile
+                                kc, jj = divmod(map_row, 2)
+                                word_in_row = bx * box_cols * 4 + box_col            # + (n0 & 127) * 4
+                                assert (map_row, word_in_row) == (row, nl * 4 + t)
+                                # layout v2: word (kc, jj, n_in, wd) holds k = 64 kc + 32 jj + 8 wd .. +7
+                                assert 64 * kc + 32 * jj + 8 * t == row * 32 + 8 * t
     assert len(seen) == cb * rows * 4
     # every block: copies inside its tile, Y written once
     cols = set()
@@ -362,7 +372,7 @@ def test_gemv_column_block_widths():
 
 DECODE_SHAPES = sorted(set((m, n, k, g) for (m, n, k, g) in SHAPES if m <= DECODE_MAX_M and k % 32 == 0
                            and n * k <= 22016 * 4096)
-                       | {(1, 73728, 18432, 128), (8, 73728, 18432, 128), (16, 12288, 4096, 128),
+                       | {(1, 73728, 18432, 128), (8, 73728, 18432, 128), (16, 73728, 18432, 128), (16, 12288, 4096, 128),
                           (9, 1024, 2048, 64), (2, 264, 544, 32), (13, 4104, 1024, 128), (1, 4096, 4000, 4000)})
 
 
@@ -374,13 +384,15 @@ def test_decode_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
 def test_dispatch_rule():
     """The automatic choice for the 4-bit FP16 format: the decode kernel (path 3) for
     up to eight rows of X where K is a multiple of 32, the tensor-core kernel
-    otherwise; blocks of 64 columns for the layers 12288 wide and wider, 16 for the
-    4096-wide ones (measured on GB300)."""
+    otherwise; blocks of 128 columns for the 73728-wide layer (576 blocks, two per SM
+    and more), 64 for the 12288- and 22016-wide ones, 16 for the 4096-wide ones
+    (measured on GB300)."""
+    width = {4096: 16, 12288: 64, 22016: 64, 73728: 128}
     for (N, K) in [(4096, 4096), (12288, 4096), (22016, 4096), (4096, 11008), (73728, 18432)]:
         for M in (1, 2, 4, 8):
             P = dispatch(M, N, K, 128)
             assert P["path"] == 3 and P["tm"] == 8
-            assert P["cb"] == (16 if N == 4096 else 64)
+            assert P["cb"] == width[N]
         assert dispatch(9, N, K, 128)["path"] == 2
         assert dispatch(16, N, K, 128, force=3)["path"] == 3 and dispatch(16, N, K, 128, force=3)["tm"] == 16
         assert dispatch(17, N, K, 128, force=3)["path"] == 2

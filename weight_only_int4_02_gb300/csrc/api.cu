@@ -108,7 +108,7 @@ long long g_wait_limit_ns = 1000000000LL;
 int g_force_split = 0;
 int g_force_min_iters = 0;
 int g_force_tm = 0;   // W4A16_TILE_M: rows of X per tile (16, 32, 64, 128 or 256) for the tensor-core kernel
-int g_force_cb = 0;   // W4A16_DECODE_CB: columns per block (16, 32 or 64) for the decode kernel
+int g_force_cb = 0;   // W4A16_DECODE_CB: columns per block (16, 32, 64 or 128) for the decode kernel
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -252,17 +252,19 @@ bool gemv_applies(int M, int fmt, int force)
     return fmt == kFmtW4 && M <= kGemvMaxM && force == 1;
 }
 
-// Path 3 (decode kernel) for a shape: blocks of 64 columns where that gives at least
-// one block per SM (each row of a block is then 1 KB of contiguous packed words),
-// else of 16 (more CTAs for narrow layers); one CTA per block. Measured on the
-// decode layers: N = 4096 is fastest with 16, N >= 12288 with 64; 32 was never best.
+// Path 3 (decode kernel) for a shape: blocks of 128 columns (whole 2 KB rows of
+// packed words, X read once per 128 columns) where that gives two blocks per SM, else
+// of 64 (1 KB of each row) where that gives one, else of 16 (more CTAs for narrow
+// layers); one CTA per block. Measured on GB300: 18432 x 73728 at M = 1 119.4 us with
+// 128 against 121.3 with 64; 4096 x 22016 14.6 us with 64 against 15.1 with 128;
+// N = 4096 fastest with 16; 32 was never best.
 Plan make_decode_plan(int M, int N, int K, int G, int sms)
 {
     Plan P = {};
     P.path = 3;
     P.dec_mr = M <= 8 ? 8 : 16;
-    int cb = ceil_div(N, 64) >= sms ? 64 : 16;
-    if (g_force_cb == 16 || g_force_cb == 32 || g_force_cb == 64) cb = g_force_cb;
+    int cb = ceil_div(N, 128) >= 2 * sms ? 128 : ceil_div(N, 64) >= sms ? 64 : 16;
+    if (g_force_cb == 16 || g_force_cb == 32 || g_force_cb == 64 || g_force_cb == 128) cb = g_force_cb;
     P.dec_cb = cb;
     P.grid = ceil_div(N, cb);
     P.n_tiles = ceil_div(N, kTileN);
@@ -471,7 +473,7 @@ bool encode_decode_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tx, const
     cuuint32_t estr[3] = {1, 1, 1};
     cuuint64_t wdims[2] = {512, (cuuint64_t)n_tiles * tile_rows};
     cuuint64_t wstrides[1] = {2048};
-    cuuint32_t wbox[2] = {(cuuint32_t)cb * 4, (cuuint32_t)kDecStageRows};
+    cuuint32_t wbox[2] = {(cuuint32_t)(cb < 64 ? cb : 64) * 4, (cuuint32_t)kDecStageRows};   // 128: two boxes
     CUresult r = g_encode(tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(packed), wdims, wstrides, wbox,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -78,16 +78,24 @@ constexpr int kProdX = kConsumers + 1;
 static_assert(kDecThreads == 32 * (kConsumers + 2), "warp roles");
 static_assert(kDecStageRows == 2 * kConsumers, "two rows of a stage per consumer warp");
 
-// Shared memory: [ring][16][CB][16 bytes] packed words, [ring][16][CB] scales,
-// [ring][16][x_rows][64 bytes] X, then the barriers. The ring depth and X's rows
-// are launch parameters (offsets computed at run time).
+// Shared memory: [ring][CB / 64 or 1][16][min(CB, 64)][16 bytes] packed words (one
+// TMA box per 64 columns), [ring][16][CB] scales, [ring][16][x_rows][64 bytes] X,
+// then the barriers. The ring depth and X's rows are launch parameters (offsets
+// computed at run time). With 128-column blocks the two consumer teams split the
+// columns (64 each) and both take every stage; with 16 to 64 they take the stages in
+// turn over all columns.
 template <int MR, int CB>
 struct DecCfg {
+    static constexpr bool kColTeams = CB == 128;
+    static constexpr int kWarpCols = kColTeams ? 64 : CB;     // output columns of one consumer warp
+    static constexpr int kBoxCols = CB > 64 ? 64 : CB;        // columns of one weight TMA box
+    static constexpr int kBoxBytes = kDecStageRows * kBoxCols * 16;
     static constexpr int kWBytes = kDecStageRows * CB * 16;   // packed words: [16 rows][CB][4 words]
     static constexpr int kSBytes = kDecStageRows * CB * 2;    // up to 16 rows of group scales (G = 32)
-    static constexpr int kRedBytes = kConsumers * MR * CB * 4;  // per-warp sums, placed over the weight ring
+    static constexpr int kRedBytes = kConsumers * MR * kWarpCols * 4;  // per-warp sums, over the weight ring
     static constexpr int kMaxSmem = kDecSmemBudget + 3 * kDecMaxRing * 8 + 16 + 128;
     static_assert(kRedBytes <= 2 * kWBytes, "the final reduction fits in a weight ring of two slots");
+    static_assert(CB % kBoxCols == 0 && kBoxCols * 4 <= 256, "weight boxes of at most 256 words");
 };
 
 // d = a * b (the accumulator starts from zero)
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                                                                      const DecodeParams p)
 {
     using C = DecCfg<MR, CB>;
-    constexpr int NSB = CB / 16;   // 16-column sub-blocks
+    constexpr int NSB = C::kWarpCols / 16;   // 16-column sub-blocks of a consumer warp
     constexpr int NH = MR / 8;     // 8-row halves of X
     const int S = p.ring;
     const int xb = kDecStageRows * p.x_rows * 64;   // X bytes of a slot
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
         for (int s = 0; s < S; ++s) {
             mbar_init(wfull_bar(s), 1);
             mbar_init(xfull_bar(s), 1);
-            mbar_init(empty_bar(s), kConsumers / 2);   // the stage's team
+            mbar_init(empty_bar(s), C::kColTeams ? kConsumers : kConsumers / 2);   // the warps that take the stage
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -203,8 +211,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                 } else {
                     const int g0 = min((st * kDecStageRows * 32) >> p.g_shift, p.ng - 1);
                     mbar_arrive_expect_tx(wfull_bar(s), w_tx);
-                    tma_load_2d(sbase + s * C::kWBytes, &tmap_w, wfull_bar(s), (n0 & 127) * 4,
-                                nt * p.tile_rows + st * kDecStageRows);
+#pragma unroll
+                    for (int bx = 0; bx < CB / C::kBoxCols; ++bx)
+                        tma_load_2d(sbase + s * C::kWBytes + bx * C::kBoxBytes, &tmap_w, wfull_bar(s),
+                                    ((n0 & 127) + bx * C::kBoxCols) * 4, nt * p.tile_rows + st * kDecStageRows);
                     tma_load_2d(sbase + off_s + s * C::kSBytes, &tmap_s, wfull_bar(s), n0 & 127, nt * p.ng + g0);
                 }
             }
@@ -224,9 +234,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
         // The residual may be the previous kernel's output, and Y may still be read by it.
         wait_prior_grid();
         const int g = lane >> 2, t = lane & 3;
-        // Two teams of four warps take the stages in turn; warp wl of a team takes
-        // rows 4wl .. 4wl+3 (128 values of k: one group when G >= 128).
+        // Two teams of four warps take the stages in turn (or, with 128-column blocks,
+        // every stage for their own 64 columns); warp wl of a team takes rows
+        // 4wl .. 4wl+3 of a stage (128 values of k: one group when G >= 128).
         const int team = warp >> 2, wl = warp & 3;
+        const int cbase = C::kColTeams ? team * C::kWarpCols : 0;   // the warp's first column in the block
+        constexpr int kStep = C::kColTeams ? 1 : 2;                  // stages between two of a warp's stages
         const int rpg = p.g_shift >= 7 ? 4 : 1 << (p.g_shift - 5);   // rows per group: 4, 2 (G = 64) or 1 (G = 32)
         float acc[NSB][NH][4];
 #pragma unroll
@@ -236,9 +249,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[sb][h][e] = 0.f;
         bool ok = true;
-        int s = team;   // slot of stage st; S >= 2
+        int s = C::kColTeams ? 0 : team;   // slot of stage st; S >= 2
         uint32_t ph = 0;
-        for (int st = team; st < p.stages; st += 2) {
+        for (int st = C::kColTeams ? 0 : team; st < p.stages; st += kStep) {
             if (!wait_warp<true>(wfull_bar(s), ph, ctl) || !wait_warp<true>(xfull_bar(s), ph, ctl)) {
                 ok = false;
                 break;
@@ -258,7 +271,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
                         xv[h] = *reinterpret_cast<const uint4*>(xa + min(8 * h + g, p.x_rows - 1) * 64);
-                    const uint8_t* wa = smem + s * C::kWBytes + (rl * CB + g) * 16 + t * 4;
+                    // the box of the warp's columns; within it column 16 sb + g (and + 8) of row rl
+                    const uint8_t* wa = smem + s * C::kWBytes + (cbase / C::kBoxCols) * C::kBoxBytes +
+                                        (rl * C::kBoxCols + cbase % C::kBoxCols + g) * 16 + t * 4;
                     const bool first = (rr & (rpg - 1)) == 0;
 #pragma unroll
                     for (int sb = 0; sb < NSB; ++sb) {
@@ -280,7 +295,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                         // the group's sums, times the scales of columns g and g + 8 of
                         // each sub-block, go to the running sums
                         const int gl = min((row * 32) >> p.g_shift, p.ng - 1) - g0;
-                        const __half* sc = reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) + gl * CB + g;
+                        const __half* sc =
+                            reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) + gl * CB + cbase + g;
 #pragma unroll
                         for (int sb = 0; sb < NSB; ++sb) {
                             const float s_lo = __half2float(sc[16 * sb]), s_hi = __half2float(sc[16 * sb + 8]);
@@ -297,7 +313,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
-            s += 2;
+            s += kStep;
             if (s >= S) {
                 s -= S;
                 ph ^= 1;
@@ -305,7 +321,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
         }
 
         // Every consumer is done with the ring (or gave up): the weight ring holds
-        // the warps' sums, [warp][MR][CB], added in warp order.
+        // the warps' sums, [warp][MR][the warp's columns], added in warp order over
+        // the warps that hold a column (all eight, or the four of its team).
+        constexpr int WC = C::kWarpCols;
         named_bar_sync(1, 32 * kConsumers);
         float* red = reinterpret_cast<float*>(smem);
         if (ok) {
@@ -314,11 +332,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     const int m = 8 * h + 2 * t, c = 16 * sb + g;
-                    float* r = red + (warp * MR + m) * CB + c;
+                    float* r = red + (warp * MR + m) * WC + c;
                     r[0] = acc[sb][h][0];
-                    r[CB] = acc[sb][h][1];
+                    r[WC] = acc[sb][h][1];
                     r[8] = acc[sb][h][2];
-                    r[CB + 8] = acc[sb][h][3];
+                    r[WC + 8] = acc[sb][h][3];
                 }
         }
         named_bar_sync(1, 32 * kConsumers);
@@ -327,8 +345,14 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                 const int m = i / CB, c = i % CB, n = n0 + c;
                 if (m < p.M && n < p.N) {
                     float v = 0.f;
+                    if constexpr (C::kColTeams) {
+                        const int tm = c / WC, cl = c % WC;
 #pragma unroll
-                    for (int w = 0; w < kConsumers; ++w) v += red[(w * MR + m) * CB + c];
+                        for (int w = 0; w < kConsumers / 2; ++w) v += red[((tm * 4 + w) * MR + m) * WC + cl];
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < kConsumers; ++w) v += red[(w * MR + m) * WC + c];
+                    }
                     if constexpr (EPI)
                         v = epilogue_op(p.act, v, ld16<false>(p.bias, n), ld16<false>(p.residual, (size_t)m * p.ldr + n));
                     p.y[(size_t)m * p.ldy + n] = __float2half_rn(v);
@@ -371,6 +395,7 @@ cudaError_t launch_mr(const CUtensorMap& tw, const CUtensorMap& ts, const CUtens
         case 16: return launch_one<MR, 16>(tw, ts, tx, p, epi, grid, stream);
         case 32: return launch_one<MR, 32>(tw, ts, tx, p, epi, grid, stream);
         case 64: return launch_one<MR, 64>(tw, ts, tx, p, epi, grid, stream);
+        case 128: return launch_one<MR, 128>(tw, ts, tx, p, epi, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -381,7 +406,8 @@ cudaError_t setup_mr()
     cudaError_t e;
     if ((e = setup_one<MR, 16, false>()) != cudaSuccess || (e = setup_one<MR, 16, true>()) != cudaSuccess ||
         (e = setup_one<MR, 32, false>()) != cudaSuccess || (e = setup_one<MR, 32, true>()) != cudaSuccess ||
-        (e = setup_one<MR, 64, false>()) != cudaSuccess || (e = setup_one<MR, 64, true>()) != cudaSuccess)
+        (e = setup_one<MR, 64, false>()) != cudaSuccess || (e = setup_one<MR, 64, true>()) != cudaSuccess ||
+        (e = setup_one<MR, 128, false>()) != cudaSuccess || (e = setup_one<MR, 128, true>()) != cudaSuccess)
         return e;
     return cudaSuccess;
 }
