@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
     using C = DecCfg<MR, CB>;
     constexpr int NSB = C::kWarpCols / 16;   // 16-column sub-blocks of a consumer warp
     constexpr int NH = MR / 8;     // 8-row halves of X
+    constexpr int KC = NSB >= 4 ? 1 : 4 / NSB;   // independent accumulators per sub-block in a full stage
+    constexpr bool kFullPath = MR == 8 || NSB == 1;  // sixteen rows over 32+ columns keep the generic loop (registers)
     const int S = p.ring;
     const int xb = kDecStageRows * p.x_rows * 64;   // X bytes of a slot
     const int off_s = S * C::kWBytes;
@@ -241,6 +243,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
         const int cbase = C::kColTeams ? team * C::kWarpCols : 0;   // the warp's first column in the block
         constexpr int kStep = C::kColTeams ? 1 : 2;                  // stages between two of a warp's stages
         const int rpg = p.g_shift >= 7 ? 4 : 1 << (p.g_shift - 5);   // rows per group: 4, 2 (G = 64) or 1 (G = 32)
+        // lane offsets: X rows g and 8 + g (lanes past the last row of X read the last
+        // row again, for output columns that are never stored), the warp's words
+        int xoff[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) xoff[h] = min(8 * h + g, p.x_rows - 1) * 64 + t * 16;
+        const int woff = (cbase / C::kBoxCols) * C::kBoxBytes + (4 * wl * C::kBoxCols + cbase % C::kBoxCols + g) * 16 + t * 4;
         float acc[NSB][NH][4];
 #pragma unroll
         for (int sb = 0; sb < NSB; ++sb)
@@ -257,6 +265,57 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                 break;
             }
             const int g0 = min((st * kDecStageRows * 32) >> p.g_shift, p.ng - 1);
+            if (kFullPath && rpg == 4 && (st + 1) * kDecStageRows <= p.rows) {
+                // A full stage with G >= 128: the warp's four rows are 128 values of k
+                // of one group. No guard between the rows, so their loads can be issued
+                // together; with fewer than four sub-blocks the rows go to independent
+                // accumulators (KC chains) that are added before the scale.
+                float ch[KC][NSB][NH][4];
+                const uint8_t* xs = smem + off_x + s * xb + 4 * wl * p.x_rows * 64;
+                const uint8_t* ws = smem + s * C::kWBytes + woff;
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    uint4 xv[NH];
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        xv[h] = *reinterpret_cast<const uint4*>(xs + rr * p.x_rows * 64 + xoff[h]);
+                    const uint8_t* wa = ws + rr * C::kBoxCols * 16;
+#pragma unroll
+                    for (int sb = 0; sb < NSB; ++sb) {
+                        uint32_t pa[4], pb[4];
+                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + sb * 256), pa);
+                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + sb * 256 + 128), pb);
+                        const uint32_t a1[4] = {pa[0], pb[0], pa[1], pb[1]};
+                        const uint32_t a2[4] = {pa[2], pb[2], pa[3], pb[3]};
+#pragma unroll
+                        for (int h = 0; h < NH; ++h) {
+                            if (rr < KC)
+                                mma_16816_zero(ch[rr % KC][sb][h], a1, xv[h].x, xv[h].y);
+                            else
+                                mma_16816(ch[rr % KC][sb][h], a1, xv[h].x, xv[h].y);
+                            mma_16816(ch[rr % KC][sb][h], a2, xv[h].z, xv[h].w);
+                        }
+                    }
+                }
+                const int gl = ((st * kDecStageRows + 4 * wl) * 32 >> p.g_shift) - g0;
+                const __half* sc =
+                    reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) + gl * CB + cbase + g;
+#pragma unroll
+                for (int sb = 0; sb < NSB; ++sb) {
+                    const float s_lo = __half2float(sc[16 * sb]), s_hi = __half2float(sc[16 * sb + 8]);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+#pragma unroll
+                        for (int c = 1; c < KC; ++c)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) ch[0][sb][h][e] += ch[c][sb][h][e];
+                        acc[sb][h][0] = fmaf(s_lo, ch[0][sb][h][0], acc[sb][h][0]);
+                        acc[sb][h][1] = fmaf(s_lo, ch[0][sb][h][1], acc[sb][h][1]);
+                        acc[sb][h][2] = fmaf(s_hi, ch[0][sb][h][2], acc[sb][h][2]);
+                        acc[sb][h][3] = fmaf(s_hi, ch[0][sb][h][3], acc[sb][h][3]);
+                    }
+                }
+            } else {
             // sums of the current group: the first MMA of a group starts from zero
             float gacc[NSB][NH][4];
 #pragma unroll
@@ -266,11 +325,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                 if (row < p.rows) {
                     // rows g and 8 + g of X; lanes past the last row read the last row
                     // again, for output columns that are never stored
-                    const uint8_t* xa = smem + off_x + s * xb + rl * p.x_rows * 64 + t * 16;
+                    const uint8_t* xa = smem + off_x + s * xb + rl * p.x_rows * 64;
                     uint4 xv[NH];
 #pragma unroll
-                    for (int h = 0; h < NH; ++h)
-                        xv[h] = *reinterpret_cast<const uint4*>(xa + min(8 * h + g, p.x_rows - 1) * 64);
+                    for (int h = 0; h < NH; ++h) xv[h] = *reinterpret_cast<const uint4*>(xa + xoff[h]);
                     // the box of the warp's columns; within it column 16 sb + g (and + 8) of row rl
                     const uint8_t* wa = smem + s * C::kWBytes + (cbase / C::kBoxCols) * C::kBoxBytes +
                                         (rl * C::kBoxCols + cbase % C::kBoxCols + g) * 16 + t * 4;
@@ -310,6 +368,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                         }
                     }
                 }
+            }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
