@@ -80,11 +80,10 @@ def load_peaks():
 def kernel_name(plan, N):
     """The kernel instance a plan (path, tile or rows, grid) of w4a16_plan launches for
     N output columns: the decode kernel by rows of X and columns per block (one CTA
-    per block of 16, 32, 64 or 128 columns, read back from the grid), the others by
-    rows of X."""
+    per block of 16 to 128 columns, read back from the grid), the others by rows of X."""
     path, tile, grid = plan
     if path == 3:
-        cb = next(c for c in (16, 32, 64, 128) if grid == -(-N // c))
+        cb = next(c for c in (16, 32, 48, 64, 80, 128) if grid == -(-N // c))
         return "w4a16_decode_kernel<%d,%d>" % (tile, cb)
     return ("w4a16_gemv_kernel<%d>" if path == 1 else "w4a16_tc_kernel<%d>") % tile
 

@@ -383,7 +383,7 @@ long long w4a16_set_wait_limit_ns(long long limit_ns);
  *   *path = 3: the decode kernel for one to sixteen rows of X ("quant_marlin_kernel",
  *              "The architecture": register-level unpack feeding the tensor-core
  *              MMA from registers; here warp-level MMAs). *tile_m = the rows of X
- *              it is built for (8 or 16); *grid = CTAs, one per block of 16 or 64
+ *              it is built for (8 or 16); *grid = CTAs, one per block of 16 to 128
  *              output columns, each over the whole of K (no workspace is used).
  * The other weight formats always run path 2. */
 w4a16_status w4a16_plan(int M, int N, int K, int group_size, int* path, int* tile_m, int* grid);

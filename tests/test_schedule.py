@@ -57,17 +57,29 @@ DEC_SMEM_BUDGET = 104 * 1024
 DEC_WORDS_IN_FLIGHT = 64 * 1024
 
 
+def decode_block_cols(N, mr, sms=SMS):
+    """Mirror of decode_block_cols: with eight rows of X, the narrowest block width that
+    gives more CTAs than SMs and at most two per SM; else 128, 64 or 16."""
+    if mr == 8:
+        for cb in (16, 32, 48, 64, 80, 128):
+            if sms < ceil_div(N, cb) <= 2 * sms:
+                return cb
+    return 128 if ceil_div(N, 128) >= 2 * sms else 64 if ceil_div(N, 64) >= sms else 16
+
+
 def decode_plan(M, N, K, G, sms=SMS):
     """Mirror of make_decode_plan and of the launch's ring sizing: the decode kernel
-    for one to sixteen rows of X, one CTA per block of cb output columns (64 when
-    that gives at least one block per SM, else 16) over the whole of K."""
+    for one to sixteen rows of X, one CTA per block of cb output columns over the whole
+    of K; an even ring where the two warp teams take the stages in turn."""
     mr = 8 if M <= 8 else 16
-    cb = 128 if ceil_div(N, 128) >= 2 * sms else 64 if ceil_div(N, 64) >= sms else 16
+    cb = decode_block_cols(N, mr, sms)
     blocks = ceil_div(N, cb)
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     rows = K // 32
     slot = DEC_STAGE_ROWS * (cb * 16 + cb * 2 + M * 64)
     ring = min(DEC_WORDS_IN_FLIGHT // (DEC_STAGE_ROWS * cb * 16), DEC_SMEM_BUDGET // slot, DEC_MAX_RING)
+    if cb != 128:
+        ring &= ~1
     sh = group_shift(G)
     return dict(path=3, tm=mr, mr=mr, cb=cb, blocks=blocks, grid=blocks, KC=KC, ng=ceil_div(K, G),
                 n_tiles=ceil_div(N, 128), rows=rows, tile_rows=2 * KC, stages=ceil_div(rows, DEC_STAGE_ROWS),
@@ -94,24 +106,60 @@ def dispatch(M, N, K, G, sms=SMS, fmt="int4", force=0):
 
 
 def check_decode_shape(M, N, K, G, sms=SMS):
-    """Mirror of the decode kernel's indexing. In one column block every (column,
-    row of 32 k, word) is unpacked by exactly one lane of one warp (the stage's team
-    for blocks of 16 to 64 columns; with 128 columns both teams take every stage, each
-    its own 64), and the shared-memory word it reads (one TMA box per 64 columns) is the
-    global word of layout v2 that holds that column's codes; the X it reads lies inside
-    X; every block's copies stay inside its own tile of the packed words and scales;
-    every Y element is written once; the ring, the reduction and the shared memory fit."""
+    """Mirror of the decode kernel's indexing. In a column block every (column, row of
+    32 k, word) is unpacked by exactly one lane of one warp (the stage's team for blocks
+    of 16 to 80 columns; with 128 columns both teams take every stage, each its own 64),
+    and the shared-memory word it reads (the kernel's own offset arithmetic: one TMA box
+    per 64 columns, or per 16 for blocks of 48 and 80, which can straddle two tiles) is
+    the global word of layout v2 that holds that column's codes, and the scale it reads
+    that column's group scale; the X it reads lies inside X; each box stays inside one
+    tile of the packed words and scales; every Y element is written once; with teams
+    taking stages in turn, a slot's consecutive stages go to the same team; the ring,
+    the reduction and the shared memory fit."""
     P = decode_plan(M, N, K, G, sms)
     cb, mr, rows = P["cb"], P["mr"], P["rows"]
     col_teams = cb == 128
+    narrow = cb in (48, 80)
     warp_cols = 64 if col_teams else cb
-    box_cols = min(cb, 64)
+    box_cols = 16 if narrow else min(cb, 64)
+    box_words = DEC_STAGE_ROWS * box_cols * 4
     assert K % 32 == 0 and M <= DECODE_MAX_M
     assert 2 <= P["ring"] <= DEC_MAX_RING
     assert 8 * mr * warp_cols * 4 <= P["ring"] * DEC_STAGE_ROWS * cb * 16    # warps' sums fit the weight ring
     assert 2 * (P["smem"] + 1024) <= 228 * 1024                              # two CTAs per SM
-    assert 128 % cb == 0 and box_cols * 4 <= 256                             # TMA boxes of at most 256 words
-    # one block, every lane's reads
+    assert cb % box_cols == 0 and box_cols * 4 <= 256                        # TMA boxes of at most 256 words
+    assert mr == 8 or not narrow
+    if not col_teams:   # stages st and st + ring share a slot: the same team takes both
+        assert all(st % 2 == (st + P["ring"]) % 2 for st in range(P["stages"]))
+
+    def sb_words(sb):   # the kernel's byte offset of sub-block sb, in words
+        return ((16 * sb // box_cols) * box_words * 4 + (16 * sb % box_cols) * 16) // 4
+
+    def sb_scales(sb):
+        return sb * DEC_STAGE_ROWS * 16 if narrow else 16 * sb
+
+    # blocks 0 .. 3 and the last, every lane's reads
+    for b in sorted({0, 1, 2, 3, P["blocks"] - 1} & set(range(P["blocks"]))):
+        check_decode_block(P, M, N, K, b, cb, mr, rows, col_teams, narrow, warp_cols, box_cols, box_words,
+                           sb_words, sb_scales)
+    # every block: each box inside one tile, Y written once
+    cols = set()
+    for b in range(P["blocks"]):
+        n0 = b * cb
+        for bx in range(cb // box_cols):
+            col = n0 + bx * box_cols
+            assert (col & 127) + box_cols <= 128 and ((col & 127) * 4) % 4 == 0
+        for c in range(cb):
+            if n0 + c < N:
+                assert n0 + c not in cols
+                cols.add(n0 + c)
+    assert len(cols) == N
+    return P
+
+
+def check_decode_block(P, M, N, K, b, cb, mr, rows, col_teams, narrow, warp_cols, box_cols, box_words, sb_words,
+                       sb_scales):
+    n0 = b * cb
     seen = set()
     for st in range(P["stages"]):
         teams = (0, 1) if col_teams else (st % 2,)
@@ -126,45 +174,47 @@ def check_decode_shape(M, N, K, G, sms=SMS):
                         continue
                     gl = min((row * 32) >> P["g_shift"], P["ng"] - 1) - g0
                     assert 0 <= gl < P["scale_rows"]
-                    assert gl * cb + cbase + 7 + 16 * (warp_cols // 16 - 1) + 8 < DEC_STAGE_ROWS * cb   # scales
                     for lane in range(32):
                         g, t = lane >> 2, lane & 3
                         for h in range(mr // 8):
                             m = min(8 * h + g, M - 1)
                             assert 0 <= m < M and row * 32 + 8 * t + 7 < K
+                        # the kernel's word offset: the warp's box, its row and lane, then the sub-block
+                        woff = ((cbase // box_cols) * box_words + (4 * wl * box_cols + cbase % box_cols + g) * 4 + t
+                                + rr * box_cols * 4)
+                        sc0 = (gl * 16 if narrow else gl * cb + cbase) + g
                         for sb in range(warp_cols // 16):
                             for off in (0, 8):
-                                nl = cbase + 16 * sb + g + off
-                                bx, nb = divmod(nl, box_cols)
-                                smem_word = bx * DEC_STAGE_ROWS * box_cols * 4 + (rl * box_cols + nb) * 4 + t
+                                smem_word = woff + sb_words(sb) + off * 4
                                 assert smem_word < DEC_STAGE_ROWS * cb * 4
+                                nl = cbase + 16 * sb + g + off          # the column this lane stands for
                                 key = (nl, row, t)
                                 assert key not in seen
                                 seen.add(key)
-                                # box bx starts at word ((n0 & 127) + 64 bx) * 4 of map row
-                                # nt * tile_rows + st * 16
-                                within = smem_word - bx * DEC_STAGE_ROWS * box_cols * 4
-                                box_row, box_col = divmod(within, box_cols * 4)
+                                # box bx holds [16 rows][box_cols][4 words] from map row
+                                # (col >> 7) * tile_rows + st * 16, word (col & 127) * 4 on
+                                bx, within = divmod(smem_word, box_words)
+                                box_row, box_word = divmod(within, box_cols * 4)
+                                col = n0 + bx * box_cols
+                                gcol = (col >> 7) * 128 + (col & 127) + box_word // 4
+                                assert gcol == n0 + nl and box_word % 4 == t
                                 map_row = st * DEC_STAGE_ROWS + box_row              # within the tile
+                                assert map_row == row
                                 kc, jj = divmod(map_row, 2)
-                                word_in_row = bx * box_cols * 4 + box_col            # + (n0 & 127) * 4
-                                assert (map_row, word_in_row) == (row, nl * 4 + t)
                                 # layout v2: word (kc, jj, n_in, wd) holds k = 64 kc + 32 jj + 8 wd .. +7
                                 assert 64 * kc + 32 * jj + 8 * t == row * 32 + 8 * t
+                                # the scale: [scale_rows][cb] or, with 16-column boxes,
+                                # [cb / 16][16 rows][16] from scale row (col >> 7) * ng + g0
+                                si = sc0 + sb_scales(sb) + off
+                                assert si < DEC_STAGE_ROWS * cb
+                                if narrow:
+                                    sbx, sw = divmod(si, DEC_STAGE_ROWS * 16)
+                                    srow, scol = divmod(sw, 16)
+                                    assert n0 + sbx * 16 + scol == n0 + nl and srow == gl
+                                else:
+                                    srow, scol = divmod(si, cb)
+                                    assert scol == nl and srow == gl
     assert len(seen) == cb * rows * 4
-    # every block: copies inside its tile, Y written once
-    cols = set()
-    for b in range(P["blocks"]):
-        n0 = b * cb
-        nt = n0 >> 7
-        assert nt < P["n_tiles"] and (n0 & 127) + cb <= 128
-        assert (n0 & 127) * 4 + cb * 4 <= 512
-        for c in range(cb):
-            if n0 + c < N:
-                assert n0 + c not in cols
-                cols.add(n0 + c)
-    assert len(cols) == N
-    return P
 
 
 def check_gemv_shape(M, N, K, G, sms=SMS):
@@ -387,7 +437,7 @@ def test_dispatch_rule():
     otherwise; blocks of 128 columns for the 73728-wide layer (576 blocks, two per SM
     and more), 64 for the 12288- and 22016-wide ones, 16 for the 4096-wide ones
     (measured on GB300)."""
-    width = {4096: 16, 12288: 64, 22016: 64, 73728: 128}
+    width = {4096: 16, 12288: 48, 22016: 80, 73728: 128}
     for (N, K) in [(4096, 4096), (12288, 4096), (22016, 4096), (4096, 11008), (73728, 18432)]:
         for M in (1, 2, 4, 8):
             P = dispatch(M, N, K, 128)
@@ -401,8 +451,9 @@ def test_dispatch_rule():
     assert dispatch(4, 4096, 4096, 128, fmt="w8")["tm"] == 16
     assert dispatch(1, 4096, 4096, 128, force=2)["tm"] == 16
     # ring depth: about 64 KB of packed words in flight, fewer where shared memory says so
-    assert decode_plan(1, 4096, 4096, 128)["ring"] == 16 and decode_plan(1, 22016, 4096, 128)["ring"] == 4
-    assert decode_plan(16, 22016, 4096, 128)["ring"] == 3
+    assert decode_plan(1, 4096, 4096, 128)["ring"] == 16 and decode_plan(1, 73728, 18432, 128)["ring"] == 2
+    assert decode_plan(1, 22016, 4096, 128)["ring"] == 2 and decode_plan(1, 12288, 4096, 128)["ring"] == 4
+    assert decode_plan(16, 22016, 4096, 128)["ring"] == 2   # even: 3 slots fit, the teams alternate
 
 
 @pytest.mark.parametrize("fmt", ["w8", "sparse"])

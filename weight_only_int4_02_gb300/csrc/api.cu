@@ -108,7 +108,7 @@ long long g_wait_limit_ns = 1000000000LL;
 int g_force_split = 0;
 int g_force_min_iters = 0;
 int g_force_tm = 0;   // W4A16_TILE_M: rows of X per tile (16, 32, 64, 128 or 256) for the tensor-core kernel
-int g_force_cb = 0;   // W4A16_DECODE_CB: columns per block (16, 32, 64 or 128) for the decode kernel
+int g_force_cb = 0;   // W4A16_DECODE_CB: columns per block (16, 32, 48, 64, 80 or 128) for the decode kernel
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -162,7 +162,7 @@ struct Plan {
     int gemv_cw;  // path 1: output columns per block (8, 16, 32)
     int gemv_blocks;
     int dec_mr;   // path 3: rows of X the kernel is built for (8, 16)
-    int dec_cb;   // path 3: output columns per block (16, 32, 64)
+    int dec_cb;   // path 3: output columns per block (16, 32, 48, 64, 80, 128)
 };
 
 size_t ws_bytes_for(int grid, int tm) { return kPartialsOff + (size_t)2 * grid * tm * kTileN * sizeof(float); }
@@ -258,15 +258,32 @@ bool gemv_applies(int M, int fmt, int force)
 // layers); one CTA per block. Measured on GB300: 18432 x 73728 at M = 1 119.4 us with
 // 128 against 121.3 with 64; 4096 x 22016 14.6 us with 64 against 15.1 with 128;
 // N = 4096 fastest with 16; 32 was never best.
+// Columns per block of the decode kernel. Two CTAs share an SM, and a launch chained
+// behind another takes the slots as they free, so an SM ends up with two CTAs of it or
+// none and the busiest SMs hold two blocks: with eight rows of X, the narrowest block
+// that gives more CTAs than SMs and at most two per SM (one wave); else 128 where the
+// layer has two 128-column blocks per SM, 64 where it has one 64-column block per SM,
+// and 16 below.
+int decode_block_cols(int N, int mr, int sms)
+{
+    if (g_force_cb == 16 || g_force_cb == 32 || g_force_cb == 64 || g_force_cb == 128 ||
+        (mr == 8 && (g_force_cb == 48 || g_force_cb == 80)))
+        return g_force_cb;
+    if (mr == 8)
+        for (int cb : {16, 32, 48, 64, 80, 128}) {
+            const int ctas = ceil_div(N, cb);
+            if (ctas > sms && ctas <= 2 * sms) return cb;
+        }
+    return ceil_div(N, 128) >= 2 * sms ? 128 : ceil_div(N, 64) >= sms ? 64 : 16;
+}
+
 Plan make_decode_plan(int M, int N, int K, int G, int sms)
 {
     Plan P = {};
     P.path = 3;
     P.dec_mr = M <= 8 ? 8 : 16;
-    int cb = ceil_div(N, 128) >= 2 * sms ? 128 : ceil_div(N, 64) >= sms ? 64 : 16;
-    if (g_force_cb == 16 || g_force_cb == 32 || g_force_cb == 64 || g_force_cb == 128) cb = g_force_cb;
-    P.dec_cb = cb;
-    P.grid = ceil_div(N, cb);
+    P.dec_cb = decode_block_cols(N, P.dec_mr, sms);
+    P.grid = ceil_div(N, P.dec_cb);
     P.n_tiles = ceil_div(N, kTileN);
     P.KC = ceil_div(ceil_div(K, kChunkK), kKPad) * kKPad;
     P.ng = ceil_div(K, G);
@@ -473,14 +490,17 @@ bool encode_decode_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tx, const
     cuuint32_t estr[3] = {1, 1, 1};
     cuuint64_t wdims[2] = {512, (cuuint64_t)n_tiles * tile_rows};
     cuuint64_t wstrides[1] = {2048};
-    cuuint32_t wbox[2] = {(cuuint32_t)(cb < 64 ? cb : 64) * 4, (cuuint32_t)kDecStageRows};   // 128: two boxes
+    // boxes of up to 64 columns (128: two boxes); 48 and 80 columns: boxes of 16
+    const bool narrow = cb == 48 || cb == 80;
+    const int box_cols = narrow ? 16 : cb < 64 ? cb : 64;
+    cuuint32_t wbox[2] = {(cuuint32_t)box_cols * 4, (cuuint32_t)kDecStageRows};
     CUresult r = g_encode(tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(packed), wdims, wstrides, wbox,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     cuuint64_t sdims[2] = {128, (cuuint64_t)n_tiles * ng};
     cuuint64_t sstrides[1] = {256};
-    cuuint32_t sbox[2] = {(cuuint32_t)cb, (cuuint32_t)scale_rows};
+    cuuint32_t sbox[2] = {(cuuint32_t)(narrow ? 16 : cb), (cuuint32_t)scale_rows};
     r = g_encode(ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(scales), sdims, sstrides, sbox, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -544,6 +564,12 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
         d.ring = kDecWordsInFlight / (kDecStageRows * P.dec_cb * 16);
         if (d.ring > kDecSmemBudget / decode_slot_bytes(P.dec_cb, M)) d.ring = kDecSmemBudget / decode_slot_bytes(P.dec_cb, M);
         if (d.ring > kDecMaxRing) d.ring = kDecMaxRing;
+        // Two warp teams take the stages in turn (all blocks but those of 128 columns):
+        // stages st and st + ring share a slot, and an even ring gives both to the same
+        // team, which waits for the later one only after it has consumed the earlier.
+        // An odd ring would let the other team wait two phases ahead on the slot's
+        // barrier, where the parity of the earlier phase passes for the later one.
+        if (P.dec_cb != 128) d.ring &= ~1;
         if (d.ring < 2) return W4A16_ERR_INVALID_ARG;   // cannot happen for M <= 16
         CUtensorMap tw, ts, tx;
         if (!encode_decode_maps(&tw, &ts, &tx, packed, scales_packed, x, P.n_tiles, d.tile_rows, P.ng, P.dec_cb,

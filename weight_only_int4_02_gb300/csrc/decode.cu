@@ -35,15 +35,18 @@
 // running sums. Products of (q - 8) and X are exact in the MMA; the scale multiplies
 // once per group.
 //
-// Work split: the output columns are cut into blocks of CB (16, 32 or 64); one CTA
-// takes one block over the whole of K, so no partial sum leaves the CTA. A stage is
-// 16 rows of 32 values of k (512 values); two teams of four consumer warps take the
-// stages in turn, warp w of a team rows 4w .. 4w+3 (128 values of k) for all CB
-// columns. At the end the eight warps' sums are added in warp order through shared
-// memory (bit-identical results from run to run).
+// Work split: the output columns are cut into blocks of CB (16, 32, 48, 64, 80 or
+// 128); one CTA takes one block over the whole of K, so no partial sum leaves the
+// CTA. A stage is 16 rows of 32 values of k (512 values); two teams of four consumer
+// warps take the stages in turn (an even number of ring slots, so that the two stages
+// sharing a slot go to one team), warp w of a team rows 4w .. 4w+3 (128 values of k)
+// for all CB columns; with 128 columns both teams take every stage, each 64 of the
+// columns. At the end the warps' sums are added in warp order through shared memory
+// (bit-identical results from run to run).
 //
-// Staging: one producer warp streams the stage's packed words (one 2-D TMA of 16
-// rows x CB columns) and group scales (another) into a ring; it needs nothing from
+// Staging: one producer warp streams the stage's packed words (2-D TMA boxes of 16
+// rows x up to 64 columns, each inside one 128-column tile) and group scales into a
+// ring; it needs nothing from
 // the previous kernel, so the ring fills while that kernel finishes (programmatic
 // dependent launch). A second producer waits for the previous kernel, then brings
 // the stage's X with one 3-D TMA as [16 rows][mr rows of X][32 values]: 64 bytes per
@@ -78,24 +81,32 @@ constexpr int kProdX = kConsumers + 1;
 static_assert(kDecThreads == 32 * (kConsumers + 2), "warp roles");
 static_assert(kDecStageRows == 2 * kConsumers, "two rows of a stage per consumer warp");
 
-// Shared memory: [ring][CB / 64 or 1][16][min(CB, 64)][16 bytes] packed words (one
-// TMA box per 64 columns), [ring][16][CB] scales, [ring][16][x_rows][64 bytes] X,
-// then the barriers. The ring depth and X's rows are launch parameters (offsets
-// computed at run time). With 128-column blocks the two consumer teams split the
-// columns (64 each) and both take every stage; with 16 to 64 they take the stages in
-// turn over all columns.
+// Shared memory: [ring][CB / box][16][box][16 bytes] packed words (one TMA box of
+// `box` columns each), [ring][16][CB] scales (or [CB / 16][16][16] with 16-column
+// boxes), [ring][16][x_rows][64 bytes] X, then the barriers. The ring depth and X's
+// rows are launch parameters (offsets computed at run time). With 128-column blocks
+// the two consumer teams split the columns (64 each) and both take every stage; with
+// 16 to 80 they take the stages in turn over all columns. Blocks of 48 and 80 columns
+// can straddle two 128-column tiles of the packed layout: their words and scales come
+// in boxes of 16 columns, each within one tile.
 template <int MR, int CB>
 struct DecCfg {
     static constexpr bool kColTeams = CB == 128;
+    static constexpr bool kNarrowBoxes = CB == 48 || CB == 80;
     static constexpr int kWarpCols = kColTeams ? 64 : CB;     // output columns of one consumer warp
-    static constexpr int kBoxCols = CB > 64 ? 64 : CB;        // columns of one weight TMA box
+    static constexpr int kBoxCols = kNarrowBoxes ? 16 : CB > 64 ? 64 : CB;   // columns of one weight TMA box
     static constexpr int kBoxBytes = kDecStageRows * kBoxCols * 16;
+    static constexpr int kSBoxHalves = kDecStageRows * 16;   // one 16-column box of scales (up to 16 rows)
     static constexpr int kWBytes = kDecStageRows * CB * 16;   // packed words: [16 rows][CB][4 words]
     static constexpr int kSBytes = kDecStageRows * CB * 2;    // up to 16 rows of group scales (G = 32)
     static constexpr int kRedBytes = kConsumers * MR * kWarpCols * 4;  // per-warp sums, over the weight ring
     static constexpr int kMaxSmem = kDecSmemBudget + 3 * kDecMaxRing * 8 + 16 + 128;
     static_assert(kRedBytes <= 2 * kWBytes, "the final reduction fits in a weight ring of two slots");
     static_assert(CB % kBoxCols == 0 && kBoxCols * 4 <= 256, "weight boxes of at most 256 words");
+    // byte offset of 16-column sub-block sb of a warp's columns in a slot's words, and
+    // of its scales (in halves) from the warp's first column
+    __host__ __device__ static constexpr int sb_words(int sb) { return (16 * sb / kBoxCols) * kBoxBytes + (16 * sb % kBoxCols) * 16; }
+    __host__ __device__ static constexpr int sb_scales(int sb) { return kNarrowBoxes ? sb * kSBoxHalves : 16 * sb; }
 };
 
 // d = a * b (the accumulator starts from zero)
@@ -214,10 +225,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                     const int g0 = min((st * kDecStageRows * 32) >> p.g_shift, p.ng - 1);
                     mbar_arrive_expect_tx(wfull_bar(s), w_tx);
 #pragma unroll
-                    for (int bx = 0; bx < CB / C::kBoxCols; ++bx)
+                    for (int bx = 0; bx < CB / C::kBoxCols; ++bx) {
+                        const int col = n0 + bx * C::kBoxCols;   // the box's first column: one tile holds it
                         tma_load_2d(sbase + s * C::kWBytes + bx * C::kBoxBytes, &tmap_w, wfull_bar(s),
-                                    ((n0 & 127) + bx * C::kBoxCols) * 4, nt * p.tile_rows + st * kDecStageRows);
-                    tma_load_2d(sbase + off_s + s * C::kSBytes, &tmap_s, wfull_bar(s), n0 & 127, nt * p.ng + g0);
+                                    (col & 127) * 4, (col >> 7) * p.tile_rows + st * kDecStageRows);
+                        if constexpr (C::kNarrowBoxes)
+                            tma_load_2d(sbase + off_s + s * C::kSBytes + bx * C::kSBoxHalves * 2, &tmap_s,
+                                        wfull_bar(s), col & 127, (col >> 7) * p.ng + g0);
+                    }
+                    if constexpr (!C::kNarrowBoxes)
+                        tma_load_2d(sbase + off_s + s * C::kSBytes, &tmap_s, wfull_bar(s), n0 & 127, nt * p.ng + g0);
                 }
             }
             __syncwarp();
@@ -283,8 +300,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
 #pragma unroll
                     for (int sb = 0; sb < NSB; ++sb) {
                         uint32_t pa[4], pb[4];
-                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + sb * 256), pa);
-                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + sb * 256 + 128), pb);
+                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + C::sb_words(sb)), pa);
+                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + C::sb_words(sb) + 128), pb);
                         const uint32_t a1[4] = {pa[0], pb[0], pa[1], pb[1]};
                         const uint32_t a2[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
@@ -298,11 +315,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                     }
                 }
                 const int gl = ((st * kDecStageRows + 4 * wl) * 32 >> p.g_shift) - g0;
-                const __half* sc =
-                    reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) + gl * CB + cbase + g;
+                const __half* sc = reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) +
+                                   (C::kNarrowBoxes ? gl * 16 : gl * CB + cbase) + g;
 #pragma unroll
                 for (int sb = 0; sb < NSB; ++sb) {
-                    const float s_lo = __half2float(sc[16 * sb]), s_hi = __half2float(sc[16 * sb + 8]);
+                    const float s_lo = __half2float(sc[C::sb_scales(sb)]), s_hi = __half2float(sc[C::sb_scales(sb) + 8]);
 #pragma unroll
                     for (int h = 0; h < NH; ++h) {
 #pragma unroll
@@ -336,8 +353,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
 #pragma unroll
                     for (int sb = 0; sb < NSB; ++sb) {
                         uint32_t pa[4], pb[4];
-                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + sb * 256), pa);         // column 16 sb + g
-                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + sb * 256 + 128), pb);   // column 16 sb + g + 8
+                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + C::sb_words(sb)), pa);         // column 16 sb + g
+                        unpack_q8(*reinterpret_cast<const uint32_t*>(wa + C::sb_words(sb) + 128), pb);   // column 16 sb + g + 8
                         const uint32_t a1[4] = {pa[0], pb[0], pa[1], pb[1]};
                         const uint32_t a2[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
@@ -353,11 +370,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                         // the group's sums, times the scales of columns g and g + 8 of
                         // each sub-block, go to the running sums
                         const int gl = min((row * 32) >> p.g_shift, p.ng - 1) - g0;
-                        const __half* sc =
-                            reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) + gl * CB + cbase + g;
+                        const __half* sc = reinterpret_cast<const __half*>(smem + off_s + s * C::kSBytes) +
+                                           (C::kNarrowBoxes ? gl * 16 : gl * CB + cbase) + g;
 #pragma unroll
                         for (int sb = 0; sb < NSB; ++sb) {
-                            const float s_lo = __half2float(sc[16 * sb]), s_hi = __half2float(sc[16 * sb + 8]);
+                            const float s_lo = __half2float(sc[C::sb_scales(sb)]),
+                                        s_hi = __half2float(sc[C::sb_scales(sb) + 8]);
 #pragma unroll
                             for (int h = 0; h < NH; ++h) {
                                 acc[sb][h][0] = fmaf(s_lo, gacc[sb][h][0], acc[sb][h][0]);
@@ -453,7 +471,13 @@ cudaError_t launch_mr(const CUtensorMap& tw, const CUtensorMap& ts, const CUtens
     switch (cb) {
         case 16: return launch_one<MR, 16>(tw, ts, tx, p, epi, grid, stream);
         case 32: return launch_one<MR, 32>(tw, ts, tx, p, epi, grid, stream);
+        case 48:
+            if constexpr (MR == 8) return launch_one<MR, 48>(tw, ts, tx, p, epi, grid, stream);
+            return cudaErrorInvalidValue;
         case 64: return launch_one<MR, 64>(tw, ts, tx, p, epi, grid, stream);
+        case 80:
+            if constexpr (MR == 8) return launch_one<MR, 80>(tw, ts, tx, p, epi, grid, stream);
+            return cudaErrorInvalidValue;
         case 128: return launch_one<MR, 128>(tw, ts, tx, p, epi, grid, stream);
         default: return cudaErrorInvalidValue;
     }
@@ -468,6 +492,11 @@ cudaError_t setup_mr()
         (e = setup_one<MR, 64, false>()) != cudaSuccess || (e = setup_one<MR, 64, true>()) != cudaSuccess ||
         (e = setup_one<MR, 128, false>()) != cudaSuccess || (e = setup_one<MR, 128, true>()) != cudaSuccess)
         return e;
+    if constexpr (MR == 8) {
+        if ((e = setup_one<MR, 48, false>()) != cudaSuccess || (e = setup_one<MR, 48, true>()) != cudaSuccess ||
+            (e = setup_one<MR, 80, false>()) != cudaSuccess || (e = setup_one<MR, 80, true>()) != cudaSuccess)
+            return e;
+    }
     return cudaSuccess;
 }
 

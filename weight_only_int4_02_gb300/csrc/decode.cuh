@@ -1,7 +1,7 @@
 // Parameters and launch of the decode kernel (decode.cu): the W4A16 matmul for up
 // to sixteen rows of X with the register-level unpack feeding warp-level MMAs,
-// column blocks of 16, 32 or 64 output features, each processed by one CTA over
-// the whole reduction dimension, weights, scales and X staged by TMA.
+// column blocks of 16 to 128 output features, each processed by one CTA over the
+// whole reduction dimension, weights, scales and X staged by TMA.
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -28,7 +28,7 @@ struct DecodeParams {
     int stages;              // ceil(rows / kDecStageRows)
     int scale_rows;          // group rows the scale map's box brings per stage
     int x_rows;              // rows of X the X map's box brings per row of k: M (<= mr)
-    int ring;                // pipeline slots (2 .. kDecMaxRing)
+    int ring;                // pipeline slots (2 .. kDecMaxRing); even unless CB = 128
 };
 
 constexpr int kDecMaxRing = 16;
@@ -44,11 +44,14 @@ constexpr int decode_smem_bytes(int cb, int x_rows, int ring)
 }
 
 // Tensor maps (built on the host):
-//   tmap_w: the packed words as uint32 [n_tiles * tile_rows][512], box {cb * 4, 16};
-//   tmap_s: the tile-ordered scales as 16-bit [n_tiles * ng][128], box {cb, scale_rows};
+//   tmap_w: the packed words as uint32 [n_tiles * tile_rows][512], box {box * 4, 16};
+//   tmap_s: the tile-ordered scales as 16-bit [n_tiles * ng][128], box {cb, scale_rows}
+//           (box {16, scale_rows} for cb 48 and 80);
+//   box = 16 for cb 48 and 80 (blocks that can straddle two tiles), else min(cb, 64);
 //   tmap_x: X as 16-bit {32, M, K / 32} with strides {2 ldx, 64} bytes, box {32, M, 16},
 //           so a stage lands as [16 rows of k][M rows of X][32 values].
-// mr: 8 or 16 (rows of X the kernel is built for, >= M); cb: 16, 32 or 64; grid = ceil(N / cb);
+// mr: 8 or 16 (rows of X the kernel is built for, >= M); cb: 16, 32, 64 or 128, and 48 or
+// 80 with mr = 8; grid = ceil(N / cb);
 // the dynamic shared memory is decode_smem_bytes(cb, M, p.ring).
 cudaError_t launch_decode(const CUtensorMap& tmap_w, const CUtensorMap& tmap_s, const CUtensorMap& tmap_x,
                           const DecodeParams& p, int mr, int cb, bool epi, int grid, cudaStream_t stream);
