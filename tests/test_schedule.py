@@ -54,7 +54,10 @@ DECODE_AUTO_MAX_M = 8
 DEC_STAGE_ROWS = 16
 DEC_MAX_RING = 16
 DEC_SMEM_BUDGET = 104 * 1024
-DEC_WORDS_IN_FLIGHT = 64 * 1024
+
+
+def dec_words_in_flight(cb):
+    return 24 * 1024 if cb == 16 else 80 * 1024 if cb == 80 else 64 * 1024
 
 
 def decode_block_cols(N, mr, sms=SMS):
@@ -70,16 +73,14 @@ def decode_block_cols(N, mr, sms=SMS):
 def decode_plan(M, N, K, G, sms=SMS):
     """Mirror of make_decode_plan and of the launch's ring sizing: the decode kernel
     for one to sixteen rows of X, one CTA per block of cb output columns over the whole
-    of K; an even ring where the two warp teams take the stages in turn."""
+    of K."""
     mr = 8 if M <= 8 else 16
     cb = decode_block_cols(N, mr, sms)
     blocks = ceil_div(N, cb)
     KC = ceil_div(ceil_div(K, 64), 4) * 4
     rows = K // 32
     slot = DEC_STAGE_ROWS * (cb * 16 + cb * 2 + M * 64)
-    ring = min(DEC_WORDS_IN_FLIGHT // (DEC_STAGE_ROWS * cb * 16), DEC_SMEM_BUDGET // slot, DEC_MAX_RING)
-    if cb != 128:
-        ring &= ~1
+    ring = min(dec_words_in_flight(cb) // (DEC_STAGE_ROWS * cb * 16), DEC_SMEM_BUDGET // slot, DEC_MAX_RING)
     sh = group_shift(G)
     return dict(path=3, tm=mr, mr=mr, cb=cb, blocks=blocks, grid=blocks, KC=KC, ng=ceil_div(K, G),
                 n_tiles=ceil_div(N, 128), rows=rows, tile_rows=2 * KC, stages=ceil_div(rows, DEC_STAGE_ROWS),
@@ -129,8 +130,8 @@ def check_decode_shape(M, N, K, G, sms=SMS):
     assert 2 * (P["smem"] + 1024) <= 228 * 1024                              # two CTAs per SM
     assert cb % box_cols == 0 and box_cols * 4 <= 256                        # TMA boxes of at most 256 words
     assert mr == 8 or not narrow
-    if not col_teams:   # stages st and st + ring share a slot: the same team takes both
-        assert all(st % 2 == (st + P["ring"]) % 2 for st in range(P["stages"]))
+    if not col_teams:
+        check_alternating_teams(P["ring"], P["stages"])
 
     def sb_words(sb):   # the kernel's byte offset of sub-block sb, in words
         return ((16 * sb // box_cols) * box_words * 4 + (16 * sb % box_cols) * 16) // 4
@@ -155,6 +156,24 @@ def check_decode_shape(M, N, K, G, sms=SMS):
                 cols.add(n0 + c)
     assert len(cols) == N
     return P
+
+
+def check_alternating_teams(S, stages):
+    """Mirror of the consumers' slot and parity tracking with two teams taking the
+    stages in turn: each team's (slot, parity) is the stage's; and a wait on a slot's
+    full barrier never runs two phases ahead of the slot's earlier stage, because with
+    an odd ring (where the earlier stage belongs to the other team) the team first
+    waits for that stage's consumption."""
+    for team in (0, 1):
+        s, ph = team, 0
+        for st in range(team, stages, 2):
+            assert (s, ph) == (st % S, (st // S) & 1)
+            if st >= S and (st - S) % 2 != team:
+                assert S % 2 == 1   # only an odd ring hands a slot to the other team, and it waits
+            s += 2
+            if s >= S:
+                s -= S
+                ph ^= 1
 
 
 def check_decode_block(P, M, N, K, b, cb, mr, rows, col_teams, narrow, warp_cols, box_cols, box_words, sb_words,
@@ -451,9 +470,9 @@ def test_dispatch_rule():
     assert dispatch(4, 4096, 4096, 128, fmt="w8")["tm"] == 16
     assert dispatch(1, 4096, 4096, 128, force=2)["tm"] == 16
     # ring depth: about 64 KB of packed words in flight, fewer where shared memory says so
-    assert decode_plan(1, 4096, 4096, 128)["ring"] == 16 and decode_plan(1, 73728, 18432, 128)["ring"] == 2
-    assert decode_plan(1, 22016, 4096, 128)["ring"] == 2 and decode_plan(1, 12288, 4096, 128)["ring"] == 4
-    assert decode_plan(16, 22016, 4096, 128)["ring"] == 2   # even: 3 slots fit, the teams alternate
+    assert decode_plan(1, 4096, 4096, 128)["ring"] == 6 and decode_plan(1, 73728, 18432, 128)["ring"] == 2
+    assert decode_plan(1, 22016, 4096, 128)["ring"] == 4 and decode_plan(8, 22016, 4096, 128)["ring"] == 3
+    assert decode_plan(1, 12288, 4096, 128)["ring"] == 5 and decode_plan(16, 22016, 4096, 128)["ring"] == 3
 
 
 @pytest.mark.parametrize("fmt", ["w8", "sparse"])

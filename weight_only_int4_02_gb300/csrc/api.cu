@@ -561,15 +561,9 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
         d.scale_rows = ((G & (G - 1)) == 0 && G <= kDecStageRows * 32) ? kDecStageRows * 32 / G : 1;
         d.x_rows = M;
         // slots for about 64 KB of packed words in flight, within the shared-memory budget
-        d.ring = kDecWordsInFlight / (kDecStageRows * P.dec_cb * 16);
+        d.ring = decode_words_in_flight(P.dec_cb) / (kDecStageRows * P.dec_cb * 16);
         if (d.ring > kDecSmemBudget / decode_slot_bytes(P.dec_cb, M)) d.ring = kDecSmemBudget / decode_slot_bytes(P.dec_cb, M);
         if (d.ring > kDecMaxRing) d.ring = kDecMaxRing;
-        // Two warp teams take the stages in turn (all blocks but those of 128 columns):
-        // stages st and st + ring share a slot, and an even ring gives both to the same
-        // team, which waits for the later one only after it has consumed the earlier.
-        // An odd ring would let the other team wait two phases ahead on the slot's
-        // barrier, where the parity of the earlier phase passes for the later one.
-        if (P.dec_cb != 128) d.ring &= ~1;
         if (d.ring < 2) return W4A16_ERR_INVALID_ARG;   // cannot happen for M <= 16
         CUtensorMap tw, ts, tx;
         if (!encode_decode_maps(&tw, &ts, &tx, packed, scales_packed, x, P.n_tiles, d.tile_rows, P.ng, P.dec_cb,

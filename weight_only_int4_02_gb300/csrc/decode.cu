@@ -38,8 +38,7 @@
 // Work split: the output columns are cut into blocks of CB (16, 32, 48, 64, 80 or
 // 128); one CTA takes one block over the whole of K, so no partial sum leaves the
 // CTA. A stage is 16 rows of 32 values of k (512 values); two teams of four consumer
-// warps take the stages in turn (an even number of ring slots, so that the two stages
-// sharing a slot go to one team), warp w of a team rows 4w .. 4w+3 (128 values of k)
+// warps take the stages in turn, warp w of a team rows 4w .. 4w+3 (128 values of k)
 // for all CB columns; with 128 columns both teams take every stage, each 64 of the
 // columns. At the end the warps' sums are added in warp order through shared memory
 // (bit-identical results from run to run).
@@ -276,7 +275,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
         bool ok = true;
         int s = C::kColTeams ? 0 : team;   // slot of stage st; S >= 2
         uint32_t ph = 0;
+        // With the teams taking stages in turn and an odd ring, stages st and st + S
+        // share a slot but go to different teams: a team first waits until the slot's
+        // earlier stage is consumed (the producer's own wait), so that it never waits
+        // on the full barriers two phases ahead, where the parity of the earlier phase
+        // would pass for the later one.
+        const bool odd_ring = !C::kColTeams && (S & 1);
         for (int st = C::kColTeams ? 0 : team; st < p.stages; st += kStep) {
+            if (odd_ring && !wait_warp<true>(empty_bar(s), ph ^ 1, ctl)) {
+                ok = false;
+                break;
+            }
             if (!wait_warp<true>(wfull_bar(s), ph, ctl) || !wait_warp<true>(xfull_bar(s), ph, ctl)) {
                 ok = false;
                 break;

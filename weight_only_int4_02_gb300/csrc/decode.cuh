@@ -28,12 +28,16 @@ struct DecodeParams {
     int stages;              // ceil(rows / kDecStageRows)
     int scale_rows;          // group rows the scale map's box brings per stage
     int x_rows;              // rows of X the X map's box brings per row of k: M (<= mr)
-    int ring;                // pipeline slots (2 .. kDecMaxRing); even unless CB = 128
+    int ring;                // pipeline slots (2 .. kDecMaxRing)
 };
 
 constexpr int kDecMaxRing = 16;
 constexpr int kDecSmemBudget = 104 * 1024;   // the ring; two CTAs share an SM
-constexpr int kDecWordsInFlight = 64 * 1024;  // packed bytes the ring holds (fewer where the budget says so)
+// Packed bytes the ring holds (fewer where the budget says so), by block width, as
+// measured on GB300 for launches chained back to back: 24 KB (six stages) for blocks
+// of 16 columns, whose deeper rings ran slower, 80 KB (four stages) for 80 columns,
+// 64 KB for the others.
+constexpr int decode_words_in_flight(int cb) { return cb == 16 ? 24 * 1024 : cb == 80 ? 80 * 1024 : 64 * 1024; }
 
 // Shared-memory bytes of one pipeline slot, and of a launch with `ring` slots
 // (ring * slot <= kDecSmemBudget).
