@@ -481,7 +481,7 @@ def run_ours(args):
         "kernels": {n: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3} for n, v in kernels.items()},
         "byte_ratio_fp16_over_w4g128": fp16_over_int4_byte_ratio(G),
     }
-    if args.workload == DEFAULT_WORKLOAD:
+    if args.workload == DEFAULT_WORKLOAD and not args.no_probes:
         out["fp16_peak"] = fp16_peak_probe()
         out["workloads"] = workloads_probe(G, peaks)
         out["fused_epilogue"] = fused_epilogue_probe(G)
@@ -1102,6 +1102,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-probes", action="store_true",
+                    help="leave out the other workloads and side probes (profiling aid: the launch list of "
+                         "the decode sweep alone)")
     ap.add_argument("--case", default=None, help="M,K,N: time one GEMM shape (profiling aid)")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--format", default="int4", choices=["int4", "w8", "sparse"],
