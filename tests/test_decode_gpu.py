@@ -3,7 +3,7 @@ MMAs, one to sixteen rows of X) against the CPU oracle.
 
 The dispatcher picks it by itself for up to eight rows of X when K is a multiple of
 32; here it is also forced for nine to sixteen rows. Covered: small and ragged
-shapes spanning several column blocks of both widths (16 and 64) and every group
+shapes spanning several column blocks of every width (16, 32, 48, 64, 80) and every group
 size (32, 64, 128, K, K not a power of two), beside the tensor-core kernel forced on
 the same inputs; the four full-size decode layers at M = 1, 3, 8 and 16 compared
 element by element; the 18432 x 73728 layer on sampled columns; the edge sweep;
@@ -62,6 +62,13 @@ SHAPES = [
     (1, 4096, 4000, 4000, "loguniform"),
     (6, 9736, 2048, 32, "halfnormal"),
     (11, 256, 16384, 128, "loguniform"),
+    # blocks of 48 and 80 columns (boxes of 16 columns, blocks straddling two 128-column
+    # tiles, ragged last blocks past N) and of 32, with groups of 32, 64, 128 and K
+    (1, 20008, 2048, 64, "halfnormal"),
+    (8, 19464, 1024, 128, "loguniform"),
+    (3, 12296, 1024, 32, "halfnormal"),
+    (5, 24320, 512, 512, "loguniform"),
+    (2, 7304, 2048, 128, "halfnormal"),
 ]
 
 

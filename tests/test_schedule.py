@@ -442,12 +442,15 @@ def test_gemv_column_block_widths():
 DECODE_SHAPES = sorted(set((m, n, k, g) for (m, n, k, g) in SHAPES if m <= DECODE_MAX_M and k % 32 == 0
                            and n * k <= 22016 * 4096)
                        | {(1, 73728, 18432, 128), (8, 73728, 18432, 128), (16, 73728, 18432, 128), (16, 12288, 4096, 128),
-                          (9, 1024, 2048, 64), (2, 264, 544, 32), (13, 4104, 1024, 128), (1, 4096, 4000, 4000)})
+                          (9, 1024, 2048, 64), (2, 264, 544, 32), (13, 4104, 1024, 128), (1, 4096, 4000, 4000),
+                          (1, 20008, 2048, 64), (8, 19464, 1024, 128), (3, 12296, 1024, 32), (5, 24320, 512, 512),
+                          (2, 7304, 2048, 128)})
 
 
 @pytest.mark.parametrize("M,N,K,G", DECODE_SHAPES)
 def test_decode_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
     check_decode_shape(M, N, K, G)
+
 
 
 def test_dispatch_rule():
