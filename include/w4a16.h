@@ -369,7 +369,8 @@ long long w4a16_set_wait_limit_ns(long long limit_ns);
 
 /* Which kernel the dispatcher picks for a shape of the 4-bit FP16 format
  * (w4a16_gemm, w4a16_gemm_ws, w4a16_gemm_fused) on the current device. It picks
- * path 3 by itself for up to eight rows of X when K is a multiple of 32 (where it
+ * path 3 by itself for up to eight rows of X when K is a multiple of 32, and for up to
+ * sixteen on layers of at most 4096 x 4096 with N >= 16 x the SM count (where it
  * measured faster on GB300), path 2 otherwise; path 1 only when forced:
  *   *path = 1: the CUDA-core kernel for one to four rows of X ("Low-Precision
  *              Quantization Kernels in Production" (llms.blog), section 2: the

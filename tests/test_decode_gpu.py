@@ -2,7 +2,8 @@
 MMAs, one to sixteen rows of X) against the CPU oracle.
 
 The dispatcher picks it by itself for up to eight rows of X when K is a multiple of
-32; here it is also forced for nine to sixteen rows. Covered: small and ragged
+32 (sixteen on layers of at most 4096 x 4096); here it is also forced for nine to
+sixteen rows. Covered: small and ragged
 shapes spanning several column blocks of every width (16, 32, 48, 64, 80) and every group
 size (32, 64, 128, K, K not a power of two), beside the tensor-core kernel forced on
 the same inputs; the four full-size decode layers at M = 1, 3, 8 and 16 compared

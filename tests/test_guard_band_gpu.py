@@ -66,7 +66,8 @@ def same_call_twice(fn, M, N, dtype, what):
 SHAPES = [
     (1, 256, 16384, 128),     # split-K, 16-row tile
     (3, 136, 200, 200),       # ragged N, one group per column
-    (16, 4096, 4096, 128),    # tile-aligned split into quarters
+    (16, 4096, 4096, 128),    # the decode kernel, sixteen rows of X
+    (32, 2048, 4096, 128),    # tile-aligned split of 32-row tiles
     (17, 264, 520, 32),       # 32-row tile, ragged M and N
     (100, 392, 776, 128),     # 128-row tile pair, odd tile count (phantom tile)
     (300, 264, 136, 32),      # 256-row tiles, ragged last row tile

@@ -99,7 +99,7 @@ def dispatch(M, N, K, G, sms=SMS, fmt="int4", force=0):
     forced or, by itself, for up to eight rows of X, where K is a multiple of 32;
     path 1 (CUDA-core kernel) only when forced; else the tensor-core plan."""
     if fmt == "int4" and M <= DECODE_MAX_M and K % 32 == 0:
-        if force == 3 or (force == 0 and M <= DECODE_AUTO_MAX_M):
+        if force == 3 or (force == 0 and (M <= DECODE_AUTO_MAX_M or (N <= 4096 and K <= 4096 and N >= 16 * sms))):
             return decode_plan(M, N, K, G, sms)
     if fmt == "int4" and M <= GEMV_MAX_M and force == 1:
         return gemv_plan(M, N, K, G, sms)
@@ -455,9 +455,10 @@ def test_decode_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
 
 def test_dispatch_rule():
     """The automatic choice for the 4-bit FP16 format: the decode kernel (path 3) for
-    up to eight rows of X where K is a multiple of 32, the tensor-core kernel
-    otherwise; blocks of 128 columns for the 73728-wide layer (576 blocks, two per SM
-    and more), 64 for the 12288- and 22016-wide ones, 16 for the 4096-wide ones
+    up to eight rows of X where K is a multiple of 32 (sixteen on layers of at most
+    4096 x 4096 with a 16-column block per SM), the tensor-core kernel otherwise; blocks
+    of 128 columns for the 73728-wide layer (576 blocks, two per SM and more), 48 for
+    the 12288-wide one, 80 for the 22016-wide one, 16 for the 4096-wide ones
     (measured on GB300)."""
     width = {4096: 16, 12288: 48, 22016: 80, 73728: 128}
     for (N, K) in [(4096, 4096), (12288, 4096), (22016, 4096), (4096, 11008), (73728, 18432)]:
@@ -465,11 +466,15 @@ def test_dispatch_rule():
             P = dispatch(M, N, K, 128)
             assert P["path"] == 3 and P["tm"] == 8
             assert P["cb"] == width[N]
-        assert dispatch(9, N, K, 128)["path"] == 2
+        # nine to sixteen rows: the decode kernel on the 4096 x 4096 layer, the tensor-core kernel elsewhere
+        assert dispatch(9, N, K, 128)["path"] == (3 if (N, K) == (4096, 4096) else 2)
+        assert dispatch(16, N, K, 128)["path"] == (3 if (N, K) == (4096, 4096) else 2)
         assert dispatch(16, N, K, 128, force=3)["path"] == 3 and dispatch(16, N, K, 128, force=3)["tm"] == 16
         assert dispatch(17, N, K, 128, force=3)["path"] == 2
         assert dispatch(1, N, K, 128, force=2)["path"] == 2
     assert dispatch(1, 4096, 4040, 128)["path"] == 2          # K not a multiple of 32
+    assert dispatch(16, 2048, 4096, 128)["path"] == 2          # fewer 16-column blocks than SMs
+    assert dispatch(17, 4096, 4096, 128)["path"] == 2
     assert dispatch(4, 4096, 4096, 128, fmt="w8")["tm"] == 16
     assert dispatch(1, 4096, 4096, 128, force=2)["tm"] == 16
     # ring depth: about 64 KB of packed words in flight, fewer where shared memory says so

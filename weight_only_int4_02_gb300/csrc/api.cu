@@ -142,7 +142,7 @@ constexpr int kGemvMaxM = 4;
 // picks it by itself for up to eight, where it measured faster than the tensor-core
 // kernel on every decode layer (4096 x 4096: 5.3 against 7.9 us; 18432 x 73728:
 // 121 against 138 us). From nine rows on the second half of X doubles its MMAs and
-// the tensor-core kernel wins on all but the smallest layers.
+// the tensor-core kernel wins on all but the smallest layers (decode_applies).
 constexpr int kDecodeMaxM = 16;
 constexpr int kDecodeAutoMaxM = 8;
 // Forced path (0 = the dispatcher's choice, 1 = CUDA-core kernel, 2 = tensor-core
@@ -252,18 +252,15 @@ bool gemv_applies(int M, int fmt, int force)
     return fmt == kFmtW4 && M <= kGemvMaxM && force == 1;
 }
 
-// Path 3 (decode kernel) for a shape: blocks of 128 columns (whole 2 KB rows of
-// packed words, X read once per 128 columns) where that gives two blocks per SM, else
-// of 64 (1 KB of each row) where that gives one, else of 16 (more CTAs for narrow
-// layers); one CTA per block. Measured on GB300: 18432 x 73728 at M = 1 119.4 us with
-// 128 against 121.3 with 64; 4096 x 22016 14.6 us with 64 against 15.1 with 128;
-// N = 4096 fastest with 16; 32 was never best.
-// Columns per block of the decode kernel. Two CTAs share an SM, and a launch chained
-// behind another takes the slots as they free, so an SM ends up with two CTAs of it or
-// none and the busiest SMs hold two blocks: with eight rows of X, the narrowest block
-// that gives more CTAs than SMs and at most two per SM (one wave); else 128 where the
-// layer has two 128-column blocks per SM, 64 where it has one 64-column block per SM,
-// and 16 below.
+// Columns per block of the decode kernel (path 3; one CTA per block). Two CTAs share
+// an SM, and a launch chained behind another takes the slots as they free, so an SM
+// ends up with two CTAs of it or none and the busiest SMs hold two blocks: with eight
+// rows of X, the narrowest block that gives more CTAs than SMs and at most two per SM
+// (one wave); else 128 where the layer has two 128-column blocks per SM, 64 where it
+// has one 64-column block per SM, and 16 below. Measured on GB300 (launches of one
+// shape chained, M = 1): 4096 x 12288 7.5 us with 48 against 8.3 with 64; 4096 x 22016
+// 10.8 with 80 against 14.1 with 64 and 14.6 with 128; 18432 x 73728 115 with 128 or
+// 64; N = 4096 fastest with 16.
 int decode_block_cols(int N, int mr, int sms)
 {
     if (g_force_cb == 16 || g_force_cb == 32 || g_force_cb == 64 || g_force_cb == 128 ||
@@ -291,17 +288,23 @@ Plan make_decode_plan(int M, int N, int K, int G, int sms)
     return P;
 }
 
-bool decode_applies(int M, int K, int fmt, int force)
+// The decode kernel takes up to eight rows of X by itself, and nine to sixteen on a
+// layer of at most 4096 x 4096 with one 16-column block per SM or more: there the
+// tensor-core kernel's split-K exchange outweighs the second pair of warp-level MMAs
+// (16 x 4096 x 4096: 6.9 against 8.3 us per launch; the wider and deeper decode layers
+// stay faster on the tensor-core kernel from nine rows on).
+bool decode_applies(int M, int N, int K, int sms, int fmt, int force)
 {
     if (fmt != kFmtW4 || M > kDecodeMaxM || K % 32 != 0) return false;
-    return force == 3 || (force == 0 && M <= kDecodeAutoMaxM);
+    if (force != 0) return force == 3;
+    return M <= kDecodeAutoMaxM || (N <= 4096 && K <= 4096 && N >= 16 * sms);
 }
 
 // The plan of a shape on this device.
 Plan device_plan(const DeviceState* st, int M, int N, int K, int G, int fmt)
 {
     const int force = g_force_path.load();
-    if (decode_applies(M, K, fmt, force)) return make_decode_plan(M, N, K, G, st->sms);
+    if (decode_applies(M, N, K, st->sms, fmt, force)) return make_decode_plan(M, N, K, G, st->sms);
     if (gemv_applies(M, fmt, force)) {
         Plan P = make_gemv_plan(M, N, K, G, st->sms);
         // persistent: no more CTAs than the SMs hold at once
