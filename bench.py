@@ -88,6 +88,21 @@ def kernel_name(plan, N):
     return ("w4a16_gemv_kernel<%d>" if path == 1 else "w4a16_tc_kernel<%d>") % tile
 
 
+def kernel_roofline(name, k, peaks, workload):
+    """Per-step time of one kernel instance in the sweep and its roofline fraction:
+    algorithmic bytes (or flops, when the tensor pipe bounds it) over its mean launch,
+    against the measured peak; the committed ncu traffic per launch when the sources
+    match."""
+    us = k["ms"] * 1e3
+    hbm_s = k["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    tc_s = k["flops"] / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if hbm_s >= tc_s else "tensor"
+    return {"launches_per_step": k["launches"], "us_per_step": us, "bound": bound,
+            "roofline_frac": max(hbm_s, tc_s) / (us * 1e-6),
+            "algorithmic_bytes_per_launch": k["bytes"] / k["launches"],
+            "traffic": load_traffic(name, workload)}
+
+
 def roofline_seconds(M, K, N, G, peaks):
     return max(algorithmic_bytes(M, K, N, G) / (peaks["hbm_gbs"] * 1e9),
                flops(M, K, N) / (peaks["bf16_tflops"] * 1e12))
@@ -329,7 +344,12 @@ def run_ours(args):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
             st = torch.cuda.current_stream()
-            cud.record_external(ev[0], st)
+            # the step's start is recorded on the side branch too, so that no event node
+            # precedes the first GEMM
+            start = torch.cuda.Event()
+            start.record(st)
+            side.wait_event(start)
+            cud.record_external(ev[0], side)
             for b in range(len(bounds) - 1):
                 for ci in range(bounds[b], bounds[b + 1]):
                     c = per_case[ci]
@@ -478,7 +498,7 @@ def run_ours(args):
                       "weight_gbs": weight_bytes(c["K"], c["N"], G) / (mean_ms[ci] * 1e-3) / 1e9,
                       "roofline_frac": roofline_seconds(c["M"], c["K"], c["N"], G, peaks) / (mean_ms[ci] * 1e-3)}
                      for ci, c in enumerate(per_case)],
-        "kernels": {n: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3} for n, v in kernels.items()},
+        "kernels": {n: kernel_roofline(n, v, peaks, args.workload) for n, v in kernels.items()},
         "byte_ratio_fp16_over_w4g128": fp16_over_int4_byte_ratio(G),
     }
     if args.workload == DEFAULT_WORKLOAD and not args.no_probes:
