@@ -87,6 +87,33 @@ def test_decode_and_tensor_core_against_the_oracle(w, oracle_mod, M, N, K, G, ki
         check_within(y.cpu().numpy(), y_ref, absum, "path %d M=%d N=%d K=%d G=%d" % (path, M, N, K, G))
 
 
+def random_shapes(n, seed):
+    """Seeded random shapes: 1..16 rows of X, N a multiple of 8 up to 16000, K a
+    multiple of 32 up to 4000, groups of 32, 64, 128 or K; every block width, ragged
+    last blocks and stages, odd and even rings."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.integers(1, 17))
+        N = 8 * int(rng.integers(1, 2001))
+        K = 32 * int(rng.integers(1, 126))
+        G = int(rng.choice([32, 64, 128, K]))
+        out.append((M, N, K, G))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,G", random_shapes(24, 77))
+def test_random_shapes_against_the_oracle(w3, oracle_mod, M, N, K, G):
+    w = w3
+    x, q, s = inputs.problem(M, K, N, G, seed=M + N + K, scale_kind="loguniform")
+    packed, sp = w.pack(to_dev(q), to_dev(s), G)
+    assert w.plan(M, N, K, G)[0] == 3
+    y = w.gemm(to_dev(x), packed, sp, N, G)
+    torch.cuda.synchronize()
+    check_within(y.cpu().numpy(), *oracle_mod.gemm(x, q, s, G), "random M=%d N=%d K=%d G=%d" % (M, N, K, G))
+    assert w.check_device_status() == w.OK
+
+
 def test_full_size_decode_layers_elementwise(w, oracle_mod):
     """The four Llama-2-7B-like decode layers at M = 1, 3, 8 (the dispatcher's own
     choice) and 16 (forced), every element."""

@@ -9,6 +9,7 @@ split-K reducer reads exactly the slots the contributors wrote.
 import re
 import os
 
+import numpy as np
 import pytest
 
 from weight_only_int4_02_gb300 import inputs
@@ -449,6 +450,26 @@ DECODE_SHAPES = sorted(set((m, n, k, g) for (m, n, k, g) in SHAPES if m <= DECOD
 
 @pytest.mark.parametrize("M,N,K,G", DECODE_SHAPES)
 def test_decode_schedule_covers_once_and_stays_in_bounds(M, N, K, G):
+    check_decode_shape(M, N, K, G)
+
+
+def random_decode_shapes(n, seed):
+    """Seeded random shapes of the decode kernel: 1..16 rows of X, N a multiple of 8,
+    K a multiple of 32, groups of 32, 64, 128 or K (the block width, the ring depth and
+    its parity follow from them)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.integers(1, 17))
+        N = 8 * int(rng.integers(1, 3500))
+        K = 32 * int(rng.integers(1, 200))
+        G = int(rng.choice([32, 64, 128, K]))
+        out.append((M, N, K, G))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,G", random_decode_shapes(60, 2026))
+def test_decode_schedule_random_shapes(M, N, K, G):
     check_decode_shape(M, N, K, G)
 
 
