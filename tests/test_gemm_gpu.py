@@ -240,7 +240,7 @@ def test_device_plan_matches_host_mirror(w):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shapes = [(m, n, k) for (m, k, n) in inputs.WORKLOADS["llama2_7b_decode_sweep"]["cases"] if m <= 32]
     shapes += [(1, 256, 16384), (3, 136, 200), (17, 4096, 4000), (1, 73728, 18432), (16, 73728, 18432),
-               (2, 8192, 4096)]
+               (2, 8192, 4096), (64, 4096, 4096), (128, 4096, 4096), (128, 4096, 11008), (100, 392, 776)]
     for force in (0, 1, 2, 3):
         prev = w.force_path(force)
         try:
