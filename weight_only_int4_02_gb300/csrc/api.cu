@@ -563,7 +563,8 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
         d.stages = ceil_div(d.rows, kDecStageRows);
         d.scale_rows = ((G & (G - 1)) == 0 && G <= kDecStageRows * 32) ? kDecStageRows * 32 / G : 1;
         d.x_rows = M;
-        // slots for about 64 KB of packed words in flight, within the shared-memory budget
+        // slots for 24 to 80 KB of packed words in flight (decode_words_in_flight), within
+        // the shared-memory budget
         d.ring = decode_words_in_flight(P.dec_cb) / (kDecStageRows * P.dec_cb * 16);
         if (d.ring > kDecSmemBudget / decode_slot_bytes(P.dec_cb, M)) d.ring = kDecSmemBudget / decode_slot_bytes(P.dec_cb, M);
         if (d.ring > kDecMaxRing) d.ring = kDecMaxRing;

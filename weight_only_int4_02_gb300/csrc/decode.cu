@@ -45,9 +45,10 @@
 //
 // Staging: one producer warp streams the stage's packed words (2-D TMA boxes of 16
 // rows x up to 64 columns, each inside one 128-column tile) and group scales into a
-// ring; it needs nothing from
-// the previous kernel, so the ring fills while that kernel finishes (programmatic
-// dependent launch). A second producer waits for the previous kernel, then brings
+// ring of 24 to 80 KB of words (by block width); it needs nothing from the previous
+// kernel, so the ring fills while that kernel finishes (programmatic dependent
+// launch). With an odd number of slots a team first waits for the other team to
+// consume a slot's earlier stage. A second producer waits for the previous kernel, then brings
 // the stage's X with one 3-D TMA as [16 rows][mr rows of X][32 values]: 64 bytes per
 // row of X, so the eight rows a quarter-warp reads sit in different banks.
 // A CTA holds under half of an SM (about 100 KB of shared memory, 320 threads), so
