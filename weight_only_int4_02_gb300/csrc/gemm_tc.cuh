@@ -141,9 +141,14 @@ struct TcCfg {
     // waits on the MMA; and X, freed by the MMA's commit.
     static constexpr int kWStageBytes = kPkBytes + kScBytes + kZpBytes;
     // a multiple of the team count; 8-bit stages of 128-row tiles and up are 4 deep
-    // (64 KB of codes in flight, as 8 stages of 4-bit codes) to leave room for X
-    static constexpr int kWStages =
-        (FMT == kFmtW8 || kSp) ? (TM >= 128 ? 4 : 8) : (TM <= 32 || KSUB == 2) ? 8 : 6;
+    // (64 KB of codes in flight, as 8 stages of 4-bit codes) to leave room for X.
+    // 256-row tiles keep two: a stage of X is 64 KB there and one X slot more (three
+    // instead of two) is worth more than W stages ahead, since each W stage feeds
+    // 1024 cycles of MMAs (measured: 7-13% faster at M = 512 .. 4096).
+    static constexpr int kWStages = (FMT == kFmtW8 || kSp) ? (TM >= 128 ? 4 : 8)
+                                    : TM == 256                  ? 2
+                                    : (TM <= 32 || KSUB == 2)    ? 8
+                                                                 : 6;
     static constexpr int kXFit = (220 * 1024 - kWStages * kWStageBytes) / kXBytes;
     static constexpr int kXStages = kXFit > 8 ? 8 : kXFit;
     // Dequant teams take stages in turn; a team is KSUB/2 groups of four warps.
@@ -296,6 +301,118 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
     g.kb = (int)(i - (long long)g.t * p.iters);
     g.ke = (int)min((long long)p.iters, g.kb + (it_end - i));
     return g;
+}
+
+// Epilogue stores of Y. An epilogue lane holds one output feature n (its TMEM lane)
+// and 16 consecutive rows m of X (a tcgen05.ld of 16 columns), while Y is row-major in
+// m with n contiguous, so a store straight from the registers writes 2 bytes per lane
+// and row: 16 narrow stores per chunk, which measured about 1000 cycles per chunk with
+// the GPU's memory busy. The chunk is transposed across lanes with shuffles first, so
+// each lane stores two 16-byte vectors. (FP32 partials, 4 bytes per lane and row, measured
+// slower with the same transpose: they keep the direct stores.)
+
+// 8 x 8 transpose of 32-bit elements within each group of eight lanes: on return,
+// x[k] of lane 8g + j is the x[j] that lane 8g + k held.
+__device__ __forceinline__ void transpose8_lanes(uint32_t (&x)[8], int lane)
+{
+#pragma unroll
+    for (int b = 4; b >= 1; b >>= 1) {
+        const bool up = (lane & b) != 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k & b) continue;
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, up ? x[k] : x[k | b], b);
+            if (up) x[k] = recv;
+            else x[k | b] = recv;
+        }
+    }
+}
+
+// Rows m0 .. m0+15 of Y for the warp's 32 features n0 .. n0+31 (lane = feature), from
+// the lane's FP32 accumulators r[e] (row m0 + e). After the transpose lane 8g + j holds
+// rows m0 + 2j and m0 + 2j + 1 of features n0 + 8g .. +7 and writes each as one 16-byte
+// vector (vec: Y rows 16-byte aligned), else element by element inside M and N.
+template <bool BF>
+__device__ __forceinline__ void store_y_rows16(const GemmParams& p, const uint32_t (&r)[16], int m0, int n0,
+                                               int lane, bool vec)
+{
+    uint32_t h[8];   // h[k]: rows 2k (low half) and 2k+1 (high half), 16-bit
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float a = __uint_as_float(r[2 * k]), b = __uint_as_float(r[2 * k + 1]);
+        if constexpr (BF) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+            h[k] = *reinterpret_cast<const uint32_t*>(&v);
+        } else {
+            const __half2 v = __floats2half2_rn(a, b);
+            h[k] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+    }
+    transpose8_lanes(h, lane);   // h[k]: rows 2j, 2j+1 of feature 8g + k
+    const int g = lane >> 3, j = lane & 7;
+    const int n = n0 + 8 * g;
+#pragma unroll
+    for (int hi = 0; hi < 2; ++hi) {
+        const int m = m0 + 2 * j + hi;
+        if (m >= p.M) continue;
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = __byte_perm(h[2 * q], h[2 * q + 1], hi ? 0x7632u : 0x5410u);
+        __half* dst = p.y + (size_t)m * p.ldy + n;
+        if (vec && n + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (n + e < p.N) dst[e] = __ushort_as_half((unsigned short)(o[e >> 1] >> (16 * (e & 1))));
+        }
+    }
+}
+
+// Rows m0 .. m0+15 of the residual for the warp's 32 features in the epilogue's layout
+// (lane = feature, rv[e] = row m0 + e): lane 8g + j reads rows m0 + 2j and m0 + 2j + 1
+// of features n0 + 8g .. +7 as two 16-byte vectors (vec: residual rows 16-byte
+// aligned), else element by element, and the 8 x 8 transpose hands each lane its own
+// feature's sixteen rows. Zero outside M and N or without a residual.
+template <bool BF>
+__device__ __forceinline__ void load_residual_rows16(const GemmParams& p, int m0, int n0, int lane, bool vec,
+                                                     float (&rv)[16])
+{
+    const int g = lane >> 3, j = lane & 7;
+    const int n = n0 + 8 * g;
+    uint32_t w[2][4];
+#pragma unroll
+    for (int hi = 0; hi < 2; ++hi) {
+        const int m = m0 + 2 * j + hi;
+        const __half* src = p.residual + (size_t)m * p.ldr + n;
+        if (m < p.M && vec && n + 8 <= p.N) {
+            const uint4 u = *reinterpret_cast<const uint4*>(src);
+            w[hi][0] = u.x; w[hi][1] = u.y; w[hi][2] = u.z; w[hi][3] = u.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t v = 0;
+                if (m < p.M && n + 2 * q < p.N) v = __half_as_ushort(src[2 * q]);
+                if (m < p.M && n + 2 * q + 1 < p.N) v |= (uint32_t)__half_as_ushort(src[2 * q + 1]) << 16;
+                w[hi][q] = v;
+            }
+        }
+    }
+    uint32_t h[8];   // h[k]: rows 2j (low half) and 2j+1 (high half) of feature 8g + k
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = __byte_perm(w[0][k >> 1], w[1][k >> 1], (k & 1) ? 0x7632u : 0x5410u);
+    transpose8_lanes(h, lane);   // h[k]: rows 2k, 2k+1 of the lane's own feature
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+            const uint32_t b16 = (h[k] >> (16 * hi)) & 0xffffu;
+            if constexpr (BF)
+                rv[2 * k + hi] = __uint_as_float(b16 << 16);
+            else
+                rv[2 * k + hi] = __half2float(__ushort_as_half((unsigned short)b16));
+        }
+    }
 }
 
 // Split-K fix-up of a tile by its last contributor: Y = the sum of every
@@ -741,34 +858,25 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + ((uint32_t)(warp * 32) << 16) + C::kDCol + d * TM;
             float* part = p.partials + (size_t)slot_of(p, cta, t) * TM * kTileN + n_in;
+            const bool yvec = (p.ldy & 7) == 0;   // Y rows 16-byte aligned (Y itself is)
+            const bool rvec = ((reinterpret_cast<uintptr_t>(p.residual) | (uintptr_t)(p.ldr * 2)) & 15) == 0;
             for (int c = 0; c < chunks; ++c) {
                 uint32_t r[16];
                 tmem_ld16(d_tmem + c * 16, r);
                 if (!split) {
-                    if (n < p.N) {
-                        if constexpr (EPI) {
-                            const float bv = bias_n;
-                            float rv[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = m0 + c * 16 + e;
-                                rv[e] = m < p.M ? ld16<BF>(p.residual, (size_t)m * p.ldr + n) : 0.f;
-                            }
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = m0 + c * 16 + e;
-                                if (m < p.M)
-                                    p.y[(size_t)m * p.ldy + n] =
-                                        st16<BF>(epilogue_op(p.act, __uint_as_float(r[e]), bv, rv[e]));
-                            }
+                    if constexpr (EPI) {
+                        float rv[16];
+                        if (p.residual) {
+                            load_residual_rows16<BF>(p, m0 + c * 16, n - lane, lane, rvec, rv);
                         } else {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = m0 + c * 16 + e;
-                                if (m < p.M) p.y[(size_t)m * p.ldy + n] = st16<BF>(__uint_as_float(r[e]));
-                            }
+                            for (int e = 0; e < 16; ++e) rv[e] = 0.f;
                         }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            r[e] = __float_as_uint(epilogue_op(p.act, __uint_as_float(r[e]), bias_n, rv[e]));
                     }
+                    store_y_rows16<BF>(p, r, m0 + c * 16, n - lane, lane, yvec);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
