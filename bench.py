@@ -271,10 +271,20 @@ def cpu_baseline(wl, budget_s=15.0):
     stride = max(1, int(total / max(want, 1.0)))
     t, done = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), stride,
                                 threads, cache)
+    if stride == 1:
+        # the whole workload fits the budget: repeat it (up to 8 passes) for a steadier rate
+        passes = 1
+        while passes < 8 and t * (passes + 1) / passes <= budget_s:
+            dt, dd = oracle_sample_run(cases, wl["group_size"], wl["scale_mult"], wl.get("outlier_frac", 0.0), 1,
+                                       threads, cache)
+            t, done, passes = t + dt, done + dd, passes + 1
+        sample = "the whole workload (every case, all rows and columns), %d pass%s, %.1f s" % (
+            passes, "" if passes == 1 else "es", t)
+    else:
+        sample = ("every case of the workload, all rows, every %d-th output column (%.3g of the "
+                  "workload's flops), %.1f s" % (stride, done / total, t))
     return {"value": done / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "every case of the workload, all rows, every %d-th output column (%.3g of the "
-                      "workload's flops), %.1f s" % (stride, done / total, t),
-            "seconds": t}
+            "sample": sample, "seconds": t}
 
 
 # --------------------------------------------------------------------------- our arm
