@@ -42,6 +42,11 @@ CASES = [
     (40, 1024, 2048, 32, 2, 8, 8, 16),
     (300, 1032, 520, 520, 2, 56, 8, 8),
     (3, 4104, 1000, 1000, 2, 24, 16, 8),
+    # Y and residual rows that are not 16-byte aligned (row strides not a multiple of 8):
+    # the tensor-core kernel's unsplit tiles then store and read element by element
+    (300, 1032, 520, 520, 2, 56, 3, 5),
+    (3, 4104, 1000, 1000, 2, 24, 1, 3),
+    (128, 1024, 512, 128, 2, 8, 5, 7),
     (2, 1024, 2048, 128, 1, 64, 8, 8),
     (4, 264, 520, 32, 1, 8, 8, 8),
 ]
