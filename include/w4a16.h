@@ -34,7 +34,9 @@
  *    W4A16_ERR_CUDA from a failed launch (see w4a16_last_cuda_error()).
  *  - Group size G must be 32, 64 or 128, or equal to K (one scale per column);
  *    G = -1 is accepted as "equal to K". K must be a multiple of 8 (16-byte X
- *    rows) and N a multiple of 8 (16-byte Y rows).
+ *    rows) and N a multiple of 8 (16-byte Y rows). A shape whose tensor-core
+ *    schedule would exceed 2^31 pipeline stages (about 2^31 * 16384 multiply-adds,
+ *    far beyond device memory) is rejected with W4A16_ERR_INVALID_ARG.
  *  - The GEMM kernels are launched with programmatic dependent launch: a GEMM
  *    may start, and start streaming its packed weights, scales and zero-points,
  *    before the kernel enqueued just ahead of it on the stream has finished; it

@@ -309,20 +309,24 @@ def plan(M, N, K, G, sms=SMS, fmt="int4"):
                 best, best_s = cost, s
             s += 1
         units = work_tiles * best_s
+        sk_tiles = work_tiles
     else:
         min_iters = max(4, iters // 2 if tm >= 64 else (iters // 4 if tm == 32 else 0))
-        units = min(units, -(-total // min_iters))
+        units = max(1, min(units, -(-total // min_iters)))
+        sk_tiles = work_tiles % units    # tiles past the last whole wave: split, run first
+        if 0 < sk_tiles and 2 * sk_tiles < units:
+            sk_tiles += units            # at least half a wave: about two contributors a tile
     units = max(1, units)
     return dict(path=2, tm=tm, ksub=ksub, xblocks=xblocks, fmt=fmt, m_tiles=m_tiles, n_tiles=n_tiles,
-                KC=KC, iters=iters, ng=ng, total=total, grid=units)
+                KC=KC, iters=iters, ng=ng, total=total, sk_tiles=sk_tiles, sk_iters=sk_tiles * iters, grid=units)
 
 
 def cta_begin(P, c):
-    return c * P["total"] // P["grid"]
+    return c * P["sk_iters"] // P["grid"]
 
 
 def cta_of(P, i):
-    c = (i * P["grid"]) // P["total"]
+    c = (i * P["grid"]) // P["sk_iters"]
     while c + 1 < P["grid"] and cta_begin(P, c + 1) <= i:
         c += 1
     while c > 0 and cta_begin(P, c) > i:
@@ -335,6 +339,8 @@ def slot_of(P, c, t):
 
 
 def segments(P, c):
+    """Mirror of work_begin / work_next: the CTA's range of the split region, then its
+    whole tiles sk_tiles + c, + grid, ..."""
     i, end = cta_begin(P, c), cta_begin(P, c + 1)
     while i < end:
         t = i // P["iters"]
@@ -342,6 +348,10 @@ def segments(P, c):
         ke = min(P["iters"], kb + (end - i))
         yield t, kb, ke
         i += ke - kb
+    t = P["sk_tiles"] + c
+    while t < P["n_tiles"] * P["m_tiles"]:
+        yield t, 0, P["iters"]
+        t += P["grid"]
 
 
 def check_shape(M, N, K, G, sms=SMS, fmt="int4"):
@@ -410,7 +420,9 @@ SHAPES = sorted(set(
     + [(m, 4096, 4096, g) for m in inputs.EDGE_M for g in (32, 4096)]
     + [(m, 256, 16384, 128) for m in inputs.EDGE_M]
     + [(m, 4096, k, 128) for m in inputs.EDGE_M for k in (4000, 4040)]
-    + [(1, 8, 8, 8), (1, 128, 64, 64), (3, 136, 200, 200), (300, 264, 136, 32), (1, 8, 4040, 4040)]))
+    + [(1, 8, 8, 8), (1, 128, 64, 64), (3, 136, 200, 200), (300, 264, 136, 32), (1, 8, 4040, 4040)]
+    # a few tiles past the last whole wave, with too few stages for every CTA
+    + [(1, 20008, 2048, 64), (1, 19464, 512, 128), (40, 19592, 1024, 32)]))
 
 
 @pytest.mark.parametrize("M,N,K,G", SHAPES)
@@ -532,7 +544,7 @@ def tc_cfg(tm, ks, fmt):
     pk = ks * (8192 if w8 else 6144 if sp else 4096)
     sc = (stage_k // 32) * 256
     zpb = (stage_k // 32) * 64 if zp else 0
-    SW = (4 if tm >= 128 else 8) if (w8 or sp) else (8 if (tm <= 32 or ks == 2) else 6)
+    SW = (4 if tm >= 128 else 8) if (w8 or sp) else (2 if tm == 256 else 8 if (tm <= 32 or ks == 2) else 6)
     SX = min(8, (220 * 1024 - SW * (pk + sc + zpb)) // xbytes)
     dbufs = 2 if tm <= 128 else 1
     slot = ks * 32 + (ks * 4 * 8 if sp else 0)
@@ -572,6 +584,7 @@ def test_layout_mirror_matches_the_compiled_sizes():
     assert tc_cfg(16, 4, "int4")["smem"] == 214408
     assert tc_cfg(64, 4, "int4")["smem"] == 210200
     assert tc_cfg(128, 2, "int4")["smem"] == 206184
+    assert tc_cfg(256, 2, "int4")["smem"] == 216312
     assert tc_cfg(16, 2, "w8")["smem"] == 173480
     assert tc_cfg(256, 2, "w8")["smem"] == 201992
     assert tc_cfg(16, 2, "sparse")["smem"] == 181640
@@ -616,3 +629,46 @@ def test_no_alloc_scratch_admission():
             assert fits == (M <= 32 or (M == 64 and N == 12288)), (M, N, K, need(M, N, K))
     assert need(64, 4096, 4096) == limit + partials_off
     assert need(128, 22016, 4096) > limit and need(16, 4096, 4096) <= limit
+
+
+def test_split_region_runs_first_and_whole_tiles_close_every_cta():
+    """With at least as many tiles as CTAs, the tiles past the last whole wave form the
+    split region: every CTA takes an equal share of its stages first, then the same
+    number of whole tiles, round-robin, so that the launch ends on whole tiles (direct
+    stores) and every partial and fix-up comes before a CTA's whole tiles."""
+    for (M, N, K) in [(16, 22016, 4096), (128, 22016, 4096), (16, 73728, 18432), (128, 73728, 18432),
+                      (1024, 15360, 5120), (4096, 27648, 5120), (256, 19456, 4096)]:
+        P = plan(M, N, K, 128)
+        T = P["n_tiles"] * P["m_tiles"]
+        assert T >= P["grid"]
+        rest = T % P["grid"]
+        assert P["sk_tiles"] == (rest + P["grid"] if 0 < 2 * rest < P["grid"] else rest)
+        assert P["sk_tiles"] == 0 or P["sk_iters"] >= P["grid"] * P["iters"] // 2   # about two contributors a tile
+        whole = (T - P["sk_tiles"]) // P["grid"]
+        for c in range(P["grid"]):
+            segs = list(segments(P, c))
+            full = [s for s in segs if s[1] == 0 and s[2] == P["iters"] and s[0] >= P["sk_tiles"]]
+            assert len(full) == whole
+            assert segs[len(segs) - len(full):] == full          # whole tiles last
+            assert all(t < P["sk_tiles"] for (t, kb, ke) in segs[:len(segs) - len(full)])
+
+
+def random_tc_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.choice([1, 3, 16, 17, 40, 64, 100, 128, 200, 256, 300, 1024]))
+        N = int(rng.integers(1, 400)) * 8 * int(rng.choice([1, 8, 16]))
+        K = int(rng.integers(1, 200)) * 8 * int(rng.choice([1, 4, 16]))
+        G = int(rng.choice([32, 64, 128, -1]))
+        out.append((M, N, K, K if G == -1 else G))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,G", random_tc_shapes(80, 7))
+def test_schedule_random_shapes(M, N, K, G):
+    """Random shapes through the tensor-core kernel's schedule mirror: covered once,
+    in bounds, every split tile's reducer reading exactly its writers' slots."""
+    if K % G or K < 8 or N < 8:
+        pytest.skip("shape outside the entry points' rules")
+    check_shape(M, N, K, G)

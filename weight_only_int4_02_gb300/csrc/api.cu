@@ -104,9 +104,11 @@ long long g_wait_limit_ns = 1000000000LL;
 // Ablation knobs, read once from the environment: W4A16_SPLIT forces the number of
 // parts every tile is cut into when there are fewer tiles than SMs (clamped to what
 // the shape allows); W4A16_MIN_ITERS forces the fewest stages a CTA takes when
-// there are more. 0 keeps the dispatcher's own choice.
+// there are more; W4A16_SPLIT_ALL=1 puts every tile in the split region then (stream-K
+// over the whole space, with no whole tiles). 0 keeps the dispatcher's own choice.
 int g_force_split = 0;
 int g_force_min_iters = 0;
+int g_force_split_all = 0;
 int g_force_tm = 0;   // W4A16_TILE_M: rows of X per tile (16, 32, 64, 128 or 256) for the tensor-core kernel
 int g_force_cb = 0;   // W4A16_DECODE_CB: columns per block (16, 32, 48, 64, 80 or 128) for the decode kernel
 
@@ -156,6 +158,7 @@ struct Plan {
     int xblocks;  // 64-wide blocks of X per stage (the X tensor map's box depth)
     int m_tiles, n_tiles, KC, ng, iters;
     long long total;
+    int sk_tiles; // tiles of the split region (the first ones); the rest are whole tiles
     int grid;     // CTAs, one work unit each
     size_t ws_bytes;
     int gemv_mr;  // path 1: rows of X the kernel is built for (1, 2, 4)
@@ -212,6 +215,7 @@ Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
         if (g_force_split > 0) best_s = g_force_split < s_max ? (g_force_split < P.iters ? g_force_split : P.iters) : s_max;
         if (best_s < 1) best_s = 1;
         units = work_tiles * best_s;
+        P.sk_tiles = (int)work_tiles;
     } else {
         // Stream-K over every SM, but a work unit takes at least kMinItersPerCta
         // stages, and with 32 or more rows of X at least a quarter (32 rows) or a
@@ -223,6 +227,19 @@ Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
         if (g_force_min_iters > 0) min_iters = g_force_min_iters;
         const long long by_work = (P.total + min_iters - 1) / min_iters;
         if (units > by_work) units = by_work;
+        if (units < 1) units = 1;
+        // Whole waves of tiles go to the CTAs whole, round-robin; the tiles past the
+        // last whole wave are the split region, cut into one stream-K range per CTA
+        // and run first, so their partials and fix-ups overlap the whole tiles' MMAs
+        // and every CTA ends on a whole tile. A split tile's last contributor reads
+        // every other contributor's partial, one round trip per few rows, so the region
+        // must not spread a few tiles over many CTAs: with fewer tiles than half the
+        // CTAs it takes one whole wave more (about two contributors a tile; measured:
+        // 20 tiles over 152 CTAs, 7.6 contributors each, ran the 4096x22016 layer at
+        // M = 128 in 61 us against 27). That also gives every CTA's range a stage.
+        const long long rest = work_tiles % units;
+        const long long sk = (rest > 0 && 2 * rest < units) ? rest + units : rest;
+        P.sk_tiles = g_force_split_all ? (int)work_tiles : (int)sk;
     }
     if (units < 1) units = 1;
     P.grid = (int)units;
@@ -394,6 +411,7 @@ w4a16_status device_state(DeviceState** out)
             if (const char* s = std::getenv("W4A16_WAIT_LIMIT_NS")) g_wait_limit_ns = std::atoll(s);
             if (const char* s = std::getenv("W4A16_SPLIT")) g_force_split = std::atoi(s);
             if (const char* s = std::getenv("W4A16_MIN_ITERS")) g_force_min_iters = std::atoi(s);
+            if (const char* s = std::getenv("W4A16_SPLIT_ALL")) g_force_split_all = std::atoi(s);
             if (const char* s = std::getenv("W4A16_TILE_M")) g_force_tm = std::atoi(s);
             if (const char* s = std::getenv("W4A16_DECODE_CB")) g_force_cb = std::atoi(s);
         }
@@ -542,6 +560,8 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     w4a16_status rc = device_state(&st);
     if (rc != W4A16_OK) return rc;
     const Plan P = device_plan(st, M, N, K, G, fmt);
+    // the tensor-core kernel counts a CTA's stages in 32 bits
+    if (P.path == 2 && P.total >= (1LL << 31)) return W4A16_ERR_INVALID_ARG;
     if (P.path == 3) {
         DecodeParams d;
         d.y = reinterpret_cast<__half*>(y);
@@ -633,7 +653,8 @@ w4a16_status gemm_impl(const uint16_t* x, const uint32_t* packed, const uint16_t
     p.m_tiles = P.m_tiles;
     p.KC = fmt == kFmtW4Sp ? P.KC / 2 : P.KC;   // packed chunks per column (128 values of k when sparse)
     p.iters = P.iters;
-    p.total_iters = P.total;
+    p.sk_tiles = P.sk_tiles;
+    p.sk_iters = (long long)P.sk_tiles * P.iters;
     p.grid = P.grid;
     p.wait_limit_ns = g_wait_limit_ns;
     p.bias = reinterpret_cast<const __half*>(bias);

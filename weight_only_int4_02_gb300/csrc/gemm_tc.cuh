@@ -72,7 +72,8 @@ struct GemmParams {
     int n_tiles, m_tiles;
     int KC;                 // 64-value sub-chunks per weight column in the packed layout
     int iters;              // stages per tile = KC / KSUB
-    long long total_iters;  // n_tiles * m_tiles * iters
+    int sk_tiles;           // tiles of the split region (the first ones), the rest whole
+    long long sk_iters;     // sk_tiles * iters: the split region's stages
     int grid;               // CTAs: one work unit each
     int x_3d;               // X tensor map is 3-D {64, M, K/64}: one TMA per stage
     int x_rows;             // rows of X each TMA box brings (<= TM, a multiple of 8); the
@@ -191,22 +192,30 @@ struct TcCfg {
     static_assert(!kSp || KSUB == 2, "sparse stages are two 128-value sub-chunks");
 };
 
-// First iteration of CTA c.
+// Work of CTA c: first its range [cta_begin(c), cta_begin(c + 1)) of the split
+// region's stages (tiles 0 .. sk_tiles-1, tile-major), then the whole tiles
+// sk_tiles + c, sk_tiles + c + grid, ... The split region is every tile when there
+// are fewer tiles than CTAs (each tile cut into the same number of parts), and the
+// tiles past the last whole wave otherwise, so that a CTA's split work comes first:
+// its partial and the tile's fix-up run under the MMAs of its whole tiles, and the
+// launch ends on a whole tile's direct store.
+
+// First split-region iteration of CTA c.
 __device__ __forceinline__ long long cta_begin(const GemmParams& p, int c)
 {
-    return (long long)c * p.total_iters / p.grid;
+    return (long long)c * p.sk_iters / p.grid;
 }
 
-// The CTA whose range holds iteration i.
+// The CTA whose range holds split-region iteration i.
 __device__ __forceinline__ int cta_of(const GemmParams& p, long long i)
 {
-    int c = (int)((i * p.grid) / p.total_iters);
+    int c = (int)((i * p.grid) / p.sk_iters);
     while (c + 1 < p.grid && cta_begin(p, c + 1) <= i) ++c;
     while (c > 0 && cta_begin(p, c) > i) --c;
     return c;
 }
 
-// Partial slot of CTA c for tile t: 2c if t holds the CTA's first iteration, else 2c + 1.
+// Partial slot of CTA c for split tile t: 2c if t holds the CTA's first iteration, else 2c + 1.
 __device__ __forceinline__ int slot_of(const GemmParams& p, int c, int t)
 {
     return cta_begin(p, c) >= (long long)t * p.iters ? 2 * c : 2 * c + 1;
@@ -300,6 +309,27 @@ __device__ __forceinline__ Segment segment_at(const GemmParams& p, long long i, 
     g.t = (int)(i / p.iters);
     g.kb = (int)(i - (long long)g.t * p.iters);
     g.ke = (int)min((long long)p.iters, g.kb + (it_end - i));
+    return g;
+}
+
+// A CTA's work as one run of local iterations v = 0 .. v_end: its split range of
+// sk_len iterations from b = cta_begin(c) first, then its whole tiles, iters each.
+// (The host keeps every count of stages below 2^31.)
+__device__ __forceinline__ int work_len(const GemmParams& p, int c, int sk_len)
+{
+    const int tiles = p.n_tiles * p.m_tiles;
+    const int whole = c + p.sk_tiles < tiles ? (tiles - p.sk_tiles - c + p.grid - 1) / p.grid : 0;
+    return sk_len + whole * p.iters;
+}
+
+// The segment holding local iteration v of CTA c.
+__device__ __forceinline__ Segment work_segment(const GemmParams& p, int c, long long b, int sk_len, int v)
+{
+    if (v < sk_len) return segment_at(p, b + v, b + sk_len);
+    Segment g;
+    g.t = p.sk_tiles + c + ((v - sk_len) / p.iters) * p.grid;
+    g.kb = 0;
+    g.ke = p.iters;
     return g;
 }
 
@@ -579,7 +609,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
 
     const int cta = blockIdx.x;
     const long long it_begin = cta_begin(p, cta);
-    const long long it_end = cta_begin(p, cta + 1);
+    const int sk_len = (int)(cta_begin(p, cta + 1) - it_begin);
+    const int v_end = work_len(p, cta, sk_len);
 
     // Every role walks the same stage sequence seq = 0, 1, ... over the CTA's
     // range; stage seq uses slot seq % S of the shared ring and slot seq % A of
@@ -595,8 +626,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         const int S = is_x ? SX : SW;
         uint32_t seq = 0;
         bool ok = true;
-        for (long long i = it_begin; ok && i < it_end;) {
-            const Segment g = segment_at(p, i, it_end);
+        for (int v = 0; ok && v < v_end;) {
+            const Segment g = work_segment(p, cta, it_begin, sk_len, v);
             const int nt = g.t / p.m_tiles, mt = g.t - nt * p.m_tiles;
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
                 const int s = (int)(seq % S);
@@ -633,7 +664,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                 }
                 __syncwarp();
             }
-            i += g.ke - g.kb;
+            v += g.ke - g.kb;
         }
         // Wind down: let the last copies land before the CTA can exit.
         if (lane == 0) {
@@ -651,8 +682,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         int d = 0;
         uint32_t dph = 0;
         bool ok = true;
-        for (long long i = it_begin; ok && i < it_end;) {
-            const Segment g = segment_at(p, i, it_end);
+        for (int v = 0; ok && v < v_end;) {
+            const Segment g = work_segment(p, cta, it_begin, sk_len, v);
             if (!wait_warp(dempty_bar(d), dph ^ 1, ctl)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem + C::kDCol + d * TM;
@@ -703,7 +734,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             if (elect_one()) mma_commit(dfull_bar(d));
             __syncwarp();
             if (++d == C::kDBufs) { d = 0; dph ^= 1; }
-            i += g.ke - g.kb;
+            v += g.ke - g.kb;
         }
         // Wind down: every MMA issued so far completes before TMEM is freed.
         if (lane == 0) {
@@ -726,8 +757,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         uint32_t seq = 0;
         bool ok = true;
-        for (long long i = it_begin; ok && i < it_end;) {
-            const Segment g = segment_at(p, i, it_end);
+        for (int v = 0; ok && v < v_end;) {
+            const Segment g = work_segment(p, cta, it_begin, sk_len, v);
             for (int kc = g.kb; kc < g.ke; ++kc, ++seq) {
                 if ((int)(seq % C::kTeams) != team) continue;
                 const int s = (int)(seq % SW);
@@ -834,15 +865,15 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull_bar(a));
             }
-            i += g.ke - g.kb;
+            v += g.ke - g.kb;
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int n_in = warp * 32 + lane;
         int d = 0;
         uint32_t dph = 0;
-        for (long long i = it_begin; i < it_end;) {
-            const Segment g = segment_at(p, i, it_end);
+        for (int v = 0; v < v_end;) {
+            const Segment g = work_segment(p, cta, it_begin, sk_len, v);
             const int t = g.t;
             const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
             const int n = nt * kTileN + n_in;
@@ -889,7 +920,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dempty_bar(d));
             if (++d == C::kDBufs) { d = 0; dph ^= 1; }
-            i += g.ke - g.kb;
+            v += g.ke - g.kb;
 
             if (split) {
                 // Deterministic split-K fix-up: the last contributor sums every
@@ -907,7 +938,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                 }
                 named_bar_sync(1, 128);
                 const int last = *last_flag;
-                if (last && i >= it_end) {
+                if (last && v >= v_end) {
                     // the CTA's final tile: every warp reduces it once all roles are done
                     if (threadIdx.x == 0) {
                         int* dfr = reinterpret_cast<int*>(smem + C::kOffMisc + 24);
