@@ -8,7 +8,7 @@ elements, which the oracle evaluates one by one. The acceptance bound is
 import numpy as np
 import pytest
 
-from tests.parity import check_within
+from tests.parity import check_within, forced_path
 from tests.test_oracle import hand_inputs, read_golden
 from weight_only_int4_02_gb300 import inputs
 
@@ -328,3 +328,23 @@ def test_chained_gemms_read_the_previous_output(w, oracle_mod):
                                np.abs(resid[np.ix_(rows, c)].astype(np.float64)) if resid is not None else 0.0,
                                "chain stage %d" % i)
         prev = y
+
+
+@pytest.mark.parametrize("M,N,K,G", [(16, 32768, 1024, 128), (100, 40000, 512, 64), (300, 20000, 264, 264)])
+def test_split_region_then_whole_tiles(w, oracle_mod, M, N, K, G):
+    """Shapes with more tiles than SMs: the tiles past the last whole wave are split
+    among every CTA and run first, the rest go whole (one region of 104 tiles with 1
+    whole tile per CTA, and regions grown by a wave with 1 whole tile per CTA, at 16,
+    128 and 256 rows per tile). Every element against the oracle, bit-identical over
+    three runs."""
+    with forced_path(w, 2):
+        assert w.plan(M, N, K, G)[0] == 2
+        x, q, s = inputs.problem(M, K, N, G, seed=M + N)
+        packed, sp = w.pack(to_dev(q), to_dev(s), G)
+        xd = to_dev(x)
+        ys = [w.gemm(xd, packed, sp, N, G).cpu().numpy() for _ in range(3)]
+    z, absum = oracle_mod.gemm(x, q, s, G)
+    check_within(ys[0], z, absum, "split region M=%d N=%d K=%d" % (M, N, K))
+    assert np.array_equal(ys[0].view(np.uint16), ys[1].view(np.uint16))
+    assert np.array_equal(ys[0].view(np.uint16), ys[2].view(np.uint16))
+    assert w.check_device_status() == w.OK

@@ -28,7 +28,7 @@ import numpy as np
 
 from weight_only_int4_02_gb300 import inputs
 
-KNOBS = ("W4A16_DECODE_CB", "W4A16_TILE_M", "W4A16_SPLIT")
+KNOBS = ("W4A16_DECODE_CB", "W4A16_TILE_M", "W4A16_SPLIT", "W4A16_SPLIT_ALL", "W4A16_MIN_ITERS")
 DEFAULT_SHAPES = [(M, K, N) for M in (1, 8, 16, 32, 64, 128)
                   for (K, N) in ((4096, 12288), (4096, 4096), (4096, 22016), (11008, 4096))]
 
