@@ -338,8 +338,9 @@ __device__ __forceinline__ Segment work_segment(const GemmParams& p, int c, long
 // m with n contiguous, so a store straight from the registers writes 2 bytes per lane
 // and row: 16 narrow stores per chunk, which measured about 1000 cycles per chunk with
 // the GPU's memory busy. The chunk is transposed across lanes with shuffles first, so
-// each lane stores two 16-byte vectors. (FP32 partials, 4 bytes per lane and row, measured
-// slower with the same transpose: they keep the direct stores.)
+// each lane stores two 16-byte vectors. FP32 partials keep their direct 4-byte stores
+// (a warp writes 128 contiguous bytes per row; the transpose measured slower there, and
+// a feature-major partial layout gave wrong sums on 128-row stream-K tiles: section 9).
 
 // 8 x 8 transpose of 32-bit elements within each group of eight lanes: on return,
 // x[k] of lane 8g + j is the x[j] that lane 8g + k held.
@@ -447,93 +448,62 @@ __device__ __forceinline__ void load_residual_rows16(const GemmParams& p, int m0
 
 // Split-K fix-up of a tile by its last contributor: Y = the sum of every
 // contributor's FP32 partial, added in contributor (CTA) order. Partials are
-// column-major ([TM][128] per slot), so one 16-byte load brings four rows of a
-// column: thread j of the nw participating warps (the four epilogue warps, or the
-// whole CTA for its last tile) takes rows 4(j mod 32) .. +3 of columns j/32,
-// j/32 + nw, j/32 + 2nw, ... A round issues L4 such loads (L4/NCP columns of NCP
-// contributors) before any is added, so it costs one global round trip. n_base is
-// the tile's first output feature.
-template <int TM, int NCP, int L4, bool EPI, bool BF>
-__device__ __forceinline__ void fix_reduce(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0,
-                                           int n_base, int nw)
-{
-    constexpr int CPR = L4 / NCP;
-    const int rg = threadIdx.x & 31;
-    const int m_first = threadIdx.x >> 5;
-    const int ncols = valid > m_first ? (valid - m_first + nw - 1) / nw : 0;   // columns m_first + nw*q, q < ncols
-    const int n = n_base + 4 * rg;
-    float b4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (EPI && p.bias && n < p.N)
-        for (int j = 0; j < 4; ++j) b4[j] = ld16<BF>(p.bias, n + j);
-    for (int q0 = 0; q0 < ncols; q0 += CPR) {
-        float4 acc[CPR];
-#pragma unroll
-        for (int e = 0; e < CPR; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc0 = c_lo; cc0 <= c_hi; cc0 += NCP) {
-            float4 v[NCP][CPR];
-#pragma unroll
-            for (int u = 0; u < NCP; ++u) {
-                const int cc = cc0 + u;
-                const float* base = p.partials + (size_t)slot_of(p, min(cc, c_hi), t) * TM * kTileN + 4 * rg;
-#pragma unroll
-                for (int e = 0; e < CPR; ++e) {
-                    const int m = m_first + nw * (q0 + e);
-                    v[u][e] = (cc <= c_hi && q0 + e < ncols)
-                                  ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)m * kTileN))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < NCP; ++u) {
-                if (cc0 + u > c_hi) continue;
-#pragma unroll
-                for (int e = 0; e < CPR; ++e) {
-                    acc[e].x += v[u][e].x;
-                    acc[e].y += v[u][e].y;
-                    acc[e].z += v[u][e].z;
-                    acc[e].w += v[u][e].w;
-                }
-            }
-        }
-        if (n < p.N) {   // N is a multiple of 8, so n .. n+3 are all in range
-#pragma unroll
-            for (int e = 0; e < CPR; ++e) {
-                if (q0 + e >= ncols) continue;
-                const int m = m0 + m_first + nw * (q0 + e);
-                __half* out = p.y + (size_t)m * p.ldy + n;
-                if constexpr (EPI) {
-                    const size_t ri = (size_t)m * p.ldr + n;
-                    const float r0 = ld16<BF>(p.residual, ri), r1 = ld16<BF>(p.residual, ri + 1);
-                    const float r2 = ld16<BF>(p.residual, ri + 2), r3 = ld16<BF>(p.residual, ri + 3);
-                    out[0] = st16<BF>(epilogue_op(p.act, acc[e].x, b4[0], r0));
-                    out[1] = st16<BF>(epilogue_op(p.act, acc[e].y, b4[1], r1));
-                    out[2] = st16<BF>(epilogue_op(p.act, acc[e].z, b4[2], r2));
-                    out[3] = st16<BF>(epilogue_op(p.act, acc[e].w, b4[3], r3));
-                } else {
-                    out[0] = st16<BF>(acc[e].x);
-                    out[1] = st16<BF>(acc[e].y);
-                    out[2] = st16<BF>(acc[e].z);
-                    out[3] = st16<BF>(acc[e].w);
-                }
-            }
-        }
-    }
-}
-
-// fix_reduce with the contributor batch chosen by the contributor count.
-template <int TM, int KSUB, bool EPI, bool BF>
+// [TM][128] per slot (row-major in m, the epilogue's lanes writing consecutive
+// features). The nw participating warps (the four epilogue warps, or the whole CTA
+// for its last tile) take (32-feature group, 16-row chunk) items in turn: a lane sums
+// its feature's 16 rows over the contributors, NCP contributors' loads in flight at
+// once (each load of a warp reads 128 contiguous bytes, one row of 32 features, from
+// L2), and the warp writes the sums as the epilogue does (transposed across lanes,
+// 16-byte stores). n_base is the tile's first feature.
+template <int TM, int NCP, bool EPI, bool BF>
 __device__ __forceinline__ void fix_tile(const GemmParams& p, int t, int c_lo, int c_hi, int valid, int m0, int n_base,
                                          int nw)
 {
-    // 16-byte loads per round: 8 where 23 warps cap registers at 80, else 16.
-    constexpr int L4 = KSUB == 4 ? 8 : 16;
-    const int ncontrib = c_hi - c_lo + 1;
-    if (ncontrib <= 2)
-        fix_reduce<TM, 2, L4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n_base, nw);
-    else if (ncontrib <= 4)
-        fix_reduce<TM, 4, L4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n_base, nw);
-    else
-        fix_reduce<TM, 8, L4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n_base, nw);
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const int chunks = (valid + 15) >> 4;
+    const bool yvec = (p.ldy & 7) == 0;
+    const bool rvec = ((reinterpret_cast<uintptr_t>(p.residual) | (uintptr_t)(p.ldr * 2)) & 15) == 0;
+    for (int item = wi; item < 4 * chunks; item += nw) {
+        const int fg = item & 3, c = item >> 2;
+        const int n_in = fg * 32 + lane;
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        for (int cc0 = c_lo; cc0 <= c_hi; cc0 += NCP) {
+            float v[NCP][16];
+#pragma unroll
+            for (int u = 0; u < NCP; ++u) {
+                const int cc = cc0 + u <= c_hi ? cc0 + u : c_hi;
+                const float* a = p.partials + (size_t)slot_of(p, cc, t) * TM * kTileN + n_in + (size_t)c * 16 * kTileN;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[u][e] = cc0 + u <= c_hi ? __ldcg(a + e * kTileN) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < NCP; ++u) {
+                if (cc0 + u > c_hi) break;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] += v[u][e];
+            }
+        }
+        uint32_t r[16];
+        if constexpr (EPI) {
+            const int n = n_base + n_in;
+            const float bias_n = n < p.N ? ld16<BF>(p.bias, n) : 0.f;
+            float rv[16];
+            if (p.residual) {
+                load_residual_rows16<BF>(p, m0 + c * 16, n_base + fg * 32, lane, rvec, rv);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) rv[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(epilogue_op(p.act, acc[e], bias_n, rv[e]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(acc[e]);
+        }
+        store_y_rows16<BF>(p, r, m0 + c * 16, n_base + fg * 32, lane, yvec);
+    }
 }
 
 // EPI: the instantiation with the fused epilogue (bias, activation, residual);
@@ -909,6 +879,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     }
                     store_y_rows16<BF>(p, r, m0 + c * 16, n - lane, lane, yvec);
                 } else {
+                    // the lane's 16 rows of the chunk, contiguous in its feature's row of the slot
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         if (c * 16 + e < valid) part[(size_t)(c * 16 + e) * kTileN] = __uint_as_float(r[e]);
@@ -946,7 +917,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                     }
                 } else if (last) {
                     __threadfence();
-                    fix_tile<TM, KSUB, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n - n_in, 4);
+                    fix_tile<TM, KSUB == 4 ? 2 : 4, EPI, BF>(p, t, c_lo, c_hi, valid, m0, n - n_in, 4);
                 }
                 named_bar_sync(1, 128);
             }
@@ -963,7 +934,8 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
             const int t = dfr[1];
             const int nt = t / p.m_tiles, mt = t - nt * p.m_tiles;
             const int m0 = mt * TM;
-            fix_tile<TM, KSUB, EPI, BF>(p, t, dfr[2], dfr[3], min(TM, p.M - m0), m0, nt * kTileN, C::kThreads / 32);
+            fix_tile<TM, KSUB == 4 ? 2 : 4, EPI, BF>(p, t, dfr[2], dfr[3], min(TM, p.M - m0), m0, nt * kTileN,
+                                                     C::kThreads / 32);
         }
     }
     if (warp == C::kMmaWarp) {
