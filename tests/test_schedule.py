@@ -316,6 +316,8 @@ def plan(M, N, K, G, sms=SMS, fmt="int4"):
         sk_tiles = work_tiles % units    # tiles past the last whole wave: split, run first
         if 0 < sk_tiles and 2 * sk_tiles < units:
             sk_tiles += units            # at least half a wave: about two contributors a tile
+        if fmt == "sparse" and tm >= 128:
+            sk_tiles = work_tiles        # 2:4 sparse codes on 128-row tiles: stream-K over every tile
     units = max(1, units)
     return dict(path=2, tm=tm, ksub=ksub, xblocks=xblocks, fmt=fmt, m_tiles=m_tiles, n_tiles=n_tiles,
                 KC=KC, iters=iters, ng=ng, total=total, sk_tiles=sk_tiles, sk_iters=sk_tiles * iters, grid=units)

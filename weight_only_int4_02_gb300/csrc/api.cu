@@ -237,9 +237,13 @@ Plan make_plan(int M, int N, int K, int G, int sms, int fmt = kFmtW4)
         // CTAs it takes one whole wave more (about two contributors a tile; measured:
         // 20 tiles over 152 CTAs, 7.6 contributors each, ran the 4096x22016 layer at
         // M = 128 in 61 us against 27). That also gives every CTA's range a stage.
+        // 2:4 sparse codes on 128-row tiles keep stream-K over every tile: they stage X
+        // only two deep (64 KB stages), and whole tiles taken round-robin have every CTA
+        // read the same X stage at once (18432x73728 at M = 128: 175 -> 194 us; at M = 16
+        // the whole tiles measured faster, 109 -> 106 us).
         const long long rest = work_tiles % units;
         const long long sk = (rest > 0 && 2 * rest < units) ? rest + units : rest;
-        P.sk_tiles = g_force_split_all ? (int)work_tiles : (int)sk;
+        P.sk_tiles = (g_force_split_all || (fmt == kFmtW4Sp && P.tm >= 128)) ? (int)work_tiles : (int)sk;
     }
     if (units < 1) units = 1;
     P.grid = (int)units;
