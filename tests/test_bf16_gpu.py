@@ -52,6 +52,7 @@ SHAPES = [
     (128, 1024, 2048, 32),    # 128-row tile pair, groups of 32
     (300, 264, 136, 32),      # 256-row tiles, two row tiles
     (1024, 1024, 1024, 128),  # 256-row tiles, four row tiles
+    (300, 20000, 264, 264),   # 256-row tiles, split region first, then whole tiles
 ]
 
 

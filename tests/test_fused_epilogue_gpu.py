@@ -57,6 +57,8 @@ def run_case(w, oracle_mod, M, N, K, G, activation, use_bias, use_resid, in_plac
 
 
 SHAPES = [
+    (16, 32768, 1024, 128),   # split region first, then whole tiles (more tiles than SMs)
+    (100, 40000, 512, 64),    # the same with 128-row tiles, ragged M
     (1, 256, 16384, 128),     # split-K, 16-row tile
     (3, 136, 200, 200),       # ragged, one group per column
     (17, 4096, 4000, 64),     # 32-row tile, ragged K
