@@ -22,11 +22,13 @@
 //   next warp           producer W: bulk copies of the packed words and the scales
 //   last warp           MMA issuer (one elected lane) and TMEM owner
 //
-// Work split ("stream-K"): the iteration space (tile, stage) is cut into one
-// contiguous range per CTA. A tile whose stages span several CTAs is reduced
-// in global memory: every contributor stores its FP32 partial, and the last
-// one to arrive on the tile's counter sums all partials in contributor order,
-// so the result does not depend on arrival order.
+// Work split: whole waves of tiles go to the CTAs whole, round-robin; the tiles past
+// them (the split region; every tile when there are fewer tiles than CTAs) have their
+// (tile, stage) iterations cut into one contiguous range per CTA ("stream-K"), which
+// each CTA runs before its whole tiles. A tile whose stages span several CTAs is
+// reduced in global memory: every contributor stores its FP32 partial, and the last
+// one to arrive on the tile's counter sums all partials in contributor order, so the
+// result does not depend on arrival order.
 //
 // Sources: "quant_marlin_kernel" (aicassindra.com), "The architecture: every
 // piece explained" (packed INT4, group scales, register-level unpack, async
