@@ -212,11 +212,48 @@ class ClockSampler:
                 "window": "timed region" if inside else "within 0.2 s of the timed region"}
 
 
+def strip_comments(src):
+    """C/C++ source without its comments and with runs of whitespace folded, so that
+    edits of comments alone leave the code's digest unchanged (string and character
+    literals are kept as they are, whitespace included)."""
+    parts, code, i, n = [], [], 0, len(src)
+
+    def flush():
+        if code:
+            parts.append(" ".join("".join(code).split()))
+            code.clear()
+
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            flush()
+            parts.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            code.append(" ")
+        else:
+            code.append(c)
+            i += 1
+    flush()
+    return " ".join(p for p in parts if p)
+
+
 def source_digest():
+    """Digest of the CUDA sources' code (comments and layout left out): the key under
+    which profiles/dram_traffic.txt records counters."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "weight_only_int4_02_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

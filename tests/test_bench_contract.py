@@ -96,3 +96,16 @@ def test_warmup_below_three_is_an_error():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
                          capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert out.returncode != 0 and "at least 3" in out.stderr
+
+
+def test_source_digest_ignores_comments_but_not_code():
+    """The key of the committed DRAM counters follows the code: a comment or layout edit
+    keeps it, any change of code (string literals included) does not."""
+    a = 'int f(int x) { // one\n  return x + 1; /* two */ }\nconst char* s = "// not a comment";\n'
+    b = 'int f(int x)\n{\n    return x + 1;   // changed comment\n}\nconst char* s = "// not a comment";\n'
+    c = 'int f(int x) { return x + 2; }\nconst char* s = "// not a comment";\n'
+    d = 'int f(int x) { return x + 1; }\nconst char* s = "// not a  comment";\n'
+    sa, sb, sc, sd = (bench.strip_comments(t) for t in (a, b, c, d))
+    assert sa.replace("{ ", "{").replace(" }", "}") == sb.replace("{ ", "{").replace(" }", "}")
+    assert sa != sc and sa != sd
+    assert '"// not a comment"' in sa
