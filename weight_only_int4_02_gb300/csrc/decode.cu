@@ -398,6 +398,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) w4a16_decode_kernel(const __gr
                 }
             }
             }
+            fence_proxy_async_smem();   // the loads of the slot precede its next TMA copies
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(s));
             s += kStep;

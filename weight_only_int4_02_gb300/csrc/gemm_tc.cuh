@@ -775,6 +775,7 @@ __global__ void __launch_bounds__(TcCfg<TM, KSUB, FMT>::kThreads, 1)
                         chi[h][0] = chi[h][1] = zp_hi(8);
                     }
                 }
+                fence_proxy_async_smem();   // the loads above precede the slot's next bulk copy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wempty_bar(s));   // words, scales and zero-points are in registers
 #pragma unroll

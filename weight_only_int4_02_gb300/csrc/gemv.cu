@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kGemvThreads) w4a16_gemv_kernel(const __grid_c
 #pragma unroll
                         for (int m = 0; m < MR; ++m) acc[j][m] = fmaf(pa[j][m].x + pa[j][m].y, sc[j], acc[j][m]);
                 }
+                fence_proxy_async_smem();   // the loads of the slot precede its next TMA copies
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
             }

@@ -30,6 +30,17 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Orders the executing thread's earlier generic-proxy accesses to shared memory (plain
+// loads of a ring slot that a bulk copy filled) before later async-proxy accesses, such
+// as the next bulk copy or TMA into the same slot once the slot is released. Without it
+// a consumer's loads of a slot can observe the producer's next copy into that slot when
+// loads are slow to return (found on GB300: wrong weight words in one warp's rows of a
+// tile under heavy store traffic).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
