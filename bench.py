@@ -4,9 +4,9 @@
 One step = one pass of the workload's GEMMs (default: the Llama-2-7B-like
 decode sweep, M in {1..128} x the four layer shapes, group 128), each reading
 its own copy of the packed weights so the step streams more distinct bytes
-than L2 holds. Steps are replayed from CUDA Graphs with an event node around
-every launch, so per-kernel durations come from CUDA events on the launching
-stream. Prints one JSON line.
+than L2 holds. Steps are replayed from CUDA Graphs of several consecutive steps
+with an event node at every change of M, so per-kernel durations come from CUDA
+events on the launching stream. Prints one JSON line.
 
   python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -373,47 +373,67 @@ def run_ours(args):
     if w4a16.check_device_status() != w4a16.OK:
         raise RuntimeError("kernel wait timed out during warm-up")
 
-    # ---- a pool of graphs, one step each, with an event node at every change of M.
-    # The event nodes hang off a side branch (forked after the group's last launch,
-    # joined at the end of the step): every launch follows the previous one directly,
-    # so launches overlap through programmatic dependent launch across the changes of
-    # M as well (an event node between two launches would serialise them). An event
-    # node records when every launch before it has completed.
+    # ---- a pool of graphs of R consecutive steps each, with an event node at every
+    # change of M. The event nodes hang off a side branch (forked after the group's last
+    # launch, joined once at the end of the graph): every launch follows the previous one
+    # directly, so launches overlap through programmatic dependent launch across the
+    # changes of M and across the steps inside a graph (an event node between two
+    # launches would serialise them). An event node records when every launch before it
+    # has completed. Only the first step of a graph starts from an idle GPU; the
+    # one-step-graph figure below measures what that start costs when every step pays it.
     bounds = [0] + [ci for ci in range(1, len(per_case)) if per_case[ci]["M"] != per_case[ci - 1]["M"]]
     bounds.append(len(per_case))
     cap = torch.cuda.Stream()
     side = torch.cuda.Stream()
     K = args.steps
-    pool = min(K, 64)
-    graphs, evs = [], []
-    for gi in range(pool):
-        ev = [cud.event() for _ in range(len(bounds))]
+    R = max(1, min(K, args.steps_per_graph))
+
+    def capture(nsteps):
+        """One graph of nsteps steps; returns (graph, per-step event lists), the first
+        event of a step being the last of the step before it (the graph's start for the
+        first step)."""
+        step_evs = []
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
             st = torch.cuda.current_stream()
-            # the step's start is recorded on the side branch too, so that no event node
+            # the graph's start is recorded on the side branch too, so that no event node
             # precedes the first GEMM
             start = torch.cuda.Event()
             start.record(st)
             side.wait_event(start)
-            cud.record_external(ev[0], side)
-            for b in range(len(bounds) - 1):
-                for ci in range(bounds[b], bounds[b + 1]):
-                    c = per_case[ci]
-                    w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
-                fork = torch.cuda.Event()
-                fork.record(st)
-                side.wait_event(fork)
-                cud.record_external(ev[b + 1], side)
+            prev = cud.event()
+            cud.record_external(prev, side)
+            for _ in range(nsteps):
+                ev = [prev]
+                for b in range(len(bounds) - 1):
+                    for ci in range(bounds[b], bounds[b + 1]):
+                        c = per_case[ci]
+                        w4a16.gemm(c["x"], c["packed"], c["sp"], c["N"], G, y=c["y"], stream=st)
+                    fork = torch.cuda.Event()
+                    fork.record(st)
+                    side.wait_event(fork)
+                    e = cud.event()
+                    cud.record_external(e, side)
+                    ev.append(e)
+                prev = ev[-1]
+                step_evs.append(ev)
             join = torch.cuda.Event()
             join.record(side)
             st.wait_event(join)
-        graphs.append(g)
-        evs.append(ev)
-    torch.cuda.synchronize()
+        return g, step_evs
 
-    for i in range(args.warmup):
-        graphs[i % pool].replay()
+    pool = max(1, min(K, 64) // R)
+    graphs = [capture(R) for _ in range(pool)]
+    tail = {n: capture(n) for n in {K % R, args.warmup % R} if n}
+
+    def run_steps(n):
+        for i in range(n // R):
+            graphs[i % pool][0].replay()
+        if n % R:
+            tail[n % R][0].replay()
+
+    torch.cuda.synchronize()
+    run_steps(args.warmup)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(torch.cuda.current_device())
@@ -422,8 +442,7 @@ def run_ours(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t0.record()
-    for i in range(K):
-        graphs[i % pool].replay()
+    run_steps(K)
     t1.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -433,14 +452,30 @@ def run_ours(args):
     if status != w4a16.OK:
         raise RuntimeError("a kernel wait timed out in the timed region")
 
-    # ---- per-M durations from the event nodes (the last `pool` steps of the timed region)
-    grp_ms = np.zeros((pool, len(bounds) - 1))
-    for gi in range(pool):
-        for b in range(len(bounds) - 1):
-            grp_ms[gi, b] = cud.elapsed_ms(evs[gi][b], evs[gi][b + 1])
+    # ---- per-M durations from the event nodes of every step whose graph ran last in the
+    # timed region (every pool graph runs there, and the tail graph of K % R steps)
+    timed_evs = [ev for g in graphs for ev in g[1]] + (tail[K % R][1] if K % R else [])
+    grp_ms = np.array([[cud.elapsed_ms(ev[b], ev[b + 1]) for b in range(len(bounds) - 1)] for ev in timed_evs])
     grp_mean = grp_ms.mean(axis=0)
     step_flops = sum(flops(c["M"], c["K"], c["N"]) for c in per_case)
     value = step_flops / (ms_step * 1e-3) / 1e12
+
+    # ---- the same steps issued as one graph per step (each step then starts from an
+    # idle GPU: no launch of it overlaps the step before), outside the timed region
+    one = [capture(1) for _ in range(8)]
+    n1 = max(3, min(K, 400))
+    for i in range(3):
+        one[i % 8][0].replay()
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(n1):
+        one[i % 8][0].replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms_one = t0.elapsed_time(t1) / n1
+    one_step_graphs = {"ms_per_step": ms_one, "value": step_flops / (ms_one * 1e-3) / 1e12, "steps": n1,
+                       "note": "every step its own graph, so no launch of a step overlaps the step before"}
+    del one
 
     # ---- diagnostic, outside the timed region: every launch between two event nodes
     diag = torch.cuda.CUDAGraph()
@@ -530,16 +565,18 @@ def run_ours(args):
                    "parallelism": "single-gpu",
                    "l2": "inputs larger than L2: every GEMM reads its own copy of the packed weights "
                          "(%.0f MB distinct per step vs 129 MB L2)" % (distinct_bytes / 1e6),
-                   "timing": "CUDA Graph per step with an event node at every change of M, on a side "
-                             "branch (every launch follows the previous one directly); per-kernel "
-                             "durations are the mean over the last %d steps of the timed region; "
+                   "timing": "CUDA Graphs of %d consecutive steps with an event node at every change of "
+                             "M, on a side branch (every launch follows the previous one directly, across "
+                             "steps too); per-kernel durations are the mean over the last %d steps of the "
+                             "timed region; one_step_graphs times the same steps one graph each; "
                              "per_case_isolated has an event node after every launch (outside the timed "
-                             "region), which removes the overlap of consecutive launches" % pool},
+                             "region), which removes the overlap of consecutive launches" % (R, len(timed_evs))},
         "roofline": roof,
         "gpu_launches": K * len(per_case),
         "clocks": clocks,
         "e2e": e2e,
         "per_M": per_m_out,
+        "one_step_graphs": one_step_graphs,
         "per_case_isolated": [{"M": c["M"], "K": c["K"], "N": c["N"], "us": float(mean_ms[ci] * 1e3),
                       "kernel": kernel_name(w4a16.plan(c["M"], c["N"], c["K"], G), c["N"]),
                       "weight_gbs": weight_bytes(c["K"], c["N"], G) / (mean_ms[ci] * 1e-3) / 1e9,
@@ -943,28 +980,40 @@ def workloads_probe(G, peaks):
     return rows
 
 
-def fp16_baseline(per_case, dev, reps):
-    """Mean time per M of torch.matmul with FP16 weights of the same shapes (own copy per case)."""
+def fp16_baseline(per_case, dev, reps, inner=4):
+    """Time per M of torch.matmul with FP16 weights of the same shapes (own copy per
+    case): per M, one CUDA Graph of that M's matmuls repeated `inner` times, replayed
+    `reps` times between two events, so that neither host launch costs nor a graph's
+    start are counted. One M's FP16 weights (405 MB for the four decode layers) are
+    more than L2 holds, so every matmul streams its weights from HBM."""
     import torch
     try:
         mats = []
         for c in per_case:
             wgt = torch.randn((c["K"], c["N"]), dtype=torch.float16, device=dev)
-            mats.append((c["x"], wgt, torch.empty((c["M"], c["N"]), dtype=torch.float16, device=dev)))
-        for x, wgt, y in mats:
+            mats.append((c["M"], c["x"], wgt, torch.empty((c["M"], c["N"]), dtype=torch.float16, device=dev)))
+        for _, x, wgt, y in mats:
             torch.matmul(x, wgt, out=y)
         torch.cuda.synchronize()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mats) + 1)] for _ in range(reps)]
-        for r in range(reps):
-            ev[r][0].record()
-            for i, (x, wgt, y) in enumerate(mats):
-                torch.matmul(x, wgt, out=y)
-                ev[r][i + 1].record()
-        torch.cuda.synchronize()
         per_m = {}
-        for i, c in enumerate(per_case):
-            ms = statistics.median(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps))
-            per_m[c["M"]] = per_m.get(c["M"], 0.0) + ms
+        cap = torch.cuda.Stream()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for M in sorted(set(m[0] for m in mats)):
+            grp = [m for m in mats if m[0] == M]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(inner):
+                    for _, x, wgt, y in grp:
+                        torch.matmul(x, wgt, out=y)
+            g.replay()
+            torch.cuda.synchronize()
+            t0.record()
+            for _ in range(reps):
+                g.replay()
+            t1.record()
+            torch.cuda.synchronize()
+            per_m[M] = t0.elapsed_time(t1) / (reps * inner)
+            del g
         del mats
         torch.cuda.empty_cache()
         return per_m
@@ -1166,6 +1215,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps-per-graph", type=int, default=8,
+                    help="consecutive steps captured in one CUDA Graph (decode sweep)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
