@@ -552,7 +552,7 @@ def run_ours(args):
         per_m_out.append(entry)
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(per_case, G, dev, K, args.warmup)
+    e2e = run_e2e(per_case, G, dev, K, args.warmup, R)
 
     out = {
         "metric": "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM/tensor roofline",
@@ -1021,15 +1021,19 @@ def fp16_baseline(per_case, dev, reps, inner=4):
         return None
 
 
-def run_e2e(per_case, G, dev, K, W):
+def run_e2e(per_case, G, dev, K, W, R=1):
     """Same metric through the public API with host buffers: per step, every GEMM's X
     from pinned host memory to the device, the GEMMs, and every Y back to pinned host
-    memory, all inside the timed region (one CUDA Graph per step). The copies run on
-    two side streams so that they overlap the GEMMs: the GEMMs go by groups of equal M,
-    largest M first; the first group's X is uploaded GEMM by GEMM and every later
-    group's X in one copy while the first group computes; each group's Y is downloaded
-    in one copy once its GEMMs are done, while later groups compute. What stays exposed
-    is the first GEMM's X and the last group's (smallest) Y."""
+    memory, all inside the timed region. Steps go as CUDA Graphs of R consecutive steps
+    (the device-only loop's grouping), with two sets of device X and Y buffers used in
+    turn, so that a step's uploads run while the step before computes. The copies run on
+    two side streams: the GEMMs go by groups of equal M, largest M first; in a graph's
+    first step the first group's X is uploaded GEMM by GEMM and every later group's X in
+    one copy, in the later steps all of X in one copy; each group's Y is downloaded in
+    one copy once its GEMMs are done, while later groups compute. A step's uploads wait for the GEMMs that last read their buffer set (two
+    steps back), and its first GEMM for the downloads that last read its Y buffers. What
+    stays exposed, once per graph, is the first step's first X and the last step's
+    last (smallest) Y."""
     import torch
     from weight_only_int4_02_gb300 import w4a16
     order = sorted(range(len(per_case)), key=lambda i: (-per_case[i]["M"], i))
@@ -1041,17 +1045,16 @@ def run_e2e(per_case, G, dev, K, W):
             groups.append([i])
     x_sizes = {i: per_case[i]["M"] * per_case[i]["K"] for i in order}   # multiples of 8: 16-byte aligned views
     y_sizes = {i: per_case[i]["M"] * per_case[i]["N"] for i in order}
-    x_dev = torch.empty(sum(x_sizes.values()), dtype=torch.float16, device="cuda")
-    y_dev = torch.empty(sum(y_sizes.values()), dtype=torch.float16, device="cuda")
+    NB = 2
+    x_dev = [torch.empty(sum(x_sizes.values()), dtype=torch.float16, device="cuda") for _ in range(NB)]
+    y_dev = [torch.empty(sum(y_sizes.values()), dtype=torch.float16, device="cuda") for _ in range(NB)]
     x_host = torch.empty(sum(x_sizes.values()), dtype=torch.float16).pin_memory()
     y_host = torch.empty(sum(y_sizes.values()), dtype=torch.float16).pin_memory()
-    xs, ys, ys_h, x_rng, y_rng = {}, {}, {}, {}, {}
+    ys_h, x_rng, y_rng = {}, {}, {}
     ox = oy = 0
     for i in order:
         c, nx, ny = per_case[i], x_sizes[i], y_sizes[i]
         x_host[ox:ox + nx].copy_(c["x"].reshape(-1).cpu())
-        xs[i] = x_dev[ox:ox + nx].view(c["M"], c["K"])
-        ys[i] = y_dev[oy:oy + ny].view(c["M"], c["N"])
         ys_h[i] = y_host[oy:oy + ny].view(c["M"], c["N"])
         x_rng[i], y_rng[i] = (ox, ox + nx), (oy, oy + ny)
         ox += nx
@@ -1061,51 +1064,80 @@ def run_e2e(per_case, G, dev, K, W):
     # X copies: one per GEMM of the first group, one per later group; Y copies: one per group
     x_chunks = [[i] for i in groups[0]] + groups[1:]
     cap, up, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=cap):
-        main = torch.cuda.current_stream()
-        up.wait_stream(main)
-        down.wait_stream(main)
-        ready = {}
-        with torch.cuda.stream(up):
-            for ch in x_chunks:
-                a, b = x_rng[ch[0]][0], x_rng[ch[-1]][1]
-                x_dev[a:b].copy_(x_host[a:b], non_blocking=True)
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            main = torch.cuda.current_stream()
+            up.wait_stream(main)
+            down.wait_stream(main)
+            gemms_done, dl_done = [], []
+            for s in range(nsteps):
+                xb, yb = x_dev[s % NB], y_dev[s % NB]
+                ready = {}
+                with torch.cuda.stream(up):
+                    if s >= NB:
+                        up.wait_event(gemms_done[s - NB])
+                    # after the first step the uploads run under the previous step's
+                    # GEMMs: one copy of all of X, one wait for the step's first GEMM
+                    for ch in (x_chunks if s == 0 else [order]):
+                        a, b = x_rng[ch[0]][0], x_rng[ch[-1]][1]
+                        xb[a:b].copy_(x_host[a:b], non_blocking=True)
+                        ev = torch.cuda.Event()
+                        ev.record(up)
+                        for i in ch:
+                            ready[i] = ev
+                if s >= NB:
+                    main.wait_event(dl_done[s - NB])
+                # Every launch follows the previous one directly (programmatic dependent
+                # launch) except where it waits for an upload: the first group's GEMMs each
+                # wait for their own X, and its last GEMM also for every later group's X,
+                # so the later groups start without a wait.
+                waited = set()
+                for gi, grp in enumerate(groups):
+                    for i in grp:
+                        need = [ready[i]]
+                        if gi == 0 and i == grp[-1]:
+                            need += [ready[j] for g2 in groups[1:] for j in g2]
+                        for ev in need:
+                            if id(ev) not in waited:
+                                main.wait_event(ev)
+                                waited.add(id(ev))
+                        c = per_case[i]
+                        xi = xb[x_rng[i][0]:x_rng[i][1]].view(c["M"], c["K"])
+                        yi = yb[y_rng[i][0]:y_rng[i][1]].view(c["M"], c["N"])
+                        w4a16.gemm(xi, c["packed"], c["sp"], c["N"], G, y=yi, stream=main)
+                    done = torch.cuda.Event()
+                    done.record(main)
+                    down.wait_event(done)
+                    with torch.cuda.stream(down):
+                        a, b = y_rng[grp[0]][0], y_rng[grp[-1]][1]
+                        y_host[a:b].copy_(yb[a:b], non_blocking=True)
+                gemms_done.append(done)
                 ev = torch.cuda.Event()
-                ev.record(up)
-                for i in ch:
-                    ready[i] = ev
-        # Every launch follows the previous one directly (programmatic dependent
-        # launch) except where it waits for an upload: the first group's GEMMs each wait
-        # for their own X, and its last GEMM also for every later group's X (uploaded
-        # long before), so the later groups start without a wait.
-        waited = set()
-        for gi, grp in enumerate(groups):
-            for i in grp:
-                need = [ready[i]]
-                if gi == 0 and i == grp[-1]:
-                    need += [ready[j] for g2 in groups[1:] for j in g2]
-                for ev in need:
-                    if id(ev) not in waited:
-                        main.wait_event(ev)
-                        waited.add(id(ev))
-                c = per_case[i]
-                w4a16.gemm(xs[i], c["packed"], c["sp"], c["N"], G, y=ys[i], stream=main)
-            done = torch.cuda.Event()
-            done.record(main)
-            down.wait_event(done)
-            with torch.cuda.stream(down):
-                a, b = y_rng[grp[0]][0], y_rng[grp[-1]][1]
-                y_host[a:b].copy_(y_dev[a:b], non_blocking=True)
-        main.wait_stream(up)
-        main.wait_stream(down)
-    for _ in range(max(W, 1)):
-        g.replay()
+                ev.record(down)
+                dl_done.append(ev)
+            main.wait_stream(up)
+            main.wait_stream(down)
+        return g
+
+    R = max(1, min(K, R))
+    graphs = {R: capture(R)}
+    for n in {K % R, W % R}:
+        if n:
+            graphs[n] = capture(n)
+
+    def run_steps(n):
+        for _ in range(n // R):
+            graphs[R].replay()
+        if n % R:
+            graphs[n % R].replay()
+
+    run_steps(max(W, 1))
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(K):
-        g.replay()
+    run_steps(K)
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / K
@@ -1113,7 +1145,8 @@ def run_e2e(per_case, G, dev, K, W):
     ok = all(torch.equal(ys_h[i], per_case[i]["y"].cpu()) for i in order)   # the device-timed run's Y
     return {"value": step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "outputs_match_device": ok,
-            "copies_per_step": {"h2d": len(x_chunks), "d2h": len(groups)}}
+            "steps_per_graph": R,
+            "copies_per_step": {"h2d": (len(x_chunks) + R - 1) / R, "d2h": len(groups)}}
 
 
 # --------------------------------------------------------------------------- reference arm (oracle)
