@@ -558,6 +558,9 @@ def run_ours(args):
         "metric": "W4A16 GEMM TFLOP/s and weight GB/s vs M; % of HBM/tensor roofline",
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        # the same step from the event nodes of the last steps (a check on the timed
+        # region: well below ms_per_step means a stall somewhere inside it)
+        "ms_per_step_events": float(grp_mean.sum()),
         "dtype": "f16", "data": "synthetic",
         "config": {"workload": args.workload, "gemms_per_step": len(per_case),
                    "shapes": "M in %s x (K,N) in %s, group %d" % (
